@@ -1,0 +1,491 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 INT4-weight GEMV on GB300.
+
+Headline workload: the square projection GEMV, M=1, N=K=4096, g=128
+(x bf16 ~ N(0,1), uniform 4-bit codes, scales ~ U[0.005, 0.02], zero 8).
+One step = one w4a16_gemv launch (the whole hot path: stage x, stream the
+packed weights, dequantise, multiply-accumulate, reduce, store y).
+
+Metric: achieved HBM GB/s = algorithmic bytes per step (packed weights +
+scales + activations) / device time per step.  The weights are rotated over
+enough copies that every step reads from HBM (their total exceeds twice the
+L2).  Steps are launched from a CUDA graph and timed with CUDA events on the
+launching stream.
+
+Also reported: an M sweep and the other workloads (wide MLP up/down, MoE
+expert chain, vocabulary head), end-to-end throughput through the public
+API with host buffers, SM clocks sampled during the timed region, and the
+CPU oracle's throughput on the host cores.
+
+--impl reference times the CPU oracle itself on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W4A16 GEMV achieved HBM GB/s and % of GB300 peak at M=1 (plus M=2..16 sweep)"
+WORKLOAD = "Square projection GEMV: M=1, N=4096, K=4096, g=128, zero=8, bf16 out"
+FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 8000.0
+
+
+def algo_bytes(M, N, K, g):
+    """Packed weights + scales + activations (the roofline's algorithmic bytes)."""
+    return N * K // 2 + N * (K // g) * 2 + M * K * 2
+
+
+def all_bytes(M, N, K, g, out_bytes=2):
+    return algo_bytes(M, N, K, g) + N * (K // g) + M * N * out_bytes
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemv_simt.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "w4a16_int4_weight_gemv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the M=1 kernel from the committed ncu summary,
+    or None if absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "gemv_m1_square_4096.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    s = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                             "active": parts[4], "hw": parts[5], "hwt": parts[6], "swt": parts[7],
+                             "pcap": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r["sm"] > 0.5 * r["max"]] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        pw = [r["power"] for r in loaded if r["power"] is not None]
+        return {"sm_mhz": float(np.median([r["sm"] for r in loaded])),
+                "sm_max_mhz": float(max(r["max"] for r in rows)),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def _dev(a, torch):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    elif a.dtype == np.uint32:
+        a = a.view(np.int32)
+    return torch.from_numpy(a).cuda()
+
+
+def make_rotation(torch, M, N, K, g, zmode, l2_bytes, seed=0, min_copies=2, out_dtype=None):
+    """Enough independent copies of one problem that their total is > 2x L2."""
+    per = all_bytes(M, N, K, g)
+    R = max(min_copies, int(math.ceil(2.0 * l2_bytes / per)))
+    copies = []
+    for r in range(R):
+        from w4a16_int4_weight_gemv_gb300 import synth
+        p = synth.dense_problem(M, N, K, g, zmode, seed=seed, sub=r)
+        copies.append(tuple(_dev(p[k], torch) for k in ("x", "wq", "scale", "zero")))
+    outs = [torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device="cuda") for _ in range(R)]
+    return copies, outs
+
+
+def capture(torch, fn, n):
+    """CUDA graph of n consecutive steps fn(i)."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn(0)  # make sure nothing lazy happens inside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            fn(i)
+    return g
+
+
+def time_steps(torch, fn, R, steps, warmup):
+    """Run `warmup` untimed then exactly `steps` timed steps (graph replays of
+    R steps plus a remainder graph); returns seconds per step."""
+    full = capture(torch, fn, R)
+    rem = steps % R
+    tail = capture(torch, fn, rem) if rem else None
+    for _ in range(max(1, int(math.ceil(warmup / R)))):
+        full.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps // R):
+        full.replay()
+    if tail is not None:
+        tail.replay()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3 / steps
+
+
+def gpu_gemv_gbs(torch, w, M, N, K, g, zmode, l2, steps, warmup, out_dtype=None, kernel_id=0):
+    copies, outs = make_rotation(torch, M, N, K, g, zmode, l2, out_dtype=out_dtype)
+    R = len(copies)
+
+    def step(i):
+        x, wq, s, z = copies[i % R]
+        w.w4a16_gemv(x, wq, s, z, g, out=outs[i % R], kernel_id=kernel_id)
+
+    t = time_steps(torch, step, R, steps, warmup)
+    del copies, outs
+    return t
+
+
+def moe_chain_time(torch, w, M, steps, warmup, l2):
+    """Routed SwiGLU expert chain (64 experts, gate/up [1024, 2304], down
+    [2304, 1024], top-8) over rotated expert banks; seconds per chain and
+    the distinct-expert weight bytes it streams."""
+    from w4a16_int4_weight_gemv_gb300 import synth
+    per_bank = 64 * (2 * 1024 * 2304 + 2304 * 1024) * (0.5 + 2.0 / 128)
+    R = max(2, int(math.ceil(2.0 * l2 / per_bank)))
+    banks = []
+    byts = []
+    for r in range(R):
+        p = synth.moe_problem(M=M, E=64, H=2304, F=1024, topk=8, g=128, seed=r)
+        banks.append(dict(x=_dev(p["x"], torch), ids=_dev(p["ids"], torch),
+                          r=_dev(p["route_w"], torch),
+                          gate=tuple(_dev(a, torch) for a in p["gate"]),
+                          up=tuple(_dev(a, torch) for a in p["up"]),
+                          down=tuple(_dev(a, torch) for a in p["down"])))
+        distinct = len(np.unique(p["ids"]))
+        byts.append(distinct * (2 * algo_bytes(0, 1024, 2304, 128) + algo_bytes(0, 2304, 1024, 128))
+                    + 2 * M * 2304 * 2 + M * 8 * 1024 * 2)
+
+    def step(i):
+        b = banks[i % R]
+        w.moe_ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128)
+
+    t = time_steps(torch, step, R, steps, warmup)
+    return t, float(np.mean(byts))
+
+
+def e2e_gbs(torch, w, M, N, K, g, steps):
+    """Public API with host buffers: per step copy x from pinned host memory,
+    run w4a16_gemv on resident weights, read y back to host."""
+    from w4a16_int4_weight_gemv_gb300 import synth
+    p = synth.dense_problem(M, N, K, g, "const8", seed=0)
+    wq, s, z = (_dev(p[k], torch) for k in ("wq", "scale", "zero"))
+    xs = [torch.from_numpy(synth.activations(0, (M, K), sub=i).view(np.int16)).pin_memory()
+          for i in range(8)]
+    y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    y_dev = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for i in range(20):
+        x_dev.copy_(xs[i % 8], non_blocking=True)
+        w.w4a16_gemv(x_dev, wq, s, z, g, out=y_dev)
+        y_host.copy_(y_dev, non_blocking=True)
+        stream.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        x_dev.copy_(xs[i % 8], non_blocking=True)
+        w.w4a16_gemv(x_dev, wq, s, z, g, out=y_dev)
+        y_host.copy_(y_dev, non_blocking=True)
+        stream.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": algo_bytes(M, N, K, g) / dt / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
+            "us_per_step": dt * 1e6}
+
+
+def cpu_baseline(seconds=10.0):
+    """The CPU oracle as it stands, single-threaded, on full 4096x4096 GEMVs."""
+    import oracle
+    from w4a16_int4_weight_gemv_gb300 import synth
+    oracle.build()
+    p = synth.dense_problem(1, 4096, 4096, 128, "const8", seed=0)
+    args = (p["x"], p["wq"], p["scale"], p["zero"], 128)
+    oracle.gemv(*args)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.gemv(*args)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n * algo_bytes(1, 4096, 4096, 128) / dt / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": "%d full M=1 4096x4096 GEMVs (fp64 C oracle, one thread) in %.1f s" % (n, dt)}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from w4a16_int4_weight_gemv_gb300 import binding as w
+
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2**20
+    M, N, K, g = 1, 4096, 4096, 128
+    copies, outs = make_rotation(torch, M, N, K, g, "const8", l2)
+    R = len(copies)
+
+    def step(i):
+        x, wq, s, z = copies[i % R]
+        w.w4a16_gemv(x, wq, s, z, g, out=outs[i % R])
+
+    full = capture(torch, step, R)
+    rem = args.steps % R
+    tail = capture(torch, step, rem) if rem else None
+    # warm-up: W untimed steps (at least 3)
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    full.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.perf_counter()
+    start.record()
+    for _ in range(args.steps // R):
+        full.replay()
+    if tail is not None:
+        tail.replay()
+    end.record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed = start.elapsed_time(end) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    per_step = elapsed / args.steps
+    bytes_step = algo_bytes(M, N, K, g)
+    value = world * bytes_step * args.steps / elapsed / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = bytes_step / per_step / 1e9
+    y_check = outs[0].float()
+    assert torch.isfinite(y_check).all()
+    del copies, outs, full, tail
+    torch.cuda.empty_cache()
+
+    extra = {}
+    if rank == 0 and not args.no_sweep:
+        sweep = {}
+        sw_steps, sw_warm = 400, 40
+        for name, (n_, k_) in (("up", (14336, 4096)), ("down", (4096, 14336))):
+            for m in (1, 2, 4, 8, 16):
+                t = gpu_gemv_gbs(torch, w, m, n_, k_, 128, "uniform6to10", l2, sw_steps, sw_warm)
+                sweep["%s_M%d" % (name, m)] = {
+                    "us": round(t * 1e6, 3), "GB/s": round(algo_bytes(m, n_, k_, 128) / t / 1e9, 1),
+                    "frac_measured_peak": round(algo_bytes(m, n_, k_, 128) / t / 1e9 / peak, 4)}
+        for m in (1, 2, 4, 8, 16):
+            tu = sweep["up_M%d" % m]["us"]
+            td = sweep["down_M%d" % m]["us"]
+            sweep["mlp_chain_M%d_tokens_per_s" % m] = round(m / ((2 * tu + td) * 1e-6), 1)
+        t = gpu_gemv_gbs(torch, w, 1, 163840, 4096, 128, "uniform6to10", l2, 200, 20,
+                         out_dtype=torch.float32)
+        sweep["vocab_M1"] = {"us": round(t * 1e6, 3),
+                             "GB/s": round(algo_bytes(1, 163840, 4096, 128) / t / 1e9, 1),
+                             "frac_measured_peak": round(algo_bytes(1, 163840, 4096, 128) / t / 1e9 / peak, 4)}
+        t = gpu_gemv_gbs(torch, w, 1, 4096, 4096, 128, "const8", l2, 2000, 100, kernel_id=2)
+        sweep["square_M1_warp_mma_variant"] = {"us": round(t * 1e6, 3),
+                                               "GB/s": round(bytes_step / t / 1e9, 1)}
+        for m in (1, 2, 4):
+            t, byts = moe_chain_time(torch, w, m, 200, 20, l2)
+            sweep["moe_chain_M%d" % m] = {"us": round(t * 1e6, 3), "GB/s": round(byts / t / 1e9, 1),
+                                          "frac_measured_peak": round(byts / t / 1e9 / peak, 4),
+                                          "tokens_per_s": round(m / t, 1)}
+        extra["sweep"] = sweep
+        extra["e2e"] = e2e_gbs(torch, w, M, N, K, g, min(args.steps, 3000))
+        if not args.no_cpu_baseline:
+            extra["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        plan = w.gemv_plan(M, N, K, g)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "w4a16: int4 weights, bf16 activations/outputs, fp32 accumulate",
+            "data": "synthetic (seeded: x~N(0,1) bf16, uniform 4-bit codes, scales~U[0.005,0.02], zero=8)",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "g": g,
+                       "l2_policy": "inputs larger than L2: %d rotating weight copies, %.0f MB total"
+                                    % (R, R * all_bytes(M, N, K, g) / 1e6),
+                       "launch": "CUDA graph of %d w4a16_gemv launches, replayed" % R,
+                       "plan": plan, "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                         "frac_of_8TBs_spec": round(achieved / SPEC_HBM_GBS, 4),
+                         "traffic": profiled_traffic(),
+                         "algorithmic_bytes_per_launch": bytes_step},
+            "clocks": clk,
+            "gpu_launches": args.steps,
+            "wall_s_timed_region": round(t_wall, 4),
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from w4a16_int4_weight_gemv_gb300 import synth
+    oracle.build()
+    M, N, K, g = 1, 4096, 4096, 128
+    p = synth.dense_problem(M, N, K, g, "const8", seed=0)
+    # time one row to size a bounded per-step sample (whole run ~ a minute)
+    t0 = time.perf_counter()
+    oracle.gemv_rows(p["x"], p["wq"], p["scale"], p["zero"], g, np.arange(64, dtype=np.int64))
+    t_row = (time.perf_counter() - t0) / 64
+    budget = 60.0
+    rows_per_step = int(max(1, min(N, budget / max(1, args.steps + args.warmup) / t_row)))
+    rng = np.random.default_rng(0)
+    for i in range(args.warmup):
+        oracle.gemv_rows(p["x"], p["wq"], p["scale"], p["zero"], g,
+                         rng.integers(0, N, rows_per_step).astype(np.int64))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.gemv_rows(p["x"], p["wq"], p["scale"], p["zero"], g,
+                         rng.integers(0, N, rows_per_step).astype(np.int64))
+    dt = time.perf_counter() - t0
+    bytes_step = rows_per_step * (K // 2 + (K // g) * 2) + M * K * 2
+    value = bytes_step * args.steps / dt / 1e9
+    sample = ("%d of the 4096 output rows per step (fp64 C oracle, one thread), %d steps"
+              % (rows_per_step, args.steps))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (same seeded workload)",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "g": g},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 INT4-weight GEMV library.
+ *
+ * The operation is the decode-time product described in the local-kimi
+ * README (RightNow-AI/local-kimi), technical-detail section: a matrix of
+ * group-quantised 4-bit weights times a handful (M <= 16) of 16-bit
+ * activation rows, done as a true matrix-vector product -- the reduction
+ * axis K contiguous in memory, one accumulator row per output, and no
+ * per-call partial buffers (same section).  The grouped-expert variant of the
+ * same section is w4a16_moe_gemv.
+ *
+ * Data layout (all row-major, all device memory unless stated otherwise):
+ *   x      bf16   [M][K]        activations (IEEE bfloat16 bit patterns)
+ *   wq     uint32 [N][K/8]      packed codes: code(n,k) = (wq[n][k/8] >> 4*(k%8)) & 15,
+ *                               i.e. eight codes per word, lowest nibble = lowest k
+ *   scale  bf16   [N][K/g]      one scale per (row, group of g consecutive k)
+ *   zero   uint8  [N][K/g]      one integer zero point per (row, group)
+ *   W[n][k] = (code(n,k) - zero[n][k/g]) * scale[n][k/g]
+ *   y      [M][N]  bf16 or fp32: y[m][n] = sum_k x[m][k] * W[n][k]
+ *
+ * Conventions shared by every call:
+ *   - bf16 values are passed as uint16_t bit patterns.
+ *   - Every pointer is a device pointer owned by the caller; the library never
+ *     allocates device memory.  A `stream` is a cudaStream_t passed as void*
+ *     (NULL = the legacy default stream).  Calls are asynchronous: they
+ *     enqueue kernels on `stream` and return without synchronising.
+ *   - Arguments are validated before anything is launched.  An invalid call
+ *     returns a status other than W4A16_OK and leaves every output untouched.
+ *     Nothing is thrown across this interface.  W4A16_ERR_CUDA means a launch
+ *     was refused by the CUDA runtime; faults of kernels already enqueued
+ *     surface, as usual in CUDA, at the caller's next synchronisation.
+ *   - Data-dependent problems that only the GPU can see (an expert id out of
+ *     range, a staging wait that timed out) never trap: the kernel skips the
+ *     affected work, writes zeros there, and sets a bit in a per-device error
+ *     word that w4a16_device_error reads.
+ *   - All tensor pointers must be 16-byte aligned (W4A16_ERR_ALIGN otherwise).
+ *   - Shape limits: 1 <= M <= 16; K % 32 == 0; g % 32 == 0; K % g == 0;
+ *     N >= 1; K <= 65536; N*K/8 < 2^31 words per matrix.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbol visibility: the library is built with hidden visibility and exports
+ * exactly the functions declared here. */
+#if defined(__GNUC__)
+#define W4A16_API __attribute__((visibility("default")))
+#else
+#define W4A16_API
+#endif
+
+typedef enum w4a16_status {
+    W4A16_OK = 0,
+    W4A16_ERR_NULL = 1,        /* a required pointer is NULL */
+    W4A16_ERR_SHAPE = 2,       /* a size is out of range or inconsistent */
+    W4A16_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    W4A16_ERR_UNSUPPORTED = 4, /* valid request outside what is implemented (e.g. M > 16) */
+    W4A16_ERR_WORKSPACE = 5,   /* workspace missing or smaller than *_workspace_bytes */
+    W4A16_ERR_CUDA = 6         /* the CUDA runtime refused a launch or query */
+} w4a16_status;
+
+typedef enum w4a16_out_dtype {
+    W4A16_OUT_BF16 = 0, /* outputs rounded to bf16, nearest-even */
+    W4A16_OUT_F32 = 1   /* outputs stored as fp32 (e.g. vocabulary logits) */
+} w4a16_out_dtype;
+
+/* Bits of the per-device error word (see w4a16_device_error). */
+#define W4A16_DEVERR_EXPERT_ID 0x1u /* an expert id was outside [0, E) */
+#define W4A16_DEVERR_TIMEOUT 0x2u   /* a bounded wait for staged data expired */
+
+/* Version of this interface; bumped on any incompatible change. */
+W4A16_API int w4a16_abi_version(void);
+
+/* Static, NUL-terminated description of a status code. */
+W4A16_API const char* w4a16_status_string(w4a16_status status);
+
+/*
+ * int4_pack -- pack 4-bit codes into the wq layout above.
+ *   codes  uint8 [N][K], each 0..15 (only the low nibble is used)
+ *   wq     uint32 [N][K/8] output
+ * Requires K % 8 == 0.  Bit-exact integer work.
+ * (Packing order: the problem statement accompanying the README's
+ *  technical-detail section -- eight codes per word, low nibble first along K.)
+ */
+W4A16_API w4a16_status int4_pack(const uint8_t* codes, uint32_t* wq, int64_t N, int64_t K, void* stream);
+
+/*
+ * int4_dequant -- expand packed weights to W[n][k] = (code - zero) * scale.
+ *   w  [N][K] output, bf16 (the exact value rounded to nearest-even) or fp32
+ *      (exact: |code - zero| <= 15 times an 8-bit significand fits in 24 bits).
+ * Requires K % 32 == 0, g % 32 == 0, K % g == 0.
+ */
+W4A16_API w4a16_status int4_dequant(const uint32_t* wq, const uint16_t* scale, const uint8_t* zero,
+                          void* w, w4a16_out_dtype out_dtype, int64_t N, int64_t K, int64_t g,
+                          void* stream);
+
+/*
+ * w4a16_gemv_workspace_bytes -- device workspace w4a16_gemv needs for this
+ * shape.  The dense GEMV needs none (0): split-K partials are combined
+ * on chip through thread-block-cluster shared memory.  Kept so callers can
+ * size a workspace generically.
+ */
+W4A16_API size_t w4a16_gemv_workspace_bytes(int M, int64_t N, int64_t K, int64_t g);
+
+/*
+ * w4a16_gemv -- y[M][N] = x[M][K] . W^T with W dequantised on the fly
+ * (README technical-detail section: the GEMV rewrite of the dense W4A16
+ * kernel).  Products are formed exactly and accumulated in fp32; y is stored
+ * as bf16 (round to nearest-even) or fp32 per out_dtype.
+ *   workspace/workspace_bytes: may be NULL/0 (none is needed; see above).
+ * Kernel choice (fixed by M, N, K; see w4a16_gemv_plan): M == 1 runs the
+ * CUDA-core kernel, 2 <= M <= 16 the warp-MMA kernel.
+ */
+W4A16_API w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
+                        const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,
+                        int64_t N, int64_t K, int64_t g, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
+ * w4a16_gemv_plan -- describe the launch w4a16_gemv would make for a shape,
+ * without launching: kernel id (1 = CUDA-core M=1 kernel, 2 = warp-MMA
+ * kernel), CTAs, threads per CTA, K-split factor (cluster size) and dynamic
+ * shared memory bytes.  Any output pointer may be NULL.  Needs the current
+ * device's properties (W4A16_ERR_CUDA without a device).
+ */
+W4A16_API w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, int* kernel_id, int* ctas,
+                             int* threads, int* k_split, int* smem_bytes);
+
+/*
+ * w4a16_gemv_variant -- w4a16_gemv with the kernel forced (for measurement):
+ * kernel_id 1 (CUDA-core, M == 1 only) or 2 (warp-MMA, any M); k_split 0 =
+ * automatic, else the K-split factor (1..8).  Same contract as w4a16_gemv.
+ */
+W4A16_API w4a16_status w4a16_gemv_variant(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
+                                const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,
+                                int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
+                                void* stream);
+
+/*
+ * w4a16_moe_workspace_bytes -- workspace w4a16_moe_gemv needs: fp32 partials
+ * [M][topk][N] when route weights are given (route != 0), else 0.
+ */
+W4A16_API size_t w4a16_moe_workspace_bytes(int M, int topk, int64_t N, int route);
+
+/*
+ * w4a16_moe_gemv -- expert-indexed W4A16 GEMV (README technical-detail
+ * section, the grouped expert kernel).  For token t and routed slot j with
+ * e = expert_ids[t][j]:
+ *     d[t][j][n] = sum_k xin[k] * W_e[n][k],
+ *     xin = x[t] (x_per_slot == 0, x is [M][K]) or x[t][j] (x is [M][topk][K]).
+ * Experts are stacked: wq [E][N][K/8], scale and zero [E][N][K/g].
+ * Each distinct expert's weights are streamed once per call however many
+ * slots select it.
+ *   route_w == NULL: y is bf16 [M][topk][N], y[t][j] = d[t][j].
+ *   route_w != NULL: fp32 [M][topk]; y is bf16 [M][N],
+ *                    y[t][n] = sum_j route_w[t][j] * d[t][j][n] (fp32, j ascending);
+ *                    needs a workspace of w4a16_moe_workspace_bytes(M, topk, N, 1).
+ * Limits: M*topk <= 256, E >= 1.  Expert ids outside [0, E) are skipped
+ * (their contribution is zero) and flagged with W4A16_DEVERR_EXPERT_ID.
+ */
+W4A16_API w4a16_status w4a16_moe_gemv(const uint16_t* x, int x_per_slot, const int32_t* expert_ids,
+                            const float* route_w, const uint32_t* wq, const uint16_t* scale,
+                            const uint8_t* zero, uint16_t* y, int M, int topk, int E, int64_t N,
+                            int64_t K, int64_t g, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * w4a16_swiglu -- h[r][n] = bf16(silu(gate[r][n]) * up[r][n]), computed in
+ * fp32, silu(v) = v / (1 + e^-v).  The activation between the gate/up and
+ * down expert products (the README's kernel registry names a SwiGLU op).
+ *   gate, up: bf16 rows with leading dimension ld_in (elements); h: bf16 rows
+ *   with leading dimension ld_out.  Lets gate/up be the two halves of one
+ *   stacked [rows][2N] output (up = gate + N, ld_in = 2N).
+ * Requires ld_in >= N, ld_out >= N; pointers 4-byte aligned; N even.
+ */
+W4A16_API w4a16_status w4a16_swiglu(const uint16_t* gate, const uint16_t* up, int64_t ld_in, uint16_t* h,
+                          int64_t ld_out, int64_t rows, int64_t N, void* stream);
+
+/*
+ * w4a16_device_error -- synchronise `stream`, then copy the current device's
+ * error word (W4A16_DEVERR_* bits set by kernels since the last clear) to
+ * *bits_out (host pointer); reset it to 0 if clear != 0.
+ */
+W4A16_API w4a16_status w4a16_device_error(uint32_t* bits_out, int clear, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

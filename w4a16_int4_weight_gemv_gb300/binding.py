@@ -1,0 +1,278 @@
+"""ctypes binding of libw4a16.so (declared in include/w4a16.h).
+
+Argument marshalling only: each function checks tensor dtypes, shapes and
+devices, passes raw pointers and the current CUDA stream to the C ABI, and
+raises W4A16Error on a non-OK status.  Every step of the computation runs in
+the library's CUDA kernels; there is no CPU fallback, and importing this
+module fails if the library has not been built.
+
+bf16 tensors may be passed as torch.bfloat16 or as their int16/uint16 bit
+patterns.  Packed weights are int32 (bit patterns of the uint32 words).
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_DEFAULT_LIB = os.path.join(_HERE, "_build", "libw4a16.so")
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_NULL = 1
+    ERR_SHAPE = 2
+    ERR_ALIGN = 3
+    ERR_UNSUPPORTED = 4
+    ERR_WORKSPACE = 5
+    ERR_CUDA = 6
+
+
+DEVERR_EXPERT_ID = 0x1
+DEVERR_TIMEOUT = 0x2
+OUT_BF16 = 0
+OUT_F32 = 1
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = Status(status)
+        super().__init__("%s: %s (%s)" % (where, status_string(status), self.status.name))
+
+
+def lib_path() -> str:
+    return os.environ.get("W4A16_LIB", _DEFAULT_LIB)
+
+
+_lib = None
+
+
+def load_library():
+    """Load libw4a16.so; raises if it is missing (build it with build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise ImportError("libw4a16.so not built (expected at %s); run "
+                          "w4a16_int4_weight_gemv_gb300.build_ext.build()" % path)
+    lib = ctypes.CDLL(path)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.w4a16_abi_version.restype = I32
+    lib.w4a16_abi_version.argtypes = []
+    lib.w4a16_status_string.restype = ctypes.c_char_p
+    lib.w4a16_status_string.argtypes = [I32]
+    lib.int4_pack.restype = I32
+    lib.int4_pack.argtypes = [P, P, I64, I64, P]
+    lib.int4_dequant.restype = I32
+    lib.int4_dequant.argtypes = [P, P, P, P, I32, I64, I64, I64, P]
+    lib.w4a16_gemv_workspace_bytes.restype = SZ
+    lib.w4a16_gemv_workspace_bytes.argtypes = [I32, I64, I64, I64]
+    lib.w4a16_gemv.restype = I32
+    lib.w4a16_gemv.argtypes = [P, P, P, P, P, I32, I32, I64, I64, I64, P, SZ, P]
+    lib.w4a16_gemv_variant.restype = I32
+    lib.w4a16_gemv_variant.argtypes = [P, P, P, P, P, I32, I32, I64, I64, I64, I32, I32, P]
+    lib.w4a16_gemv_plan.restype = I32
+    lib.w4a16_gemv_plan.argtypes = [I32, I64, I64, I64] + [ctypes.POINTER(I32)] * 5
+    lib.w4a16_moe_workspace_bytes.restype = SZ
+    lib.w4a16_moe_workspace_bytes.argtypes = [I32, I32, I64, I32]
+    lib.w4a16_moe_gemv.restype = I32
+    lib.w4a16_moe_gemv.argtypes = [P, I32, P, P, P, P, P, P, I32, I32, I32, I64, I64, I64,
+                                   P, SZ, P]
+    lib.w4a16_swiglu.restype = I32
+    lib.w4a16_swiglu.argtypes = [P, P, I64, P, I64, I64, I64, P]
+    lib.w4a16_device_error.restype = I32
+    lib.w4a16_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), I32, P]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().w4a16_status_string(int(status)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise W4A16Error(rc, where)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtypes, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype not in dtypes:
+        raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+_U8 = (torch.uint8,)
+_U32 = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+
+
+def int4_pack(codes: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """codes uint8 [N, K] (0..15) -> packed int32 [N, K/8] (uint32 bit patterns)."""
+    _need(codes, "codes", _U8)
+    N, K = codes.shape
+    if out is None:
+        out = torch.empty((N, K // 8), dtype=torch.int32, device=codes.device)
+    _need(out, "out", _U32, (N, K // 8))
+    _check(load_library().int4_pack(_ptr(codes), _ptr(out), N, K, _stream(stream)), "int4_pack")
+    return out
+
+
+def int4_dequant(wq, scale, zero, g: int, out_dtype=torch.bfloat16, out=None, stream=None):
+    """Packed weights -> W [N, K] = (code - zero) * scale, bf16 or fp32."""
+    _need(wq, "wq", _U32)
+    N, K8 = wq.shape
+    K = K8 * 8
+    _need(scale, "scale", _BF16, (N, K // g))
+    _need(zero, "zero", _U8, (N, K // g))
+    if out is None:
+        out = torch.empty((N, K), dtype=out_dtype, device=wq.device)
+    _need(out, "out", (torch.bfloat16, torch.float32), (N, K))
+    kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(load_library().int4_dequant(_ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
+                                       N, K, g, _stream(stream)), "int4_dequant")
+    return out
+
+
+def w4a16_gemv_workspace_bytes(M: int, N: int, K: int, g: int) -> int:
+    return int(load_library().w4a16_gemv_workspace_bytes(M, N, K, g))
+
+
+def gemv_plan(M: int, N: int, K: int, g: int) -> dict:
+    """The launch w4a16_gemv makes for this shape (kernel id, CTAs, threads,
+    K split, shared memory)."""
+    vals = [ctypes.c_int(0) for _ in range(5)]
+    _check(load_library().w4a16_gemv_plan(M, N, K, g, *[ctypes.byref(v) for v in vals]),
+           "w4a16_gemv_plan")
+    keys = ("kernel_id", "ctas", "threads", "k_split", "smem_bytes")
+    return {k: v.value for k, v in zip(keys, vals)}
+
+
+def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
+               kernel_id: int = 0, k_split: int = 0, stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] . dequant(wq, scale, zero)^T.
+
+    kernel_id 0 (default) lets the library choose; 1 or 2 force the CUDA-core
+    or warp-MMA kernel (measurement only)."""
+    _need(x, "x", _BF16)
+    M, K = x.shape
+    _need(wq, "wq", _U32)
+    N = wq.shape[0]
+    if tuple(wq.shape) != (N, K // 8):
+        raise ValueError("wq shape %s does not match K=%d" % (tuple(wq.shape), K))
+    _need(scale, "scale", _BF16, (N, K // g))
+    _need(zero, "zero", _U8, (N, K // g))
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _need(out, "out", (torch.bfloat16, torch.float32), (M, N))
+    kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    lib = load_library()
+    if kernel_id == 0 and k_split == 0:
+        rc = lib.w4a16_gemv(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
+                            M, N, K, g, None, 0, _stream(stream))
+    else:
+        rc = lib.w4a16_gemv_variant(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out),
+                                    kind, M, N, K, g, kernel_id or (1 if M == 1 else 2),
+                                    k_split, _stream(stream))
+    _check(rc, "w4a16_gemv")
+    return out
+
+
+def w4a16_moe_workspace_bytes(M: int, topk: int, N: int, route: bool) -> int:
+    return int(load_library().w4a16_moe_workspace_bytes(M, topk, N, int(bool(route))))
+
+
+def w4a16_moe_gemv(x, expert_ids, wq, scale, zero, g: int, route_w=None, x_per_slot=False,
+                   out=None, workspace=None, stream=None) -> torch.Tensor:
+    """Expert-indexed GEMV.  wq int32 [E, N, K/8]; scale/zero [E, N, K/g];
+    expert_ids int32 [M, topk]; x [M, K] or (x_per_slot) [M, topk, K].
+    Returns bf16 [M, topk, N] (no route_w) or [M, N] (routed sum)."""
+    _need(expert_ids, "expert_ids", (torch.int32,))
+    M, topk = expert_ids.shape
+    _need(wq, "wq", _U32)
+    E, N, K8 = wq.shape
+    K = K8 * 8
+    _need(x, "x", _BF16, (M, topk, K) if x_per_slot else (M, K))
+    _need(scale, "scale", _BF16, (E, N, K // g))
+    _need(zero, "zero", _U8, (E, N, K // g))
+    lib = load_library()
+    if route_w is not None:
+        _need(route_w, "route_w", (torch.float32,), (M, topk))
+        shape = (M, N)
+        need = w4a16_moe_workspace_bytes(M, topk, N, True)
+        if workspace is None:
+            workspace = torch.empty(need // 4, dtype=torch.float32, device=x.device)
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+        rw = _ptr(route_w)
+    else:
+        shape = (M, topk, N)
+        ws_ptr, ws_bytes, rw = None, 0, None
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", _BF16, shape)
+    _check(lib.w4a16_moe_gemv(_ptr(x), int(bool(x_per_slot)), _ptr(expert_ids), rw, _ptr(wq),
+                              _ptr(scale), _ptr(zero), _ptr(out), M, topk, E, N, K, g,
+                              ws_ptr, ws_bytes, _stream(stream)), "w4a16_moe_gemv")
+    return out
+
+
+def w4a16_swiglu(gate, up, out=None, stream=None) -> torch.Tensor:
+    """h = bf16(silu(gate) * up).  gate/up may be views with a row stride
+    (e.g. the two halves of a stacked [rows, 2N] tensor)."""
+    for t, name in ((gate, "gate"), (up, "up")):
+        if not t.is_cuda or t.dtype not in _BF16 or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("%s must be a CUDA bf16 matrix with unit column stride" % name)
+    if gate.shape != up.shape or gate.stride(0) != up.stride(0):
+        raise ValueError("gate and up must have the same shape and row stride")
+    rows, N = gate.shape
+    if out is None:
+        out = torch.empty((rows, N), dtype=torch.bfloat16, device=gate.device)
+    if out.dim() != 2 or tuple(out.shape) != (rows, N) or out.stride(1) != 1:
+        raise ValueError("out must be [rows, N] with unit column stride")
+    _check(load_library().w4a16_swiglu(_ptr(gate), _ptr(up), gate.stride(0), _ptr(out),
+                                       out.stride(0), rows, N, _stream(stream)), "w4a16_swiglu")
+    return out
+
+
+def w4a16_device_error(clear: bool = True, stream=None) -> int:
+    bits = ctypes.c_uint32(0)
+    _check(load_library().w4a16_device_error(ctypes.byref(bits), int(bool(clear)),
+                                             _stream(stream)), "w4a16_device_error")
+    return int(bits.value)
+
+
+def moe_ffn(x, expert_ids, route_w, gate, up, down, g: int, stream=None) -> torch.Tensor:
+    """Routed SwiGLU FFN for M tokens: gate/up products of every routed slot
+    in one expert-indexed call each, SwiGLU, then the down products with the
+    route-weighted sum.  gate/up/down are (wq, scale, zero) triples with
+    gate/up [E, F, H] and down [E, H, F].  Returns bf16 [M, H]."""
+    M, topk = expert_ids.shape
+    g_out = w4a16_moe_gemv(x, expert_ids, *gate, g, stream=stream)
+    u_out = w4a16_moe_gemv(x, expert_ids, *up, g, stream=stream)
+    F = g_out.shape[-1]
+    h = w4a16_swiglu(g_out.view(M * topk, F), u_out.view(M * topk, F), stream=stream)
+    return w4a16_moe_gemv(h.view(M, topk, F), expert_ids, *down, g, route_w=route_w,
+                          x_per_slot=True, stream=stream)
+
+
+load_library()

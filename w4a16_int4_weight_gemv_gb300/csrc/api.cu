@@ -1,0 +1,278 @@
+// C ABI of the W4A16 library: argument validation, launch planning and
+// dispatch.  Declarations and the contract of each call are in w4a16.h.
+//
+// Every entry point validates all arguments before it enqueues anything, so
+// an invalid call has no effect on the device.  The library allocates no
+// device memory: the only device state it owns is one 32-bit error word per
+// device (a __device__ variable), where kernels record data-dependent
+// problems instead of trapping.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "w4a16.h"
+
+namespace w4a16 {
+namespace {
+
+__device__ uint32_t g_error_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceCache {
+    bool ready = false;
+    DeviceInfo info{};
+    uint32_t* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceCache g_dev[kMaxDevices];
+
+// Properties and the error word's address for the current device (once per device).
+w4a16_status current_device(DeviceCache** out) {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return W4A16_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceCache& c = g_dev[d];
+    if (!c.ready) {
+        int sms = 0, smem = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+            return W4A16_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) !=
+            cudaSuccess)
+            return W4A16_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return W4A16_ERR_CUDA;
+        c.info.sms = sms;
+        c.info.max_smem_optin = smem;
+        c.err = static_cast<uint32_t*>(p);
+        c.ready = true;
+    }
+    *out = &c;
+    return W4A16_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+w4a16_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return W4A16_OK;
+    (void)cudaGetLastError();  // clear a sticky launch-configuration error
+    return W4A16_ERR_CUDA;
+}
+
+// Shape rules shared by the GEMV entry points.
+w4a16_status check_gemv_shape(int M, int64_t N, int64_t K, int64_t g) {
+    if (M < 1 || N < 1 || K < 32 || g < 32) return W4A16_ERR_SHAPE;
+    if (K % 32 != 0 || g % 32 != 0 || K % g != 0) return W4A16_ERR_SHAPE;
+    if (M > 16) return W4A16_ERR_UNSUPPORTED;
+    if (K > 65536) return W4A16_ERR_UNSUPPORTED;
+    if (N > (int64_t(1) << 31) / (K / 8) - 1) return W4A16_ERR_UNSUPPORTED;
+    return W4A16_OK;
+}
+
+w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
+                       GemvPlan* plan, DeviceCache** dev) {
+    w4a16_status st = current_device(dev);
+    if (st != W4A16_OK) return st;
+    if (kernel_id == 0) kernel_id = (M == 1) ? 1 : 2;
+    if (kernel_id == 1 && M != 1) return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id == 2 && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id != 1 && kernel_id != 2) return W4A16_ERR_UNSUPPORTED;
+    if (k_split < 0 || k_split > 8) return W4A16_ERR_UNSUPPORTED;
+    const int n = static_cast<int>(N), k = static_cast<int>(K);
+    *plan = (kernel_id == 1) ? plan_gemv_simt((*dev)->info, n, k, k_split)
+                             : plan_gemv_mma((*dev)->info, M, n, k, k_split);
+    if (plan->smem_bytes > (*dev)->info.max_smem_optin) return W4A16_ERR_UNSUPPORTED;
+    return W4A16_OK;
+}
+
+w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
+                       const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M, int64_t N,
+                       int64_t K, int64_t g, int kernel_id, int k_split, void* stream) {
+    if (!x || !wq || !scale || !zero || !y) return W4A16_ERR_NULL;
+    w4a16_status st = check_gemv_shape(M, N, K, g);
+    if (st != W4A16_OK) return st;
+    if (out_dtype != W4A16_OUT_BF16 && out_dtype != W4A16_OUT_F32) return W4A16_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(wq) || !aligned16(scale) || !aligned16(zero) || !aligned16(y))
+        return W4A16_ERR_ALIGN;
+    if (M >= 2 && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
+    GemvPlan plan{};
+    DeviceCache* dev = nullptr;
+    st = make_plan(M, N, K, g, kernel_id, k_split, &plan, &dev);
+    if (st != W4A16_OK) return st;
+    GemvArgs a{x, wq, scale, zero, y, out_dtype == W4A16_OUT_F32 ? 1 : 0, M,
+               static_cast<int>(N), static_cast<int>(K), static_cast<int>(g), dev->err};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(plan.kernel_id == 1 ? launch_gemv_simt(a, plan, s)
+                                         : launch_gemv_mma(a, plan, s));
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+int w4a16_abi_version(void) { return 1; }
+
+const char* w4a16_status_string(w4a16_status status) {
+    switch (status) {
+        case W4A16_OK: return "ok";
+        case W4A16_ERR_NULL: return "a required pointer is NULL";
+        case W4A16_ERR_SHAPE: return "a size is out of range or inconsistent";
+        case W4A16_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case W4A16_ERR_UNSUPPORTED: return "request outside what is implemented";
+        case W4A16_ERR_WORKSPACE: return "workspace missing or too small";
+        case W4A16_ERR_CUDA: return "the CUDA runtime refused a launch or query";
+    }
+    return "unknown status";
+}
+
+w4a16_status int4_pack(const uint8_t* codes, uint32_t* wq, int64_t N, int64_t K, void* stream) {
+    if (!codes || !wq) return W4A16_ERR_NULL;
+    if (N < 0 || K < 0 || K % 8 != 0) return W4A16_ERR_SHAPE;
+    if (!aligned16(codes) || !aligned16(wq)) return W4A16_ERR_ALIGN;
+    if (N == 0 || K == 0) return W4A16_OK;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    return from_cuda(launch_pack(codes, wq, N, K, dev->info.sms, static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status int4_dequant(const uint32_t* wq, const uint16_t* scale, const uint8_t* zero, void* w,
+                          w4a16_out_dtype out_dtype, int64_t N, int64_t K, int64_t g,
+                          void* stream) {
+    if (!wq || !scale || !zero || !w) return W4A16_ERR_NULL;
+    if (N < 0 || K < 0 || g < 32 || K % 32 != 0 || g % 32 != 0 || K % g != 0)
+        return W4A16_ERR_SHAPE;
+    if (out_dtype != W4A16_OUT_BF16 && out_dtype != W4A16_OUT_F32) return W4A16_ERR_UNSUPPORTED;
+    if (!aligned16(wq) || !aligned16(scale) || !aligned16(zero) || !aligned16(w))
+        return W4A16_ERR_ALIGN;
+    if (N == 0 || K == 0) return W4A16_OK;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    return from_cuda(launch_dequant(wq, scale, zero, w, out_dtype == W4A16_OUT_F32 ? 1 : 0, N, K,
+                                    g, dev->info.sms, static_cast<cudaStream_t>(stream)));
+}
+
+size_t w4a16_gemv_workspace_bytes(int M, int64_t N, int64_t K, int64_t g) {
+    (void)M;
+    (void)N;
+    (void)K;
+    (void)g;
+    return 0;
+}
+
+w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
+                        const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M, int64_t N,
+                        int64_t K, int64_t g, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return gemv_impl(x, wq, scale, zero, y, out_dtype, M, N, K, g, 0, 0, stream);
+}
+
+w4a16_status w4a16_gemv_variant(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
+                                const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,
+                                int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
+                                void* stream) {
+    if (kernel_id != 1 && kernel_id != 2) return W4A16_ERR_UNSUPPORTED;
+    return gemv_impl(x, wq, scale, zero, y, out_dtype, M, N, K, g, kernel_id, k_split, stream);
+}
+
+w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, int* kernel_id, int* ctas,
+                             int* threads, int* k_split, int* smem_bytes) {
+    w4a16_status st = check_gemv_shape(M, N, K, g);
+    if (st != W4A16_OK) return st;
+    if (M >= 2 && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
+    GemvPlan plan{};
+    DeviceCache* dev = nullptr;
+    st = make_plan(M, N, K, g, 0, 0, &plan, &dev);
+    if (st != W4A16_OK) return st;
+    if (kernel_id) *kernel_id = plan.kernel_id;
+    if (ctas) *ctas = plan.ctas;
+    if (threads) *threads = plan.threads;
+    if (k_split) *k_split = plan.k_split;
+    if (smem_bytes) *smem_bytes = plan.smem_bytes;
+    return W4A16_OK;
+}
+
+size_t w4a16_moe_workspace_bytes(int M, int topk, int64_t N, int route) {
+    if (!route || M < 1 || topk < 1 || N < 1) return 0;
+    return static_cast<size_t>(M) * static_cast<size_t>(topk) * static_cast<size_t>(N) *
+           sizeof(float);
+}
+
+w4a16_status w4a16_moe_gemv(const uint16_t* x, int x_per_slot, const int32_t* expert_ids,
+                            const float* route_w, const uint32_t* wq, const uint16_t* scale,
+                            const uint8_t* zero, uint16_t* y, int M, int topk, int E, int64_t N,
+                            int64_t K, int64_t g, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    if (!x || !expert_ids || !wq || !scale || !zero || !y) return W4A16_ERR_NULL;
+    if (M < 1 || topk < 1 || E < 1 || N < 1 || K < 128 || g < 128) return W4A16_ERR_SHAPE;
+    if (K % 32 != 0 || g % 32 != 0 || K % g != 0) return W4A16_ERR_SHAPE;
+    if (g % 128 != 0 || M * topk > 256 || K > 65536) return W4A16_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(E) * N > (int64_t(1) << 31) / (K / 8) - 1)
+        return W4A16_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(expert_ids) || !aligned16(wq) || !aligned16(scale) ||
+        !aligned16(zero) || !aligned16(y) || (route_w && !aligned16(route_w)))
+        return W4A16_ERR_ALIGN;
+    if (route_w) {
+        const size_t need = w4a16_moe_workspace_bytes(M, topk, N, 1);
+        if (!workspace || workspace_bytes < need) return W4A16_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return W4A16_ERR_ALIGN;
+    }
+    // the whole activation set of one expert pass must fit in shared memory
+    const int nblk = static_cast<int>(K / 128);
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    const int need_smem = 16 * (nblk * 256 + 64) + nblk * 16 * 4 + 4096;
+    if (need_smem > dev->info.max_smem_optin) return W4A16_ERR_UNSUPPORTED;
+    MoeArgs a{x, x_per_slot ? 1 : 0, expert_ids, route_w, wq, scale, zero, y,
+              static_cast<float*>(workspace), M, topk, E, static_cast<int>(N), static_cast<int>(K),
+              static_cast<int>(g), dev->err};
+    return from_cuda(launch_moe(a, dev->info, static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_swiglu(const uint16_t* gate, const uint16_t* up, int64_t ld_in, uint16_t* h,
+                          int64_t ld_out, int64_t rows, int64_t N, void* stream) {
+    if (!gate || !up || !h) return W4A16_ERR_NULL;
+    if (rows < 0 || N < 0 || N % 2 != 0 || ld_in < N || ld_out < N || ld_in % 2 != 0 ||
+        ld_out % 2 != 0)
+        return W4A16_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(gate) & 3u) || (reinterpret_cast<uintptr_t>(up) & 3u) ||
+        (reinterpret_cast<uintptr_t>(h) & 3u))
+        return W4A16_ERR_ALIGN;
+    if (rows == 0 || N == 0) return W4A16_OK;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    return from_cuda(launch_swiglu(gate, up, ld_in, h, ld_out, rows, N, dev->info.sms,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_device_error(uint32_t* bits_out, int clear, void* stream) {
+    if (!bits_out) return W4A16_ERR_NULL;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return from_cuda(cudaErrorUnknown);
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, dev->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return from_cuda(cudaErrorUnknown);
+    const uint32_t zero_word = 0;
+    if (clear && cudaMemcpy(dev->err, &zero_word, sizeof zero_word, cudaMemcpyHostToDevice) !=
+                     cudaSuccess)
+        return from_cuda(cudaErrorUnknown);
+    *bits_out = v;
+    return W4A16_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,152 @@
+// Warp-MMA building blocks of the W4A16 kernels with 1 <= M <= 16 tokens
+// (dense GEMV and expert-indexed GEMV).  Internal to the library.
+//
+// Dequantisation in registers.  For a 32-bit word of eight codes, the LOP3
+// (w >> 4i) & 0x000F000F | 0x43004300 yields two bf16 values 128 + code for
+// nibbles i and i + 4 (0x4300 is 128.0 and its 7-bit mantissa holds the code
+// exactly).  The MMA thus accumulates sum_k (128 + code_k) x_k over a block
+// of 128 k; since g % 128 == 0 the block lies in one quantisation group, and
+//     sum_k (code_k - z) s x_k = s * (C - (128 + z) * sum_k x_k),
+// applied once per block with the block's activation sums precomputed.
+//
+// K order.  A thread's 16-byte load holds 32 consecutive k of one row; the
+// MMA fragment wants two values of the same k-pair slots per register.  The
+// k order inside the MMA is free (a dot product does not depend on it), so
+// the activations are staged in shared memory permuted to match: for each
+// 8-value group x[k..k+7] the staged words are (x0,x4), (x1,x5), (x2,x6),
+// (x3,x7) -- exactly the pairs the LOP3 above produces from the weights.
+//
+#pragma once
+
+#include "common.cuh"
+
+namespace w4a16 {
+
+template <int NT>
+struct MmaLayout {
+    static constexpr int kMpad = 8 * NT;
+    int bpc;         // 128-k blocks per CTA slice
+    int tok_stride;  // bytes between tokens in the permuted x (== 64 mod 128)
+    __device__ __host__ static int token_stride(int bpc) { return bpc * 256 + 64; }
+    __device__ __host__ static int bytes(int bpc, int warps, int tpc, int S) {
+        return kMpad * token_stride(bpc)          // permuted x
+               + bpc * kMpad * 4                  // per-block activation sums
+               + warps * 16 * kMpad * 4           // cross-warp partials
+               + (S > 1 ? tpc * 16 * kMpad * 4 : 0);  // split-K partials
+    }
+};
+
+// Stage activation rows for k in [kbeg, kbeg + nb*128) into the permuted
+// layout.  Token n (< Mpad) is row rowsel[n] of x (row stride K, bf16), or row
+// n when rowsel is null; tokens n >= M, or with rowsel[n] < 0, are zero.
+template <int NT>
+__device__ __forceinline__ void stage_x_permuted(const uint16_t* __restrict__ x,
+                                                 const int* rowsel, int M, int K, int kbeg,
+                                                 int nb, unsigned char* xs, float* xsum,
+                                                 int tok_stride) {
+    constexpr int Mpad = 8 * NT;
+    // 16-byte pieces: token n, block b, quad c, step-pair q -> 8 consecutive k
+    const int pieces = Mpad * nb * 16;
+    for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+        const int n = i / (nb * 16);
+        const int rem = i - n * nb * 16;
+        const int b = rem >> 4;
+        const int c = (rem >> 2) & 3;
+        const int q = rem & 3;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        const int row = (n < M) ? (rowsel ? rowsel[n] : n) : -1;
+        if (row >= 0) {
+            const int k = kbeg + b * 128 + c * 32 + q * 8;
+            v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * K + k));
+        }
+        uint4 o;
+        o.x = __byte_perm(v.x, v.z, 0x5410);  // (x0, x4)
+        o.y = __byte_perm(v.x, v.z, 0x7632);  // (x1, x5)
+        o.z = __byte_perm(v.y, v.w, 0x5410);  // (x2, x6)
+        o.w = __byte_perm(v.y, v.w, 0x7632);  // (x3, x7)
+        *reinterpret_cast<uint4*>(xs + n * tok_stride + b * 256 + q * 64 + c * 16) = o;
+    }
+    // activation sums per (block, token), fp32
+    for (int i = threadIdx.x; i < nb * Mpad; i += blockDim.x) {
+        const int b = i / Mpad;
+        const int n = i - b * Mpad;
+        float sum = 0.f;
+        const int row = (n < M) ? (rowsel ? rowsel[n] : n) : -1;
+        if (row >= 0) {
+            const uint16_t* p = x + static_cast<size_t>(row) * K + kbeg + b * 128;
+            for (int j = 0; j < 128; j += 8) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(p + j));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    sum += bf16_to_f32(w[e] & 0xFFFFu) + bf16_to_f32(w[e] >> 16);
+            }
+        }
+        xsum[b * Mpad + n] = sum;
+    }
+}
+
+// One 128-k block of a 16-row tile: accumulate into acc[NT][4].
+//   w0, w1: the thread's 16-byte loads of rows r and r + 8 (r = lane / 4)
+//   sz0, sz1: scale bits | zero << 16 of those rows for this block's group
+//   xb: permuted x of this block for token 0 (token stride tok_stride)
+//   xsb: activation sums of this block, [Mpad]
+template <int NT>
+__device__ __forceinline__ void mma_block(float (&acc)[NT][4], const uint4 w0, const uint4 w1,
+                                          uint32_t sz0, uint32_t sz1,
+                                          const unsigned char* xb, const float* xsb,
+                                          int tok_stride, int lane) {
+    const int c = lane & 3;
+    const int n = lane >> 2;
+    const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
+    const uint32_t r1[4] = {w1.x, w1.y, w1.z, w1.w};
+    uint32_t bq[NT][4][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = *reinterpret_cast<const uint4*>(xb + (t * 8 + n) * tok_stride +
+                                                            q * 64 + c * 16);
+            bq[t][q][0] = v.x;
+            bq[t][q][1] = v.y;
+            bq[t][q][2] = v.z;
+            bq[t][q][3] = v.w;
+        }
+    float cacc[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cacc[t][i] = 0.f;
+#pragma unroll
+    for (int sgm = 0; sgm < 8; ++sgm) {
+        const int j = sgm >> 1;
+        const int h = sgm & 1;
+        const uint32_t a_lo0 = ((r0[j] >> (8 * h)) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t a_hi0 = ((r0[j] >> (8 * h + 4)) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t a_lo1 = ((r1[j] >> (8 * h)) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t a_hi1 = ((r1[j] >> (8 * h + 4)) & 0x000F000Fu) | 0x43004300u;
+        const uint32_t a[4] = {a_lo0, a_lo1, a_hi0, a_hi1};
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            mma_bf16_16816(cacc[t], a, bq[t][j][2 * h], bq[t][j][2 * h + 1], cacc[t]);
+    }
+    const float s0 = __uint_as_float(sz0 << 16);
+    const float s1 = __uint_as_float(sz1 << 16);
+    const float o0 = __uint_as_float(__byte_perm(sz0, 0x4B000000u, 0x7542)) - (8388608.f - 128.f);
+    const float o1 = __uint_as_float(__byte_perm(sz1, 0x4B000000u, 0x7542)) - (8388608.f - 128.f);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const float2 xs2 = *reinterpret_cast<const float2*>(xsb + t * 8 + 2 * c);
+        acc[t][0] = fmaf(s0, fmaf(-o0, xs2.x, cacc[t][0]), acc[t][0]);
+        acc[t][1] = fmaf(s0, fmaf(-o0, xs2.y, cacc[t][1]), acc[t][1]);
+        acc[t][2] = fmaf(s1, fmaf(-o1, xs2.x, cacc[t][2]), acc[t][2]);
+        acc[t][3] = fmaf(s1, fmaf(-o1, xs2.y, cacc[t][3]), acc[t][3]);
+    }
+}
+
+__device__ __forceinline__ void store_out(void* y, int out_f32, size_t idx, float v) {
+    if (out_f32) static_cast<float*>(y)[idx] = v;
+    else static_cast<uint16_t*>(y)[idx] = f32_to_bf16_rn(v);
+}
+
+}  // namespace w4a16
