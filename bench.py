@@ -206,13 +206,15 @@ def time_steps(torch, fn, R, steps, warmup):
     return start.elapsed_time(end) / 1e3 / steps
 
 
-def gpu_gemv_gbs(torch, w, M, N, K, g, zmode, l2, steps, warmup, out_dtype=None, kernel_id=0):
+def gpu_gemv_gbs(torch, w, M, N, K, g, zmode, l2, steps, warmup, out_dtype=None, kernel_id=0,
+                 weights_static=False):
     copies, outs = make_rotation(torch, M, N, K, g, zmode, l2, out_dtype=out_dtype)
     R = len(copies)
 
     def step(i):
         x, wq, s, z = copies[i % R]
-        w.w4a16_gemv(x, wq, s, z, g, out=outs[i % R], kernel_id=kernel_id)
+        w.w4a16_gemv(x, wq, s, z, g, out=outs[i % R], kernel_id=kernel_id,
+                     weights_static=weights_static)
 
     t = time_steps(torch, step, R, steps, warmup)
     del copies, outs
@@ -295,6 +297,36 @@ def cpu_baseline(seconds=10.0):
     return {"value": n * algo_bytes(1, 4096, 4096, 128) / dt / 1e9, "unit": "GB/s", "cores": 1,
             "kind": "oracle",
             "sample": "%d full M=1 4096x4096 GEMVs (fp64 C oracle, one thread) in %.1f s" % (n, dt)}
+
+
+WORKLOADS = {
+    # name: (M, N, K, zero mode, out dtype name)
+    "square": (1, 4096, 4096, "const8", "bf16"),
+    "up": (1, 14336, 4096, "uniform6to10", "bf16"),
+    "down": (1, 4096, 14336, "uniform6to10", "bf16"),
+    "vocab": (1, 163840, 4096, "uniform6to10", "f32"),
+}
+
+
+def run_profile(args):
+    """Plain stream launches of one workload (no graph, no timing): the
+    command ncu captures.  --M overrides the token count."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from w4a16_int4_weight_gemv_gb300 import binding as w
+    M, N, K, zmode, od = WORKLOADS[args.workload]
+    M = args.M or M
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or 126 * 2**20
+    copies, outs = make_rotation(torch, M, N, K, 128, zmode, l2,
+                                 out_dtype=torch.float32 if od == "f32" else torch.bfloat16)
+    R = len(copies)
+    for i in range(args.warmup + args.steps):
+        x, wq, s, z = copies[i % R]
+        w.w4a16_gemv(x, wq, s, z, 128, out=outs[i % R], kernel_id=args.kernel_id)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_workload": args.workload, "M": M, "N": N, "K": K, "copies": R,
+                      "launches": args.warmup + args.steps, "plan": w.gemv_plan(M, N, K, 128)}))
 
 
 def run_gpu(args):
@@ -386,6 +418,15 @@ def run_gpu(args):
         t = gpu_gemv_gbs(torch, w, 1, 4096, 4096, 128, "const8", l2, 2000, 100, kernel_id=2)
         sweep["square_M1_warp_mma_variant"] = {"us": round(t * 1e6, 3),
                                                "GB/s": round(bytes_step / t / 1e9, 1)}
+        t = gpu_gemv_gbs(torch, w, 1, 4096, 4096, 128, "const8", l2, 2000, 100,
+                         weights_static=True)
+        sweep["square_M1_weights_static"] = {"us": round(t * 1e6, 3),
+                                             "GB/s": round(bytes_step / t / 1e9, 1)}
+        for name, (n_, k_) in (("up", (14336, 4096)), ("down", (4096, 14336))):
+            t = gpu_gemv_gbs(torch, w, 2, n_, k_, 128, "uniform6to10", l2, sw_steps, sw_warm,
+                             kernel_id=1)
+            sweep["%s_M2_cuda_core_variant" % name] = {
+                "us": round(t * 1e6, 3), "GB/s": round(algo_bytes(2, n_, k_, 128) / t / 1e9, 1)}
         for m in (1, 2, 4):
             t, byts = moe_chain_time(torch, w, m, 200, 20, l2)
             sweep["moe_chain_M%d" % m] = {"us": round(t * 1e6, 3), "GB/s": round(byts / t / 1e9, 1),
@@ -480,8 +521,15 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="plain launches of --workload for a profiler; prints no bench line")
+    ap.add_argument("--workload", default="square", choices=sorted(WORKLOADS))
+    ap.add_argument("--M", type=int, default=0)
+    ap.add_argument("--kernel-id", type=int, default=0)
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

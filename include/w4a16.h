@@ -70,6 +70,10 @@ typedef enum w4a16_out_dtype {
     W4A16_OUT_F32 = 1   /* outputs stored as fp32 (e.g. vocabulary logits) */
 } w4a16_out_dtype;
 
+/* Flags of w4a16_gemv_ex. */
+#define W4A16_FLAG_WEIGHTS_STATIC 0x1u /* wq, scale and zero are not written by work
+                                          still running on the stream (see w4a16_gemv_ex) */
+
 /* Bits of the per-device error word (see w4a16_device_error). */
 #define W4A16_DEVERR_EXPERT_ID 0x1u /* an expert id was outside [0, E) */
 #define W4A16_DEVERR_TIMEOUT 0x2u   /* a bounded wait for staged data expired */
@@ -116,6 +120,9 @@ W4A16_API size_t w4a16_gemv_workspace_bytes(int M, int64_t N, int64_t K, int64_t
  *   workspace/workspace_bytes: may be NULL/0 (none is needed; see above).
  * Kernel choice (fixed by M, N, K; see w4a16_gemv_plan): M == 1 runs the
  * CUDA-core kernel, 2 <= M <= 16 the warp-MMA kernel.
+ * The kernel is launched with programmatic dependent launch: it may begin
+ * while the previous kernel on `stream` drains, but reads and writes no
+ * global memory until that kernel has completed, so stream order is kept.
  */
 W4A16_API w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
                         const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,
@@ -123,19 +130,34 @@ W4A16_API w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const u
                         void* stream);
 
 /*
+ * w4a16_gemv_ex -- w4a16_gemv with flags.  W4A16_FLAG_WEIGHTS_STATIC lets the
+ * kernel start loading wq/scale/zero before the previous kernel on `stream`
+ * has completed (x is still read, and y written, only after it completes).
+ * Set it only when no kernel that may still be running on the stream writes
+ * those three buffers -- the case of resident model weights in a decode loop.
+ * Otherwise identical to w4a16_gemv (workspace is not needed).
+ */
+W4A16_API w4a16_status w4a16_gemv_ex(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
+                                     const uint8_t* zero, void* y, w4a16_out_dtype out_dtype,
+                                     int M, int64_t N, int64_t K, int64_t g, unsigned flags,
+                                     void* stream);
+
+/*
  * w4a16_gemv_plan -- describe the launch w4a16_gemv would make for a shape,
  * without launching: kernel id (1 = CUDA-core M=1 kernel, 2 = warp-MMA
- * kernel), CTAs, threads per CTA, K-split factor (cluster size) and dynamic
- * shared memory bytes.  Any output pointer may be NULL.  Needs the current
- * device's properties (W4A16_ERR_CUDA without a device).
+ * kernel), CTAs, threads per CTA, K-split factor (how many warps share one
+ * row tile, counting the CTAs of a thread-block cluster) and dynamic shared
+ * memory bytes.  Any output pointer may be NULL.  Needs the current device's
+ * properties (W4A16_ERR_CUDA without a device).
  */
 W4A16_API w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, int* kernel_id, int* ctas,
                              int* threads, int* k_split, int* smem_bytes);
 
 /*
  * w4a16_gemv_variant -- w4a16_gemv with the kernel forced (for measurement):
- * kernel_id 1 (CUDA-core, M == 1 only) or 2 (warp-MMA, any M); k_split 0 =
- * automatic, else the K-split factor (1..8).  Same contract as w4a16_gemv.
+ * kernel_id 1 (CUDA-core, M <= 2) or 2 (warp-MMA, any M); k_split 0 =
+ * automatic, else the K-split factor (a power of two, 1..32; warps of a CTA
+ * first, then up to 8 CTAs of a cluster).  Same contract as w4a16_gemv.
  */
 W4A16_API w4a16_status w4a16_gemv_variant(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
                                 const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,

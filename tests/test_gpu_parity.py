@@ -132,11 +132,20 @@ def test_gemv_matches_oracle(w, oracle, M, N, K, g, zmode, out_dtype):
     check_close(host_f64(y), ref, "M=%d N=%d K=%d g=%d" % (M, N, K, g))
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 64, 4096), (1, 48, 3072), (3, 64, 4096), (12, 40, 2048)])
-@pytest.mark.parametrize("k_split", [2, 3, 4])
-def test_gemv_cluster_split_k(w, oracle, M, N, K, k_split):
+@pytest.mark.parametrize("M,N,K", [(1, 64, 4096), (1, 48, 3072), (1, 40, 14336), (3, 64, 4096),
+                                   (12, 40, 2048), (16, 72, 14336)])
+@pytest.mark.parametrize("k_split", [1, 2, 4, 8, 16, 32])
+def test_gemv_forced_k_split(w, oracle, M, N, K, k_split):
+    # in-CTA (named barrier) and cluster (DSMEM) K splits, including more
+    # parts than the K range has units (some warps or CTAs get no work)
     p = synth.dense_problem(M, N, K, 128, "uniform6to10", seed=31 + k_split)
     ref = oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 128)
+    if M * K * 2 > 200 * 1024 * k_split:
+        # the activation slice of one CTA cannot fit in shared memory
+        with pytest.raises(w.W4A16Error) as ei:
+            w.w4a16_gemv(*dense_dev(p), 128, out_dtype=torch.float32, k_split=k_split)
+        assert ei.value.status == w.Status.ERR_UNSUPPORTED
+        return
     y = w.w4a16_gemv(*dense_dev(p), 128, out_dtype=torch.float32, k_split=k_split)
     torch.cuda.synchronize()
     check_close(host_f64(y), ref, "split %d" % k_split)
@@ -144,10 +153,10 @@ def test_gemv_cluster_split_k(w, oracle, M, N, K, k_split):
 
 @pytest.mark.parametrize("M", [1, 2, 5])
 def test_gemv_kernels_agree_on_m1_and_variants(w, oracle, M):
-    # the warp-MMA kernel also serves M = 1 when forced; both meet the bar
+    # both kernels serve M <= 2 when forced; both meet the bar
     p = synth.dense_problem(M, 96, 2048, 128, "uniform6to10", seed=41)
     ref = oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 128)
-    ids = (1, 2) if M == 1 else (2,)
+    ids = (1, 2) if M <= 2 else (2,)
     for kid in ids:
         y = w.w4a16_gemv(*dense_dev(p), 128, out_dtype=torch.float32, kernel_id=kid)
         torch.cuda.synchronize()
@@ -171,12 +180,62 @@ def test_gemv_one_hot_is_bit_exact(w, oracle, M):
         assert np.array_equal(got[m], oracle.bf16_round(W[:, k0])), (m, k0)
 
 
+@pytest.mark.parametrize("M,N,K,g", [(2, 300, 1024, 128), (2, 77, 3072, 32), (2, 4096, 4096, 128),
+                                     (2, 40, 14336, 128)])
+def test_gemv_cuda_core_two_tokens(w, oracle, M, N, K, g):
+    p = synth.dense_problem(M, N, K, g, "uniform6to10", seed=N + K)
+    ref = oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], g)
+    for k_split in (0, 2, 16):
+        y = w.w4a16_gemv(*dense_dev(p), g, out_dtype=torch.float32, kernel_id=1, k_split=k_split)
+        torch.cuda.synchronize()
+        check_close(host_f64(y), ref, "cuda-core M=2 split %d" % k_split)
+
+
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_gemv_weights_static_flag(w, oracle, M):
+    # the flag only moves weight loads ahead of the grid-dependency wait
+    p = synth.dense_problem(M, 512, 4096, 128, "uniform6to10", seed=55)
+    args = dense_dev(p)
+    a = w.w4a16_gemv(*args, 128, out_dtype=torch.float32)
+    b = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, weights_static=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    check_close(host_f64(b), oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 128), "static")
+
+
+@pytest.mark.parametrize("static", [False, True])
+def test_gemv_chain_keeps_stream_order(w, static):
+    # back-to-back dependent GEMVs (y of one is x of the next) launched with
+    # programmatic dependent launch must equal the same chain with a host
+    # synchronisation between the calls
+    K = 4096
+    layers = [synth.dense_problem(1, K, K, 128, "uniform6to10", seed=60 + i) for i in range(6)]
+    devs = [dense_dev(p) for p in layers]
+    x0 = devs[0][0]
+    outs = [torch.empty((1, K), dtype=torch.bfloat16, device="cuda") for _ in layers]
+    for _ in range(3):
+        cur = x0
+        for (xx, wq, s, z), o in zip(devs, outs):
+            w.w4a16_gemv(cur, wq, s, z, 128, out=o, weights_static=static)
+            cur = o
+    torch.cuda.synchronize()
+    chained = outs[-1].clone()
+    cur = x0
+    for (xx, wq, s, z), o in zip(devs, outs):
+        o.zero_()
+        torch.cuda.synchronize()
+        w.w4a16_gemv(cur, wq, s, z, 128, out=o)
+        torch.cuda.synchronize()
+        cur = o
+    assert torch.equal(chained, outs[-1])
+
+
 def test_gemv_is_deterministic(w):
     p = synth.dense_problem(4, 512, 4096, 128, "uniform6to10", seed=45)
     args = dense_dev(p)
     a = w.w4a16_gemv(*args, 128, out_dtype=torch.float32)
-    b = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, k_split=2)
-    c = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, k_split=2)
+    b = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, k_split=16)
+    c = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, k_split=16)
     d = w.w4a16_gemv(*args, 128, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert torch.equal(a, d) and torch.equal(b, c)

@@ -73,6 +73,8 @@ def load_library():
     lib.w4a16_gemv_workspace_bytes.argtypes = [I32, I64, I64, I64]
     lib.w4a16_gemv.restype = I32
     lib.w4a16_gemv.argtypes = [P, P, P, P, P, I32, I32, I64, I64, I64, P, SZ, P]
+    lib.w4a16_gemv_ex.restype = I32
+    lib.w4a16_gemv_ex.argtypes = [P, P, P, P, P, I32, I32, I64, I64, I64, ctypes.c_uint, P]
     lib.w4a16_gemv_variant.restype = I32
     lib.w4a16_gemv_variant.argtypes = [P, P, P, P, P, I32, I32, I64, I64, I64, I32, I32, P]
     lib.w4a16_gemv_plan.restype = I32
@@ -168,12 +170,18 @@ def gemv_plan(M: int, N: int, K: int, g: int) -> dict:
     return {k: v.value for k, v in zip(keys, vals)}
 
 
+FLAG_WEIGHTS_STATIC = 0x1
+
+
 def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
-               kernel_id: int = 0, k_split: int = 0, stream=None) -> torch.Tensor:
+               kernel_id: int = 0, k_split: int = 0, weights_static: bool = False,
+               stream=None) -> torch.Tensor:
     """y[M, N] = x[M, K] . dequant(wq, scale, zero)^T.
 
     kernel_id 0 (default) lets the library choose; 1 or 2 force the CUDA-core
-    or warp-MMA kernel (measurement only)."""
+    or warp-MMA kernel (measurement only).  weights_static declares that no
+    kernel still running on the stream writes wq/scale/zero (resident
+    weights), so their loads may start before that kernel completes."""
     _need(x, "x", _BF16)
     M, K = x.shape
     _need(wq, "wq", _U32)
@@ -187,7 +195,10 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
     _need(out, "out", (torch.bfloat16, torch.float32), (M, N))
     kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     lib = load_library()
-    if kernel_id == 0 and k_split == 0:
+    if kernel_id == 0 and k_split == 0 and weights_static:
+        rc = lib.w4a16_gemv_ex(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
+                               M, N, K, g, FLAG_WEIGHTS_STATIC, _stream(stream))
+    elif kernel_id == 0 and k_split == 0:
         rc = lib.w4a16_gemv(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
                             M, N, K, g, None, 0, _stream(stream))
     else:

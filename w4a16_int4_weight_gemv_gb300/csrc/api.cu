@@ -44,10 +44,15 @@ w4a16_status current_device(DeviceCache** out) {
         if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) !=
             cudaSuccess)
             return W4A16_ERR_CUDA;
+        int smem_sm = 0;
+        if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d) !=
+            cudaSuccess)
+            return W4A16_ERR_CUDA;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return W4A16_ERR_CUDA;
         c.info.sms = sms;
         c.info.max_smem_optin = smem;
+        c.info.smem_per_sm = smem_sm;
         c.err = static_cast<uint32_t*>(p);
         c.ready = true;
     }
@@ -75,23 +80,26 @@ w4a16_status check_gemv_shape(int M, int64_t N, int64_t K, int64_t g) {
 
 w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
                        GemvPlan* plan, DeviceCache** dev) {
-    w4a16_status st = current_device(dev);
-    if (st != W4A16_OK) return st;
     if (kernel_id == 0) kernel_id = (M == 1) ? 1 : 2;
-    if (kernel_id == 1 && M != 1) return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id == 1 && M > 2) return W4A16_ERR_UNSUPPORTED;
     if (kernel_id == 2 && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
     if (kernel_id != 1 && kernel_id != 2) return W4A16_ERR_UNSUPPORTED;
-    if (k_split < 0 || k_split > 8) return W4A16_ERR_UNSUPPORTED;
+    if (k_split < 0 || k_split > 32 || (k_split & (k_split - 1))) return W4A16_ERR_UNSUPPORTED;
+    w4a16_status st = current_device(dev);
+    if (st != W4A16_OK) return st;
     const int n = static_cast<int>(N), k = static_cast<int>(K);
-    *plan = (kernel_id == 1) ? plan_gemv_simt((*dev)->info, n, k, k_split)
+    *plan = (kernel_id == 1) ? plan_gemv_simt((*dev)->info, M, n, k, k_split)
                              : plan_gemv_mma((*dev)->info, M, n, k, k_split);
-    if (plan->smem_bytes > (*dev)->info.max_smem_optin) return W4A16_ERR_UNSUPPORTED;
+    if (plan->ctas < 1 || plan->smem_bytes > (*dev)->info.max_smem_optin)
+        return W4A16_ERR_UNSUPPORTED;
     return W4A16_OK;
 }
 
 w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
                        const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M, int64_t N,
-                       int64_t K, int64_t g, int kernel_id, int k_split, void* stream) {
+                       int64_t K, int64_t g, int kernel_id, int k_split, unsigned flags,
+                       void* stream) {
+    if (flags & ~static_cast<unsigned>(W4A16_FLAG_WEIGHTS_STATIC)) return W4A16_ERR_UNSUPPORTED;
     if (!x || !wq || !scale || !zero || !y) return W4A16_ERR_NULL;
     w4a16_status st = check_gemv_shape(M, N, K, g);
     if (st != W4A16_OK) return st;
@@ -104,7 +112,8 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
     st = make_plan(M, N, K, g, kernel_id, k_split, &plan, &dev);
     if (st != W4A16_OK) return st;
     GemvArgs a{x, wq, scale, zero, y, out_dtype == W4A16_OUT_F32 ? 1 : 0, M,
-               static_cast<int>(N), static_cast<int>(K), static_cast<int>(g), dev->err};
+               static_cast<int>(N), static_cast<int>(K), static_cast<int>(g), dev->err,
+               (flags & W4A16_FLAG_WEIGHTS_STATIC) ? 1 : 0};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return from_cuda(plan.kernel_id == 1 ? launch_gemv_simt(a, plan, s)
                                          : launch_gemv_mma(a, plan, s));
@@ -174,7 +183,13 @@ w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const uint16_t* s
                         void* stream) {
     (void)workspace;
     (void)workspace_bytes;
-    return gemv_impl(x, wq, scale, zero, y, out_dtype, M, N, K, g, 0, 0, stream);
+    return gemv_impl(x, wq, scale, zero, y, out_dtype, M, N, K, g, 0, 0, 0u, stream);
+}
+
+w4a16_status w4a16_gemv_ex(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
+                           const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,
+                           int64_t N, int64_t K, int64_t g, unsigned flags, void* stream) {
+    return gemv_impl(x, wq, scale, zero, y, out_dtype, M, N, K, g, 0, 0, flags, stream);
 }
 
 w4a16_status w4a16_gemv_variant(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
@@ -182,7 +197,8 @@ w4a16_status w4a16_gemv_variant(const uint16_t* x, const uint32_t* wq, const uin
                                 int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
                                 void* stream) {
     if (kernel_id != 1 && kernel_id != 2) return W4A16_ERR_UNSUPPORTED;
-    return gemv_impl(x, wq, scale, zero, y, out_dtype, M, N, K, g, kernel_id, k_split, stream);
+    return gemv_impl(x, wq, scale, zero, y, out_dtype, M, N, K, g, kernel_id, k_split, 0u,
+                     stream);
 }
 
 w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, int* kernel_id, int* ctas,
@@ -197,7 +213,7 @@ w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, int* kernel
     if (kernel_id) *kernel_id = plan.kernel_id;
     if (ctas) *ctas = plan.ctas;
     if (threads) *threads = plan.threads;
-    if (k_split) *k_split = plan.k_split;
+    if (k_split) *k_split = plan.k_split * plan.wpt;
     if (smem_bytes) *smem_bytes = plan.smem_bytes;
     return W4A16_OK;
 }

@@ -131,6 +131,21 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
           "f"(c[2]), "f"(c[3]));
 }
 
+// Programmatic dependent launch: let the next grid on the stream start its
+// CTAs, and wait until the preceding grid has completed and its memory
+// operations are visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Barrier among `threads` threads (whole warps) of the CTA, id 1..15.
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ void raise_device_error(uint32_t* err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }

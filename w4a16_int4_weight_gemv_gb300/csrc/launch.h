@@ -20,6 +20,7 @@ struct GemvArgs {
     int K;
     int g;
     uint32_t* err;
+    int weights_static;  // wq/scale/zero may be read before the preceding grid completes
 };
 
 struct GemvPlan {
@@ -29,16 +30,60 @@ struct GemvPlan {
     int k_split;     // cluster size along K (1 = no split)
     int smem_bytes;  // dynamic shared memory per CTA
     int units_per_cta;  // 32-chunk spans (kernel 1) or 128-k blocks (kernel 2) per CTA
-    int tiles_per_cluster;
+    int tiles_per_cluster;  // upper bound of tiles one tile group processes
+    int wpt;                // warps sharing one tile (K split inside the CTA)
 };
 
 struct DeviceInfo {
     int sms;
-    int max_smem_optin;
+    int max_smem_optin;  // per CTA
+    int smem_per_sm;     // per SM
 };
 
+// Choose the K split of a GEMV launch: total factor f = wpt * S (wpt warps of
+// a CTA share a tile, S CTAs of a cluster share it), minimising the critical
+// path -- tiles per warp group times K units per warp -- at full residency.
+struct SplitChoice {
+    int wpt, S, ctas, tiles_per_group, units_per_cta, smem_bytes;
+};
+template <class SmemFn>
+SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int warps_per_cta,
+                         int max_ctas_per_sm, int forced_f, SmemFn smem_fn) {
+    SplitChoice best{};
+    long best_cost = -1;
+    for (int f = 1; f <= 32; f *= 2) {
+        if (forced_f > 0 && f != forced_f) continue;
+        if (forced_f == 0 && f > units_all) break;
+        for (int wpt = 1; wpt <= warps_per_cta && wpt <= f; wpt *= 2) {
+            const int S = f / wpt;
+            if (S > 8 || wpt * S != f) continue;
+            const int upc = (units_all + S - 1) / S;
+            const int tg = warps_per_cta / wpt;
+            // residency with tiles_per_group unknown: size with one tile first
+            int smem = smem_fn(upc, tg, wpt, 1, S);
+            if (smem > dev.max_smem_optin) continue;
+            int per_sm = dev.smem_per_sm / (smem + 1024);
+            if (per_sm > max_ctas_per_sm) per_sm = max_ctas_per_sm;
+            if (per_sm < 1) continue;
+            int clusters = (per_sm * dev.sms) / S;
+            const int max_clusters = (ntiles + tg - 1) / tg;
+            if (clusters > max_clusters) clusters = max_clusters;
+            if (clusters < 1) clusters = 1;
+            const int tpg = (ntiles + clusters * tg - 1) / (clusters * tg);
+            smem = smem_fn(upc, tg, wpt, tpg, S);
+            if (smem > dev.max_smem_optin) continue;
+            const long cost = static_cast<long>(tpg) * ((upc + wpt - 1) / wpt);
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                best = SplitChoice{wpt, S, clusters * S, tpg, upc, smem};
+            }
+        }
+    }
+    return best;
+}
+
 // Launch-shape choices (pure host arithmetic, no CUDA calls).
-GemvPlan plan_gemv_simt(const DeviceInfo& dev, int N, int K, int k_split_req);
+GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int k_split_req);
 GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int k_split_req);
 
 cudaError_t launch_gemv_simt(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);

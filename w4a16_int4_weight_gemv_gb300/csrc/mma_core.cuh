@@ -22,31 +22,22 @@
 
 namespace w4a16 {
 
-template <int NT>
-struct MmaLayout {
-    static constexpr int kMpad = 8 * NT;
-    int bpc;         // 128-k blocks per CTA slice
-    int tok_stride;  // bytes between tokens in the permuted x (== 64 mod 128)
-    __device__ __host__ static int token_stride(int bpc) { return bpc * 256 + 64; }
-    __device__ __host__ static int bytes(int bpc, int warps, int tpc, int S) {
-        return kMpad * token_stride(bpc)          // permuted x
-               + bpc * kMpad * 4                  // per-block activation sums
-               + warps * 16 * kMpad * 4           // cross-warp partials
-               + (S > 1 ? tpc * 16 * kMpad * 4 : 0);  // split-K partials
-    }
-};
+// Bytes between tokens in the permuted activation layout for nb 128-k blocks
+// (== 64 mod 128, so the two tokens a quarter-warp reads hit different banks).
+__host__ __device__ inline int mma_token_stride(int nb) { return nb * 256 + 64; }
 
 // Stage activation rows for k in [kbeg, kbeg + nb*128) into the permuted
-// layout.  Token n (< Mpad) is row rowsel[n] of x (row stride K, bf16), or row
-// n when rowsel is null; tokens n >= M, or with rowsel[n] < 0, are zero.
+// layout (m tokens, token stride tok_stride bytes) and their per-block sums
+// xsum[b][Mpad] (tokens >= m get 0).  Token n is row rowsel[n] of x (row
+// stride K, bf16), or row n when rowsel is null; rowsel[n] < 0 means zeros.
 template <int NT>
 __device__ __forceinline__ void stage_x_permuted(const uint16_t* __restrict__ x,
-                                                 const int* rowsel, int M, int K, int kbeg,
+                                                 const int* rowsel, int m, int K, int kbeg,
                                                  int nb, unsigned char* xs, float* xsum,
                                                  int tok_stride) {
     constexpr int Mpad = 8 * NT;
     // 16-byte pieces: token n, block b, quad c, step-pair q -> 8 consecutive k
-    const int pieces = Mpad * nb * 16;
+    const int pieces = m * nb * 16;
     for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
         const int n = i / (nb * 16);
         const int rem = i - n * nb * 16;
@@ -54,7 +45,7 @@ __device__ __forceinline__ void stage_x_permuted(const uint16_t* __restrict__ x,
         const int c = (rem >> 2) & 3;
         const int q = rem & 3;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        const int row = (n < M) ? (rowsel ? rowsel[n] : n) : -1;
+        const int row = rowsel ? rowsel[n] : n;
         if (row >= 0) {
             const int k = kbeg + b * 128 + c * 32 + q * 8;
             v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * K + k));
@@ -71,7 +62,7 @@ __device__ __forceinline__ void stage_x_permuted(const uint16_t* __restrict__ x,
         const int b = i / Mpad;
         const int n = i - b * Mpad;
         float sum = 0.f;
-        const int row = (n < M) ? (rowsel ? rowsel[n] : n) : -1;
+        const int row = (n < m) ? (rowsel ? rowsel[n] : n) : -1;
         if (row >= 0) {
             const uint16_t* p = x + static_cast<size_t>(row) * K + kbeg + b * 128;
             for (int j = 0; j < 128; j += 8) {
@@ -86,54 +77,88 @@ __device__ __forceinline__ void stage_x_permuted(const uint16_t* __restrict__ x,
     }
 }
 
-// One 128-k block of a 16-row tile: accumulate into acc[NT][4].
-//   w0, w1: the thread's 16-byte loads of rows r and r + 8 (r = lane / 4)
-//   sz0, sz1: scale bits | zero << 16 of those rows for this block's group
-//   xb: permuted x of this block for token 0 (token stride tok_stride)
+// Packed codes, scale and zero of one thread for one 128-k block of a 16-row
+// tile: rows r and r + 8 (r = lane / 4), 32 consecutive k each.
+struct MmaBlockLoad {
+    uint4 w0, w1;
+    uint32_t sz0, sz1;  // scale bits | zero << 16
+};
+
+__device__ __forceinline__ void mma_block_issue(MmaBlockLoad& L, const uint4* wq,
+                                                const uint16_t* scale, const uint8_t* zero,
+                                                int N, int Q, int G, int g, int tile, int blk,
+                                                int lane) {
+    const int r = lane >> 2;
+    const int c = lane & 3;
+    const int grp = (blk << 7) / g;
+    const int n0 = tile * 16 + r;
+    const int n1 = n0 + 8;
+    const int chunk = blk * 4 + c;
+    if (n0 < N) {
+        L.w0 = ldg_stream_u4(wq + static_cast<size_t>(n0) * Q + chunk);
+        const size_t gi = static_cast<size_t>(n0) * G + grp;
+        L.sz0 = ldg_nc_u16(scale + gi) | (ldg_nc_u8(zero + gi) << 16);
+    } else {
+        L.w0 = make_uint4(0u, 0u, 0u, 0u);
+        L.sz0 = 0u;
+    }
+    if (n1 < N) {
+        L.w1 = ldg_stream_u4(wq + static_cast<size_t>(n1) * Q + chunk);
+        const size_t gi = static_cast<size_t>(n1) * G + grp;
+        L.sz1 = ldg_nc_u16(scale + gi) | (ldg_nc_u8(zero + gi) << 16);
+    } else {
+        L.w1 = make_uint4(0u, 0u, 0u, 0u);
+        L.sz1 = 0u;
+    }
+}
+
+// One 128-k block of a 16-row tile: accumulate into acc[NT][4] (C-fragment
+// layout: rows r, r + 8; tokens 2c, 2c + 1 of each 8-token tile).
+//   xb: permuted x of this block for token 0; tokens >= m read as zero
 //   xsb: activation sums of this block, [Mpad]
 template <int NT>
-__device__ __forceinline__ void mma_block(float (&acc)[NT][4], const uint4 w0, const uint4 w1,
-                                          uint32_t sz0, uint32_t sz1,
+__device__ __forceinline__ void mma_block(float (&acc)[NT][4], const MmaBlockLoad& L,
                                           const unsigned char* xb, const float* xsb,
-                                          int tok_stride, int lane) {
+                                          int tok_stride, int m, int lane) {
     const int c = lane & 3;
     const int n = lane >> 2;
-    const uint32_t r0[4] = {w0.x, w0.y, w0.z, w0.w};
-    const uint32_t r1[4] = {w1.x, w1.y, w1.z, w1.w};
-    uint32_t bq[NT][4][4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 v = *reinterpret_cast<const uint4*>(xb + (t * 8 + n) * tok_stride +
-                                                            q * 64 + c * 16);
-            bq[t][q][0] = v.x;
-            bq[t][q][1] = v.y;
-            bq[t][q][2] = v.z;
-            bq[t][q][3] = v.w;
-        }
+    const uint32_t r0[4] = {L.w0.x, L.w0.y, L.w0.z, L.w0.w};
+    const uint32_t r1[4] = {L.w1.x, L.w1.y, L.w1.z, L.w1.w};
     float cacc[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int i = 0; i < 4; ++i) cacc[t][i] = 0.f;
 #pragma unroll
-    for (int sgm = 0; sgm < 8; ++sgm) {
-        const int j = sgm >> 1;
-        const int h = sgm & 1;
-        const uint32_t a_lo0 = ((r0[j] >> (8 * h)) & 0x000F000Fu) | 0x43004300u;
-        const uint32_t a_hi0 = ((r0[j] >> (8 * h + 4)) & 0x000F000Fu) | 0x43004300u;
-        const uint32_t a_lo1 = ((r1[j] >> (8 * h)) & 0x000F000Fu) | 0x43004300u;
-        const uint32_t a_hi1 = ((r1[j] >> (8 * h + 4)) & 0x000F000Fu) | 0x43004300u;
-        const uint32_t a[4] = {a_lo0, a_lo1, a_hi0, a_hi1};
+    for (int j = 0; j < 4; ++j) {
+        uint32_t bq[NT][4];
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
-            mma_bf16_16816(cacc[t], a, bq[t][j][2 * h], bq[t][j][2 * h + 1], cacc[t]);
+        for (int t = 0; t < NT; ++t) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (t * 8 + n < m)
+                v = *reinterpret_cast<const uint4*>(xb + (t * 8 + n) * tok_stride + j * 64 +
+                                                    c * 16);
+            bq[t][0] = v.x;
+            bq[t][1] = v.y;
+            bq[t][2] = v.z;
+            bq[t][3] = v.w;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t a_lo0 = ((r0[j] >> (8 * h)) & 0x000F000Fu) | 0x43004300u;
+            const uint32_t a_hi0 = ((r0[j] >> (8 * h + 4)) & 0x000F000Fu) | 0x43004300u;
+            const uint32_t a_lo1 = ((r1[j] >> (8 * h)) & 0x000F000Fu) | 0x43004300u;
+            const uint32_t a_hi1 = ((r1[j] >> (8 * h + 4)) & 0x000F000Fu) | 0x43004300u;
+            const uint32_t a[4] = {a_lo0, a_lo1, a_hi0, a_hi1};
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                mma_bf16_16816(cacc[t], a, bq[t][2 * h], bq[t][2 * h + 1], cacc[t]);
+        }
     }
-    const float s0 = __uint_as_float(sz0 << 16);
-    const float s1 = __uint_as_float(sz1 << 16);
-    const float o0 = __uint_as_float(__byte_perm(sz0, 0x4B000000u, 0x7542)) - (8388608.f - 128.f);
-    const float o1 = __uint_as_float(__byte_perm(sz1, 0x4B000000u, 0x7542)) - (8388608.f - 128.f);
+    const float s0 = __uint_as_float(L.sz0 << 16);
+    const float s1 = __uint_as_float(L.sz1 << 16);
+    const float o0 = __uint_as_float(__byte_perm(L.sz0, 0x4B000000u, 0x7542)) - (8388608.f - 128.f);
+    const float o1 = __uint_as_float(__byte_perm(L.sz1, 0x4B000000u, 0x7542)) - (8388608.f - 128.f);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const float2 xs2 = *reinterpret_cast<const float2*>(xsb + t * 8 + 2 * c);

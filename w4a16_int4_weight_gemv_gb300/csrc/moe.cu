@@ -62,7 +62,7 @@ k_moe_mma(const MoeKernelArgs a) {
     const int nblk = a.K >> 7;
     const int Q = a.K >> 5;
     const int G = a.K / a.g;
-    const int tok_stride = MmaLayout<NT>::token_stride(nblk);
+    const int tok_stride = mma_token_stride(nblk);
     unsigned char* xs = smem_raw;
     float* xsum = reinterpret_cast<float*>(smem_raw + Mpad * tok_stride);
 
@@ -113,39 +113,21 @@ k_moe_mma(const MoeKernelArgs a) {
     const uint8_t* zero = a.zero + static_cast<size_t>(e) * a.N * G;
     const int r = lane >> 2;
     const int c = lane & 3;
-    const int row0 = (blockIdx.x * kWarps + warp) * 16;
-    const int n0 = row0 + r;
+    const int n0 = (blockIdx.x * kWarps + warp) * 16 + r;
     const int n1 = n0 + 8;
 
-    auto issue = [&](int blk, uint4& w0, uint4& w1, uint32_t& z0, uint32_t& z1) {
-        const int grp = (blk << 7) / a.g;
-        const int chunk = blk * 4 + c;
-        if (n0 < a.N) {
-            w0 = ldg_stream_u4(wq + static_cast<size_t>(n0) * Q + chunk);
-            const size_t gi = static_cast<size_t>(n0) * G + grp;
-            z0 = ldg_nc_u16(scale + gi) | (ldg_nc_u8(zero + gi) << 16);
-        } else {
-            w0 = make_uint4(0u, 0u, 0u, 0u);
-            z0 = 0u;
-        }
-        if (n1 < a.N) {
-            w1 = ldg_stream_u4(wq + static_cast<size_t>(n1) * Q + chunk);
-            const size_t gi = static_cast<size_t>(n1) * G + grp;
-            z1 = ldg_nc_u16(scale + gi) | (ldg_nc_u8(zero + gi) << 16);
-        } else {
-            w1 = make_uint4(0u, 0u, 0u, 0u);
-            z1 = 0u;
-        }
+    const int tile = blockIdx.x * kWarps + warp;  // 16-row tile of expert e
+    auto issue = [&](int blk, MmaBlockLoad& L) {
+        mma_block_issue(L, wq, scale, zero, a.N, Q, G, a.g, tile, blk, lane);
     };
 
     // 2. passes of up to Mpad slots routed to expert e (normally one)
     for (int base = 0; base < nslots; base += Mpad) {
         const int m = min(Mpad, nslots - base);
-        uint4 wa[kPD], wb[kPD];
-        uint32_t sa[kPD], sb[kPD];
+        MmaBlockLoad ring[kPD];
 #pragma unroll
         for (int p = 0; p < kPD; ++p)
-            if (p < nblk) issue(p, wa[p], wb[p], sa[p], sb[p]);
+            if (p < nblk) issue(p, ring[p]);
         if (threadIdx.x < Mpad) {
             int rs = -1;
             if (static_cast<int>(threadIdx.x) < m) {
@@ -155,7 +137,7 @@ k_moe_mma(const MoeKernelArgs a) {
             s_rowsel[threadIdx.x] = rs;
         }
         __syncthreads();
-        stage_x_permuted<NT>(a.x, s_rowsel, Mpad, a.K, 0, nblk, xs, xsum, tok_stride);
+        stage_x_permuted<NT>(a.x, s_rowsel, m, a.K, 0, nblk, xs, xsum, tok_stride);
         __syncthreads();
 
         float acc[NT][4];
@@ -168,9 +150,9 @@ k_moe_mma(const MoeKernelArgs a) {
             for (int p = 0; p < kPD; ++p) {
                 const int b = b0 + p;
                 if (b < nblk) {
-                    mma_block<NT>(acc, wa[p], wb[p], sa[p], sb[p], xs + b * 256,
-                                  xsum + b * Mpad, tok_stride, lane);
-                    if (b + kPD < nblk) issue(b + kPD, wa[p], wb[p], sa[p], sb[p]);
+                    mma_block<NT>(acc, ring[p], xs + b * 256, xsum + b * Mpad, tok_stride, m,
+                                  lane);
+                    if (b + kPD < nblk) issue(b + kPD, ring[p]);
                 }
             }
         }
@@ -235,12 +217,12 @@ cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) 
     const dim3 grid(chunks, dmax);
     cudaError_t e;
     if (a.M <= 8) {
-        const int smem = MmaLayout<1>::bytes(nblk, 0, 0, 1);
+        const int smem = 8 * mma_token_stride(nblk) + nblk * 8 * 4;
         e = cudaFuncSetAttribute(k_moe_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         k_moe_mma<1><<<grid, kWarps * 32, smem, s>>>(k);
     } else {
-        const int smem = MmaLayout<2>::bytes(nblk, 0, 0, 1);
+        const int smem = 16 * mma_token_stride(nblk) + nblk * 16 * 4;
         e = cudaFuncSetAttribute(k_moe_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         k_moe_mma<2><<<grid, kWarps * 32, smem, s>>>(k);
