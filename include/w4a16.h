@@ -118,8 +118,10 @@ W4A16_API size_t w4a16_gemv_workspace_bytes(int M, int64_t N, int64_t K, int64_t
  * kernel).  Products are formed exactly and accumulated in fp32; y is stored
  * as bf16 (round to nearest-even) or fp32 per out_dtype.
  *   workspace/workspace_bytes: may be NULL/0 (none is needed; see above).
- * Kernel choice (fixed by M, N, K; see w4a16_gemv_plan): M == 1 runs the
- * CUDA-core kernel, 2 <= M <= 16 the warp-MMA kernel.
+ * Kernel choice (fixed by M, N, K, g; see w4a16_gemv_plan): M == 1 runs the
+ * CUDA-core kernel, 2 <= M <= 16 the warp-MMA kernel, which needs
+ * g % 128 == 0 (M == 2 with finer groups runs the CUDA-core kernel; M > 2 with
+ * finer groups is W4A16_ERR_UNSUPPORTED).
  * The kernel is launched with programmatic dependent launch: it may begin
  * while the previous kernel on `stream` drains, but reads and writes no
  * global memory until that kernel has completed, so stream order is kept.

@@ -79,7 +79,7 @@ def test_gemv_validation_before_any_launch(lib):
     assert _gemv(lib, dtype=7) == Status.ERR_UNSUPPORTED
     assert _gemv(lib, wq=MIS) == Status.ERR_ALIGN
     assert _gemv(lib, y=MIS) == Status.ERR_ALIGN
-    assert _gemv(lib, M=2, K=128, g=64) == Status.ERR_UNSUPPORTED   # warp-MMA needs g % 128 == 0
+    assert _gemv(lib, M=3, K=128, g=64) == Status.ERR_UNSUPPORTED   # warp-MMA needs g % 128 == 0
     var = lib.w4a16_gemv_variant
     assert var(A16, A16, A16, A16, A16, 0, 1, 64, 128, 128, 3, 0, None) == Status.ERR_UNSUPPORTED
     assert var(A16, A16, A16, A16, A16, 0, 3, 64, 128, 128, 1, 0, None) == Status.ERR_UNSUPPORTED

@@ -80,7 +80,9 @@ w4a16_status check_gemv_shape(int M, int64_t N, int64_t K, int64_t g) {
 
 w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
                        GemvPlan* plan, DeviceCache** dev) {
-    if (kernel_id == 0) kernel_id = (M == 1) ? 1 : 2;
+    // default: CUDA-core kernel for one token, and for two when the groups are
+    // finer than the warp-MMA kernel's 128-k blocks; warp MMA otherwise
+    if (kernel_id == 0) kernel_id = (M == 1 || (M == 2 && g % 128 != 0)) ? 1 : 2;
     if (kernel_id == 1 && M > 2) return W4A16_ERR_UNSUPPORTED;
     if (kernel_id == 2 && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
     if (kernel_id != 1 && kernel_id != 2) return W4A16_ERR_UNSUPPORTED;
@@ -106,7 +108,6 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
     if (out_dtype != W4A16_OUT_BF16 && out_dtype != W4A16_OUT_F32) return W4A16_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(wq) || !aligned16(scale) || !aligned16(zero) || !aligned16(y))
         return W4A16_ERR_ALIGN;
-    if (M >= 2 && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
     GemvPlan plan{};
     DeviceCache* dev = nullptr;
     st = make_plan(M, N, K, g, kernel_id, k_split, &plan, &dev);
@@ -205,7 +206,6 @@ w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, int* kernel
                              int* threads, int* k_split, int* smem_bytes) {
     w4a16_status st = check_gemv_shape(M, N, K, g);
     if (st != W4A16_OK) return st;
-    if (M >= 2 && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
     GemvPlan plan{};
     DeviceCache* dev = nullptr;
     st = make_plan(M, N, K, g, 0, 0, &plan, &dev);

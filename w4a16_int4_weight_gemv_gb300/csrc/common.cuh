@@ -76,12 +76,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-// Wait for phase `parity` of `bar` with an iteration limit; false on timeout.
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` nanoseconds for
+// the phase to complete instead of returning at once, so waiting warps do not
+// take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+// Wait for phase `parity` of `bar`, bounded: at most max_iters sleeps of up to
+// 100 microseconds each (about 0.8 s in all); false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t max_iters = (1u << 22)) {
+                                                  uint32_t max_iters = 8192) {
     for (uint32_t i = 0; i < max_iters; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     return false;
+}
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
@@ -92,6 +113,29 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
             "r"(smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Asynchronous copies of 16 or 8 bytes global -> shared (cp.async), and an
+// arrive on `bar` once all of this thread's earlier cp.async copies landed.
+// The arrive does not raise the barrier's expected count, so the barrier's
+// initial count must include every thread that performs it.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 (src 16-byte aligned, bytes a
+// multiple of 16).  A hint: it completes asynchronously and signals nothing.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -26,19 +26,26 @@
 // flush-to-zero); the exact product of a bf16 x and a 4-bit code stays normal
 // unless |code * x| < 2^-62.  Inputs need |x| < 2^40 so x * 2^85 stays finite.
 //
-// Work split.  One persistent CTA of 16 warps per SM.  Warps own tiles of kTR
-// rows and stream their packed words through a ring of kSP spans x kTR rows of
-// 16-byte loads per lane (a span = 32 consecutive chunks = 512 contiguous
-// bytes of a row, one chunk per lane).  When rows are few, the K range of a
-// tile is split over WPT warps of the CTA (partials added in shared memory
-// behind a named barrier, once per tile) and over the CTAs of a thread-block
-// cluster (added through distributed shared memory, once per kernel), always
-// in a fixed order, so results are deterministic.
+// Work split.  One persistent CTA of 16 warps per SM.  Warps own tiles of TR
+// rows (4, or 8 when rows are plentiful); a step of a warp is one span of its
+// tile (32 consecutive chunks = 512 contiguous bytes of each row, one chunk
+// per lane).  Everything a step reads from memory lands in a per-warp ring of
+// shared-memory stages and completes on the stage's mbarrier: the packed words
+// by bulk copies (the TMA engine, one 512-byte copy per row, issued by one
+// lane) and the step's scales and zero points by cp.async pieces from a few
+// lanes.  So the bytes in flight are bounded by shared memory rather than by
+// registers or by the L1's outstanding-request tracking, and the step loop is
+// a small non-unrolled loop that stays in the instruction cache.  When rows
+// are few, the K range of a tile is split over WPT warps of the CTA (partials
+// added in shared memory behind a named barrier, once per tile) and over the
+// CTAs of a thread-block cluster (added through distributed shared memory,
+// once per kernel), always in a fixed order, so results are deterministic.
 //
 // Activations.  The CTA's K slice of x is read once with 16-byte loads,
-// scaled per nibble position into fp32 x' and stored in shared memory with an
-// XOR swizzle (the 8 lanes of a quarter-warp read 8 distinct bank groups);
-// per-chunk sums are reduced with warp shuffles in the same pass.
+// scaled per nibble position into fp32 x' and stored in shared memory
+// lane-major ([span][piece][lane][4 floats]) so that a warp's 16-byte reads of
+// one piece are consecutive (conflict-free) at immediate offsets; per-chunk
+// sums are reduced with warp shuffles in the same pass.
 //
 // Launch.  Kernels are launched with programmatic stream serialisation: the
 // next launch on the stream may start its CTAs as this grid drains, and every
@@ -52,19 +59,20 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kTR = 4;  // rows per warp tile
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kCtasPerSm = 1;  // CTAs of this kernel resident per SM
+constexpr int kMaxStages = 8;
 
-template <int MT>
-struct SimtTraits;
-template <>
-struct SimtTraits<1> {
-    static constexpr int kSP = 4;  // spans of loads in flight per warp
-};
-template <>
-struct SimtTraits<2> {
-    static constexpr int kSP = 3;
+// Shared-memory stage of one warp step for tiles of TR rows: the rows' 512-byte
+// spans of packed words, then their scales (up to 64 bytes a row) and zero
+// points (up to 32 bytes a row).
+template <int TR>
+struct Stage {
+    static constexpr int kWords = 0;
+    static constexpr int kScales = TR * 512;
+    static constexpr int kZeros = TR * 512 + TR * 64;
+    static constexpr int kBytes = TR * 608;
 };
 
 struct SimtKernelArgs {
@@ -81,6 +89,7 @@ struct SimtKernelArgs {
     int ksplit;           // CTAs per cluster (K split across the cluster)
     int spans_per_cta;    // 32-chunk spans in one CTA's K slice
     int tiles_per_group;  // upper bound of tiles any tile group processes
+    int stages;           // shared-memory stages per warp
     int weights_static;   // weights may be read before the preceding grid completes
     uint32_t* err;
 };
@@ -92,14 +101,15 @@ __device__ __forceinline__ float position_factor(int i) {
     return exp2i(85 - p);
 }
 
-// acc += sum over the 16 codes of two words of code * x'
+// acc += sum over the 16 codes of two words of code * x'.  The shift by 8
+// is a high multiply, which issues on the FMA pipe instead of the ALU pipe.
 __device__ __forceinline__ void dot_words(float& a0, float& a1, uint32_t v0, uint32_t v1,
                                           const float* xr) {
     const uint32_t vs[2] = {v0, v1};
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const uint32_t v = vs[j];
-        const uint32_t t = v >> 8;
+        const uint32_t t = __umulhi(v, 0x01000000u);  // v >> 8
         a0 = fmaf(__uint_as_float(v & 0x0000000Fu), xr[8 * j + 0], a0);
         a1 = fmaf(__uint_as_float(v & 0x000000F0u), xr[8 * j + 1], a1);
         a0 = fmaf(__uint_as_float(v & 0x00000F00u), xr[8 * j + 2], a0);
@@ -111,16 +121,53 @@ __device__ __forceinline__ void dot_words(float& a0, float& a1, uint32_t v0, uin
     }
 }
 
+// Same sum with packed fp32 pairs: two products per fma.rn.f32x2.
+__device__ __forceinline__ void ffma2(float2& acc, uint32_t a0, uint32_t a1, float x0, float x1) {
+    asm("{\n\t.reg .b64 ra, rx, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rx, {%4, %5};\n\t"
+        "mov.b64 rc, {%0, %1};\n\t"
+        "fma.rn.f32x2 rc, ra, rx, rc;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y)
+        : "r"(a0), "r"(a1), "f"(x0), "f"(x1));
+}
+__device__ __forceinline__ void dot_words2(float2& a, float2& b, uint32_t v0, uint32_t v1,
+                                           const float* xr) {
+    const uint32_t vs[2] = {v0, v1};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t v = vs[j];
+        const uint32_t t = __umulhi(v, 0x01000000u);  // v >> 8
+        ffma2(a, v & 0x0000000Fu, v & 0x000000F0u, xr[8 * j + 0], xr[8 * j + 1]);
+        ffma2(b, v & 0x00000F00u, v & 0x0000F000u, xr[8 * j + 2], xr[8 * j + 3]);
+        ffma2(a, v & 0x000F0000u, v & 0x00F00000u, xr[8 * j + 4], xr[8 * j + 5]);
+        ffma2(b, t & 0x000F0000u, t & 0x00F00000u, xr[8 * j + 6], xr[8 * j + 7]);
+    }
+}
+
 __device__ __forceinline__ void store_y(void* y, int out_f32, size_t i, float v) {
     v *= exp2i(64);
     if (out_f32) static_cast<float*>(y)[i] = v;
     else static_cast<uint16_t*>(y)[i] = f32_to_bf16_rn(v);
 }
 
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+__host__ __device__ inline int simt_base_bytes(int MT, int TR, int spans, int tg, int wpt,
+                                               int tpg, int S) {
+    const int b = MT * spans * (4096 + 128) + 2 * tg * wpt * TR * MT * 4 +
+                  (S > 1 ? tpg * tg * TR * MT * 4 : 0);
+    return (b + 127) & ~127;
+}
+
+// CPG > 0: g = 32 * CPG with CPG in {1, 2, 4}; the step's scales and zero
+// points are copied into its stage with cp.async (needs K % 1024 == 0 and
+// 16-byte aligned row pieces).  CPG == 0: any g; every lane loads the pair of
+// its own chunk for each row.
+template <int MT, int TR, int CPG>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 k_gemv_simt(const SimtKernelArgs a) {
-    constexpr int kSP = SimtTraits<MT>::kSP;
+    using St = Stage<TR>;
+    constexpr bool kAsyncSZ = CPG > 0;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -137,14 +184,27 @@ k_gemv_simt(const SimtKernelArgs a) {
     const int SP = a.spans_per_cta;
     const int span0 = rank * SP;
     const int nspan = max(0, min(nspan_all, span0 + SP) - span0);
-    const int ntiles = (a.N + kTR - 1) / kTR;
+    const int ntiles = (a.N + TR - 1) / TR;
     const int G = a.K / a.g;
     const int cpg = a.g >> 5;  // chunks per quantisation group
+    const int NS = a.stages;
+    // async scale/zero pieces per row: scales GS * 2 bytes in 16-byte pieces,
+    // zeros GS bytes in 16-byte pieces (one 8-byte piece when GS == 8)
+    constexpr int GS = kAsyncSZ ? 32 / CPG : 1;
+    constexpr int kSPR = kAsyncSZ ? (GS * 2) / 16 : 0;
+    constexpr int kZPR = kAsyncSZ ? (GS >= 16 ? GS / 16 : 1) : 0;
+    constexpr int kPPR = kSPR + kZPR;
+    constexpr int kPieces = TR * kPPR;
+    constexpr int n_arrive = kPieces < 32 ? kPieces : 32;
 
     float* xs = reinterpret_cast<float*>(smem_raw);  // [MT][SP * 1024] swizzled x'
     float* xsum = xs + MT * SP * 1024;              // [MT][SP * 32] chunk sums * 2^-64
-    float* red = xsum + MT * SP * 32;               // [2][TG][WPT][kTR * MT]
-    float* part = red + 2 * TG * WPT * kTR * MT;    // [tpg][TG][kTR * MT] (S > 1)
+    float* red = xsum + MT * SP * 32;               // [2][TG][WPT][TR * MT]
+    float* part = red + 2 * TG * WPT * TR * MT;     // [tpg][TG][TR * MT] (S > 1)
+    const int base = simt_base_bytes(MT, TR, SP, TG, WPT, a.tiles_per_group, S);
+    unsigned char* ring = smem_raw + base + warp * NS * St::kBytes;
+    uint64_t* bars =
+        reinterpret_cast<uint64_t*>(smem_raw + base + kWarps * NS * St::kBytes) + warp * NS;
 
     const int gid = cid * TG + tg;
     const int NG = ncl * TG;
@@ -153,61 +213,80 @@ k_gemv_simt(const SimtKernelArgs a) {
     const int nss = my_tiles * my_spans;  // (tile, span) steps of this warp
 
     grid_dependents_launch();
+    if (lane == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(bars + i, 1 + (kAsyncSZ ? n_arrive : 0));
+        mbar_init_fence();
+    }
+    __syncwarp();
 
-    // load cursor: tile and span (within the slice) of the next step to issue
-    int l_tile = gid, l_span = kp;
-    uint4 ring[kSP][kTR];
-    uint32_t szr[kSP][kTR];  // scale bits | zero << 16
-
-    auto issue = [&](uint4 (&wv)[kTR], uint32_t (&szv)[kTR]) {
-        const int c = ((span0 + l_span) << 5) + lane;  // global chunk
-        const bool cok = c < Q;
-        const int grp = c / cpg;
-        const uint4* wp = a.wq + static_cast<size_t>(l_tile) * kTR * Q + c;
-        const size_t gb = static_cast<size_t>(l_tile) * kTR * G + grp;
-#pragma unroll
-        for (int r = 0; r < kTR; ++r) {
-            const int n = l_tile * kTR + r;
-            if (cok && n < a.N) {
-                wv[r] = ldg_stream_u4(wp + static_cast<size_t>(r) * Q);
-                szv[r] = ldg_nc_u16(a.scale + gb + r * G) | (ldg_nc_u8(a.zero + gb + r * G) << 16);
-            } else {
-                wv[r] = make_uint4(0u, 0u, 0u, 0u);
-                szv[r] = 0u;
-            }
+    // producer cursor: step (w_tile, w_span) goes to stage w_stage
+    int w_tile = gid, w_span = kp, w_stage = 0, w_issued = 0;
+    auto issue = [&]() {
+        uint64_t* bar = bars + w_stage;
+        unsigned char* dst = ring + w_stage * St::kBytes;
+        const int c0 = (span0 + w_span) << 5;
+        const int rows = min(TR, a.N - w_tile * TR);
+        const size_t row0 = static_cast<size_t>(w_tile) * TR;
+        // lane 0 announces the bytes; lanes r < rows copy row r (the copies may
+        // land before the announcement: the phase needs both)
+        const uint32_t row_bytes = static_cast<uint32_t>(min(32, Q - c0)) * 16u;
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, row_bytes * static_cast<uint32_t>(rows));
         }
-        l_span += WPT;
-        if (l_span >= nspan) {
-            l_span = kp;
-            l_tile += NG;
+        if (lane < rows)
+            bulk_copy_g2s(dst + St::kWords + lane * 512, a.wq + (row0 + lane) * Q + c0, row_bytes,
+                          bar);
+        if constexpr (kAsyncSZ) {
+            const int first = c0 / CPG;  // first group of the span
+#pragma unroll
+            for (int pc0 = 0; pc0 < kPieces; pc0 += 32) {
+                const int pc = pc0 + lane;
+                const int r = pc / kPPR;
+                const int j = pc - r * kPPR;
+                if (pc < kPieces && r < rows) {
+                    const size_t gi = (row0 + r) * G + first;
+                    if (j < kSPR)
+                        cp_async_16(dst + St::kScales + r * 64 + j * 16, a.scale + gi + j * 8);
+                    else if (GS >= 16)
+                        cp_async_16(dst + St::kZeros + r * 32 + (j - kSPR) * 16,
+                                    a.zero + gi + (j - kSPR) * 16);
+                    else
+                        cp_async_8(dst + St::kZeros + r * 32, a.zero + gi);
+                }
+            }
+            if (lane < n_arrive) cp_async_arrive_noinc(bar);
+        }
+        if (++w_stage == NS) w_stage = 0;
+        ++w_issued;
+        w_span += WPT;
+        if (w_span >= nspan) {
+            w_span = kp;
+            w_tile += NG;
         }
     };
 
     if (a.weights_static) {
-#pragma unroll
-        for (int j = 0; j < kSP; ++j)
-            if (j < nss) issue(ring[j], szr[j]);
+        while (w_issued < NS && w_issued < nss) issue();
         grid_dependency_wait();
     } else {
         grid_dependency_wait();
-#pragma unroll
-        for (int j = 0; j < kSP; ++j)
-            if (j < nss) issue(ring[j], szr[j]);
+        while (w_issued < NS && w_issued < nss) issue();
     }
 
     // stage x' and the chunk sums of this CTA's K slice (one pass)
     {
         const int kbeg = span0 << 10;
         const int kend = min(a.K, (span0 + nspan) << 10);
-        const int pieces = nspan << 7;  // 8 consecutive k per piece, 4 pieces per chunk
+        const int npieces = nspan << 7;  // 8 consecutive k per piece, 4 pieces per chunk
         for (int m = 0; m < MT; ++m) {
-            for (int base = 0; base < pieces; base += blockDim.x) {
-                const int i = base + threadIdx.x;
+            for (int b0 = 0; b0 < npieces; b0 += blockDim.x) {
+                const int i = b0 + threadIdx.x;
                 const int k0 = i << 3;   // local k
                 const int cl = k0 >> 5;  // local chunk
                 const int q0 = (k0 >> 2) & 7;
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (i < pieces && kbeg + k0 < kend)
+                if (i < npieces && kbeg + k0 < kend)
                     v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * a.K +
                                                              kbeg + k0));
                 const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
@@ -223,12 +302,11 @@ k_gemv_simt(const SimtKernelArgs a) {
                 }
                 sum += __shfl_xor_sync(0xffffffffu, sum, 1);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                if (i < pieces) {
-                    float* base_p = xs + m * SP * 1024 + cl * 32;
-                    *reinterpret_cast<float4*>(base_p + ((q0 ^ (cl & 7)) << 2)) =
-                        make_float4(f[0], f[1], f[2], f[3]);
-                    *reinterpret_cast<float4*>(base_p + (((q0 + 1) ^ (cl & 7)) << 2)) =
-                        make_float4(f[4], f[5], f[6], f[7]);
+                if (i < npieces) {
+                    float4* bp = reinterpret_cast<float4*>(xs + m * SP * 1024) +
+                                 (cl >> 5) * 256 + (cl & 31);
+                    bp[q0 * 32] = make_float4(f[0], f[1], f[2], f[3]);
+                    bp[(q0 + 1) * 32] = make_float4(f[4], f[5], f[6], f[7]);
                     if ((i & 3) == 0) xsum[m * SP * 32 + cl] = sum * exp2i(-64);
                 }
             }
@@ -236,106 +314,159 @@ k_gemv_simt(const SimtKernelArgs a) {
     }
     __syncthreads();
 
-    float acc[kTR][MT];
+    float acc[TR][MT];
 #pragma unroll
-    for (int r = 0; r < kTR; ++r)
+    for (int r = 0; r < TR; ++r)
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
-    int c_tile = gid, c_span = kp, ti = 0;
+    int c_tile = gid, c_span = kp, ti = 0, c_stage = 0;
+    uint32_t c_phase = 0;
+    bool timed_out = false;
 
-    // lane l < kTR * MT owns output (row l / MT, token l % MT) of the tile
-    auto tile_end = [&]() {
-        float mine = 0.f;
+    // Reduce the TR * MT partials of every lane across the warp.  Halving
+    // exchanges first (each lane keeps the half of the values its partner
+    // does not), then a butterfly on the last value: lane l ends with the sum
+    // of value v(l) = its low log2(TR * MT) bits read in reverse order.
+    constexpr int NV = TR * MT;
+    constexpr int LV = NV == 16 ? 4 : (NV == 8 ? 3 : (NV == 4 ? 2 : (NV == 2 ? 1 : 0)));
+    auto warp_reduce_scatter = [&](float (&v)[NV]) -> float {
 #pragma unroll
-        for (int r = 0; r < kTR; ++r)
+        for (int lvl = 0; lvl < LV; ++lvl) {
+            const int half = NV >> (lvl + 1);
+            const bool upper = (lane >> lvl) & 1;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                float s = acc[r][m];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == r * MT + m) mine = s;
-                acc[r][m] = 0.f;
-            }
-        const int orow = lane / MT;
-        const int otok = lane - orow * MT;
-        if (WPT > 1) {
-            float* rb = red + ((ti & 1) * TG + tg) * WPT * kTR * MT;
-            if (lane < kTR * MT) rb[kp * kTR * MT + lane] = mine;
-            named_barrier_sync(1 + tg, WPT * 32);
-            if (kp == 0 && lane < kTR * MT) {
-                mine = 0.f;
-                for (int q = 0; q < WPT; ++q) mine += rb[q * kTR * MT + lane];
+            for (int i = 0; i < half; ++i) {
+                const float send = upper ? v[i] : v[i + half];
+                const float keep = upper ? v[i + half] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << lvl);
             }
         }
-        if (kp == 0 && lane < kTR * MT) {
+        float s = v[0];
+#pragma unroll
+        for (int o = 1 << LV; o < 32; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        return s;
+    };
+    // value index held by this lane after the reduce-scatter
+    int vid = 0;
+#pragma unroll
+    for (int lvl = 0; lvl < LV; ++lvl) vid |= ((lane >> lvl) & 1) << (LV - 1 - lvl);
+
+    // lane l < NV owns output value vid (row vid / MT, token vid % MT)
+    auto tile_end = [&]() {
+        float v[NV];
+#pragma unroll
+        for (int r = 0; r < TR; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                v[r * MT + m] = acc[r][m];
+                acc[r][m] = 0.f;
+            }
+        float mine = warp_reduce_scatter(v);
+        const int orow = vid / MT;
+        const int otok = vid - orow * MT;
+        if (WPT > 1) {
+            float* rb = red + ((ti & 1) * TG + tg) * WPT * NV;
+            if (lane < NV) rb[kp * NV + vid] = mine;
+            named_barrier_sync(1 + tg, WPT * 32);
+            if (kp == 0 && lane < NV) {
+                mine = 0.f;
+                for (int q = 0; q < WPT; ++q) mine += rb[q * NV + vid];
+            }
+        }
+        if (kp == 0 && lane < NV) {
             if (S == 1) {
-                const int n = c_tile * kTR + orow;
+                const int n = c_tile * TR + orow;
                 if (n < a.N) store_y(a.y, a.out_f32, static_cast<size_t>(otok) * a.N + n, mine);
             } else {
-                part[(ti * TG + tg) * kTR * MT + lane] = mine;
+                part[(ti * TG + tg) * NV + vid] = mine;
             }
         }
     };
 
-    for (int ss0 = 0; ss0 < nss; ss0 += kSP) {
+#pragma unroll 1
+    for (int ss = 0; ss < nss; ++ss) {
+        if (!mbar_wait_bounded(bars + c_stage, c_phase)) timed_out = true;
+        const unsigned char* stg = ring + c_stage * St::kBytes;
+        const int cl = (c_span << 5) + lane;  // chunk within the slice
+        const int c = (span0 << 5) + cl;      // global chunk
+        if (c < Q) {
+            uint32_t sz[TR];
+            if constexpr (kAsyncSZ) {
+                const int lg = lane / CPG;  // group within the span
 #pragma unroll
-        for (int j = 0; j < kSP; ++j) {
-            const int ss = ss0 + j;
-            if (ss < nss) {
-                const int cl = (c_span << 5) + lane;  // chunk within the slice
-                if (((span0 << 5) + cl) < Q) {
-                    float d0[kTR][MT], d1[kTR][MT];
+                for (int r = 0; r < TR; ++r)
+                    sz[r] = *reinterpret_cast<const uint16_t*>(stg + St::kScales + r * 64 + lg * 2) |
+                            (static_cast<uint32_t>(stg[St::kZeros + r * 32 + lg]) << 16);
+            } else {
+                const int grp = c / cpg;
 #pragma unroll
-                    for (int r = 0; r < kTR; ++r)
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) d0[r][m] = d1[r][m] = 0.f;
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const float* xb = xs + m * SP * 1024 + cl * 32;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            float xr[16];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float4 t = *reinterpret_cast<const float4*>(
-                                    xb + (((4 * h + q) ^ (cl & 7)) << 2));
-                                xr[4 * q + 0] = t.x;
-                                xr[4 * q + 1] = t.y;
-                                xr[4 * q + 2] = t.z;
-                                xr[4 * q + 3] = t.w;
-                            }
-#pragma unroll
-                            for (int r = 0; r < kTR; ++r) {
-                                const uint4 w = ring[j][r];
-                                if (h == 0) dot_words(d0[r][m], d1[r][m], w.x, w.y, xr);
-                                else dot_words(d0[r][m], d1[r][m], w.z, w.w, xr);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int r = 0; r < kTR; ++r) {
-                        const float sc = __uint_as_float(szr[j][r] << 16);
-                        const float zf =
-                            __uint_as_float(__byte_perm(szr[j][r], 0x4B000000u, 0x7542)) -
-                            8388608.f;
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const float xc = xsum[m * SP * 32 + cl];
-                            acc[r][m] = fmaf(sc, fmaf(-zf, xc, d0[r][m] + d1[r][m]), acc[r][m]);
-                        }
+                for (int r = 0; r < TR; ++r) {
+                    const int n = c_tile * TR + r;
+                    sz[r] = 0u;
+                    if (n < a.N) {
+                        const size_t gi = static_cast<size_t>(n) * G + grp;
+                        sz[r] = ldg_nc_u16(a.scale + gi) | (ldg_nc_u8(a.zero + gi) << 16);
                     }
                 }
-                if (ss + kSP < nss) issue(ring[j], szr[j]);
-                c_span += WPT;
-                if (c_span >= nspan) {
-                    tile_end();
-                    c_span = kp;
-                    c_tile += NG;
-                    ++ti;
+            }
+            uint4 wv[TR];
+#pragma unroll
+            for (int r = 0; r < TR; ++r)
+                wv[r] = *reinterpret_cast<const uint4*>(stg + St::kWords + r * 512 + lane * 16);
+            float d0[TR][MT], d1[TR][MT];
+#pragma unroll
+            for (int r = 0; r < TR; ++r)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) d0[r][m] = d1[r][m] = 0.f;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const float4* xb = reinterpret_cast<const float4*>(xs + m * SP * 1024) +
+                                   c_span * 256 + lane;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float xr[16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 t = xb[(4 * h + q) * 32];
+                        xr[4 * q + 0] = t.x;
+                        xr[4 * q + 1] = t.y;
+                        xr[4 * q + 2] = t.z;
+                        xr[4 * q + 3] = t.w;
+                    }
+#pragma unroll
+                    for (int r = 0; r < TR; ++r) {
+                        if (h == 0) dot_words(d0[r][m], d1[r][m], wv[r].x, wv[r].y, xr);
+                        else dot_words(d0[r][m], d1[r][m], wv[r].z, wv[r].w, xr);
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < TR; ++r) {
+                const float sc = __uint_as_float(sz[r] << 16);
+                const float zf =
+                    __uint_as_float(__byte_perm(sz[r], 0x4B000000u, 0x7542)) - 8388608.f;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float xc = xsum[m * SP * 32 + cl];
+                    acc[r][m] = fmaf(sc, fmaf(-zf, xc, d0[r][m] + d1[r][m]), acc[r][m]);
                 }
             }
         }
+        __syncwarp();  // every lane is done with stage c_stage
+        if (w_issued < nss) issue();
+        if (++c_stage == NS) {
+            c_stage = 0;
+            c_phase ^= 1u;
+        }
+        c_span += WPT;
+        if (c_span >= nspan) {
+            tile_end();
+            c_span = kp;
+            c_tile += NG;
+            ++ti;
+        }
     }
+    if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
     // a warp with no span in the slice still joins its group's reductions
     if (my_spans == 0)
         for (; ti < my_tiles; ++ti) {
@@ -346,42 +477,50 @@ k_gemv_simt(const SimtKernelArgs a) {
     // cluster K split: add the ranks' partials in rank order through DSMEM
     if (S > 1) {
         cluster_barrier();
-        const int per_t = TG * kTR * MT;
+        const int per_t = TG * TR * MT;
         const int tot = a.tiles_per_group * per_t;
         for (int idx = threadIdx.x; idx < tot; idx += blockDim.x) {
             const int t = idx / per_t;
             const int rem = idx - t * per_t;
-            const int g2 = rem / (kTR * MT);
-            const int l = rem - g2 * kTR * MT;
+            const int g2 = rem / (TR * MT);
+            const int l = rem - g2 * TR * MT;
             const int gid2 = cid * TG + g2;
             const int mt = (ntiles > gid2) ? (ntiles - gid2 + NG - 1) / NG : 0;
             if (t >= mt || (t % S) != rank) continue;
             float v = 0.f;
             for (int q = 0; q < S; ++q) v += ld_dsmem_f32(part + idx, static_cast<uint32_t>(q));
             const int orow = l / MT;
-            const int n = (gid2 + t * NG) * kTR + orow;
+            const int n = (gid2 + t * NG) * TR + orow;
             if (n < a.N) store_y(a.y, a.out_f32, static_cast<size_t>(l - orow * MT) * a.N + n, v);
         }
         cluster_barrier();
     }
 }
 
-template <int MT>
-int smem_bytes_simt(int spans, int tg, int wpt, int tpg, int S) {
-    return MT * spans * (4096 + 128) + 2 * tg * wpt * kTR * MT * 4 +
-           (S > 1 ? tpg * tg * kTR * MT * 4 : 0);
+// rows per warp tile: 8 when there are rows enough to keep every warp busy
+int tile_rows_for(const DeviceInfo& dev, int N) { return (N / 8 >= dev.sms * kWarps) ? 8 : 4; }
+
+bool async_sz_ok(int K, int g) {
+    const int G = K / g;
+    if (K % 1024 != 0) return false;
+    if (g == 128) return G % 8 == 0;
+    if (g == 64 || g == 32) return G % 16 == 0;
+    return false;
 }
 
 }  // namespace
 
 GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int k_split_req) {
     const int nspan_all = (K / 32 + 31) / 32;
-    const int ntiles = (N + kTR - 1) / kTR;
-    const SplitChoice c = choose_split(dev, ntiles, nspan_all, kWarps, 1, k_split_req,
-                                       [M](int upc, int tg, int wpt, int tpg, int S) {
-                                           return M == 1 ? smem_bytes_simt<1>(upc, tg, wpt, tpg, S)
-                                                         : smem_bytes_simt<2>(upc, tg, wpt, tpg, S);
-                                       });
+    const int TR = tile_rows_for(dev, N);
+    const int ntiles = (N + TR - 1) / TR;
+    const int stage = TR * 608;
+    // feasibility and residency with the minimum two stages per warp
+    const SplitChoice c = choose_split(
+        dev, ntiles, nspan_all, kWarps, kCtasPerSm, k_split_req,
+        [M, TR, stage](int upc, int tg, int wpt, int tpg, int S) {
+            return simt_base_bytes(M, TR, upc, tg, wpt, tpg, S) + kWarps * 2 * (stage + 8);
+        });
     GemvPlan p{};
     p.kernel_id = 1;
     p.k_split = c.S;
@@ -390,7 +529,21 @@ GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int k_split_
     p.threads = kThreads;
     p.ctas = c.ctas;
     p.tiles_per_cluster = c.tiles_per_group;
-    p.smem_bytes = c.smem_bytes;
+    p.tile_rows = TR;
+    if (c.ctas > 0) {
+        const int base = simt_base_bytes(M, TR, c.units_per_cta, kWarps / c.wpt, c.wpt,
+                                         c.tiles_per_group, c.S);
+        // a warp runs at most tiles_per_group * ceil(units / wpt) steps; more
+        // stages than that only occupy shared memory the next launch could use
+        const int max_steps = c.tiles_per_group * ((c.units_per_cta + c.wpt - 1) / c.wpt);
+        int budget = dev.smem_per_sm / kCtasPerSm - 1024;
+        if (budget > dev.max_smem_optin) budget = dev.max_smem_optin;
+        int ns = (budget - base) / (kWarps * (stage + 8));
+        if (ns > kMaxStages) ns = kMaxStages;
+        if (ns > max_steps) ns = max_steps < 2 ? 2 : max_steps;
+        p.stages = ns;
+        p.smem_bytes = base + kWarps * ns * (stage + 8);
+    }
     return p;
 }
 
@@ -409,9 +562,22 @@ cudaError_t launch_gemv_simt(const GemvArgs& a, const GemvPlan& p, cudaStream_t 
     k.ksplit = p.k_split;
     k.spans_per_cta = p.units_per_cta;
     k.tiles_per_group = p.tiles_per_cluster;
+    k.stages = p.stages;
     k.weights_static = a.weights_static;
     k.err = a.err;
-    auto kern = (a.M == 1) ? k_gemv_simt<1> : k_gemv_simt<2>;
+    const int cpg = async_sz_ok(a.K, a.g) ? a.g / 32 : 0;
+    void (*kern)(SimtKernelArgs) = nullptr;
+#define W4A16_SIMT_PICK(MT_, TR_)                                                   \
+    kern = cpg == 1   ? k_gemv_simt<MT_, TR_, 1>                                   \
+           : cpg == 2 ? k_gemv_simt<MT_, TR_, 2>                                   \
+           : cpg == 4 ? k_gemv_simt<MT_, TR_, 4>                                   \
+                      : k_gemv_simt<MT_, TR_, 0>;
+    if (a.M == 1) {
+        if (p.tile_rows == 8) { W4A16_SIMT_PICK(1, 8) } else { W4A16_SIMT_PICK(1, 4) }
+    } else {
+        if (p.tile_rows == 8) { W4A16_SIMT_PICK(2, 8) } else { W4A16_SIMT_PICK(2, 4) }
+    }
+#undef W4A16_SIMT_PICK
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          p.smem_bytes);
     if (e != cudaSuccess) return e;

@@ -32,6 +32,8 @@ struct GemvPlan {
     int units_per_cta;  // 32-chunk spans (kernel 1) or 128-k blocks (kernel 2) per CTA
     int tiles_per_cluster;  // upper bound of tiles one tile group processes
     int wpt;                // warps sharing one tile (K split inside the CTA)
+    int stages;             // shared-memory stages per warp (CUDA-core kernel)
+    int tile_rows;          // rows per warp tile (CUDA-core kernel)
 };
 
 struct DeviceInfo {
