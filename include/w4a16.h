@@ -194,6 +194,34 @@ W4A16_API w4a16_status w4a16_moe_gemv(const uint16_t* x, int x_per_slot, const i
                             int64_t K, int64_t g, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* Size of the library's fixed scratch buffer (per device), in bytes. */
+#define W4A16_FIXED_SCRATCH_BYTES (1u << 20)
+
+/*
+ * w4a16_moe_gemv_fixed_scratch -- w4a16_moe_gemv for callers that cannot
+ * allocate device memory or lend a workspace: code that runs while a CUDA
+ * graph is being captured, engines whose device memory is split into fixed
+ * pools, plug-ins whose host runtime owns the allocator.  (The README has no
+ * counterpart; this is an integration convenience of this library.)
+ * Same arguments and results as w4a16_moe_gemv, minus the workspace: the
+ * fp32 partials of the routed sum go to a buffer of
+ * W4A16_FIXED_SCRATCH_BYTES compiled into the library, one per device, held
+ * until the process exits.  Nothing is allocated by the call.
+ *   - Requests needing more than W4A16_FIXED_SCRATCH_BYTES
+ *     (M * topk * N * 4 bytes with route_w) return W4A16_ERR_WORKSPACE.
+ *   - The first call on a device looks the buffer up (cudaGetSymbolAddress);
+ *     make that first call before any stream capture.
+ *   - All calls on a device share the buffer: calls whose kernels can overlap
+ *     on the GPU race on it; calls ordered on one stream are safe.  Nothing
+ *     left in it by an earlier call is read.
+ */
+W4A16_API w4a16_status w4a16_moe_gemv_fixed_scratch(const uint16_t* x, int x_per_slot,
+                                                    const int32_t* expert_ids, const float* route_w,
+                                                    const uint32_t* wq, const uint16_t* scale,
+                                                    const uint8_t* zero, uint16_t* y, int M,
+                                                    int topk, int E, int64_t N, int64_t K,
+                                                    int64_t g, void* stream);
+
 /*
  * w4a16_swiglu -- h[r][n] = bf16(silu(gate[r][n]) * up[r][n]), computed in
  * fp32, silu(v) = v / (1 + e^-v).  The activation between the gate/up and
