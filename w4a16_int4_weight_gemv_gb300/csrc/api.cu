@@ -90,8 +90,9 @@ w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, in
     w4a16_status st = current_device(dev);
     if (st != W4A16_OK) return st;
     const int n = static_cast<int>(N), k = static_cast<int>(K);
-    *plan = (kernel_id == 1) ? plan_gemv_simt((*dev)->info, M, n, k, k_split)
-                             : plan_gemv_mma((*dev)->info, M, n, k, k_split);
+    const int gg = static_cast<int>(g);
+    *plan = (kernel_id == 1) ? plan_gemv_simt((*dev)->info, M, n, k, gg, k_split)
+                             : plan_gemv_mma((*dev)->info, M, n, k, gg, k_split);
     if (plan->ctas < 1 || plan->smem_bytes > (*dev)->info.max_smem_optin)
         return W4A16_ERR_UNSUPPORTED;
     return W4A16_OK;
@@ -121,6 +122,49 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
 }
 
 }  // namespace
+
+int max_active_clusters(const void* kernel, int threads, int smem, int S) {
+    struct Entry {
+        const void* kernel;
+        int device, threads, smem, S, value;
+    };
+    static std::mutex mu;
+    static Entry cache[256];
+    static int used = 0;
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+        const Entry& e = cache[i];
+        if (e.kernel == kernel && e.device == d && e.threads == threads && e.smem == smem &&
+            e.S == S)
+            return e.value;
+    }
+    int n = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(S * 64);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    if (used < 256) cache[used++] = Entry{kernel, d, threads, smem, S, n};
+    return n;
+}
+
 }  // namespace w4a16
 
 using namespace w4a16;

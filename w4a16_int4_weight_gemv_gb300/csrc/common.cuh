@@ -115,7 +115,7 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
-// Asynchronous copies of 16 or 8 bytes global -> shared (cp.async), and an
+// Asynchronous copies of 16, 8 or 4 bytes global -> shared (cp.async), and an
 // arrive on `bar` once all of this thread's earlier cp.async copies landed.
 // The arrive does not raise the barrier's expected count, so the barrier's
 // initial count must include every thread that performs it.
@@ -125,6 +125,10 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_8(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {

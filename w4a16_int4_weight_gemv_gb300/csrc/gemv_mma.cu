@@ -6,18 +6,20 @@
 // long before HBM is saturated, so the multiply-accumulate moves to
 // mma.sync.m16n8k16 (bf16 in, fp32 accumulate): weights are the 16-row A
 // operand, the M tokens (padded to 8 or 16) the B operand.  The dense tile is
-// tiny (n = 8 or 16), so warp MMA fed from registers is the right tool; the
-// weights never touch shared memory.  (Dequantisation and the K permutation
-// are described in mma_core.cuh.)
+// tiny (n = 8 or 16), so warp MMA fed from registers is the right tool.
+// (Dequantisation and the K permutation are described in mma_core.cuh.)
 //
-// Memory-level parallelism.  Each warp owns 16-row tiles and keeps kPD
-// 128-k blocks of 16-byte loads in flight ahead of the MMAs.  Warps work
-// independently; when there are too few tiles to occupy the GPU the K range
-// of a tile is split over WPT warps of a CTA (partials added in shared memory
-// behind a named barrier, once per tile) and over the CTAs of a thread-block
-// cluster (added through distributed shared memory, once per kernel), always
-// in a fixed order.  Launches use programmatic dependent launch, as the
-// CUDA-core kernel does (see gemv_simt.cu).
+// Memory path (as in the CUDA-core kernel, gemv_simt.cu): each warp owns
+// 16-row tiles; a step is 512 k of the tile (kSB 128-k blocks).  The step's
+// packed words reach a per-warp ring of shared-memory stages by bulk copies
+// (one 256-byte copy per row, into rows padded to kRowPitch so the A-fragment
+// reads are free of bank conflicts), its scales and zero points by cp.async,
+// all completing on the stage's mbarrier.  Warps work independently; when
+// there are too few tiles to occupy the GPU the K range of a tile is split
+// over WPT warps of a CTA (partials added in shared memory behind a named
+// barrier, once per tile) and over the CTAs of a thread-block cluster (added
+// through distributed shared memory, once per kernel), always in a fixed
+// order.  Launches use programmatic dependent launch.
 #include "common.cuh"
 #include "launch.h"
 #include "mma_core.cuh"
@@ -25,17 +27,20 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kSB = 4;          // 128-k blocks per step (512 k)
+constexpr int kRowPitch = 320;  // 256 bytes of a row's step + 64: the two rows a
+                                // quarter-warp reads fall in different bank halves
+constexpr int kMaxStages = 8;
 
-template <int NT>
-struct MmaTraits;
-template <>
-struct MmaTraits<1> {
-    static constexpr int kPD = 8;
-};
-template <>
-struct MmaTraits<2> {
-    static constexpr int kPD = 4;
+// Shared-memory stage of one warp step: 16 rows x kSB blocks of packed words,
+// then (fast path) the rows' kSB scales and zero points.
+struct MmaStage {
+    static constexpr int kA = 0;
+    static constexpr int kScales = 16 * kRowPitch;           // 16 rows x kSB bf16
+    static constexpr int kZeros = kScales + 16 * kSB * 2;    // 16 rows x kSB u8
+    static constexpr int kBytes = kZeros + 16 * kSB;         // 5312
 };
 
 struct MmaKernelArgs {
@@ -51,32 +56,35 @@ struct MmaKernelArgs {
     int g;
     int wpt;
     int ksplit;
-    int blocks_per_cta;
+    int steps_per_cta;  // 512-k steps in one CTA's K slice
     int tiles_per_group;
+    int stages;
     int weights_static;
     uint32_t* err;
 };
 
-template <int NT>
-int smem_bytes_mma(int M, int bpc, int tg, int wpt, int tpg, int S) {
-    constexpr int Mpad = 8 * NT;
-    return M * mma_token_stride(bpc)                   // permuted activations
-           + bpc * Mpad * 4                           // per-block activation sums
-           + (wpt > 1 ? 2 * tg * wpt * 16 * Mpad * 4 : 0)  // in-CTA K-split partials
-           + (S > 1 ? tpg * tg * 16 * Mpad * 4 : 0);   // cluster K-split partials
+__host__ __device__ inline int mma_base_bytes(int M, int NT, int upc, int tg, int wpt, int tpg,
+                                              int S) {
+    const int Mpad = 8 * NT;
+    const int bpc = upc * kSB;
+    const int b = M * mma_token_stride(bpc) + bpc * Mpad * 4 +
+                  (wpt > 1 ? 2 * tg * wpt * 16 * Mpad * 4 : 0) +
+                  (S > 1 ? tpg * tg * 16 * Mpad * 4 : 0);
+    return (b + 127) & ~127;
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 4)
+// kFast: g == 128 and K % 512 == 0 -- a step's scales and zero points are
+// whole 8- and 4-byte pieces per row, copied with cp.async into the stage.
+// Otherwise the consumer loads the two rows' pair for each block itself.
+template <int NT, bool kFast>
+__global__ void __launch_bounds__(kThreads, 1)
 k_gemv_mma(const MmaKernelArgs a) {
     constexpr int Mpad = 8 * NT;
-    constexpr int kPD = MmaTraits<NT>::kPD;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int W = blockDim.x >> 5;
     const int WPT = a.wpt;
-    const int TG = W / WPT;
+    const int TG = kWarps / WPT;
     const int tg = warp / WPT;
     const int kp = warp - tg * WPT;
     const int Q = a.K >> 5;
@@ -85,44 +93,81 @@ k_gemv_mma(const MmaKernelArgs a) {
     const int rank = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
     const int cid = blockIdx.x / S;
     const int ncl = gridDim.x / S;
-    const int BPC = a.blocks_per_cta;
+    const int BPC = a.steps_per_cta * kSB;          // blocks per CTA slice
     const int b0 = rank * BPC;
     const int nb = max(0, min(nblk_all, b0 + BPC) - b0);
+    const int nsteps_slice = (nb + kSB - 1) / kSB;
     const int ntiles = (a.N + 15) >> 4;
     const int G = a.K / a.g;
     const int tok_stride = mma_token_stride(BPC);
+    const int NS = a.stages;
+    const int r = lane >> 2;
+    const int c = lane & 3;
 
     unsigned char* xs = smem_raw;
     float* xsum = reinterpret_cast<float*>(smem_raw + a.M * tok_stride);
-    float* red = xsum + BPC * Mpad;                               // [2][TG][WPT][16][Mpad]
-    float* part = red + (WPT > 1 ? 2 * TG * WPT * 16 * Mpad : 0);  // [tpg][TG][16][Mpad]
+    float* red = xsum + BPC * Mpad;                                 // [2][TG][WPT][16][Mpad]
+    float* part = red + (WPT > 1 ? 2 * TG * WPT * 16 * Mpad : 0);    // [tpg][TG][16][Mpad]
+    const int base = mma_base_bytes(a.M, NT, a.steps_per_cta, TG, WPT, a.tiles_per_group, S);
+    unsigned char* ring = smem_raw + base + warp * NS * MmaStage::kBytes;
+    uint64_t* bars =
+        reinterpret_cast<uint64_t*>(smem_raw + base + kWarps * NS * MmaStage::kBytes) + warp * NS;
 
     const int gid = cid * TG + tg;
     const int NG = ncl * TG;
     const int my_tiles = (ntiles > gid) ? (ntiles - gid + NG - 1) / NG : 0;
-    const int my_blocks = (nb > kp) ? (nb - kp + WPT - 1) / WPT : 0;
-    const int nsteps = my_tiles * my_blocks;
-    const int r = lane >> 2;
-    const int c = lane & 3;
+    const int my_steps = (nsteps_slice > kp) ? (nsteps_slice - kp + WPT - 1) / WPT : 0;
+    const int nss = my_tiles * my_steps;
 
-    MmaBlockLoad ring[kPD];
-    auto issue = [&](int s, MmaBlockLoad& L) {
-        const int ti = s / my_blocks;
-        const int bi = s - ti * my_blocks;
-        mma_block_issue(L, a.wq, a.scale, a.zero, a.N, Q, G, a.g, gid + ti * NG,
-                        b0 + kp + bi * WPT, lane);
-    };
     grid_dependents_launch();
+    if (lane == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(bars + i, 1 + (kFast ? 32 : 0));
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    // producer cursor
+    int w_tile = gid, w_step = kp, w_stage = 0, w_issued = 0;
+    auto issue = [&]() {
+        uint64_t* bar = bars + w_stage;
+        unsigned char* dst = ring + w_stage * MmaStage::kBytes;
+        const int blk0 = b0 + w_step * kSB;                 // first global block of the step
+        const int nbs = min(kSB, b0 + nb - blk0);           // blocks in this step
+        const int rows = min(16, a.N - w_tile * 16);
+        const size_t row0 = static_cast<size_t>(w_tile) * 16;
+        const uint32_t row_bytes = static_cast<uint32_t>(nbs) * 64u;
+        if (lane == 0) {
+            if (w_issued >= NS) fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, row_bytes * static_cast<uint32_t>(rows));
+        }
+        if (lane < rows)
+            bulk_copy_g2s(dst + MmaStage::kA + lane * kRowPitch,
+                          a.wq + (row0 + lane) * Q + blk0 * 4, row_bytes, bar);
+        if constexpr (kFast) {
+            // lanes 0..15 copy row lane's 4 zero points, lanes 16..31 its 4 scales
+            const int rr = lane & 15;
+            if (rr < rows) {
+                const size_t gi = (row0 + rr) * G + blk0;  // g == 128: block == group
+                if (lane < 16) cp_async_4(dst + MmaStage::kZeros + rr * kSB, a.zero + gi);
+                else cp_async_8(dst + MmaStage::kScales + rr * kSB * 2, a.scale + gi);
+            }
+            cp_async_arrive_noinc(bar);
+        }
+        if (++w_stage == NS) w_stage = 0;
+        ++w_issued;
+        w_step += WPT;
+        if (w_step >= nsteps_slice) {
+            w_step = kp;
+            w_tile += NG;
+        }
+    };
+
     if (a.weights_static) {
-#pragma unroll
-        for (int p = 0; p < kPD; ++p)
-            if (p < nsteps) issue(p, ring[p]);
+        while (w_issued < NS && w_issued < nss) issue();
         grid_dependency_wait();
     } else {
         grid_dependency_wait();
-#pragma unroll
-        for (int p = 0; p < kPD; ++p)
-            if (p < nsteps) issue(p, ring[p]);
+        while (w_issued < NS && w_issued < nss) issue();
     }
 
     stage_x_permuted<NT>(a.x, nullptr, a.M, a.K, b0 << 7, nb, xs, xsum, tok_stride);
@@ -133,11 +178,12 @@ k_gemv_mma(const MmaKernelArgs a) {
     for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
-    int ti = 0, bi = 0;
+    int c_tile = gid, c_step = kp, ti = 0, c_stage = 0;
+    uint32_t c_phase = 0;
+    bool timed_out = false;
 
     // fragment position i of n-tile t: row r (+8 for i >= 2), token t*8 + 2c + (i & 1)
     auto tile_end = [&]() {
-        const int tile = gid + ti * NG;
         if (WPT > 1) {
             float* rb = red + ((ti & 1) * TG + tg) * WPT * 16 * Mpad;
 #pragma unroll
@@ -169,7 +215,7 @@ k_gemv_mma(const MmaKernelArgs a) {
                     const int tok = t * 8 + 2 * c + (i & 1);
                     if (tok >= a.M) continue;
                     if (S == 1) {
-                        const int n = tile * 16 + row;
+                        const int n = c_tile * 16 + row;
                         if (n < a.N)
                             store_out(a.y, a.out_f32, static_cast<size_t>(tok) * a.N + n, acc[t][i]);
                     } else {
@@ -183,24 +229,62 @@ k_gemv_mma(const MmaKernelArgs a) {
             for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
     };
 
-    for (int s0 = 0; s0 < nsteps; s0 += kPD) {
+#pragma unroll 1
+    for (int ss = 0; ss < nss; ++ss) {
+        if (!mbar_wait_bounded(bars + c_stage, c_phase)) timed_out = true;
+        const unsigned char* stg = ring + c_stage * MmaStage::kBytes;
+        const int lb0 = c_step * kSB;  // first block of the step within the slice
+        const int nbs = min(kSB, nb - lb0);
+        const int n0 = c_tile * 16 + r;
 #pragma unroll
-        for (int p = 0; p < kPD; ++p) {
-            const int s = s0 + p;
-            if (s < nsteps) {
-                const int lb = kp + bi * WPT;  // block within the slice
-                mma_block<NT>(acc, ring[p], xs + lb * 256, xsum + lb * Mpad, tok_stride, a.M,
-                              lane);
-                if (s + kPD < nsteps) issue(s + kPD, ring[p]);
-                if (++bi == my_blocks) {
-                    bi = 0;
-                    tile_end();
-                    ++ti;
+        for (int bb = 0; bb < kSB; ++bb) {
+            if (bb < nbs) {
+                MmaBlockLoad L;
+                L.w0 = *reinterpret_cast<const uint4*>(stg + MmaStage::kA + r * kRowPitch +
+                                                       bb * 64 + c * 16);
+                L.w1 = *reinterpret_cast<const uint4*>(stg + MmaStage::kA + (r + 8) * kRowPitch +
+                                                       bb * 64 + c * 16);
+                if constexpr (kFast) {
+                    L.sz0 = *reinterpret_cast<const uint16_t*>(stg + MmaStage::kScales +
+                                                               r * kSB * 2 + bb * 2) |
+                            (static_cast<uint32_t>(stg[MmaStage::kZeros + r * kSB + bb]) << 16);
+                    L.sz1 = *reinterpret_cast<const uint16_t*>(stg + MmaStage::kScales +
+                                                               (r + 8) * kSB * 2 + bb * 2) |
+                            (static_cast<uint32_t>(stg[MmaStage::kZeros + (r + 8) * kSB + bb])
+                             << 16);
+                } else {
+                    const int grp = ((b0 + lb0 + bb) << 7) / a.g;
+                    L.sz0 = 0u;
+                    L.sz1 = 0u;
+                    if (n0 < a.N) {
+                        const size_t gi = static_cast<size_t>(n0) * G + grp;
+                        L.sz0 = ldg_nc_u16(a.scale + gi) | (ldg_nc_u8(a.zero + gi) << 16);
+                    }
+                    if (n0 + 8 < a.N) {
+                        const size_t gi = static_cast<size_t>(n0 + 8) * G + grp;
+                        L.sz1 = ldg_nc_u16(a.scale + gi) | (ldg_nc_u8(a.zero + gi) << 16);
+                    }
                 }
+                mma_block<NT>(acc, L, xs + (lb0 + bb) * 256, xsum + (lb0 + bb) * Mpad, tok_stride,
+                              a.M, lane);
             }
         }
+        __syncwarp();  // every lane is done with stage c_stage
+        if (w_issued < nss) issue();
+        if (++c_stage == NS) {
+            c_stage = 0;
+            c_phase ^= 1u;
+        }
+        c_step += WPT;
+        if (c_step >= nsteps_slice) {
+            tile_end();
+            c_step = kp;
+            c_tile += NG;
+            ++ti;
+        }
     }
-    if (my_blocks == 0)
+    if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
+    if (my_steps == 0)
         for (; ti < my_tiles; ++ti) tile_end();
 
     if (S > 1) {
@@ -227,18 +311,28 @@ k_gemv_mma(const MmaKernelArgs a) {
     }
 }
 
+using MmaKernel = void (*)(MmaKernelArgs);
+
+MmaKernel pick_mma_kernel(int M, int K, int g) {
+    const bool fast = (g == 128) && (K % 512 == 0);
+    return (M <= 8) ? (fast ? k_gemv_mma<1, true> : k_gemv_mma<1, false>)
+                    : (fast ? k_gemv_mma<2, true> : k_gemv_mma<2, false>);
+}
+
 }  // namespace
 
-GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int k_split_req) {
-    const int W = kThreads / 32;
+GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req) {
     const int nblk = K / 128;
+    const int units_all = (nblk + kSB - 1) / kSB;
     const int ntiles = (N + 15) / 16;
-    const bool two = M > 8;
+    const int NT = (M <= 8) ? 1 : 2;
+    const void* kern = reinterpret_cast<const void*>(pick_mma_kernel(M, K, g));
     const SplitChoice c = choose_split(
-        dev, ntiles, nblk, W, 4, k_split_req, [M, two](int upc, int tg, int wpt, int tpg, int S) {
-            return two ? smem_bytes_mma<2>(M, upc, tg, wpt, tpg, S)
-                       : smem_bytes_mma<1>(M, upc, tg, wpt, tpg, S);
-        });
+        dev, ntiles, units_all, kWarps, 1, k_split_req,
+        [M, NT](int upc, int tg, int wpt, int tpg, int S) {
+            return mma_base_bytes(M, NT, upc, tg, wpt, tpg, S) + kWarps * 2 * (MmaStage::kBytes + 8);
+        },
+        [kern](int S, int smem) { return max_active_clusters(kern, kThreads, smem, S); });
     GemvPlan p{};
     p.kernel_id = 2;
     p.k_split = c.S;
@@ -247,7 +341,16 @@ GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int k_split_r
     p.threads = kThreads;
     p.ctas = c.ctas;
     p.tiles_per_cluster = c.tiles_per_group;
-    p.smem_bytes = c.smem_bytes;
+    if (c.ctas > 0) {
+        const int base = mma_base_bytes(M, NT, c.units_per_cta, kWarps / c.wpt, c.wpt,
+                                        c.tiles_per_group, c.S);
+        const int max_steps = c.tiles_per_group * ((c.units_per_cta + c.wpt - 1) / c.wpt);
+        int ns = (dev.max_smem_optin - base) / (kWarps * (MmaStage::kBytes + 8));
+        if (ns > kMaxStages) ns = kMaxStages;
+        if (ns > max_steps) ns = max_steps < 2 ? 2 : max_steps;
+        p.stages = ns;
+        p.smem_bytes = base + kWarps * ns * (MmaStage::kBytes + 8);
+    }
     return p;
 }
 
@@ -265,10 +368,15 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s
     k.g = a.g;
     k.wpt = p.wpt;
     k.ksplit = p.k_split;
-    k.blocks_per_cta = p.units_per_cta;
+    k.steps_per_cta = p.units_per_cta;
     k.tiles_per_group = p.tiles_per_cluster;
+    k.stages = p.stages;
     k.weights_static = a.weights_static;
     k.err = a.err;
+    MmaKernel kern = pick_mma_kernel(a.M, a.K, a.g);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         p.smem_bytes);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.ctas);
     cfg.blockDim = dim3(p.threads);
@@ -288,17 +396,7 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    cudaError_t e;
-    if (a.M <= 8) {
-        e = cudaFuncSetAttribute(k_gemv_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 p.smem_bytes);
-        if (e != cudaSuccess) return e;
-        return cudaLaunchKernelEx(&cfg, k_gemv_mma<1>, k);
-    }
-    e = cudaFuncSetAttribute(k_gemv_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             p.smem_bytes);
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, k_gemv_mma<2>, k);
+    return cudaLaunchKernelEx(&cfg, kern, k);
 }
 
 }  // namespace w4a16

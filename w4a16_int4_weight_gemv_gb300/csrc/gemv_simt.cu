@@ -508,19 +508,41 @@ bool async_sz_ok(int K, int g) {
     return false;
 }
 
+
+using SimtKernel = void (*)(SimtKernelArgs);
+
+SimtKernel pick_simt_kernel(int M, int tile_rows, int K, int g) {
+    const int cpg = async_sz_ok(K, g) ? g / 32 : 0;
+    SimtKernel kern = nullptr;
+#define W4A16_SIMT_PICK(MT_, TR_)                                                   \
+    kern = cpg == 1   ? k_gemv_simt<MT_, TR_, 1>                                   \
+           : cpg == 2 ? k_gemv_simt<MT_, TR_, 2>                                   \
+           : cpg == 4 ? k_gemv_simt<MT_, TR_, 4>                                   \
+                      : k_gemv_simt<MT_, TR_, 0>;
+    if (M == 1) {
+        if (tile_rows == 8) { W4A16_SIMT_PICK(1, 8) } else { W4A16_SIMT_PICK(1, 4) }
+    } else {
+        if (tile_rows == 8) { W4A16_SIMT_PICK(2, 8) } else { W4A16_SIMT_PICK(2, 4) }
+    }
+#undef W4A16_SIMT_PICK
+    return kern;
+}
+
 }  // namespace
 
-GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int k_split_req) {
+GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req) {
     const int nspan_all = (K / 32 + 31) / 32;
     const int TR = tile_rows_for(dev, N);
     const int ntiles = (N + TR - 1) / TR;
     const int stage = TR * 608;
+    const void* kern = reinterpret_cast<const void*>(pick_simt_kernel(M, TR, K, g));
     // feasibility and residency with the minimum two stages per warp
     const SplitChoice c = choose_split(
         dev, ntiles, nspan_all, kWarps, kCtasPerSm, k_split_req,
         [M, TR, stage](int upc, int tg, int wpt, int tpg, int S) {
             return simt_base_bytes(M, TR, upc, tg, wpt, tpg, S) + kWarps * 2 * (stage + 8);
-        });
+        },
+        [kern](int S, int smem) { return max_active_clusters(kern, kThreads, smem, S); });
     GemvPlan p{};
     p.kernel_id = 1;
     p.k_split = c.S;
@@ -565,19 +587,7 @@ cudaError_t launch_gemv_simt(const GemvArgs& a, const GemvPlan& p, cudaStream_t 
     k.stages = p.stages;
     k.weights_static = a.weights_static;
     k.err = a.err;
-    const int cpg = async_sz_ok(a.K, a.g) ? a.g / 32 : 0;
-    void (*kern)(SimtKernelArgs) = nullptr;
-#define W4A16_SIMT_PICK(MT_, TR_)                                                   \
-    kern = cpg == 1   ? k_gemv_simt<MT_, TR_, 1>                                   \
-           : cpg == 2 ? k_gemv_simt<MT_, TR_, 2>                                   \
-           : cpg == 4 ? k_gemv_simt<MT_, TR_, 4>                                   \
-                      : k_gemv_simt<MT_, TR_, 0>;
-    if (a.M == 1) {
-        if (p.tile_rows == 8) { W4A16_SIMT_PICK(1, 8) } else { W4A16_SIMT_PICK(1, 4) }
-    } else {
-        if (p.tile_rows == 8) { W4A16_SIMT_PICK(2, 8) } else { W4A16_SIMT_PICK(2, 4) }
-    }
-#undef W4A16_SIMT_PICK
+    SimtKernel kern = pick_simt_kernel(a.M, p.tile_rows, a.K, a.g);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          p.smem_bytes);
     if (e != cudaSuccess) return e;

@@ -45,12 +45,16 @@ struct DeviceInfo {
 // Choose the K split of a GEMV launch: total factor f = wpt * S (wpt warps of
 // a CTA share a tile, S CTAs of a cluster share it), minimising the critical
 // path -- tiles per warp group times K units per warp -- at full residency.
+// max_clusters(S, smem) is how many clusters of S CTAs with that much shared
+// memory the device can hold at once (clusters are co-scheduled inside a GPC,
+// so it can be less than SMs / S); the persistent grid never exceeds it.
 struct SplitChoice {
     int wpt, S, ctas, tiles_per_group, units_per_cta, smem_bytes;
 };
-template <class SmemFn>
+template <class SmemFn, class ClusterFn>
 SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int warps_per_cta,
-                         int max_ctas_per_sm, int forced_f, SmemFn smem_fn) {
+                         int max_ctas_per_sm, int forced_f, SmemFn smem_fn,
+                         ClusterFn max_clusters) {
     SplitChoice best{};
     long best_cost = -1;
     for (int f = 1; f <= 32; f *= 2) {
@@ -58,7 +62,7 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
         if (forced_f == 0 && f > units_all) break;
         for (int wpt = 1; wpt <= warps_per_cta && wpt <= f; wpt *= 2) {
             const int S = f / wpt;
-            if (S > 8 || wpt * S != f) continue;
+            if (S > 8 || wpt * S != f || warps_per_cta % wpt) continue;
             const int upc = (units_all + S - 1) / S;
             const int tg = warps_per_cta / wpt;
             // residency with tiles_per_group unknown: size with one tile first
@@ -68,8 +72,13 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
             if (per_sm > max_ctas_per_sm) per_sm = max_ctas_per_sm;
             if (per_sm < 1) continue;
             int clusters = (per_sm * dev.sms) / S;
-            const int max_clusters = (ntiles + tg - 1) / tg;
-            if (clusters > max_clusters) clusters = max_clusters;
+            if (S > 1) {
+                const int mc = max_clusters(S, smem);
+                if (mc < 1) continue;
+                if (clusters > mc) clusters = mc;
+            }
+            const int max_clusters_needed = (ntiles + tg - 1) / tg;
+            if (clusters > max_clusters_needed) clusters = max_clusters_needed;
             if (clusters < 1) clusters = 1;
             const int tpg = (ntiles + clusters * tg - 1) / (clusters * tg);
             smem = smem_fn(upc, tg, wpt, tpg, S);
@@ -84,9 +93,13 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
     return best;
 }
 
-// Launch-shape choices (pure host arithmetic, no CUDA calls).
-GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int k_split_req);
-GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int k_split_req);
+// Number of clusters of S CTAs (threads each, smem bytes of dynamic shared
+// memory) of `kernel` the current device can run at once; cached.
+int max_active_clusters(const void* kernel, int threads, int smem, int S);
+
+// Launch-shape choices (host arithmetic plus cached occupancy queries).
+GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
+GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
 
 cudaError_t launch_gemv_simt(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);

@@ -36,44 +36,45 @@ __device__ __forceinline__ void stage_x_permuted(const uint16_t* __restrict__ x,
                                                  int nb, unsigned char* xs, float* xsum,
                                                  int tok_stride) {
     constexpr int Mpad = 8 * NT;
-    // 16-byte pieces: token n, block b, quad c, step-pair q -> 8 consecutive k
+    // 16-byte pieces: token n, block b, quad c, step-pair q -> 8 consecutive k.
+    // The 16 pieces of one (token, block) are 16 consecutive i, i.e. 16
+    // consecutive lanes of one warp, so the block sum is a 16-lane shuffle
+    // reduction in the same pass (blockDim is a multiple of 32).
     const int pieces = m * nb * 16;
-    for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
-        const int n = i / (nb * 16);
+    for (int base = 0; base < pieces; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const bool ok = i < pieces;
+        const int n = ok ? i / (nb * 16) : 0;
         const int rem = i - n * nb * 16;
         const int b = rem >> 4;
         const int c = (rem >> 2) & 3;
         const int q = rem & 3;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        const int row = rowsel ? rowsel[n] : n;
+        const int row = ok ? (rowsel ? rowsel[n] : n) : -1;
         if (row >= 0) {
             const int k = kbeg + b * 128 + c * 32 + q * 8;
             v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * K + k));
         }
-        uint4 o;
-        o.x = __byte_perm(v.x, v.z, 0x5410);  // (x0, x4)
-        o.y = __byte_perm(v.x, v.z, 0x7632);  // (x1, x5)
-        o.z = __byte_perm(v.y, v.w, 0x5410);  // (x2, x6)
-        o.w = __byte_perm(v.y, v.w, 0x7632);  // (x3, x7)
-        *reinterpret_cast<uint4*>(xs + n * tok_stride + b * 256 + q * 64 + c * 16) = o;
-    }
-    // activation sums per (block, token), fp32
-    for (int i = threadIdx.x; i < nb * Mpad; i += blockDim.x) {
-        const int b = i / Mpad;
-        const int n = i - b * Mpad;
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float sum = 0.f;
-        const int row = (n < m) ? (rowsel ? rowsel[n] : n) : -1;
-        if (row >= 0) {
-            const uint16_t* p = x + static_cast<size_t>(row) * K + kbeg + b * 128;
-            for (int j = 0; j < 128; j += 8) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(p + j));
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    sum += bf16_to_f32(w[e] & 0xFFFFu) + bf16_to_f32(w[e] >> 16);
-            }
+        for (int e = 0; e < 4; ++e) sum += bf16_to_f32(w[e] & 0xFFFFu) + bf16_to_f32(w[e] >> 16);
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (ok) {
+            uint4 o4;
+            o4.x = __byte_perm(v.x, v.z, 0x5410);  // (x0, x4)
+            o4.y = __byte_perm(v.x, v.z, 0x7632);  // (x1, x5)
+            o4.z = __byte_perm(v.y, v.w, 0x5410);  // (x2, x6)
+            o4.w = __byte_perm(v.y, v.w, 0x7632);  // (x3, x7)
+            *reinterpret_cast<uint4*>(xs + n * tok_stride + b * 256 + q * 64 + c * 16) = o4;
+            if ((rem & 15) == 0) xsum[b * Mpad + n] = sum;
         }
-        xsum[b * Mpad + n] = sum;
+    }
+    // tokens m..Mpad-1 contribute nothing
+    for (int i = threadIdx.x; i < nb * (Mpad - m); i += blockDim.x) {
+        const int b = i / (Mpad - m);
+        xsum[b * Mpad + m + (i - b * (Mpad - m))] = 0.f;
     }
 }
 
