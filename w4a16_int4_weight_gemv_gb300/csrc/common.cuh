@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap (the type only; no driver library is linked)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -136,10 +137,29 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
                  : "memory");
 }
 
-// Bulk prefetch of [src, src + bytes) into L2 (src 16-byte aligned, bytes a
-// multiple of 16).  A hint: it completes asynchronously and signals nothing.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+// 2-D tiled bulk tensor copy global -> this CTA's shared memory through the
+// tensor map `map` (a kernel parameter), box origin (c0, c1) in elements,
+// completing on `bar` with the full box size in bytes (elements outside the
+// tensor are filled with zeros).  c0 * element size must be a multiple of 16
+// bytes; dst must be aligned as the map's swizzle mode requires (1024 bytes
+// for the 128-byte swizzle).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Four 8x8 matrices of 16-bit elements from shared memory: lanes 8i..8i+7
+// give the 16-byte row addresses of matrix i; lane l receives, from each
+// matrix, the 32-bit word at row l / 4, bytes 4 * (l % 4) .. + 3.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&d)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(addr)
+                 : "memory");
 }
 
 // ---------------------------------------------------------------------------

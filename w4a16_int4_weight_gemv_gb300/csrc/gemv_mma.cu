@@ -7,19 +7,26 @@
 // mma.sync.m16n8k16 (bf16 in, fp32 accumulate): weights are the 16-row A
 // operand, the M tokens (padded to 8 or 16) the B operand.  The dense tile is
 // tiny (n = 8 or 16), so warp MMA fed from registers is the right tool.
-// (Dequantisation and the K permutation are described in mma_core.cuh.)
+// (Dequantisation is described in mma_core.cuh.)
 //
-// Memory path (as in the CUDA-core kernel, gemv_simt.cu): each warp owns
-// 16-row tiles; a step is 512 k of the tile (kSB 128-k blocks).  The step's
-// packed words reach a per-warp ring of shared-memory stages by bulk copies
-// (one 256-byte copy per row, into rows padded to kRowPitch so the A-fragment
-// reads are free of bank conflicts), its scales and zero points by cp.async,
-// all completing on the stage's mbarrier.  Warps work independently; when
-// there are too few tiles to occupy the GPU the K range of a tile is split
-// over WPT warps of a CTA (partials added in shared memory behind a named
-// barrier, once per tile) and over the CTAs of a thread-block cluster (added
-// through distributed shared memory, once per kernel), always in a fixed
-// order.  Launches use programmatic dependent launch.
+// Memory path.  Each warp owns 16-row tiles; a step is 512 k of the tile
+// (kSB 128-k blocks, 4 KB of packed words).  The step reaches a per-warp ring
+// of shared-memory stages as two 2-D tensor copies (16 rows x 128 bytes each,
+// 128-byte swizzle) issued by one lane; its scales and zero points follow by
+// cp.async; all complete on the stage's mbarrier.  Fragments are read with
+// ldmatrix: lane (r, c) gets word c of every 16-byte chunk of rows r and
+// r + 8, i.e. 8 consecutive k per chunk, and the swizzle puts the eight rows
+// of an ldmatrix phase in eight bank groups.  With that assignment the
+// activations need no reordering beyond the pairing inside each 16-byte piece,
+// so each token's K slice is one bulk copy, issued before any weight copy so
+// that it is not queued behind the weight stream, then paired in place.
+//
+// Work split.  Warps work independently; when there are too few tiles to
+// occupy the GPU the K range of a tile is split over WPT warps of a CTA
+// (partials added in shared memory behind a named barrier, once per tile) and
+// over the CTAs of a thread-block cluster (added through distributed shared
+// memory, once per kernel), always in a fixed order.  Launches use
+// programmatic dependent launch.
 #include "common.cuh"
 #include "launch.h"
 #include "mma_core.cuh"
@@ -29,23 +36,16 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSB = 4;          // 128-k blocks per step (512 k)
-constexpr int kRowPitch = 320;  // 256 bytes of a row's step + 64: the two rows a
-                                // quarter-warp reads fall in different bank halves
+constexpr int kSB = 4;           // 128-k blocks per step (512 k)
+constexpr int kHalfBytes = 2048;  // one tensor box: 16 rows x 128 bytes
+constexpr int kStageA = 2 * kHalfBytes;
+constexpr int kStageSZ = 256;    // 16 rows x 4 zero points, then 16 rows x 4 scales
+constexpr int kSZScales = 64;
 constexpr int kMaxStages = 8;
-
-// Shared-memory stage of one warp step: 16 rows x kSB blocks of packed words,
-// then (fast path) the rows' kSB scales and zero points.
-struct MmaStage {
-    static constexpr int kA = 0;
-    static constexpr int kScales = 16 * kRowPitch;           // 16 rows x kSB bf16
-    static constexpr int kZeros = kScales + 16 * kSB * 2;    // 16 rows x kSB u8
-    static constexpr int kBytes = kZeros + 16 * kSB;         // 5312
-};
+static_assert(kWeightBoxWords * 4 * kWeightBoxRows == kHalfBytes, "box geometry");
 
 struct MmaKernelArgs {
     const uint16_t* x;
-    const uint4* wq;
     const uint16_t* scale;
     const uint8_t* zero;
     void* y;
@@ -56,13 +56,16 @@ struct MmaKernelArgs {
     int g;
     int wpt;
     int ksplit;
-    int steps_per_cta;  // 512-k steps in one CTA's K slice
+    int steps_per_cta;
     int tiles_per_group;
     int stages;
     int weights_static;
     uint32_t* err;
 };
 
+// Bytes of the CTA's shared memory before the stage rings: permuted
+// activations, block sums, the in-CTA reduction buffer and (K split over a
+// cluster) the partials the cluster adds.
 __host__ __device__ inline int mma_base_bytes(int M, int NT, int upc, int tg, int wpt, int tpg,
                                               int S) {
     const int Mpad = 8 * NT;
@@ -73,12 +76,18 @@ __host__ __device__ inline int mma_base_bytes(int M, int NT, int upc, int tg, in
     return (b + 127) & ~127;
 }
 
+// Whole dynamic shared memory for NS stages per warp; 1024 bytes of slack
+// let the A rings start on the 1024-byte boundary the swizzle needs.
+__host__ __device__ inline int mma_smem_bytes(int base, int ns) {
+    return base + 1024 + kWarps * ns * (kStageA + kStageSZ + 8) + 16;
+}
+
 // kFast: g == 128 and K % 512 == 0 -- a step's scales and zero points are
 // whole 8- and 4-byte pieces per row, copied with cp.async into the stage.
 // Otherwise the consumer loads the two rows' pair for each block itself.
 template <int NT, bool kFast>
 __global__ void __launch_bounds__(kThreads, 1)
-k_gemv_mma(const MmaKernelArgs a) {
+k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
     constexpr int Mpad = 8 * NT;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
@@ -87,7 +96,6 @@ k_gemv_mma(const MmaKernelArgs a) {
     const int TG = kWarps / WPT;
     const int tg = warp / WPT;
     const int kp = warp - tg * WPT;
-    const int Q = a.K >> 5;
     const int nblk_all = a.K >> 7;
     const int S = a.ksplit;
     const int rank = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
@@ -109,9 +117,14 @@ k_gemv_mma(const MmaKernelArgs a) {
     float* red = xsum + BPC * Mpad;                                 // [2][TG][WPT][16][Mpad]
     float* part = red + (WPT > 1 ? 2 * TG * WPT * 16 * Mpad : 0);    // [tpg][TG][16][Mpad]
     const int base = mma_base_bytes(a.M, NT, a.steps_per_cta, TG, WPT, a.tiles_per_group, S);
-    unsigned char* ring = smem_raw + base + warp * NS * MmaStage::kBytes;
-    uint64_t* bars =
-        reinterpret_cast<uint64_t*>(smem_raw + base + kWarps * NS * MmaStage::kBytes) + warp * NS;
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const int a_off = static_cast<int>(((raw_addr + base + 1023u) & ~1023u) - raw_addr);
+    unsigned char* ring_a = smem_raw + a_off + warp * NS * kStageA;
+    unsigned char* ring_sz = smem_raw + a_off + kWarps * NS * kStageA + warp * NS * kStageSZ;
+    uint64_t* bars0 =
+        reinterpret_cast<uint64_t*>(smem_raw + a_off + kWarps * NS * (kStageA + kStageSZ));
+    uint64_t* bars = bars0 + warp * NS;
+    uint64_t* xbar = bars0 + kWarps * NS;
 
     const int gid = cid * TG + tg;
     const int NG = ncl * TG;
@@ -122,34 +135,34 @@ k_gemv_mma(const MmaKernelArgs a) {
     grid_dependents_launch();
     if (lane == 0) {
         for (int i = 0; i < NS; ++i) mbar_init(bars + i, 1 + (kFast ? 32 : 0));
+        if (warp == 0) mbar_init(xbar, 1);
         mbar_init_fence();
     }
-    __syncwarp();
+    __syncthreads();
 
     // producer cursor
     int w_tile = gid, w_step = kp, w_stage = 0, w_issued = 0;
     auto issue = [&]() {
         uint64_t* bar = bars + w_stage;
-        unsigned char* dst = ring + w_stage * MmaStage::kBytes;
-        const int blk0 = b0 + w_step * kSB;                 // first global block of the step
-        const int nbs = min(kSB, b0 + nb - blk0);           // blocks in this step
-        const int rows = min(16, a.N - w_tile * 16);
-        const size_t row0 = static_cast<size_t>(w_tile) * 16;
-        const uint32_t row_bytes = static_cast<uint32_t>(nbs) * 64u;
+        unsigned char* dst = ring_a + w_stage * kStageA;
+        const int blk0 = b0 + w_step * kSB;        // first global block of the step
+        const int nbs = min(kSB, b0 + nb - blk0);  // blocks in this step
+        const int nh = (nbs + 1) >> 1;             // boxes (two blocks each)
+        const int row0 = w_tile * 16;
         if (lane == 0) {
             if (w_issued >= NS) fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, row_bytes * static_cast<uint32_t>(rows));
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nh * kHalfBytes));
+            tma_load_2d(dst, &wmap, blk0 * 16, row0, bar);
+            if (nh > 1) tma_load_2d(dst + kHalfBytes, &wmap, blk0 * 16 + 32, row0, bar);
         }
-        if (lane < rows)
-            bulk_copy_g2s(dst + MmaStage::kA + lane * kRowPitch,
-                          a.wq + (row0 + lane) * Q + blk0 * 4, row_bytes, bar);
         if constexpr (kFast) {
             // lanes 0..15 copy row lane's 4 zero points, lanes 16..31 its 4 scales
+            unsigned char* sz = ring_sz + w_stage * kStageSZ;
             const int rr = lane & 15;
-            if (rr < rows) {
-                const size_t gi = (row0 + rr) * G + blk0;  // g == 128: block == group
-                if (lane < 16) cp_async_4(dst + MmaStage::kZeros + rr * kSB, a.zero + gi);
-                else cp_async_8(dst + MmaStage::kScales + rr * kSB * 2, a.scale + gi);
+            if (row0 + rr < a.N) {
+                const size_t gi = static_cast<size_t>(row0 + rr) * G + blk0;  // block == group
+                if (lane < 16) cp_async_4(sz + rr * 4, a.zero + gi);
+                else cp_async_8(sz + kSZScales + rr * 8, a.scale + gi);
             }
             cp_async_arrive_noinc(bar);
         }
@@ -162,15 +175,24 @@ k_gemv_mma(const MmaKernelArgs a) {
         }
     };
 
-    if (a.weights_static) {
-        while (w_issued < NS && w_issued < nss) issue();
-        grid_dependency_wait();
-    } else {
-        grid_dependency_wait();
-        while (w_issued < NS && w_issued < nss) issue();
+    // Activations first (they gate every MMA), then the weight rings.  With
+    // static weights one stage per warp is already requested while the
+    // preceding grid finishes.
+    if (a.weights_static && nss > 0) issue();
+    grid_dependency_wait();
+    if (warp == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(a.M * nb * 256));
+        __syncwarp();
+        if (lane < a.M && nb > 0)
+            bulk_copy_g2s(xs + lane * tok_stride,
+                          a.x + static_cast<size_t>(lane) * a.K + (static_cast<size_t>(b0) << 7),
+                          static_cast<uint32_t>(nb * 256), xbar);
     }
+    __syncthreads();
+    while (w_issued < NS && w_issued < nss) issue();
 
-    stage_x_permuted<NT>(a.x, nullptr, a.M, a.K, b0 << 7, nb, xs, xsum, tok_stride);
+    bool timed_out = !mbar_wait_bounded(xbar, 0);
+    pair_x_in_place<NT>(a.M, nb, xs, xsum, tok_stride);
     __syncthreads();
 
     float acc[NT][4];
@@ -180,7 +202,6 @@ k_gemv_mma(const MmaKernelArgs a) {
         for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
     int c_tile = gid, c_step = kp, ti = 0, c_stage = 0;
     uint32_t c_phase = 0;
-    bool timed_out = false;
 
     // fragment position i of n-tile t: row r (+8 for i >= 2), token t*8 + 2c + (i & 1)
     auto tile_end = [&]() {
@@ -229,29 +250,38 @@ k_gemv_mma(const MmaKernelArgs a) {
             for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
     };
 
+    // ldmatrix addressing: lane l supplies row (l & 7) + 8 * ((l >> 3) & 1) of
+    // chunk (l >> 4) (+ 2 for the second load) of the block's four chunks.
+    const int lrow = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const uint32_t lbase = static_cast<uint32_t>(lrow * 128);
+    const int lsw = lane & 7;  // swizzle term: row % 8
+    const int lch = lane >> 4;
+
 #pragma unroll 1
     for (int ss = 0; ss < nss; ++ss) {
         if (!mbar_wait_bounded(bars + c_stage, c_phase)) timed_out = true;
-        const unsigned char* stg = ring + c_stage * MmaStage::kBytes;
+        const uint32_t stg = smem_addr(ring_a + c_stage * kStageA);
+        const unsigned char* sz = ring_sz + c_stage * kStageSZ;
         const int lb0 = c_step * kSB;  // first block of the step within the slice
         const int nbs = min(kSB, nb - lb0);
         const int n0 = c_tile * 16 + r;
 #pragma unroll
         for (int bb = 0; bb < kSB; ++bb) {
             if (bb < nbs) {
+                const uint32_t hb = stg + (bb >> 1) * kHalfBytes + lbase;
+                const int cb = (bb & 1) * 4 + lch;
+                uint32_t q0[4], q1[4];
+                ldmatrix_x4(q0, hb + (static_cast<uint32_t>(cb ^ lsw) << 4));
+                ldmatrix_x4(q1, hb + (static_cast<uint32_t>((cb + 2) ^ lsw) << 4));
                 MmaBlockLoad L;
-                L.w0 = *reinterpret_cast<const uint4*>(stg + MmaStage::kA + r * kRowPitch +
-                                                       bb * 64 + c * 16);
-                L.w1 = *reinterpret_cast<const uint4*>(stg + MmaStage::kA + (r + 8) * kRowPitch +
-                                                       bb * 64 + c * 16);
+                L.w0 = make_uint4(q0[0], q0[2], q1[0], q1[2]);
+                L.w1 = make_uint4(q0[1], q0[3], q1[1], q1[3]);
                 if constexpr (kFast) {
-                    L.sz0 = *reinterpret_cast<const uint16_t*>(stg + MmaStage::kScales +
-                                                               r * kSB * 2 + bb * 2) |
-                            (static_cast<uint32_t>(stg[MmaStage::kZeros + r * kSB + bb]) << 16);
-                    L.sz1 = *reinterpret_cast<const uint16_t*>(stg + MmaStage::kScales +
-                                                               (r + 8) * kSB * 2 + bb * 2) |
-                            (static_cast<uint32_t>(stg[MmaStage::kZeros + (r + 8) * kSB + bb])
-                             << 16);
+                    L.sz0 = *reinterpret_cast<const uint16_t*>(sz + kSZScales + r * 8 + bb * 2) |
+                            (static_cast<uint32_t>(sz[r * 4 + bb]) << 16);
+                    L.sz1 =
+                        *reinterpret_cast<const uint16_t*>(sz + kSZScales + (r + 8) * 8 + bb * 2) |
+                        (static_cast<uint32_t>(sz[(r + 8) * 4 + bb]) << 16);
                 } else {
                     const int grp = ((b0 + lb0 + bb) << 7) / a.g;
                     L.sz0 = 0u;
@@ -311,7 +341,7 @@ k_gemv_mma(const MmaKernelArgs a) {
     }
 }
 
-using MmaKernel = void (*)(MmaKernelArgs);
+using MmaKernel = void (*)(MmaKernelArgs, CUtensorMap);
 
 MmaKernel pick_mma_kernel(int M, int K, int g) {
     const bool fast = (g == 128) && (K % 512 == 0);
@@ -327,12 +357,15 @@ GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_
     const int ntiles = (N + 15) / 16;
     const int NT = (M <= 8) ? 1 : 2;
     const void* kern = reinterpret_cast<const void*>(pick_mma_kernel(M, K, g));
+    // the launch fills the CTA's shared memory with stages, so co-residency of
+    // clusters is queried at the full budget, not at the two-stage minimum
+    const int budget = dev.max_smem_optin;
     const SplitChoice c = choose_split(
         dev, ntiles, units_all, kWarps, 1, k_split_req,
         [M, NT](int upc, int tg, int wpt, int tpg, int S) {
-            return mma_base_bytes(M, NT, upc, tg, wpt, tpg, S) + kWarps * 2 * (MmaStage::kBytes + 8);
+            return mma_smem_bytes(mma_base_bytes(M, NT, upc, tg, wpt, tpg, S), 2);
         },
-        [kern](int S, int smem) { return max_active_clusters(kern, kThreads, smem, S); });
+        [kern, budget](int S, int) { return max_active_clusters(kern, kThreads, budget, S); });
     GemvPlan p{};
     p.kernel_id = 2;
     p.k_split = c.S;
@@ -345,11 +378,10 @@ GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_
         const int base = mma_base_bytes(M, NT, c.units_per_cta, kWarps / c.wpt, c.wpt,
                                         c.tiles_per_group, c.S);
         const int max_steps = c.tiles_per_group * ((c.units_per_cta + c.wpt - 1) / c.wpt);
-        int ns = (dev.max_smem_optin - base) / (kWarps * (MmaStage::kBytes + 8));
-        if (ns > kMaxStages) ns = kMaxStages;
-        if (ns > max_steps) ns = max_steps < 2 ? 2 : max_steps;
+        int ns = 2;
+        while (ns < kMaxStages && ns < max_steps && mma_smem_bytes(base, ns + 1) <= budget) ++ns;
         p.stages = ns;
-        p.smem_bytes = base + kWarps * ns * (MmaStage::kBytes + 8);
+        p.smem_bytes = mma_smem_bytes(base, ns);
     }
     return p;
 }
@@ -357,7 +389,6 @@ GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_
 cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
     MmaKernelArgs k{};
     k.x = a.x;
-    k.wq = reinterpret_cast<const uint4*>(a.wq);
     k.scale = a.scale;
     k.zero = a.zero;
     k.y = a.y;
@@ -373,6 +404,8 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s
     k.stages = p.stages;
     k.weights_static = a.weights_static;
     k.err = a.err;
+    CUtensorMap wmap;
+    if (!encode_weight_map(&wmap, a.wq, a.N, a.K)) return cudaErrorInvalidValue;
     MmaKernel kern = pick_mma_kernel(a.M, a.K, a.g);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          p.smem_bytes);
@@ -396,7 +429,7 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, k);
+    return cudaLaunchKernelEx(&cfg, kern, k, wmap);
 }
 
 }  // namespace w4a16

@@ -266,52 +266,66 @@ k_gemv_simt(const SimtKernelArgs a) {
         }
     };
 
-    if (a.weights_static) {
-        while (w_issued < NS && w_issued < nss) issue();
-        grid_dependency_wait();
-    } else {
-        grid_dependency_wait();
-        while (w_issued < NS && w_issued < nss) issue();
-    }
-
     // stage x' and the chunk sums of this CTA's K slice (one pass)
-    {
-        const int kbeg = span0 << 10;
-        const int kend = min(a.K, (span0 + nspan) << 10);
-        const int npieces = nspan << 7;  // 8 consecutive k per piece, 4 pieces per chunk
-        for (int m = 0; m < MT; ++m) {
-            for (int b0 = 0; b0 < npieces; b0 += blockDim.x) {
-                const int i = b0 + threadIdx.x;
-                const int k0 = i << 3;   // local k
-                const int cl = k0 >> 5;  // local chunk
-                const int q0 = (k0 >> 2) & 7;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (i < npieces && kbeg + k0 < kend)
-                    v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * a.K +
-                                                             kbeg + k0));
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-                float f[8];
-                float sum = 0.f;
+    const int kbeg = span0 << 10;
+    const int kend = min(a.K, (span0 + nspan) << 10);
+    const int npieces = nspan << 7;  // 8 consecutive k per piece, 4 pieces per chunk
+    auto load_piece = [&](int m, int i) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (i < npieces && kbeg + (i << 3) < kend)
+            v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * a.K + kbeg +
+                                                     (i << 3)));
+        return v;
+    };
+    // all lanes of the warp take part (chunk sums are 4-lane shuffles)
+    auto store_piece = [&](int m, int i, const uint4 v) {
+        const int k0 = i << 3;   // local k
+        const int cl = k0 >> 5;  // local chunk
+        const int q0 = (k0 >> 2) & 7;
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        float f[8];
+        float sum = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float lo = bf16_to_f32(wv[e] & 0xFFFFu);
-                    const float hi = bf16_to_f32(wv[e] >> 16);
-                    sum += lo + hi;
-                    f[2 * e] = lo * position_factor(2 * e);
-                    f[2 * e + 1] = hi * position_factor(2 * e + 1);
-                }
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                if (i < npieces) {
-                    float4* bp = reinterpret_cast<float4*>(xs + m * SP * 1024) +
-                                 (cl >> 5) * 256 + (cl & 31);
-                    bp[q0 * 32] = make_float4(f[0], f[1], f[2], f[3]);
-                    bp[(q0 + 1) * 32] = make_float4(f[4], f[5], f[6], f[7]);
-                    if ((i & 3) == 0) xsum[m * SP * 32 + cl] = sum * exp2i(-64);
-                }
-            }
+        for (int e = 0; e < 4; ++e) {
+            const float lo = bf16_to_f32(wv[e] & 0xFFFFu);
+            const float hi = bf16_to_f32(wv[e] >> 16);
+            sum += lo + hi;
+            f[2 * e] = lo * position_factor(2 * e);
+            f[2 * e + 1] = hi * position_factor(2 * e + 1);
         }
-    }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if (i < npieces) {
+            float4* bp = reinterpret_cast<float4*>(xs + m * SP * 1024) + (cl >> 5) * 256 + (cl & 31);
+            bp[q0 * 32] = make_float4(f[0], f[1], f[2], f[3]);
+            bp[(q0 + 1) * 32] = make_float4(f[4], f[5], f[6], f[7]);
+            if ((i & 3) == 0) xsum[m * SP * 32 + cl] = sum * exp2i(-64);
+        }
+    };
+
+    // The activations gate all arithmetic: their loads are issued before the
+    // weight rings so they are not queued behind the weight stream.  With
+    // static weights one stage per warp is already requested while the
+    // preceding grid finishes.
+    if (a.weights_static && nss > 0) issue();
+    grid_dependency_wait();
+    constexpr int kXPre = 4;  // pieces per thread and token loaded ahead
+    uint4 xpre[MT][kXPre];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int j = 0; j < kXPre; ++j) xpre[m][j] = load_piece(m, threadIdx.x + j * blockDim.x);
+    __syncthreads();
+    while (w_issued < NS && w_issued < nss) issue();
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int j = 0; j < kXPre; ++j)
+            if (j * static_cast<int>(blockDim.x) < npieces)
+                store_piece(m, threadIdx.x + j * blockDim.x, xpre[m][j]);
+    for (int m = 0; m < MT; ++m)
+        for (int b = kXPre * blockDim.x; b < npieces; b += blockDim.x)
+            store_piece(m, b + threadIdx.x, load_piece(m, b + threadIdx.x));
     __syncthreads();
 
     float acc[TR][MT];
@@ -536,13 +550,17 @@ GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int g, int k
     const int ntiles = (N + TR - 1) / TR;
     const int stage = TR * 608;
     const void* kern = reinterpret_cast<const void*>(pick_simt_kernel(M, TR, K, g));
-    // feasibility and residency with the minimum two stages per warp
+    int budget = dev.smem_per_sm / kCtasPerSm - 1024;
+    if (budget > dev.max_smem_optin) budget = dev.max_smem_optin;
+    // feasibility and residency with the minimum two stages per warp; the
+    // launch fills the budget with stages, so cluster co-residency is queried
+    // at the budget
     const SplitChoice c = choose_split(
         dev, ntiles, nspan_all, kWarps, kCtasPerSm, k_split_req,
         [M, TR, stage](int upc, int tg, int wpt, int tpg, int S) {
             return simt_base_bytes(M, TR, upc, tg, wpt, tpg, S) + kWarps * 2 * (stage + 8);
         },
-        [kern](int S, int smem) { return max_active_clusters(kern, kThreads, smem, S); });
+        [kern, budget](int S, int) { return max_active_clusters(kern, kThreads, budget, S); });
     GemvPlan p{};
     p.kernel_id = 1;
     p.k_split = c.S;
@@ -558,8 +576,6 @@ GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int g, int k
         // a warp runs at most tiles_per_group * ceil(units / wpt) steps; more
         // stages than that only occupy shared memory the next launch could use
         const int max_steps = c.tiles_per_group * ((c.units_per_cta + c.wpt - 1) / c.wpt);
-        int budget = dev.smem_per_sm / kCtasPerSm - 1024;
-        if (budget > dev.max_smem_optin) budget = dev.max_smem_optin;
         int ns = (budget - base) / (kWarps * (stage + 8));
         if (ns > kMaxStages) ns = kMaxStages;
         if (ns > max_steps) ns = max_steps < 2 ? 2 : max_steps;

@@ -4,9 +4,18 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap
 #include <cuda_runtime.h>
 
 namespace w4a16 {
+
+// Box of the packed-weight tensor map used by the warp-MMA kernel: 32 words
+// (128 bytes, 256 k) x 16 rows, 128-byte swizzle.
+constexpr unsigned kWeightBoxWords = 32;
+constexpr unsigned kWeightBoxRows = 16;
+
+// Tensor map of a packed weight matrix [N][K/8] words (host; false on failure).
+bool encode_weight_map(CUtensorMap* map, const void* wq, int N, int K);
 
 struct GemvArgs {
     const uint16_t* x;
@@ -32,7 +41,7 @@ struct GemvPlan {
     int units_per_cta;  // 32-chunk spans (kernel 1) or 128-k blocks (kernel 2) per CTA
     int tiles_per_cluster;  // upper bound of tiles one tile group processes
     int wpt;                // warps sharing one tile (K split inside the CTA)
-    int stages;             // shared-memory stages per warp (CUDA-core kernel)
+    int stages;             // shared-memory stages per warp
     int tile_rows;          // rows per warp tile (CUDA-core kernel)
 };
 
@@ -60,7 +69,8 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
     for (int f = 1; f <= 32; f *= 2) {
         if (forced_f > 0 && f != forced_f) continue;
         if (forced_f == 0 && f > units_all) break;
-        for (int wpt = 1; wpt <= warps_per_cta && wpt <= f; wpt *= 2) {
+        // largest in-CTA share first: on equal cost the fewest CTAs per cluster
+        for (int wpt = (f < warps_per_cta ? f : warps_per_cta); wpt >= 1; wpt /= 2) {
             const int S = f / wpt;
             if (S > 8 || wpt * S != f || warps_per_cta % wpt) continue;
             const int upc = (units_all + S - 1) / S;

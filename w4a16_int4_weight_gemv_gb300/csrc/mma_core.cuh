@@ -9,12 +9,18 @@
 //     sum_k (code_k - z) s x_k = s * (C - (128 + z) * sum_k x_k),
 // applied once per block with the block's activation sums precomputed.
 //
-// K order.  A thread's 16-byte load holds 32 consecutive k of one row; the
-// MMA fragment wants two values of the same k-pair slots per register.  The
-// k order inside the MMA is free (a dot product does not depend on it), so
-// the activations are staged in shared memory permuted to match: for each
-// 8-value group x[k..k+7] the staged words are (x0,x4), (x1,x5), (x2,x6),
-// (x3,x7) -- exactly the pairs the LOP3 above produces from the weights.
+// K order.  The k order inside the MMA is free (a dot product does not depend
+// on it), so the activations are staged in shared memory to match whatever
+// words each lane holds.  Within a 32-bit word of codes k..k+7 the LOP3 above
+// produces the pairs (k0,k4), (k1,k5), (k2,k6), (k3,k7), so every 16-byte
+// piece of eight activations is stored as those four pairs.  Which word of
+// which row a lane holds depends on how the weights were loaded:
+//  - ldmatrix from shared memory (dense GEMV): lane (r, c) holds word c of
+//    each 16-byte chunk j of the block, k = 32 j + 8 c + e, so the pieces stay
+//    in their natural order (pair_x_in_place);
+//  - one 16-byte global load per row (expert GEMV): lane (r, c) holds chunk c,
+//    k = 32 c + 8 j + e, so piece (c, j) moves to position (j, c)
+//    (stage_x_permuted).
 //
 #pragma once
 
@@ -78,6 +84,62 @@ __device__ __forceinline__ void stage_x_permuted(const uint16_t* __restrict__ x,
     }
 }
 
+// In-place form for the dense GEMV: m token rows of nb 128-k blocks were
+// copied verbatim to xs (token stride tok_stride bytes); pair the values
+// inside every 16-byte piece and write the per-block sums xsum[b][Mpad]
+// (tokens >= m get 0).  A thread takes a quarter block (four pieces, loaded
+// together); the quarters of a block are four consecutive lanes, so the block
+// sum is a 4-lane shuffle reduction.
+template <int NT>
+__device__ __forceinline__ void pair_x_in_place(int m, int nb, unsigned char* xs, float* xsum,
+                                                int tok_stride) {
+    constexpr int Mpad = 8 * NT;
+    const int per_tok = nb * 4;
+    const int items = m * per_tok;
+    for (int base = 0; base < items; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const bool ok = i < items;
+        const int n = ok ? i / per_tok : 0;
+        const int rem = ok ? i - n * per_tok : 0;  // block * 4 + quarter
+        uint4* p = reinterpret_cast<uint4*>(xs + n * tok_stride + rem * 64);
+        // piece order rotated by lane pair: the eight lanes of a 16-byte load
+        // phase then touch eight different bank groups
+        const int rot = (rem >> 1) & 3;
+        uint4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = ok ? p[(q + rot) & 3] : make_uint4(0u, 0u, 0u, 0u);
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s0 += bf16_to_f32(w[e] & 0xFFFFu);
+                s1 += bf16_to_f32(w[e] >> 16);
+            }
+        }
+        float sum = s0 + s1;
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if (ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 o4;
+                o4.x = __byte_perm(v[q].x, v[q].z, 0x5410);  // (x0, x4)
+                o4.y = __byte_perm(v[q].x, v[q].z, 0x7632);  // (x1, x5)
+                o4.z = __byte_perm(v[q].y, v[q].w, 0x5410);  // (x2, x6)
+                o4.w = __byte_perm(v[q].y, v[q].w, 0x7632);  // (x3, x7)
+                p[(q + rot) & 3] = o4;
+            }
+            if ((rem & 3) == 0) xsum[(rem >> 2) * Mpad + n] = sum;
+        }
+    }
+    for (int i = threadIdx.x; i < nb * (Mpad - m); i += blockDim.x) {
+        const int b = i / (Mpad - m);
+        xsum[b * Mpad + m + (i - b * (Mpad - m))] = 0.f;
+    }
+}
+
 // Packed codes, scale and zero of one thread for one 128-k block of a 16-row
 // tile: rows r and r + 8 (r = lane / 4), 32 consecutive k each.
 struct MmaBlockLoad {
@@ -125,11 +187,14 @@ __device__ __forceinline__ void mma_block(float (&acc)[NT][4], const MmaBlockLoa
     const int n = lane >> 2;
     const uint32_t r0[4] = {L.w0.x, L.w0.y, L.w0.z, L.w0.w};
     const uint32_t r1[4] = {L.w1.x, L.w1.y, L.w1.z, L.w1.w};
-    float cacc[NT][4];
+    // two independent accumulation chains (h = 0, 1), added at the end
+    float cacc[2][NT][4];
 #pragma unroll
-    for (int t = 0; t < NT; ++t)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cacc[t][i] = 0.f;
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cacc[h][t][i] = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         uint32_t bq[NT][4];
@@ -153,7 +218,7 @@ __device__ __forceinline__ void mma_block(float (&acc)[NT][4], const MmaBlockLoa
             const uint32_t a[4] = {a_lo0, a_lo1, a_hi0, a_hi1};
 #pragma unroll
             for (int t = 0; t < NT; ++t)
-                mma_bf16_16816(cacc[t], a, bq[t][2 * h], bq[t][2 * h + 1], cacc[t]);
+                mma_bf16_16816(cacc[h][t], a, bq[t][2 * h], bq[t][2 * h + 1], cacc[h][t]);
         }
     }
     const float s0 = __uint_as_float(L.sz0 << 16);
@@ -163,10 +228,10 @@ __device__ __forceinline__ void mma_block(float (&acc)[NT][4], const MmaBlockLoa
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const float2 xs2 = *reinterpret_cast<const float2*>(xsb + t * 8 + 2 * c);
-        acc[t][0] = fmaf(s0, fmaf(-o0, xs2.x, cacc[t][0]), acc[t][0]);
-        acc[t][1] = fmaf(s0, fmaf(-o0, xs2.y, cacc[t][1]), acc[t][1]);
-        acc[t][2] = fmaf(s1, fmaf(-o1, xs2.x, cacc[t][2]), acc[t][2]);
-        acc[t][3] = fmaf(s1, fmaf(-o1, xs2.y, cacc[t][3]), acc[t][3]);
+        acc[t][0] = fmaf(s0, fmaf(-o0, xs2.x, cacc[0][t][0] + cacc[1][t][0]), acc[t][0]);
+        acc[t][1] = fmaf(s0, fmaf(-o0, xs2.y, cacc[0][t][1] + cacc[1][t][1]), acc[t][1]);
+        acc[t][2] = fmaf(s1, fmaf(-o1, xs2.x, cacc[0][t][2] + cacc[1][t][2]), acc[t][2]);
+        acc[t][3] = fmaf(s1, fmaf(-o1, xs2.y, cacc[0][t][3] + cacc[1][t][3]), acc[t][3]);
     }
 }
 
