@@ -157,9 +157,13 @@ W4A16_API w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, i
 
 /*
  * w4a16_gemv_variant -- w4a16_gemv with the kernel forced (for measurement):
- * kernel_id 1 (CUDA-core, M <= 2) or 2 (warp-MMA, any M); k_split 0 =
- * automatic, else the K-split factor (a power of two, 1..32; warps of a CTA
- * first, then up to 8 CTAs of a cluster).  Same contract as w4a16_gemv.
+ * kernel_id 1 (CUDA-core, M <= 2), 2 (warp-MMA, any M, g % 128 == 0) or 3
+ * (tensor-core tcgen05, any M, g % 128 == 0); k_split 0 = automatic, else
+ * the K-split factor, a power of two: for kernels 1 and 2, 1..32 (warps of a
+ * CTA first, then up to 8 CTAs of a cluster); for kernel 3, 1..8 CTAs of a
+ * cluster.  A split the shape cannot use (a CTA's activation slice too large
+ * for shared memory, or a CTA left without K range) is
+ * W4A16_ERR_UNSUPPORTED.  Same contract as w4a16_gemv.
  */
 W4A16_API w4a16_status w4a16_gemv_variant(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
                                 const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,

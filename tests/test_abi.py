@@ -81,7 +81,10 @@ def test_gemv_validation_before_any_launch(lib):
     assert _gemv(lib, y=MIS) == Status.ERR_ALIGN
     assert _gemv(lib, M=3, K=128, g=64) == Status.ERR_UNSUPPORTED   # warp-MMA needs g % 128 == 0
     var = lib.w4a16_gemv_variant
-    assert var(A16, A16, A16, A16, A16, 0, 1, 64, 128, 128, 3, 0, None) == Status.ERR_UNSUPPORTED
+    assert var(A16, A16, A16, A16, A16, 0, 1, 64, 128, 128, 4, 0, None) == Status.ERR_UNSUPPORTED
+    # the tensor-core kernel needs g % 128 == 0 and splits K over at most 8 CTAs
+    assert var(A16, A16, A16, A16, A16, 0, 1, 64, 128, 64, 3, 0, None) == Status.ERR_UNSUPPORTED
+    assert var(A16, A16, A16, A16, A16, 0, 1, 64, 4096, 128, 3, 16, None) == Status.ERR_UNSUPPORTED
     assert var(A16, A16, A16, A16, A16, 0, 3, 64, 128, 128, 1, 0, None) == Status.ERR_UNSUPPORTED
     assert lib.w4a16_gemv_ex(A16, A16, A16, A16, A16, 0, 1, 64, 128, 128, 2, None) == Status.ERR_UNSUPPORTED
 

@@ -84,15 +84,17 @@ w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, in
     // finer than the warp-MMA kernel's 128-k blocks; warp MMA otherwise
     if (kernel_id == 0) kernel_id = (M == 1 || (M == 2 && g % 128 != 0)) ? 1 : 2;
     if (kernel_id == 1 && M > 2) return W4A16_ERR_UNSUPPORTED;
-    if (kernel_id == 2 && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
-    if (kernel_id != 1 && kernel_id != 2) return W4A16_ERR_UNSUPPORTED;
+    if ((kernel_id == 2 || kernel_id == 3) && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id < 1 || kernel_id > 3) return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id == 3 && k_split > 8) return W4A16_ERR_UNSUPPORTED;
     if (k_split < 0 || k_split > 32 || (k_split & (k_split - 1))) return W4A16_ERR_UNSUPPORTED;
     w4a16_status st = current_device(dev);
     if (st != W4A16_OK) return st;
     const int n = static_cast<int>(N), k = static_cast<int>(K);
     const int gg = static_cast<int>(g);
-    *plan = (kernel_id == 1) ? plan_gemv_simt((*dev)->info, M, n, k, gg, k_split)
-                             : plan_gemv_mma((*dev)->info, M, n, k, gg, k_split);
+    *plan = (kernel_id == 1)   ? plan_gemv_simt((*dev)->info, M, n, k, gg, k_split)
+            : (kernel_id == 2) ? plan_gemv_mma((*dev)->info, M, n, k, gg, k_split)
+                               : plan_gemv_tc((*dev)->info, M, n, k, gg, k_split);
     if (plan->ctas < 1 || plan->smem_bytes > (*dev)->info.max_smem_optin)
         return W4A16_ERR_UNSUPPORTED;
     return W4A16_OK;
@@ -117,8 +119,9 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
                static_cast<int>(N), static_cast<int>(K), static_cast<int>(g), dev->err,
                (flags & W4A16_FLAG_WEIGHTS_STATIC) ? 1 : 0};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return from_cuda(plan.kernel_id == 1 ? launch_gemv_simt(a, plan, s)
-                                         : launch_gemv_mma(a, plan, s));
+    return from_cuda(plan.kernel_id == 1   ? launch_gemv_simt(a, plan, s)
+                     : plan.kernel_id == 2 ? launch_gemv_mma(a, plan, s)
+                                           : launch_gemv_tc(a, plan, s));
 }
 
 }  // namespace
@@ -241,7 +244,7 @@ w4a16_status w4a16_gemv_variant(const uint16_t* x, const uint32_t* wq, const uin
                                 const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,
                                 int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
                                 void* stream) {
-    if (kernel_id != 1 && kernel_id != 2) return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id < 1 || kernel_id > 3) return W4A16_ERR_UNSUPPORTED;
     return gemv_impl(x, wq, scale, zero, y, out_dtype, M, N, K, g, kernel_id, k_split, 0u,
                      stream);
 }

@@ -23,12 +23,21 @@ __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
+// Output element idx of y: fp32, or bf16 rounded to nearest even.
+__device__ __forceinline__ void store_out(void* y, int out_f32, size_t idx, float v) {
+    if (out_f32) static_cast<float*>(y)[idx] = v;
+    else static_cast<uint16_t*>(y)[idx] = f32_to_bf16_rn(v);
+}
 // exact power of two 2^e for a normal exponent e in [-126, 127]
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 
 // ---------------------------------------------------------------------------
 // Global loads
 // ---------------------------------------------------------------------------
+// Bring the line holding p into L1 (a hint; no register is written).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 // Streamed, read-once data (packed weights): bypass L1 allocation.
 __device__ __forceinline__ uint4 ldg_stream_u4(const uint4* p) {
     uint4 v;
@@ -65,6 +74,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
                  : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;
@@ -131,6 +143,10 @@ __device__ __forceinline__ void cp_async_8(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
                  : "memory");
+}
+// Wait until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))

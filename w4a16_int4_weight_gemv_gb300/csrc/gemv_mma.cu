@@ -42,7 +42,8 @@ constexpr int kStageA = 2 * kHalfBytes;
 constexpr int kStageSZ = 256;    // 16 rows x 4 zero points, then 16 rows x 4 scales
 constexpr int kSZScales = 64;
 constexpr int kMaxStages = 8;
-static_assert(kWeightBoxWords * 4 * kWeightBoxRows == kHalfBytes, "box geometry");
+constexpr unsigned kBoxRows = 16;
+static_assert(kWeightBoxWords * 4 * kBoxRows == kHalfBytes, "box geometry");
 
 struct MmaKernelArgs {
     const uint16_t* x;
@@ -405,7 +406,7 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s
     k.weights_static = a.weights_static;
     k.err = a.err;
     CUtensorMap wmap;
-    if (!encode_weight_map(&wmap, a.wq, a.N, a.K)) return cudaErrorInvalidValue;
+    if (!encode_weight_map(&wmap, a.wq, a.N, a.K, kBoxRows)) return cudaErrorInvalidValue;
     MmaKernel kern = pick_mma_kernel(a.M, a.K, a.g);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          p.smem_bytes);

@@ -9,13 +9,12 @@
 
 namespace w4a16 {
 
-// Box of the packed-weight tensor map used by the warp-MMA kernel: 32 words
-// (128 bytes, 256 k) x 16 rows, 128-byte swizzle.
+// Boxes of the packed-weight tensor maps: 32 words (128 bytes, 256 k) x
+// box_rows rows, 128-byte swizzle.
 constexpr unsigned kWeightBoxWords = 32;
-constexpr unsigned kWeightBoxRows = 16;
 
 // Tensor map of a packed weight matrix [N][K/8] words (host; false on failure).
-bool encode_weight_map(CUtensorMap* map, const void* wq, int N, int K);
+bool encode_weight_map(CUtensorMap* map, const void* wq, int N, int K, unsigned box_rows);
 
 struct GemvArgs {
     const uint16_t* x;
@@ -33,7 +32,7 @@ struct GemvArgs {
 };
 
 struct GemvPlan {
-    int kernel_id;  // 1 = CUDA-core M=1 kernel, 2 = warp-MMA kernel
+    int kernel_id;  // 1 = CUDA-core kernel, 2 = warp-MMA kernel, 3 = tensor-core (tcgen05) kernel
     int ctas;
     int threads;
     int k_split;     // cluster size along K (1 = no split)
@@ -110,9 +109,11 @@ int max_active_clusters(const void* kernel, int threads, int smem, int S);
 // Launch-shape choices (host arithmetic plus cached occupancy queries).
 GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
 GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
+GemvPlan plan_gemv_tc(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
 
 cudaError_t launch_gemv_simt(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
+cudaError_t launch_gemv_tc(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 
 struct MoeArgs {
     const uint16_t* x;

@@ -235,9 +235,5 @@ __device__ __forceinline__ void mma_block(float (&acc)[NT][4], const MmaBlockLoa
     }
 }
 
-__device__ __forceinline__ void store_out(void* y, int out_f32, size_t idx, float v) {
-    if (out_f32) static_cast<float*>(y)[idx] = v;
-    else static_cast<uint16_t*>(y)[idx] = f32_to_bf16_rn(v);
-}
 
 }  // namespace w4a16

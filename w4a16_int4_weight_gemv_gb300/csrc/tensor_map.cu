@@ -1,11 +1,12 @@
 // Host side: tensor maps (TMA descriptors) of the packed weight matrix.
 //
 // The packed weights are a row-major [N][K/8] matrix of 32-bit words (eight
-// 4-bit codes each, K contiguous).  A warp-MMA step reads a 16-row x 512-k
-// tile of it: two boxes of 16 rows x 32 words (128 bytes per row), each
-// written to shared memory in the 128-byte swizzled layout (16-byte chunk j
-// of row r lands at chunk j ^ (r % 8)), so that the eight rows an ldmatrix
-// phase reads fall in eight different bank groups.
+// 4-bit codes each, K contiguous).  A box is box_rows rows x 32 words (128
+// bytes, 256 k per row), written to shared memory in the 128-byte swizzled
+// layout (16-byte chunk j of row r lands at chunk j ^ (r % 8)), so that eight
+// consecutive rows reading the same logical chunk hit eight different bank
+// groups.  The warp-MMA kernel loads 16-row boxes, the tensor-core kernel
+// 128-row boxes.
 //
 // cuTensorMapEncodeTiled is a driver function; it is looked up once through
 // the runtime's entry-point query, so the library links no driver library.
@@ -42,12 +43,12 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-bool encode_weight_map(CUtensorMap* map, const void* wq, int N, int K) {
+bool encode_weight_map(CUtensorMap* map, const void* wq, int N, int K, unsigned box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};  // bytes between rows
-    const cuuint32_t box[2] = {kWeightBoxWords, kWeightBoxRows};
+    const cuuint32_t box[2] = {kWeightBoxWords, box_rows};
     const cuuint32_t elem_strides[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(wq), dims, strides, box,
               elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
