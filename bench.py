@@ -157,15 +157,24 @@ def _dev(a, torch):
     return torch.from_numpy(a).cuda()
 
 
-def make_rotation(torch, M, N, K, g, zmode, l2_bytes, seed=0, min_copies=2, out_dtype=None):
-    """Enough independent copies of one problem that their total is > 2x L2."""
+def make_rotation(torch, M, N, K, g, zmode, l2_bytes, seed=0, min_copies=2, out_dtype=None,
+                  x_shared=True):
+    """Enough independent copies of one problem's weights (packed codes,
+    scales, zero points) that their total is > 2x L2, so every step streams
+    its weights from HBM.  With x_shared the activations are one tensor for
+    all steps: a few KB that stay L2-resident, as they are in a decode step
+    where the preceding op has just written them.  Without it every copy has
+    its own x, which is then cold too."""
     per = all_bytes(M, N, K, g)
     R = max(min_copies, int(math.ceil(2.0 * l2_bytes / per)))
     copies = []
     for r in range(R):
         from w4a16_int4_weight_gemv_gb300 import synth
         p = synth.dense_problem(M, N, K, g, zmode, seed=seed, sub=r)
-        copies.append(tuple(_dev(p[k], torch) for k in ("x", "wq", "scale", "zero")))
+        c = tuple(_dev(p[k], torch) for k in ("x", "wq", "scale", "zero"))
+        if x_shared and copies:
+            c = (copies[0][0],) + c[1:]
+        copies.append(c)
     outs = [torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device="cuda") for _ in range(R)]
     return copies, outs
 
@@ -207,8 +216,9 @@ def time_steps(torch, fn, R, steps, warmup):
 
 
 def gpu_gemv_gbs(torch, w, M, N, K, g, zmode, l2, steps, warmup, out_dtype=None, kernel_id=0,
-                 weights_static=False):
-    copies, outs = make_rotation(torch, M, N, K, g, zmode, l2, out_dtype=out_dtype)
+                 weights_static=False, x_shared=True):
+    copies, outs = make_rotation(torch, M, N, K, g, zmode, l2, out_dtype=out_dtype,
+                                 x_shared=x_shared)
     R = len(copies)
 
     def step(i):
@@ -422,6 +432,9 @@ def run_gpu(args):
                          weights_static=True)
         sweep["square_M1_weights_static"] = {"us": round(t * 1e6, 3),
                                              "GB/s": round(bytes_step / t / 1e9, 1)}
+        t = gpu_gemv_gbs(torch, w, 1, 4096, 4096, 128, "const8", l2, 2000, 100, x_shared=False)
+        sweep["square_M1_x_cold"] = {"us": round(t * 1e6, 3), "GB/s": round(bytes_step / t / 1e9, 1),
+                                     "note": "activations rotated with the weights (HBM-cold x)"}
         for name, (n_, k_) in (("up", (14336, 4096)), ("down", (4096, 14336))):
             t = gpu_gemv_gbs(torch, w, 2, n_, k_, 128, "uniform6to10", l2, sw_steps, sw_warm,
                              kernel_id=1)
@@ -445,7 +458,10 @@ def run_gpu(args):
             "dtype": "w4a16: int4 weights, bf16 activations/outputs, fp32 accumulate",
             "data": "synthetic (seeded: x~N(0,1) bf16, uniform 4-bit codes, scales~U[0.005,0.02], zero=8)",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "g": g,
-                       "l2_policy": "inputs larger than L2: %d rotating weight copies, %.0f MB total"
+                       "l2_policy": "inputs larger than L2: %d rotating weight copies (codes, "
+                                    "scales, zeros), %.0f MB total; the 8 KB activation vector "
+                                    "is shared by all steps (L2-resident, as written by the "
+                                    "preceding op; HBM-cold x: sweep.square_M1_x_cold)"
                                     % (R, R * all_bytes(M, N, K, g) / 1e6),
                        "launch": "CUDA graph of %d w4a16_gemv launches, replayed" % R,
                        "plan": plan, "parallelism": "replicas" if world > 1 else "single GPU"},

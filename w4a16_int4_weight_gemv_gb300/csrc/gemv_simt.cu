@@ -16,11 +16,12 @@
 // (word & (0xF << p)) read as a binary32 is code * 2^(p - 149) (a subnormal,
 // or for p = 20 and code >= 8 one of the smallest normals, whose value is
 // still the integer pattern times 2^-149).  Multiplying it by x * 2^(85 - p)
-// gives code * x * 2^-64 exactly, so a weight costs one LOP3 and one FFMA per
-// token, plus one shift per word that brings the top two nibbles down by 8
-// bits.  The integer ALU pipe issues LOP3 at half the FFMA rate, so this mask
-// is the per-weight cost that bounds the kernel; everything else is kept off
-// that pipe or amortised over a span of rows.  The 2^(85 - p) factors are
+// gives code * x * 2^-64 exactly, so a weight costs one LOP3 and half a packed
+// FFMA (fma.rn.f32x2 multiplies two codes by their two x' at once) per token,
+// plus one shift per word that brings the top two nibbles down by 8 bits.
+// The kernel is issue-bound: everything other than the masks and the packed
+// FMAs is kept off the issue ports as far as possible or amortised over a span
+// of rows.  The 2^(85 - p) factors are
 // folded into the staged activations and the 2^64 is restored on the output.
 // The FMAs keep subnormal operands (the library is built without
 // flush-to-zero); the exact product of a bf16 x and a 4-bit code stays normal
@@ -41,11 +42,12 @@
 // CTAs of a thread-block cluster (added through distributed shared memory,
 // once per kernel), always in a fixed order, so results are deterministic.
 //
-// Activations.  The CTA's K slice of x is read once with 16-byte loads,
-// scaled per nibble position into fp32 x' and stored in shared memory
-// lane-major ([span][piece][lane][4 floats]) so that a warp's 16-byte reads of
-// one piece are consecutive (conflict-free) at immediate offsets; per-chunk
-// sums are reduced with warp shuffles in the same pass.
+// Activations.  The CTA's K slice of x is read once with 16-byte loads --
+// issued before any weight copy, so they are not queued behind the weight
+// stream -- scaled per nibble position into fp32 x' and stored in shared
+// memory lane-major ([span][piece][lane][4 floats]) so that a warp's 16-byte
+// reads of one piece are consecutive (conflict-free) at immediate offsets;
+// per-chunk sums are reduced with warp shuffles in the same pass.
 //
 // Launch.  Kernels are launched with programmatic stream serialisation: the
 // next launch on the stream may start its CTAs as this grid drains, and every
@@ -101,49 +103,30 @@ __device__ __forceinline__ float position_factor(int i) {
     return exp2i(85 - p);
 }
 
-// acc += sum over the 16 codes of two words of code * x'.  The shift by 8
-// is a high multiply, which issues on the FMA pipe instead of the ALU pipe.
+// acc += sum over the 16 codes of two words of code * x'.  The products of
+// codes (k, k+1) go through one packed fp32 FMA (fma.rn.f32x2: two IEEE fmas
+// per instruction, subnormal operands kept), so a word costs 8 masks, 4 packed
+// FMAs and one shift.  The shift by 8 is a high multiply, which issues on the
+// FMA pipe instead of the ALU pipe.
 __device__ __forceinline__ void dot_words(float& a0, float& a1, uint32_t v0, uint32_t v1,
                                           const float* xr) {
     const uint32_t vs[2] = {v0, v1};
+    float2 acc = make_float2(a0, a1);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const uint32_t v = vs[j];
         const uint32_t t = __umulhi(v, 0x01000000u);  // v >> 8
-        a0 = fmaf(__uint_as_float(v & 0x0000000Fu), xr[8 * j + 0], a0);
-        a1 = fmaf(__uint_as_float(v & 0x000000F0u), xr[8 * j + 1], a1);
-        a0 = fmaf(__uint_as_float(v & 0x00000F00u), xr[8 * j + 2], a0);
-        a1 = fmaf(__uint_as_float(v & 0x0000F000u), xr[8 * j + 3], a1);
-        a0 = fmaf(__uint_as_float(v & 0x000F0000u), xr[8 * j + 4], a0);
-        a1 = fmaf(__uint_as_float(v & 0x00F00000u), xr[8 * j + 5], a1);
-        a0 = fmaf(__uint_as_float(t & 0x000F0000u), xr[8 * j + 6], a0);
-        a1 = fmaf(__uint_as_float(t & 0x00F00000u), xr[8 * j + 7], a1);
+        acc = __ffma2_rn(make_float2(__uint_as_float(v & 0x0000000Fu), __uint_as_float(v & 0x000000F0u)),
+                         make_float2(xr[8 * j + 0], xr[8 * j + 1]), acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(v & 0x00000F00u), __uint_as_float(v & 0x0000F000u)),
+                         make_float2(xr[8 * j + 2], xr[8 * j + 3]), acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(v & 0x000F0000u), __uint_as_float(v & 0x00F00000u)),
+                         make_float2(xr[8 * j + 4], xr[8 * j + 5]), acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(t & 0x000F0000u), __uint_as_float(t & 0x00F00000u)),
+                         make_float2(xr[8 * j + 6], xr[8 * j + 7]), acc);
     }
-}
-
-// Same sum with packed fp32 pairs: two products per fma.rn.f32x2.
-__device__ __forceinline__ void ffma2(float2& acc, uint32_t a0, uint32_t a1, float x0, float x1) {
-    asm("{\n\t.reg .b64 ra, rx, rc;\n\t"
-        "mov.b64 ra, {%2, %3};\n\t"
-        "mov.b64 rx, {%4, %5};\n\t"
-        "mov.b64 rc, {%0, %1};\n\t"
-        "fma.rn.f32x2 rc, ra, rx, rc;\n\t"
-        "mov.b64 {%0, %1}, rc;\n\t}"
-        : "+f"(acc.x), "+f"(acc.y)
-        : "r"(a0), "r"(a1), "f"(x0), "f"(x1));
-}
-__device__ __forceinline__ void dot_words2(float2& a, float2& b, uint32_t v0, uint32_t v1,
-                                           const float* xr) {
-    const uint32_t vs[2] = {v0, v1};
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const uint32_t v = vs[j];
-        const uint32_t t = __umulhi(v, 0x01000000u);  // v >> 8
-        ffma2(a, v & 0x0000000Fu, v & 0x000000F0u, xr[8 * j + 0], xr[8 * j + 1]);
-        ffma2(b, v & 0x00000F00u, v & 0x0000F000u, xr[8 * j + 2], xr[8 * j + 3]);
-        ffma2(a, v & 0x000F0000u, v & 0x00F00000u, xr[8 * j + 4], xr[8 * j + 5]);
-        ffma2(b, t & 0x000F0000u, t & 0x00F00000u, xr[8 * j + 6], xr[8 * j + 7]);
-    }
+    a0 = acc.x;
+    a1 = acc.y;
 }
 
 __device__ __forceinline__ void store_y(void* y, int out_f32, size_t i, float v) {
