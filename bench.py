@@ -231,7 +231,7 @@ def gpu_gemv_gbs(torch, w, M, N, K, g, zmode, l2, steps, warmup, out_dtype=None,
     return t
 
 
-def moe_chain_time(torch, w, M, steps, warmup, l2):
+def moe_chain_time(torch, w, M, steps, warmup, l2, fused=True):
     """Routed SwiGLU expert chain (64 experts, gate/up [1024, 2304], down
     [2304, 1024], top-8) over rotated expert banks; seconds per chain and
     the distinct-expert weight bytes it streams."""
@@ -253,7 +253,7 @@ def moe_chain_time(torch, w, M, steps, warmup, l2):
 
     def step(i):
         b = banks[i % R]
-        w.moe_ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128)
+        w.moe_ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128, fused=fused)
 
     t = time_steps(torch, step, R, steps, warmup)
     return t, float(np.mean(byts))
@@ -445,6 +445,9 @@ def run_gpu(args):
             sweep["moe_chain_M%d" % m] = {"us": round(t * 1e6, 3), "GB/s": round(byts / t / 1e9, 1),
                                           "frac_measured_peak": round(byts / t / 1e9 / peak, 4),
                                           "tokens_per_s": round(m / t, 1)}
+        t, byts = moe_chain_time(torch, w, 1, 200, 20, l2, fused=False)
+        sweep["moe_chain_M1_unfused"] = {"us": round(t * 1e6, 3), "GB/s": round(byts / t / 1e9, 1),
+                                         "note": "gate GEMV, up GEMV, SwiGLU, down GEMV + routed sum as separate calls"}
         extra["sweep"] = sweep
         extra["e2e"] = e2e_gbs(torch, w, M, N, K, g, min(args.steps, 3000))
         if not args.no_cpu_baseline:

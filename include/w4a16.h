@@ -227,6 +227,42 @@ W4A16_API w4a16_status w4a16_moe_gemv_fixed_scratch(const uint16_t* x, int x_per
                                                     int64_t g, void* stream);
 
 /*
+ * w4a16_moe_ffn_workspace_bytes -- workspace w4a16_moe_ffn needs: bf16 gate
+ * and up outputs [M][topk][F] and fp32 partials [M][topk][H], each rounded
+ * up to 256 bytes.
+ */
+W4A16_API size_t w4a16_moe_ffn_workspace_bytes(int M, int topk, int64_t H, int64_t F);
+
+/*
+ * w4a16_moe_ffn -- the routed SwiGLU expert FFN of M tokens (README
+ * technical-detail section: the grouped expert kernel; its kernel registry
+ * names the SwiGLU op), in three launches:
+ *   1. gate and up products of every routed slot, both banks in one launch:
+ *        G[t][j] = bf16(W^gate_e x[t]),  U[t][j] = bf16(W^up_e x[t]),
+ *   2. down products of h[t][j] = bf16(silu(G[t][j]) * U[t][j]) (computed in
+ *      fp32 exactly as w4a16_swiglu does, while staging the activations),
+ *   3. y[t] = bf16(sum_j route_w[t][j] * (W^down_e h[t][j])) (fp32 sum, j
+ *      ascending).
+ * Each distinct expert's three matrices are streamed once per call.
+ *   x: bf16 [M][H]; expert_ids: int32 [M][topk]; route_w: fp32 [M][topk];
+ *   gate, up: wq [E][F][H/8], scale and zero [E][F][H/g];
+ *   down: wq [E][H][F/8], scale and zero [E][H][F/g]; y: bf16 [M][H];
+ *   workspace: >= w4a16_moe_ffn_workspace_bytes(M, topk, H, F) bytes,
+ *   caller-owned, 16-byte aligned (W4A16_ERR_WORKSPACE if smaller).
+ * Limits: M*topk <= 256, g % 128 == 0, H and F multiples of g.  Expert ids
+ * outside [0, E) are skipped and flagged with W4A16_DEVERR_EXPERT_ID.
+ */
+W4A16_API w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids,
+                                     const float* route_w, const uint32_t* gate_wq,
+                                     const uint16_t* gate_scale, const uint8_t* gate_zero,
+                                     const uint32_t* up_wq, const uint16_t* up_scale,
+                                     const uint8_t* up_zero, const uint32_t* down_wq,
+                                     const uint16_t* down_scale, const uint8_t* down_zero,
+                                     uint16_t* y, int M, int topk, int E, int64_t H, int64_t F,
+                                     int64_t g, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
  * w4a16_swiglu -- h[r][n] = bf16(silu(gate[r][n]) * up[r][n]), computed in
  * fp32, silu(v) = v / (1 + e^-v).  The activation between the gate/up and
  * down expert products (the README's kernel registry names a SwiGLU op).

@@ -126,6 +126,18 @@ def test_other_entry_points_validate(lib):
     assert moe(A16, 0, A16, A16, A16, A16, A16, A16, 1, 8, 64, 1024, 2304, 128, A16, need - 4,
                None) == Status.ERR_WORKSPACE
     assert lib.w4a16_moe_workspace_bytes(1, 8, 1024, 0) == 0
+    # fused FFN: 13 pointers, then M, topk, E, H, F, g, workspace, bytes, stream
+    ffn = lib.w4a16_moe_ffn
+    ptrs = [A16] * 13
+    assert ffn(*([None] + ptrs[1:]), 1, 8, 64, 2304, 1024, 128, A16, 1 << 20, None) == Status.ERR_NULL
+    assert ffn(*ptrs, 1, 8, 64, 2304, 1000, 128, A16, 1 << 20, None) == Status.ERR_SHAPE   # F % g
+    assert ffn(*ptrs, 64, 8, 64, 2304, 1024, 128, A16, 1 << 20, None) == Status.ERR_UNSUPPORTED
+    assert ffn(*ptrs, 1, 8, 64, 2304, 1024, 64, A16, 1 << 20, None) == Status.ERR_UNSUPPORTED
+    fneed = lib.w4a16_moe_ffn_workspace_bytes(1, 8, 2304, 1024)
+    assert fneed == 2 * 8 * 1024 * 2 + 8 * 2304 * 4      # already 256-byte multiples
+    assert ffn(*ptrs, 1, 8, 64, 2304, 1024, 128, A16, fneed - 16, None) == Status.ERR_WORKSPACE
+    assert ffn(*ptrs, 1, 8, 64, 2304, 1024, 128, None, fneed, None) == Status.ERR_WORKSPACE
+    assert ffn(*ptrs[:-1], MIS, 1, 8, 64, 2304, 1024, 128, A16, fneed, None) == Status.ERR_ALIGN
     assert lib.w4a16_gemv_workspace_bytes(1, 4096, 4096, 128) == 0
     assert lib.w4a16_device_error(None, 0, None) == Status.ERR_NULL
 

@@ -400,3 +400,33 @@ def test_moe_ffn_chain_full_config(w, oracle, M):
     torch.cuda.synchronize()
     ref = oracle.moe_ffn(p["x"], p["ids"], p["route_w"], p["gate"], p["up"], p["down"], 128)
     check_close(host_f64(out), ref["out"], "moe ffn M=%d" % M)
+    # the fused chain (gate+up in one launch, SwiGLU formed while staging the
+    # down product's activations) runs the same arithmetic as the chain of
+    # single-purpose calls: bit-equal
+    chained = w.moe_ffn(dev(p["x"]), dev(p["ids"]), dev(p["route_w"]), _bank_dev(p["gate"]),
+                        _bank_dev(p["up"]), _bank_dev(p["down"]), 128, fused=False)
+    torch.cuda.synchronize()
+    assert torch.equal(out, chained)
+    assert w.w4a16_device_error(clear=True) == 0
+
+
+def test_moe_ffn_bad_ids_and_shared_experts(w, oracle):
+    # 6 tokens: one expert shared by every token, one invalid id (skipped,
+    # flagged); the fused chain still matches the oracle on the valid slots
+    p = synth.moe_problem(M=6, E=64, H=2304, F=1024, topk=8, g=128, seed=3)
+    ids = p["ids"].copy()
+    ids[:, 0] = 5
+    ids[2, 3] = 64
+    p["ids"] = ids
+    w.w4a16_device_error(clear=True)
+    out = w.moe_ffn(dev(p["x"]), dev(ids), dev(p["route_w"]), _bank_dev(p["gate"]),
+                    _bank_dev(p["up"]), _bank_dev(p["down"]), 128)
+    torch.cuda.synchronize()
+    assert w.w4a16_device_error(clear=True) & w.DEVERR_EXPERT_ID
+    # the skipped slot contributes nothing: same as a valid id with weight 0
+    ref_ids = ids.copy()
+    ref_rw = p["route_w"].copy()
+    ref_ids[2, 3] = 0
+    ref_rw[2, 3] = 0.0
+    ref = oracle.moe_ffn(p["x"], ref_ids, ref_rw, p["gate"], p["up"], p["down"], 128)
+    check_close(host_f64(out), ref["out"], "moe ffn shared/bad ids")

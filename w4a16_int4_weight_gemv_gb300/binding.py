@@ -84,6 +84,10 @@ def load_library():
     lib.w4a16_moe_gemv.restype = I32
     lib.w4a16_moe_gemv.argtypes = [P, I32, P, P, P, P, P, P, I32, I32, I32, I64, I64, I64,
                                    P, SZ, P]
+    lib.w4a16_moe_ffn_workspace_bytes.restype = SZ
+    lib.w4a16_moe_ffn_workspace_bytes.argtypes = [I32, I32, I64, I64]
+    lib.w4a16_moe_ffn.restype = I32
+    lib.w4a16_moe_ffn.argtypes = [P] * 13 + [I32, I32, I32, I64, I64, I64, P, SZ, P]
     lib.w4a16_swiglu.restype = I32
     lib.w4a16_swiglu.argtypes = [P, P, I64, P, I64, I64, I64, P]
     lib.w4a16_device_error.restype = I32
@@ -273,12 +277,33 @@ def w4a16_device_error(clear: bool = True, stream=None) -> int:
     return int(bits.value)
 
 
-def moe_ffn(x, expert_ids, route_w, gate, up, down, g: int, stream=None) -> torch.Tensor:
-    """Routed SwiGLU FFN for M tokens: gate/up products of every routed slot
-    in one expert-indexed call each, SwiGLU, then the down products with the
-    route-weighted sum.  gate/up/down are (wq, scale, zero) triples with
-    gate/up [E, F, H] and down [E, H, F].  Returns bf16 [M, H]."""
+def moe_ffn(x, expert_ids, route_w, gate, up, down, g: int, stream=None,
+            fused: bool = True) -> torch.Tensor:
+    """Routed SwiGLU FFN for M tokens.  gate/up/down are (wq, scale, zero)
+    triples with gate/up [E, F, H] and down [E, H, F].  Returns bf16 [M, H].
+
+    fused (default): w4a16_moe_ffn -- gate and up in one launch, SwiGLU formed
+    while the down product stages its activations, then the routed sum.
+    fused=False: the same chain from the single-purpose calls (one
+    expert-indexed GEMV each for gate and up, w4a16_swiglu, the down GEMV
+    with the routed sum)."""
     M, topk = expert_ids.shape
+    if fused:
+        _need(x, "x", _BF16)
+        _need(expert_ids, "expert_ids", (torch.int32,))
+        _need(route_w, "route_w", (torch.float32,), (M, topk))
+        (gw, gs, gz), (uw, us, uz), (dw, ds, dz) = gate, up, down
+        E, F, H8 = gw.shape
+        H = H8 * 8
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+        lib = load_library()
+        nbytes = int(lib.w4a16_moe_ffn_workspace_bytes(M, topk, H, F))
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+        _check(lib.w4a16_moe_ffn(_ptr(x), _ptr(expert_ids), _ptr(route_w), _ptr(gw), _ptr(gs),
+                                 _ptr(gz), _ptr(uw), _ptr(us), _ptr(uz), _ptr(dw), _ptr(ds),
+                                 _ptr(dz), _ptr(y), M, topk, E, H, F, g, _ptr(ws), nbytes,
+                                 _stream(stream)), "w4a16_moe_ffn")
+        return y
     g_out = w4a16_moe_gemv(x, expert_ids, *gate, g, stream=stream)
     u_out = w4a16_moe_gemv(x, expert_ids, *up, g, stream=stream)
     F = g_out.shape[-1]

@@ -277,7 +277,7 @@ w4a16_status w4a16_moe_gemv(const uint16_t* x, int x_per_slot, const int32_t* ex
                             int64_t K, int64_t g, void* workspace, size_t workspace_bytes,
                             void* stream) {
     if (!x || !expert_ids || !wq || !scale || !zero || !y) return W4A16_ERR_NULL;
-    if (M < 1 || topk < 1 || E < 1 || N < 1 || K < 128 || g < 128) return W4A16_ERR_SHAPE;
+    if (M < 1 || topk < 1 || E < 1 || N < 1 || K < 32 || g < 32) return W4A16_ERR_SHAPE;
     if (K % 32 != 0 || g % 32 != 0 || K % g != 0) return W4A16_ERR_SHAPE;
     if (g % 128 != 0 || M * topk > 256 || K > 65536) return W4A16_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(E) * N > (int64_t(1) << 31) / (K / 8) - 1)
@@ -290,17 +290,112 @@ w4a16_status w4a16_moe_gemv(const uint16_t* x, int x_per_slot, const int32_t* ex
         if (!workspace || workspace_bytes < need) return W4A16_ERR_WORKSPACE;
         if (!aligned16(workspace)) return W4A16_ERR_ALIGN;
     }
-    // the whole activation set of one expert pass must fit in shared memory
-    const int nblk = static_cast<int>(K / 128);
     DeviceCache* dev = nullptr;
     w4a16_status st = current_device(&dev);
     if (st != W4A16_OK) return st;
-    const int need_smem = 16 * (nblk * 256 + 64) + nblk * 16 * 4 + 4096;
-    if (need_smem > dev->info.max_smem_optin) return W4A16_ERR_UNSUPPORTED;
-    MoeArgs a{x, x_per_slot ? 1 : 0, expert_ids, route_w, wq, scale, zero, y,
-              static_cast<float*>(workspace), M, topk, E, static_cast<int>(N), static_cast<int>(K),
-              static_cast<int>(g), dev->err};
+    // the whole activation set of one expert pass must fit in shared memory
+    if (moe_smem_need(M, static_cast<int>(K), static_cast<int>(g)) > dev->info.max_smem_optin)
+        return W4A16_ERR_UNSUPPORTED;
+    MoeArgs a{};
+    a.x = x;
+    a.x_per_slot = x_per_slot ? 1 : 0;
+    a.ids = expert_ids;
+    a.route_w = route_w;
+    a.bank[0] = MoeBank{wq, scale, zero, route_w ? nullptr : y};
+    a.nbanks = 1;
+    a.y_routed = route_w ? y : nullptr;
+    a.ws = static_cast<float*>(workspace);
+    a.M = M;
+    a.topk = topk;
+    a.E = E;
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.g = static_cast<int>(g);
+    a.err = dev->err;
     return from_cuda(launch_moe(a, dev->info, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+}  // namespace
+
+size_t w4a16_moe_ffn_workspace_bytes(int M, int topk, int64_t H, int64_t F) {
+    if (M < 1 || topk < 1 || H < 1 || F < 1) return 0;
+    const size_t S = static_cast<size_t>(M) * static_cast<size_t>(topk);
+    return 2 * align256(S * static_cast<size_t>(F) * 2) + align256(S * static_cast<size_t>(H) * 4);
+}
+
+w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const float* route_w,
+                           const uint32_t* gate_wq, const uint16_t* gate_scale,
+                           const uint8_t* gate_zero, const uint32_t* up_wq,
+                           const uint16_t* up_scale, const uint8_t* up_zero,
+                           const uint32_t* down_wq, const uint16_t* down_scale,
+                           const uint8_t* down_zero, uint16_t* y, int M, int topk, int E,
+                           int64_t H, int64_t F, int64_t g, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    if (!x || !expert_ids || !route_w || !gate_wq || !gate_scale || !gate_zero || !up_wq ||
+        !up_scale || !up_zero || !down_wq || !down_scale || !down_zero || !y)
+        return W4A16_ERR_NULL;
+    if (M < 1 || topk < 1 || E < 1 || H < 32 || F < 32 || g < 32) return W4A16_ERR_SHAPE;
+    if (g % 32 != 0 || H % g != 0 || F % g != 0) return W4A16_ERR_SHAPE;
+    if (g % 128 != 0 || M * topk > 256 || H > 65536 || F > 65536) return W4A16_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(E) * F > (int64_t(1) << 31) / (H / 8) - 1 ||
+        static_cast<int64_t>(E) * H > (int64_t(1) << 31) / (F / 8) - 1)
+        return W4A16_ERR_UNSUPPORTED;
+    const void* ptrs[] = {x,      expert_ids, route_w,  gate_wq,    gate_scale, gate_zero, up_wq,
+                          up_scale, up_zero,  down_wq, down_scale, down_zero,  y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return W4A16_ERR_ALIGN;
+    const size_t need = w4a16_moe_ffn_workspace_bytes(M, topk, H, F);
+    if (!workspace || workspace_bytes < need) return W4A16_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return W4A16_ERR_ALIGN;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    if (moe_smem_need(M, static_cast<int>(H), static_cast<int>(g)) > dev->info.max_smem_optin ||
+        moe_smem_need(M, static_cast<int>(F), static_cast<int>(g)) > dev->info.max_smem_optin)
+        return W4A16_ERR_UNSUPPORTED;
+    const size_t S = static_cast<size_t>(M) * static_cast<size_t>(topk);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    uint16_t* g_out = reinterpret_cast<uint16_t*>(ws);
+    uint16_t* u_out = reinterpret_cast<uint16_t*>(ws + align256(S * F * 2));
+    float* part = reinterpret_cast<float*>(ws + 2 * align256(S * F * 2));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // gate and up products of every slot: one launch over both banks
+    MoeArgs a{};
+    a.x = x;
+    a.ids = expert_ids;
+    a.bank[0] = MoeBank{gate_wq, gate_scale, gate_zero, g_out};
+    a.bank[1] = MoeBank{up_wq, up_scale, up_zero, u_out};
+    a.nbanks = 2;
+    a.M = M;
+    a.topk = topk;
+    a.E = E;
+    a.N = static_cast<int>(F);
+    a.K = static_cast<int>(H);
+    a.g = static_cast<int>(g);
+    a.err = dev->err;
+    cudaError_t e = launch_moe(a, dev->info, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    // down products of h = silu(gate) * up (formed while staging) and the routed sum
+    MoeArgs d{};
+    d.sw_gate = g_out;
+    d.sw_up = u_out;
+    d.ids = expert_ids;
+    d.route_w = route_w;
+    d.bank[0] = MoeBank{down_wq, down_scale, down_zero, nullptr};
+    d.nbanks = 1;
+    d.early = 1;  // the gate/up launch signals its dependents only after its own wait
+    d.y_routed = y;
+    d.ws = part;
+    d.M = M;
+    d.topk = topk;
+    d.E = E;
+    d.N = static_cast<int>(H);
+    d.K = static_cast<int>(F);
+    d.g = static_cast<int>(g);
+    d.err = dev->err;
+    return from_cuda(launch_moe(d, dev->info, s));
 }
 
 w4a16_status w4a16_swiglu(const uint16_t* gate, const uint16_t* up, int64_t ld_in, uint16_t* h,

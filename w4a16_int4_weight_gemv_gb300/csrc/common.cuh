@@ -28,6 +28,12 @@ __device__ __forceinline__ void store_out(void* y, int out_f32, size_t idx, floa
     if (out_f32) static_cast<float*>(y)[idx] = v;
     else static_cast<uint16_t*>(y)[idx] = f32_to_bf16_rn(v);
 }
+// SwiGLU element in fp32: silu(gate) * up with silu(v) = v / (1 + e^-v).
+// Shared by the elementwise kernel and the expert kernel's fused staging so
+// both round the same fp32 value to bf16.
+__device__ __forceinline__ float silu_mul(float gte, float up) {
+    return gte / (1.0f + expf(-gte)) * up;
+}
 // exact power of two 2^e for a normal exponent e in [-126, 127]
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 

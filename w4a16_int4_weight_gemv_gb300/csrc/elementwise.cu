@@ -63,10 +63,6 @@ __global__ void k_dequant(const uint32_t* __restrict__ wq, const uint16_t* __res
     }
 }
 
-__device__ __forceinline__ float silu_mul(float gte, float up) {
-    return gte / (1.0f + expf(-gte)) * up;
-}
-
 // Two adjacent outputs per thread (N even, rows 4-byte aligned).
 __global__ void k_swiglu(const uint16_t* __restrict__ gate, const uint16_t* __restrict__ up,
                          int64_t ld_in, uint16_t* __restrict__ h, int64_t ld_out, int64_t rows,

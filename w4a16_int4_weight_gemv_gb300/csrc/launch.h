@@ -115,16 +115,27 @@ cudaError_t launch_gemv_simt(const GemvArgs& a, const GemvPlan& p, cudaStream_t 
 cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 cudaError_t launch_gemv_tc(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 
-struct MoeArgs {
-    const uint16_t* x;
-    int x_per_slot;
-    const int32_t* ids;
-    const float* route_w;
+// One stacked expert bank: wq [E][N][K/8], scale and zero [E][N][K/g], and
+// its bf16 per-slot output [M*topk][N] (used when there is no routed sum).
+struct MoeBank {
     const uint32_t* wq;
     const uint16_t* scale;
     const uint8_t* zero;
     uint16_t* y;
-    float* ws;  // fp32 [M][topk][N] partials when route_w != nullptr
+};
+struct MoeArgs {
+    const uint16_t* x;        // [M][K], or [M][topk][K] with x_per_slot
+    int x_per_slot;
+    const uint16_t* sw_gate;  // non-null: activations bf16(silu(gate) * up), [M*topk][K]
+    const uint16_t* sw_up;
+    const int32_t* ids;
+    const float* route_w;     // non-null: routed sum into y_routed through ws
+    MoeBank bank[2];
+    int nbanks;               // 1, or 2 banks of one shape against the same activations
+    int early;                // inputs other than the activations may be read before the
+                              // grid dependency wait (the predecessor is this chain's own)
+    uint16_t* y_routed;       // bf16 [M][N]
+    float* ws;                // fp32 [M*topk][N] partials of the routed sum
     int M;
     int topk;
     int E;
@@ -133,6 +144,8 @@ struct MoeArgs {
     int g;
     uint32_t* err;
 };
+// Dynamic shared memory the expert kernel needs at least (two stages).
+int moe_smem_need(int M, int K, int g);
 cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s);
 
 cudaError_t launch_pack(const uint8_t* codes, uint32_t* wq, int64_t N, int64_t K, int sms,

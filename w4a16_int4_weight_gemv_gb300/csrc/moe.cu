@@ -3,14 +3,28 @@
 //
 // For token t and routed slot j, expert e = ids[t][j] multiplies its own INT4
 // matrix W_e by the slot's activation row.  Tokens that route to the same
-// expert share one pass over that expert's weights: CTA (chunk, d) finds the
-// d-th distinct expert among the routed slots (in order of first
+// expert share one pass over that expert's weights: CTA (chunk, d, bank)
+// finds the d-th distinct expert among the routed slots (in order of first
 // appearance), gathers the activation rows of every slot routed to it into
-// shared memory (the same permuted layout the dense warp-MMA kernel uses)
-// and streams 16 * warps rows of W_e against all of them at once.  The
-// routed ids live on the device, so the grid is sized for the worst case
-// (min(E, M*topk) distinct experts) and CTAs beyond the actual count exit at
-// once.
+// shared memory and streams a 64-row chunk of W_e against all of them at
+// once.  The routed ids live on the device, so the grid is sized for the
+// worst case (min(E, M*topk) distinct experts) and CTAs beyond the actual
+// count exit at once.
+//
+// Transport and arithmetic are those of the dense warp-MMA kernel
+// (gemv_mma.cu, mma_core.cuh): one 2-D tensor map over the whole stacked
+// bank [E*N rows][K/8 words], per-warp rings of 16-row x 512-k stages filled
+// by two 128-byte-swizzled TMA boxes, ldmatrix fragments, mma.sync with the
+// 128 + code bf16 trick and the per-block zero-point/scale correction.  Two
+// warps share a 16-row tile (K halves, partials added in shared memory in a
+// fixed order).  A CTA's scales and zero points are gathered into a
+// shared-memory table once.
+//
+// One launch can serve two banks of the same shape against the same
+// activations (grid z): the gate and up products of a SwiGLU expert FFN.
+// The activations can also be formed while staging, h = bf16(silu(g) * u)
+// from per-slot gate and up outputs: the down product of that FFN, without a
+// separate SwiGLU pass.
 //
 // With route weights the per-slot results go to an fp32 workspace and a
 // second kernel forms y[t] = sum_j r[t][j] d[t][j] in slot order -- a fixed
@@ -22,32 +36,61 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kPD = 4;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+// A CTA covers TILES 16-row tiles of one expert: 4 (two warps per tile,
+// K halves) or, when that would take more than one wave, 8 (a warp per tile).
+constexpr int kSB = 4;                   // 128-k blocks per step (512 k)
+constexpr int kHalfBytes = 2048;         // one TMA box: 16 rows x 128 bytes
+constexpr int kStageA = 2 * kHalfBytes;
+constexpr unsigned kBoxRows = 16;
 constexpr int kMaxSlots = 256;
+constexpr int kMaxTableGroups = 64;      // scale/zero table in shared memory up to G = 64
+constexpr int kMaxStages = 4;
 
 struct MoeKernelArgs {
     const uint16_t* x;
     int x_per_slot;
+    const uint16_t* sw_gate;  // non-null: activations are h = bf16(silu(gate) * up), [S][K]
+    const uint16_t* sw_up;
     const int32_t* ids;
-    const uint4* wq;
-    const uint16_t* scale;
-    const uint8_t* zero;
-    uint16_t* y;  // per-slot bf16 output (no route weights)
-    float* ws;    // per-slot fp32 output (route weights given)
+    MoeBank bank[2];
+    float* ws;  // fp32 per-slot outputs [S][N] (a routed sum follows), else bf16 bank[z].y
     int M;
     int topk;
     int E;
     int N;
     int K;
     int g;
+    int stages;
+    int early;  // ids, weights, scales may be read before the grid dependency wait
     uint32_t* err;
 };
 
-template <int NT>
-__global__ void __launch_bounds__(kWarps * 32)
-k_moe_mma(const MoeKernelArgs a) {
+struct MoeLayout {
+    int xsum, red, tab, base;
+};
+__host__ __device__ inline MoeLayout moe_layout(int Mpad, int nblk, int G, int tiles) {
+    MoeLayout L;
+    L.xsum = Mpad * mma_token_stride(nblk);
+    L.red = L.xsum + nblk * Mpad * 4;
+    L.tab = L.red + tiles * 16 * Mpad * 4;
+    const int end = L.tab + (G <= kMaxTableGroups ? tiles * 16 * G * 4 : 0);
+    L.base = (end + 127) & ~127;
+    return L;
+}
+__host__ __device__ inline int moe_smem_bytes(int Mpad, int nblk, int G, int tiles, int ns) {
+    return moe_layout(Mpad, nblk, G, tiles).base + 1024 + kWarps * ns * (kStageA + 8);
+}
+
+template <int NT, int TILES>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
+k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
+          const __grid_constant__ CUtensorMap map1) {
     constexpr int Mpad = 8 * NT;
+    constexpr int kTiles = TILES;
+    constexpr int kWpt = kWarps / kTiles;  // warps sharing a tile (K halves)
+    constexpr int kRowsPerCta = kTiles * 16;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ int s_ids[kMaxSlots];
     __shared__ unsigned char s_first[kMaxSlots];
@@ -58,13 +101,23 @@ k_moe_mma(const MoeKernelArgs a) {
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int z = blockIdx.z;
+    const CUtensorMap* wmap = z ? &map1 : &map0;
+    const MoeBank bank = a.bank[z];
     const int S = a.M * a.topk;
     const int nblk = a.K >> 7;
-    const int Q = a.K >> 5;
+    const int nsteps = (nblk + kSB - 1) / kSB;
     const int G = a.K / a.g;
+    const bool use_table = G <= kMaxTableGroups;
     const int tok_stride = mma_token_stride(nblk);
-    unsigned char* xs = smem_raw;
-    float* xsum = reinterpret_cast<float*>(smem_raw + Mpad * tok_stride);
+    const int NS = a.stages;
+
+    // Programmatic dependent launch: without `early` everything waits for the
+    // preceding grid; with it (a launch inside the FFN chain, whose
+    // predecessor signalled only after its own wait) the routed ids, weights
+    // and scales -- inputs of the whole chain -- are read first and only the
+    // activations and outputs wait.
+    if (!a.early) grid_dependency_wait();
 
     // 1. which expert does this CTA serve?
     for (int i = threadIdx.x; i < S; i += blockDim.x) s_ids[i] = a.ids[i];
@@ -73,7 +126,7 @@ k_moe_mma(const MoeKernelArgs a) {
     for (int i = threadIdx.x; i < S; i += blockDim.x) {
         const int e = s_ids[i];
         bool first = (e >= 0 && e < a.E);
-        if (!first && blockIdx.x == 0 && blockIdx.y == 0)
+        if (!first && blockIdx.x == 0 && blockIdx.y == 0 && z == 0)
             raise_device_error(a.err, W4A16_DEVERR_EXPERT_ID);
         for (int j = 0; j < i && first; ++j) first = (s_ids[j] != e);
         s_first[i] = first ? 1 : 0;
@@ -90,14 +143,18 @@ k_moe_mma(const MoeKernelArgs a) {
 
     // invalid ids produce zero rows in the per-slot output
     if (a.ws == nullptr && blockIdx.y == 0) {
+        if (a.early) grid_dependency_wait();
         for (int i = 0; i < S; ++i) {
             if (s_ids[i] >= 0 && s_ids[i] < a.E) continue;
-            for (int row = blockIdx.x * kWarps * 16 + threadIdx.x;
-                 row < min(a.N, (blockIdx.x + 1) * kWarps * 16); row += blockDim.x)
-                a.y[static_cast<size_t>(i) * a.N + row] = 0;
+            for (int row = blockIdx.x * kRowsPerCta + threadIdx.x;
+                 row < min(a.N, (blockIdx.x + 1) * kRowsPerCta); row += blockDim.x)
+                bank.y[static_cast<size_t>(i) * a.N + row] = 0;
         }
     }
-    if (e < 0) return;
+    if (e < 0) {
+        grid_dependents_launch();
+        return;
+    }
 
     if (threadIdx.x == 0) {
         int n = 0;
@@ -105,72 +162,207 @@ k_moe_mma(const MoeKernelArgs a) {
             if (s_ids[i] == e) s_slots[n++] = i;
         s_nslots = n;
     }
-    __syncthreads();
-    const int nslots = s_nslots;
 
-    const uint4* wq = a.wq + static_cast<size_t>(e) * a.N * Q;
-    const uint16_t* scale = a.scale + static_cast<size_t>(e) * a.N * G;
-    const uint8_t* zero = a.zero + static_cast<size_t>(e) * a.N * G;
+    const MoeLayout lay = moe_layout(Mpad, nblk, G, kTiles);
+    unsigned char* xs = smem_raw;
+    float* xsum = reinterpret_cast<float*>(smem_raw + lay.xsum);
+    float* red = reinterpret_cast<float*>(smem_raw + lay.red);
+    uint32_t* tab = reinterpret_cast<uint32_t*>(smem_raw + lay.tab);
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const int a_off = static_cast<int>(((raw_addr + lay.base + 1023u) & ~1023u) - raw_addr);
+    unsigned char* ring = smem_raw + a_off + warp * NS * kStageA;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + a_off + kWarps * NS * kStageA) + warp * NS;
+
+    const int tl = warp / kWpt;  // local tile
+    const int kp = warp - tl * kWpt;
+    const int tile = blockIdx.x * kTiles + tl;  // 16-row tile of expert e
+    const bool has_rows = tile * 16 < a.N;
+    const int steps_mine = (has_rows && nsteps > kp) ? (nsteps - kp + kWpt - 1) / kWpt : 0;
+    const int row0 = e * a.N + tile * 16;  // first row in the stacked bank
+
+    if (lane == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(bars + i, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();  // s_nslots, barriers
+    const int nslots = s_nslots;
+    const int npass = (nslots + Mpad - 1) / Mpad;
+    const int total = npass * steps_mine;  // every pass streams the same weights
+
+    // producer cursor over (pass, step); the weights do not depend on the pass
+    int w_i = 0;
+    auto issue = [&]() {
+        const int stg = w_i % NS;
+        uint64_t* bar = bars + stg;
+        unsigned char* dst = ring + stg * kStageA;
+        const int ks = kp + (w_i % steps_mine) * kWpt;
+        const int blk0 = ks * kSB;
+        const int nbs = min(kSB, nblk - blk0);
+        const int nh = (nbs + 1) >> 1;
+        if (lane == 0) {
+            if (w_i >= NS) fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nh * kHalfBytes));
+            tma_load_2d(dst, wmap, blk0 * 16, row0, bar);
+            if (nh > 1) tma_load_2d(dst + kHalfBytes, wmap, blk0 * 16 + 32, row0, bar);
+        }
+        ++w_i;
+    };
+    while (w_i < NS && w_i < total) issue();
+
+    // scale | zero << 16 of every (row, group) of this CTA's rows
+    const uint16_t* escale = bank.scale + static_cast<size_t>(e) * a.N * G;
+    const uint8_t* ezero = bank.zero + static_cast<size_t>(e) * a.N * G;
+    if (use_table) {
+        for (int i = threadIdx.x; i < kTiles * 16 * G; i += blockDim.x) {
+            const int rr = i / G;
+            const int n = blockIdx.x * kRowsPerCta + rr;
+            uint32_t v = 0u;
+            if (n < a.N) {
+                const size_t gi = static_cast<size_t>(n) * G + (i - rr * G);
+                v = ldg_nc_u16(escale + gi) | (ldg_nc_u8(ezero + gi) << 16);
+            }
+            tab[i] = v;
+        }
+    }
+
+    if (a.early) grid_dependency_wait();
+    // dependents may start now: everything this grid reads is complete
+    grid_dependents_launch();
+
     const int r = lane >> 2;
     const int c = lane & 3;
-    const int n0 = (blockIdx.x * kWarps + warp) * 16 + r;
-    const int n1 = n0 + 8;
+    const int lrow = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const uint32_t lbase = static_cast<uint32_t>(lrow * 128);
+    const int lsw = lane & 7;
+    const int lch = lane >> 4;
+    const int n0 = tile * 16 + r;
+    bool timed_out = false;
+    int c_i = 0;  // consumer cursor
 
-    const int tile = blockIdx.x * kWarps + warp;  // 16-row tile of expert e
-    auto issue = [&](int blk, MmaBlockLoad& L) {
-        mma_block_issue(L, wq, scale, zero, a.N, Q, G, a.g, tile, blk, lane);
-    };
-
-    // 2. passes of up to Mpad slots routed to expert e (normally one)
     for (int base = 0; base < nslots; base += Mpad) {
         const int m = min(Mpad, nslots - base);
-        MmaBlockLoad ring[kPD];
-#pragma unroll
-        for (int p = 0; p < kPD; ++p)
-            if (p < nblk) issue(p, ring[p]);
         if (threadIdx.x < Mpad) {
             int rs = -1;
             if (static_cast<int>(threadIdx.x) < m) {
                 const int slot = s_slots[base + threadIdx.x];
-                rs = a.x_per_slot ? slot : slot / a.topk;
+                rs = (a.x_per_slot || a.sw_gate) ? slot : slot / a.topk;
             }
             s_rowsel[threadIdx.x] = rs;
         }
         __syncthreads();
-        stage_x_permuted<NT>(a.x, s_rowsel, m, a.K, 0, nblk, xs, xsum, tok_stride);
+        // 2. activations of the pass's slots, natural order, then paired in place
+        const int pieces = m * nblk * 16;  // 16-byte pieces of 8 values
+        if (a.sw_gate) {
+            for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+                const int n = i / (nblk * 16);
+                const int p = i - n * nblk * 16;
+                const size_t src = static_cast<size_t>(s_rowsel[n]) * a.K + p * 8;
+                const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.sw_gate + src));
+                const uint4 uv = __ldg(reinterpret_cast<const uint4*>(a.sw_up + src));
+                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+                uint32_t hw[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float h0 = silu_mul(bf16_to_f32(gw[q] & 0xFFFFu), bf16_to_f32(uw[q] & 0xFFFFu));
+                    const float h1 = silu_mul(bf16_to_f32(gw[q] >> 16), bf16_to_f32(uw[q] >> 16));
+                    hw[q] = f32_to_bf16_rn(h0) | (static_cast<uint32_t>(f32_to_bf16_rn(h1)) << 16);
+                }
+                *reinterpret_cast<uint4*>(xs + n * tok_stride + p * 16) =
+                    make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            }
+        } else {
+            for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+                const int n = i / (nblk * 16);
+                const int p = i - n * nblk * 16;
+                cp_async_16(xs + n * tok_stride + p * 16,
+                            a.x + static_cast<size_t>(s_rowsel[n]) * a.K + p * 8);
+            }
+            cp_async_wait_all();
+        }
+        __syncthreads();
+        pair_x_in_place<NT>(m, nblk, xs, xsum, tok_stride);
         __syncthreads();
 
+        // 3. stream this warp's K half of its tile against the pass's slots
         float acc[NT][4];
 #pragma unroll
         for (int t = 0; t < NT; ++t)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
-        for (int b0 = 0; b0 < nblk; b0 += kPD) {
+        for (int s = 0; s < steps_mine; ++s) {
+            const int stg = c_i % NS;
+            if (!mbar_wait_bounded(bars + stg, (c_i / NS) & 1)) timed_out = true;
+            const uint32_t sa = smem_addr(ring + stg * kStageA);
+            const int lb0 = (kp + s * kWpt) * kSB;
+            const int nbs = min(kSB, nblk - lb0);
 #pragma unroll
-            for (int p = 0; p < kPD; ++p) {
-                const int b = b0 + p;
-                if (b < nblk) {
-                    mma_block<NT>(acc, ring[p], xs + b * 256, xsum + b * Mpad, tok_stride, m,
-                                  lane);
-                    if (b + kPD < nblk) issue(b + kPD, ring[p]);
+            for (int bb = 0; bb < kSB; ++bb) {
+                if (bb < nbs) {
+                    const uint32_t hb = sa + (bb >> 1) * kHalfBytes + lbase;
+                    const int cb = (bb & 1) * 4 + lch;
+                    uint32_t q0[4], q1[4];
+                    ldmatrix_x4(q0, hb + (static_cast<uint32_t>(cb ^ lsw) << 4));
+                    ldmatrix_x4(q1, hb + (static_cast<uint32_t>((cb + 2) ^ lsw) << 4));
+                    MmaBlockLoad L;
+                    L.w0 = make_uint4(q0[0], q0[2], q1[0], q1[2]);
+                    L.w1 = make_uint4(q0[1], q0[3], q1[1], q1[3]);
+                    const int blk = lb0 + bb;
+                    const int grp = (blk << 7) / a.g;
+                    if (use_table) {
+                        L.sz0 = tab[(tl * 16 + r) * G + grp];
+                        L.sz1 = tab[(tl * 16 + r + 8) * G + grp];
+                    } else {
+                        L.sz0 = 0u;
+                        L.sz1 = 0u;
+                        if (n0 < a.N) {
+                            const size_t gi = static_cast<size_t>(n0) * G + grp;
+                            L.sz0 = ldg_nc_u16(escale + gi) | (ldg_nc_u8(ezero + gi) << 16);
+                        }
+                        if (n0 + 8 < a.N) {
+                            const size_t gi = static_cast<size_t>(n0 + 8) * G + grp;
+                            L.sz1 = ldg_nc_u16(escale + gi) | (ldg_nc_u8(ezero + gi) << 16);
+                        }
+                    }
+                    mma_block<NT>(acc, L, xs + blk * 256, xsum + blk * Mpad, tok_stride, m, lane);
                 }
             }
+            __syncwarp();  // every lane is done with the stage
+            ++c_i;
+            if (w_i < total) issue();
         }
-        // outputs: C fragment rows r / r + 8, tokens 2c, 2c + 1 (+ 8 t)
+
+        // 4. add the two K halves (fixed order) and store per-slot outputs
+        float* rb = red + tl * 16 * Mpad;
+        if constexpr (kWpt > 1) {
+            if (kp == 1) {
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
+                for (int t = 0; t < NT; ++t)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tok = t * 8 + 2 * c + (i & 1);
-                const int n = (i < 2) ? n0 : n1;
-                if (tok < m && n < a.N) {
-                    const size_t o = static_cast<size_t>(s_slots[base + tok]) * a.N + n;
-                    if (a.ws) a.ws[o] = acc[t][i];
-                    else a.y[o] = f32_to_bf16_rn(acc[t][i]);
-                }
+                    for (int i = 0; i < 4; ++i)
+                        rb[(r + ((i >> 1) << 3)) * Mpad + t * 8 + 2 * c + (i & 1)] = acc[t][i];
             }
-        __syncthreads();  // s_rowsel / xs are rewritten by the next pass
+            named_barrier_sync(1 + tl, kWpt * 32);
+        }
+        if (kp == 0 && has_rows) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = r + ((i >> 1) << 3);
+                    const int tok = t * 8 + 2 * c + (i & 1);
+                    const int n = tile * 16 + row;
+                    if (tok < m && n < a.N) {
+                        const float v = (kWpt > 1) ? acc[t][i] + rb[row * Mpad + tok] : acc[t][i];
+                        const size_t o = static_cast<size_t>(s_slots[base + tok]) * a.N + n;
+                        if (a.ws) a.ws[o] = v;
+                        else bank.y[o] = f32_to_bf16_rn(v);
+                    }
+                }
+        }
+        __syncthreads();  // s_rowsel, xs and red are rewritten by the next pass
     }
+    if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
 }
 
 // y[t][n] = sum_j r[t][j] * ws[t][j][n] over slots with a valid expert id.
@@ -191,17 +383,28 @@ __global__ void k_moe_route_sum(const float* __restrict__ ws, const float* __res
     }
 }
 
+using MoeKernel = void (*)(MoeKernelArgs, CUtensorMap, CUtensorMap);
+
+MoeKernel pick_moe_kernel(int Mpad, int tiles) {
+    if (Mpad == 8) return tiles == 4 ? k_moe_tma<1, 4> : k_moe_tma<1, 8>;
+    return tiles == 4 ? k_moe_tma<2, 4> : k_moe_tma<2, 8>;
+}
+
 }  // namespace
+
+int moe_smem_need(int M, int K, int g) {
+    return moe_smem_bytes(M <= 8 ? 8 : 16, K / 128, K / g, 8, 2);
+}
 
 cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) {
     MoeKernelArgs k{};
     k.x = a.x;
     k.x_per_slot = a.x_per_slot;
+    k.sw_gate = a.sw_gate;
+    k.sw_up = a.sw_up;
     k.ids = a.ids;
-    k.wq = reinterpret_cast<const uint4*>(a.wq);
-    k.scale = a.scale;
-    k.zero = a.zero;
-    k.y = a.route_w ? nullptr : a.y;
+    k.bank[0] = a.bank[0];
+    k.bank[1] = a.nbanks > 1 ? a.bank[1] : a.bank[0];
     k.ws = a.route_w ? a.ws : nullptr;
     k.M = a.M;
     k.topk = a.topk;
@@ -211,28 +414,54 @@ cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) 
     k.g = a.g;
     k.err = a.err;
     const int S = a.M * a.topk;
-    const int dmax = S < a.E ? S : a.E;
-    const int chunks = (a.N + kWarps * 16 - 1) / (kWarps * 16);
     const int nblk = a.K / 128;
-    const dim3 grid(chunks, dmax);
-    cudaError_t e;
-    if (a.M <= 8) {
-        const int smem = 8 * mma_token_stride(nblk) + nblk * 8 * 4;
-        e = cudaFuncSetAttribute(k_moe_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        k_moe_mma<1><<<grid, kWarps * 32, smem, s>>>(k);
-    } else {
-        const int smem = 16 * mma_token_stride(nblk) + nblk * 16 * 4;
-        e = cudaFuncSetAttribute(k_moe_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        k_moe_mma<2><<<grid, kWarps * 32, smem, s>>>(k);
+    const int G = a.K / a.g;
+    // slots per pass: 8 for up to 8 tokens (a token's slots normally name
+    // distinct experts, so an expert then has at most M slots), else 16;
+    // more slots on one expert take more passes
+    const int Mpad = (a.M <= 8) ? 8 : 16;
+    const int dmax = S < a.E ? S : a.E;
+    const int nz = a.nbanks > 1 ? 2 : 1;
+    // 64-row CTAs unless that takes more than one wave of two CTAs per SM
+    const int tiles = (((a.N + 63) / 64) * dmax * nz > 2 * dev.sms) ? 8 : 4;
+    const int rows = tiles * 16;
+    // stages: as many as leave room for two CTAs per SM (8-slot passes)
+    const int per_cta = dev.smem_per_sm / (Mpad == 8 ? 2 : 1) - 1024;
+    int ns = 2;
+    while (ns < kMaxStages && moe_smem_bytes(Mpad, nblk, G, tiles, ns + 1) <= per_cta &&
+           moe_smem_bytes(Mpad, nblk, G, tiles, ns + 1) <= dev.max_smem_optin)
+        ++ns;
+    k.stages = ns;
+    k.early = a.early;
+    const int smem = moe_smem_bytes(Mpad, nblk, G, tiles, ns);
+    if (smem > dev.max_smem_optin) return cudaErrorInvalidValue;
+    CUtensorMap maps[2];
+    for (int b = 0; b < 2; ++b) {
+        const MoeBank& bk = k.bank[b];
+        if (!encode_weight_map(&maps[b], bk.wq, a.E * a.N, a.K, kBoxRows)) return cudaErrorInvalidValue;
     }
+    MoeKernel kern = pick_moe_kernel(Mpad, tiles);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((a.N + rows - 1) / rows, dmax, nz);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, k, maps[0], maps[1]);
+    if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess || !a.route_w) return e;
     const int total = a.M * a.N;
     int blocks = (total + 255) / 256;
     if (blocks > 4 * dev.sms) blocks = 4 * dev.sms;
-    k_moe_route_sum<<<blocks, 256, 0, s>>>(a.ws, a.route_w, a.ids, a.y, a.M, a.topk, a.E, a.N);
+    k_moe_route_sum<<<blocks, 256, 0, s>>>(a.ws, a.route_w, a.ids, a.y_routed, a.M, a.topk, a.E,
+                                          a.N);
     return cudaGetLastError();
 }
 
