@@ -127,7 +127,10 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
     uint64_t* bars = bars0 + warp * NS;
     uint64_t* xbar = bars0 + kWarps * NS;
 
-    const int gid = cid * TG + tg;
+    // tile groups are dealt round-robin over the CTAs (group tg of CTA cid is
+    // tg * ncl + cid), so with more CTAs than a full group layout needs the
+    // tiles spread over all of them instead of filling the first ones
+    const int gid = tg * ncl + cid;
     const int NG = ncl * TG;
     const int my_tiles = (ntiles > gid) ? (ntiles - gid + NG - 1) / NG : 0;
     const int my_steps = (nsteps_slice > kp) ? (nsteps_slice - kp + WPT - 1) / WPT : 0;
@@ -329,7 +332,7 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
             rem -= g2 * 16 * a.M;
             const int tok = rem >> 4;
             const int row = rem & 15;
-            const int gid2 = cid * TG + g2;
+            const int gid2 = g2 * ncl + cid;
             const int mt = (ntiles > gid2) ? (ntiles - gid2 + NG - 1) / NG : 0;
             if (t >= mt || (t % S) != rank) continue;
             const float* src = part + ((t * TG + g2) * 16 + row) * Mpad + tok;

@@ -189,7 +189,10 @@ k_gemv_simt(const SimtKernelArgs a) {
     uint64_t* bars =
         reinterpret_cast<uint64_t*>(smem_raw + base + kWarps * NS * St::kBytes) + warp * NS;
 
-    const int gid = cid * TG + tg;
+    // tile groups are dealt round-robin over the CTAs (group tg of CTA cid is
+    // tg * ncl + cid), so with more CTAs than a full group layout needs the
+    // tiles spread over all of them instead of filling the first ones
+    const int gid = tg * ncl + cid;
     const int NG = ncl * TG;
     const int my_tiles = (ntiles > gid) ? (ntiles - gid + NG - 1) / NG : 0;
     const int my_spans = (nspan > kp) ? (nspan - kp + WPT - 1) / WPT : 0;
@@ -481,7 +484,7 @@ k_gemv_simt(const SimtKernelArgs a) {
             const int rem = idx - t * per_t;
             const int g2 = rem / (TR * MT);
             const int l = rem - g2 * TR * MT;
-            const int gid2 = cid * TG + g2;
+            const int gid2 = g2 * ncl + cid;
             const int mt = (ntiles > gid2) ? (ntiles - gid2 + NG - 1) / NG : 0;
             if (t >= mt || (t % S) != rank) continue;
             float v = 0.f;

@@ -52,7 +52,8 @@ struct DeviceInfo {
 
 // Choose the K split of a GEMV launch: total factor f = wpt * S (wpt warps of
 // a CTA share a tile, S CTAs of a cluster share it), minimising the critical
-// path -- tiles per warp group times K units per warp -- at full residency.
+// path -- tiles per warp group times K units per warp -- at full residency,
+// then the busiest CTA's work (tiles per CTA times K units of its slice).
 // max_clusters(S, smem) is how many clusters of S CTAs with that much shared
 // memory the device can hold at once (clusters are co-scheduled inside a GPC,
 // so it can be less than SMs / S); the persistent grid never exceeds it.
@@ -64,7 +65,7 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
                          int max_ctas_per_sm, int forced_f, SmemFn smem_fn,
                          ClusterFn max_clusters) {
     SplitChoice best{};
-    long best_cost = -1;
+    long best_cost = -1, best_work = 0;
     for (int f = 1; f <= 32; f *= 2) {
         if (forced_f > 0 && f != forced_f) continue;
         if (forced_f == 0 && f > units_all) break;
@@ -86,15 +87,19 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
                 if (mc < 1) continue;
                 if (clusters > mc) clusters = mc;
             }
-            const int max_clusters_needed = (ntiles + tg - 1) / tg;
-            if (clusters > max_clusters_needed) clusters = max_clusters_needed;
+            // tiles are dealt round-robin over the clusters, so every cluster
+            // up to one per tile does useful work
+            if (clusters > ntiles) clusters = ntiles;
             if (clusters < 1) clusters = 1;
             const int tpg = (ntiles + clusters * tg - 1) / (clusters * tg);
             smem = smem_fn(upc, tg, wpt, tpg, S);
             if (smem > dev.max_smem_optin) continue;
+            // first the longest warp's steps, then the busiest CTA's steps
             const long cost = static_cast<long>(tpg) * ((upc + wpt - 1) / wpt);
-            if (best_cost < 0 || cost < best_cost) {
+            const long cta_work = static_cast<long>((ntiles + clusters - 1) / clusters) * upc;
+            if (best_cost < 0 || cost < best_cost || (cost == best_cost && cta_work < best_work)) {
                 best_cost = cost;
+                best_work = cta_work;
                 best = SplitChoice{wpt, S, clusters * S, tpg, upc, smem};
             }
         }
