@@ -198,14 +198,16 @@ __device__ __forceinline__ void cluster_barrier() {
         "barrier.cluster.wait.acquire.aligned;" ::
             : "memory");
 }
-__device__ __forceinline__ float ld_dsmem_f32(const float* local_ptr, uint32_t rank) {
+
+// Store into the shared memory of CTA `rank` of the cluster, at the offset
+// local_ptr has in this CTA (fire-and-forget; a cluster barrier makes it
+// visible to the owner).
+__device__ __forceinline__ void st_dsmem_f32(float* local_ptr, uint32_t rank, float v) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                  : "=r"(remote)
                  : "r"(smem_addr(local_ptr)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -73,7 +73,7 @@ __host__ __device__ inline int mma_base_bytes(int M, int NT, int upc, int tg, in
     const int bpc = upc * kSB;
     const int b = M * mma_token_stride(bpc) + bpc * Mpad * 4 +
                   (wpt > 1 ? 2 * tg * wpt * 16 * Mpad * 4 : 0) +
-                  (S > 1 ? tpg * tg * 16 * Mpad * 4 : 0);
+                  (S > 1 ? tpg * S * tg * 16 * Mpad * 4 : 0);
     return (b + 127) & ~127;
 }
 
@@ -116,7 +116,7 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
     unsigned char* xs = smem_raw;
     float* xsum = reinterpret_cast<float*>(smem_raw + a.M * tok_stride);
     float* red = xsum + BPC * Mpad;                                 // [2][TG][WPT][16][Mpad]
-    float* part = red + (WPT > 1 ? 2 * TG * WPT * 16 * Mpad : 0);    // [tpg][TG][16][Mpad]
+    float* part = red + (WPT > 1 ? 2 * TG * WPT * 16 * Mpad : 0);    // [tpg][S][TG][16][Mpad]
     const int base = mma_base_bytes(a.M, NT, a.steps_per_cta, TG, WPT, a.tiles_per_group, S);
     const uint32_t raw_addr = smem_addr(smem_raw);
     const int a_off = static_cast<int>(((raw_addr + base + 1023u) & ~1023u) - raw_addr);
@@ -244,7 +244,9 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
                         if (n < a.N)
                             store_out(a.y, a.out_f32, static_cast<size_t>(tok) * a.N + n, acc[t][i]);
                     } else {
-                        part[((ti * TG + tg) * 16 + row) * Mpad + tok] = acc[t][i];
+                        // into the owner's shared memory (CTA ti % S of the cluster)
+                        st_dsmem_f32(part + (((ti * S + rank) * TG + tg) * 16 + row) * Mpad + tok,
+                                     static_cast<uint32_t>(ti % S), acc[t][i]);
                     }
                 }
         }
@@ -321,6 +323,9 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
     if (my_steps == 0)
         for (; ti < my_tiles; ++ti) tile_end();
 
+    // cluster K split: every rank stored its partials of tile t into the
+    // shared memory of the owner, rank t % S; after one cluster barrier the
+    // owner adds them in rank order (deterministic) and stores y
     if (S > 1) {
         cluster_barrier();
         const int per_t = TG * 16 * a.M;
@@ -335,13 +340,11 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
             const int gid2 = g2 * ncl + cid;
             const int mt = (ntiles > gid2) ? (ntiles - gid2 + NG - 1) / NG : 0;
             if (t >= mt || (t % S) != rank) continue;
-            const float* src = part + ((t * TG + g2) * 16 + row) * Mpad + tok;
             float v = 0.f;
-            for (int q = 0; q < S; ++q) v += ld_dsmem_f32(src, static_cast<uint32_t>(q));
+            for (int q = 0; q < S; ++q) v += part[(((t * S + q) * TG + g2) * 16 + row) * Mpad + tok];
             const int n = (gid2 + t * NG) * 16 + row;
             if (n < a.N) store_out(a.y, a.out_f32, static_cast<size_t>(tok) * a.N + n, v);
         }
-        cluster_barrier();
     }
 }
 

@@ -138,7 +138,7 @@ __device__ __forceinline__ void store_y(void* y, int out_f32, size_t i, float v)
 __host__ __device__ inline int simt_base_bytes(int MT, int TR, int spans, int tg, int wpt,
                                                int tpg, int S) {
     const int b = MT * spans * (4096 + 128) + 2 * tg * wpt * TR * MT * 4 +
-                  (S > 1 ? tpg * tg * TR * MT * 4 : 0);
+                  (S > 1 ? tpg * S * tg * TR * MT * 4 : 0);
     return (b + 127) & ~127;
 }
 
@@ -183,7 +183,7 @@ k_gemv_simt(const SimtKernelArgs a) {
     float* xs = reinterpret_cast<float*>(smem_raw);  // [MT][SP * 1024] swizzled x'
     float* xsum = xs + MT * SP * 1024;              // [MT][SP * 32] chunk sums * 2^-64
     float* red = xsum + MT * SP * 32;               // [2][TG][WPT][TR * MT]
-    float* part = red + 2 * TG * WPT * TR * MT;     // [tpg][TG][TR * MT] (S > 1)
+    float* part = red + 2 * TG * WPT * TR * MT;     // [tpg][S][TG][TR * MT] (S > 1)
     const int base = simt_base_bytes(MT, TR, SP, TG, WPT, a.tiles_per_group, S);
     unsigned char* ring = smem_raw + base + warp * NS * St::kBytes;
     uint64_t* bars =
@@ -378,7 +378,9 @@ k_gemv_simt(const SimtKernelArgs a) {
                 const int n = c_tile * TR + orow;
                 if (n < a.N) store_y(a.y, a.out_f32, static_cast<size_t>(otok) * a.N + n, mine);
             } else {
-                part[(ti * TG + tg) * NV + vid] = mine;
+                // into the owner's shared memory (CTA ti % S of the cluster)
+                st_dsmem_f32(part + ((ti * S + rank) * TG + tg) * NV + vid,
+                             static_cast<uint32_t>(ti % S), mine);
             }
         }
     };
@@ -474,7 +476,9 @@ k_gemv_simt(const SimtKernelArgs a) {
             c_tile += NG;
         }
 
-    // cluster K split: add the ranks' partials in rank order through DSMEM
+    // cluster K split: every rank stored its partials of tile t into the
+    // shared memory of the owner, rank t % S; after one cluster barrier the
+    // owner adds them in rank order (deterministic) and stores y
     if (S > 1) {
         cluster_barrier();
         const int per_t = TG * TR * MT;
@@ -488,12 +492,11 @@ k_gemv_simt(const SimtKernelArgs a) {
             const int mt = (ntiles > gid2) ? (ntiles - gid2 + NG - 1) / NG : 0;
             if (t >= mt || (t % S) != rank) continue;
             float v = 0.f;
-            for (int q = 0; q < S; ++q) v += ld_dsmem_f32(part + idx, static_cast<uint32_t>(q));
+            for (int q = 0; q < S; ++q) v += part[((t * S + q) * TG + g2) * (TR * MT) + l];
             const int orow = l / MT;
             const int n = (gid2 + t * NG) * TR + orow;
             if (n < a.N) store_y(a.y, a.out_f32, static_cast<size_t>(l - orow * MT) * a.N + n, v);
         }
-        cluster_barrier();
     }
 }
 

@@ -77,10 +77,11 @@ __host__ __device__ inline int tc_ntok(int MR) { return MR <= 8 ? 8 : 16; }
 
 // Shared memory before the TMA ring: B operand (bpc*16 words x ntok tokens x
 // 16 bytes), block sums [bpc][MR], tile reduction [2][4][MR][32], and (K split
-// over a cluster) the partials [tpg][MR][128].
+// over a cluster) the partials every rank stores here for the tiles this CTA
+// owns, [tpg][S][MR][128].
 __host__ __device__ inline int tc_base_bytes(int MR, int bpc, int tpg, int S) {
     const int b = bpc * 16 * tc_ntok(MR) * 16 + bpc * MR * 4 + 2 * 4 * MR * 32 * 4 +
-                  (S > 1 ? tpg * MR * kRows * 4 : 0);
+                  (S > 1 ? tpg * S * MR * kRows * 4 : 0);
     return (b + 127) & ~127;
 }
 // Whole dynamic shared memory: 1024 bytes of slack for the ring's alignment,
@@ -268,7 +269,9 @@ k_gemv_tc(const TcArgs a, const __grid_constant__ CUtensorMap wmap) {
                     if (S == 1) {
                         if (n < a.N) store_out(a.y, a.out_f32, static_cast<size_t>(m) * a.N + n, v);
                     } else {
-                        part[(i * MR + m) * kRows + row] = v;
+                        // into the owner's shared memory (CTA i % S of the cluster)
+                        st_dsmem_f32(part + ((i * S + rank) * MR + m) * kRows + row,
+                                     static_cast<uint32_t>(i % S), v);
                     }
                 }
             }
@@ -399,7 +402,9 @@ k_gemv_tc(const TcArgs a, const __grid_constant__ CUtensorMap wmap) {
         }
     }
 
-    // K split: add the ranks' partials in rank order through DSMEM
+    // K split: every rank stored its partials of tile i into the shared
+    // memory of the owner, rank i % S; after one cluster barrier the owner
+    // adds them in rank order (deterministic) and stores y
     if (S > 1) {
         cluster_barrier();
         const int per_t = a.M * kRows;
@@ -410,13 +415,11 @@ k_gemv_tc(const TcArgs a, const __grid_constant__ CUtensorMap wmap) {
             const int rem = idx - i * per_t;
             const int m = rem / kRows;
             const int row = rem - m * kRows;
-            const float* src = part + (i * MR + m) * kRows + row;
             float v = 0.f;
-            for (int r = 0; r < S; ++r) v += ld_dsmem_f32(src, static_cast<uint32_t>(r));
+            for (int r = 0; r < S; ++r) v += part[((i * S + r) * MR + m) * kRows + row];
             const int n = (cid + i * ncl) * kRows + row;
             if (n < a.N) store_out(a.y, a.out_f32, static_cast<size_t>(m) * a.N + n, v);
         }
-        cluster_barrier();
     }
 
     tc_fence_before();
