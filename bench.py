@@ -339,6 +339,18 @@ def run_profile(args):
                       "launches": args.warmup + args.steps, "plan": w.gemv_plan(M, N, K, 128)}))
 
 
+def replica_aggregate(torch, dist, world, elapsed_s, bytes_per_step, steps):
+    """Whole-job numbers of `world` independent replicas (weak scaling: every
+    rank runs the same workload on its own GPU): the timed region is the
+    slowest rank's, and `value` counts every rank's bytes.  Returns
+    (elapsed_s, seconds per step, GB/s)."""
+    if world > 1:
+        t = torch.tensor([elapsed_s], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_s = float(t.item())
+    return elapsed_s, elapsed_s / steps, world * bytes_per_step * steps / elapsed_s / 1e9
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -391,14 +403,10 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    elapsed = start.elapsed_time(end) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
-    per_step = elapsed / args.steps
     bytes_step = algo_bytes(M, N, K, g)
-    value = world * bytes_step * args.steps / elapsed / 1e9
+    elapsed, per_step, value = replica_aggregate(torch, dist, world,
+                                                 start.elapsed_time(end) / 1e3, bytes_step,
+                                                 args.steps)
     peak, peak_kind = measured_peak()
     achieved = bytes_step / per_step / 1e9
     y_check = outs[0].float()
