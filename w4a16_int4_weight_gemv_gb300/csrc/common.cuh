@@ -40,10 +40,6 @@ __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) 
 // ---------------------------------------------------------------------------
 // Global loads
 // ---------------------------------------------------------------------------
-// Bring the line holding p into L1 (a hint; no register is written).
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
 // Streamed, read-once data (packed weights): bypass L1 allocation.
 __device__ __forceinline__ uint4 ldg_stream_u4(const uint4* p) {
     uint4 v;

@@ -18,14 +18,17 @@
 // and is folded into the row's accumulator as s * (C_m - (128 + z) * sum_k x_mk)
 // because a 128-k block lies in one quantisation group (g % 128 == 0).
 //
-// Warps: 8 unpacking warps -- TMEM lane quarter (warp % 4) x block parity
-// (warp / 4) -- one TMA producer warp, one MMA-issuing warp.  Pipeline per
-// block: TMA ring stage (16 KB: 128 rows x two blocks, 128-byte swizzle)
-// -> unpack to registers -> tcgen05.st into an A slot -> "ready" mbarrier ->
-// 8 MMAs into a D slot -> tcgen05.commit to the D slot's "done" mbarrier ->
-// the unpacking warp folds that D kLag blocks later.  TMEM holds 4 A slots
-// (2 per parity, 64 columns each) and 16 D slots (8 per parity, 16 columns
-// each): all 512 columns.
+// Warps: 8 unpacking warps -- TMEM lane quarter (warp % 4) x column half
+// (warp / 4), all of them on every block -- one TMA producer warp, one
+// MMA-issuing warp.  Pipeline per block: TMA ring stage (16 KB: 128 rows x
+// two blocks, 128-byte swizzle) -> unpack to registers -> tcgen05.st into the
+// block's A slot -> "ready" mbarrier (8 arrivals) -> 8 MMAs into the block's
+// D slot -> tcgen05.commit to that D slot's "done" mbarrier -> one half-warp
+// folds the D kLag blocks later.  TMEM holds 4 A slots (64 columns each) and
+// 16 D slots (16 columns each): all 512 columns.  The MMAs of a block take
+// ~363 cycles to issue (M = 128, N = 16, K = 16 issues at ~45 cycles), which
+// bounds the kernel at ~45 weights per clock per SM; the unpacking warps run
+// up to 4 blocks ahead of them.
 //
 // Work split: a cluster of S CTAs shares tiles, rank r taking the r-th K
 // slice; partials meet through distributed shared memory in rank order, so
@@ -44,17 +47,17 @@ constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr int kRows = 128;                 // tile rows = TMEM lanes = MMA M
 constexpr int kStageBytes = kRows * 128;   // 128 rows x 128 bytes: two 128-k blocks
-constexpr int kASlots = 4;                 // 2 per block parity
-constexpr int kDSlots = 16;                // 8 per block parity
+constexpr int kASlots = 4;                 // A slot of block bg: bg % 4
+constexpr int kDSlots = 16;                // D slot of block bg: bg % 16
 constexpr int kACols = 64;                 // TMEM columns of one block's A
 constexpr int kDCol0 = kASlots * kACols;   // first D column
 constexpr int kDCols = 16;
-constexpr int kLag = 4;                    // blocks between a block's MMAs and its fold
+constexpr int kLag = 8;                    // blocks between a block's MMAs and its fold
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxStages = 10;
 constexpr uint32_t kIdesc = tc_idesc_bf16(128, 16);
 static_assert(kDCol0 + kDSlots * kDCols <= static_cast<int>(kTmemCols), "TMEM columns");
-static_assert(kLag + 2 <= kDSlots / 2, "a D slot is folded before it is reused");
+static_assert(kLag + kASlots <= kDSlots, "a D slot is folded before it is reused");
 
 struct TcArgs {
     const uint16_t* x;
@@ -76,12 +79,14 @@ struct TcArgs {
 __host__ __device__ inline int tc_ntok(int MR) { return MR <= 8 ? 8 : 16; }
 
 // Shared memory before the TMA ring: B operand (bpc*16 words x ntok tokens x
-// 16 bytes), block sums [bpc][MR], tile reduction [2][4][MR][32], and (K split
+// 16 bytes), block sums [bpc][MR], tile reduction [2][4][MR][32], per-warp
+// rings of the scale | zero words of blocks awaiting their fold
+// [8][kDSlots][32], and (K split
 // over a cluster) the partials every rank stores here for the tiles this CTA
 // owns, [tpg][S][MR][128].
 __host__ __device__ inline int tc_base_bytes(int MR, int bpc, int tpg, int S) {
     const int b = bpc * 16 * tc_ntok(MR) * 16 + bpc * MR * 4 + 2 * 4 * MR * 32 * 4 +
-                  (S > 1 ? tpg * S * MR * kRows * 4 : 0);
+                  kDeqWarps * kDSlots * 32 * 4 + (S > 1 ? tpg * S * MR * kRows * 4 : 0);
     return (b + 127) & ~127;
 }
 // Whole dynamic shared memory: 1024 bytes of slack for the ring's alignment,
@@ -126,7 +131,8 @@ k_gemv_tc(const TcArgs a, const __grid_constant__ CUtensorMap wmap) {
     unsigned char* xs = smem_raw;
     float* xsum = reinterpret_cast<float*>(smem_raw + a.bpc * 16 * kWordBytes);
     float* red = xsum + a.bpc * MR;
-    float* part = red + 2 * 4 * MR * 32;
+    uint32_t* szr = reinterpret_cast<uint32_t*>(red + 2 * 4 * MR * 32);  // [8][kDSlots][32]
+    float* part = reinterpret_cast<float*>(szr + kDeqWarps * kDSlots * 32);
     const int base = tc_base_bytes(MR, a.bpc, a.tiles_per_cluster, S);
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* ring = smem_raw + (((raw + base + 1023u) & ~1023u) - raw);
@@ -147,7 +153,7 @@ k_gemv_tc(const TcArgs a, const __grid_constant__ CUtensorMap wmap) {
             mbar_init(full + i, 1);
             mbar_init(empty + i, kDeqWarps);
         }
-        for (int i = 0; i < kASlots; ++i) mbar_init(ready + i, 4);
+        for (int i = 0; i < kASlots; ++i) mbar_init(ready + i, kDeqWarps);
         for (int i = 0; i < kDSlots; ++i) mbar_init(done + i, 1);
         *abort_flag = 0;
         mbar_init_fence();
@@ -235,32 +241,36 @@ k_gemv_tc(const TcArgs a, const __grid_constant__ CUtensorMap wmap) {
 
     if (warp < kDeqWarps) {
         // ------------------------------------------------------------------
-        // unpacking warps: lane quarter q, block parity par.  Block lc of this
-        // parity (counted over tiles) uses A slot 2 par + (lc & 1) and D slot
-        // 8 par + (lc & 7); its D is folded kLag blocks later, so the warp
-        // never waits for the MMAs it just enabled.
+        // unpacking warps: lane quarter q (rows 32q..32q+31), column half h
+        // (words 8h..8h+7 of every block).  All eight warps take every block,
+        // so a block is ready as soon as each has done half of its rows'
+        // work.  Block bg (counted over the CTA's tiles) uses A slot bg % 4 and
+        // D slot bg % 16; before writing A slot bg % 4 a warp waits for the
+        // MMAs of block bg - 4, which is long done in steady state.  Block bf
+        // is folded kLag blocks later by the half h == bf & 1; both halves end
+        // a tile at the same iteration, so their pairing barrier cannot stall
+        // the pipeline.
         // ------------------------------------------------------------------
         const int q = warp & 3;
-        const int par = warp >> 2;
+        const int h = warp >> 2;
         const int row = q * 32 + lane;
         const uint32_t lane_base = tb + (static_cast<uint32_t>(q * 32) << 16);
-        const int cntp = par ? (nb >> 1) : ((nb + 1) >> 1);  // blocks of this parity per tile
-        const int lag = min(kLag, max(cntp, 1));
-        const int total_lc = my_tiles * cntp;
-        // accumulators of even and odd tiles: with lag <= cntp, folds pending at
-        // any time belong to at most two consecutive tiles
+        const int total = my_tiles * nb;
+        const int lag = min(kLag, max(nb, 1));
+        // accumulators of even and odd tiles: with lag <= nb, pending folds
+        // belong to at most two consecutive tiles
         float acc_e[MR], acc_o[MR];
 #pragma unroll
         for (int m = 0; m < MR; ++m) acc_e[m] = acc_o[m] = 0.f;
 
         auto tile_end = [&](int i, float (&acc)[MR]) {
             float* rb = red + ((i & 1) * 4 + q) * MR * 32;
-            if (par == 1) {
+            if (h == 1) {
 #pragma unroll
                 for (int m = 0; m < MR; ++m) rb[m * 32 + lane] = acc[m];
             }
             named_barrier_sync(1 + q, 64);
-            if (par == 0) {
+            if (h == 0) {
                 const int n = (cid + i * ncl) * kRows + row;
 #pragma unroll
                 for (int m = 0; m < MR; ++m) {
@@ -278,127 +288,115 @@ k_gemv_tc(const TcArgs a, const __grid_constant__ CUtensorMap wmap) {
 #pragma unroll
             for (int m = 0; m < MR; ++m) acc[m] = 0.f;
         };
-        // fold block lcf of this parity: acc += s * (D - (128 + z) * sum x)
-        auto fold = [&](int lcf) {
-            const int ti = lcf / cntp;
-            const int j = 2 * (lcf - ti * cntp) + par;
-            const int n = (cid + ti * ncl) * kRows + row;
-            uint32_t sz = 0u;  // rows beyond N: s = 0
-            if (n < a.N) {
-                const size_t gi = static_cast<size_t>(n) * G + (((b0 + j) << 7) / a.g);
-                sz = ldg_nc_u16(a.scale + gi) | (ldg_nc_u8(a.zero + gi) << 16);
+        // block bf: its half folds acc += s * (D - (128 + z) * sum x); at the
+        // tile's last block both halves end the tile
+        auto fold_step = [&](int bf) {
+            const int ti = bf / nb;
+            const int j = bf - ti * nb;
+            if ((bf & 1) == h) {
+                const uint32_t sz = szr[(warp * kDSlots + bf % kDSlots) * 32 + lane];
+                const int dslot = bf % kDSlots;
+                tc_wait(done + dslot, (bf / kDSlots) & 1, abort_flag);
+                tc_fence_after();
+                float d[MR];
+                tmem_ld<MR>(lane_base + kDCol0 + dslot * kDCols, d);
+                tmem_wait_ld();
+                const float s = __uint_as_float(sz << 16);
+                const float o = static_cast<float>(128u + (sz >> 16));
+                const float* xsb = xsum + j * MR;
+                if (ti & 1) {
+#pragma unroll
+                    for (int m = 0; m < MR; ++m)
+                        if (m < a.M) acc_o[m] = fmaf(s, fmaf(-o, xsb[m], d[m]), acc_o[m]);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < MR; ++m)
+                        if (m < a.M) acc_e[m] = fmaf(s, fmaf(-o, xsb[m], d[m]), acc_e[m]);
+                }
             }
-            const int dslot = 8 * par + (lcf & 7);
-            tc_wait(done + dslot, (lcf >> 3) & 1, abort_flag);
-            tc_fence_after();
-            float d[MR];
-            tmem_ld<MR>(lane_base + kDCol0 + dslot * kDCols, d);
-            tmem_wait_ld();
-            const float s = __uint_as_float(sz << 16);
-            const float o = static_cast<float>(128u + (sz >> 16));
-            const float* xsb = xsum + j * MR;
-            const bool last = (lcf - ti * cntp) == cntp - 1;
-            if (ti & 1) {
-#pragma unroll
-                for (int m = 0; m < MR; ++m)
-                    if (m < a.M) acc_o[m] = fmaf(s, fmaf(-o, xsb[m], d[m]), acc_o[m]);
-                if (last) tile_end(ti, acc_o);
-            } else {
-#pragma unroll
-                for (int m = 0; m < MR; ++m)
-                    if (m < a.M) acc_e[m] = fmaf(s, fmaf(-o, xsb[m], d[m]), acc_e[m]);
-                if (last) tile_end(ti, acc_e);
+            if (j == nb - 1) {
+                if (ti & 1) tile_end(ti, acc_o);
+                else tile_end(ti, acc_e);
             }
         };
 
+        int bg = 0;
         for (int st = 0; st < total_st; ++st) {
             const int i = st / nss;
             const int s2 = st - i * nss;
-            const int j = 2 * s2 + par;
             const int sidx = st % NS;
             tc_wait(full + sidx, (st / NS) & 1, abort_flag);
-            if (j < nb) {
-                // this row's 64 bytes of the block (128-byte swizzle: chunk c
-                // of row r sits at chunk c ^ (r % 8))
-                const unsigned char* src = ring + sidx * kStageBytes + row * 128;
-                uint4 wv[4];
+            const unsigned char* src = ring + sidx * kStageBytes + row * 128;
+            for (int half = 0; half < 2; ++half) {
+                const int j = 2 * s2 + half;
+                if (j >= nb) break;
+                // this warp's 8 words of the block: chunks 2h, 2h + 1 of the
+                // block's 4 (128-byte swizzle: chunk c of row r at c ^ (r % 8))
+                const int c0 = (half << 2) + 2 * h;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(src + ((c0 ^ (row & 7)) << 4));
+                const uint4 w1 = *reinterpret_cast<const uint4*>(src + (((c0 + 1) ^ (row & 7)) << 4));
+                const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint32_t A[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    wv[c] = *reinterpret_cast<const uint4*>(
-                        src + ((((j & 1) << 2) + c) ^ (row & 7)) * 16);
-                uint32_t A0[32], A1[32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t ws[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int w = 4 * c + e;  // word: k = 8 w .. 8 w + 7 of the block
-                        uint32_t* dst = (w < 8) ? &A0[4 * w] : &A1[4 * (w - 8)];
-                        const uint32_t u = ws[e];
-                        dst[0] = (u & 0x000F000Fu) | 0x43004300u;
-                        dst[1] = ((u >> 4) & 0x000F000Fu) | 0x43004300u;
-                        dst[2] = ((u >> 8) & 0x000F000Fu) | 0x43004300u;
-                        dst[3] = ((u >> 12) & 0x000F000Fu) | 0x43004300u;
-                    }
+                for (int w = 0; w < 8; ++w) {  // word 8h + w: k = 8 (8h + w) .. + 7 of the block
+                    const uint32_t u = ws[w];
+                    A[4 * w + 0] = (u & 0x000F000Fu) | 0x43004300u;
+                    A[4 * w + 1] = ((u >> 4) & 0x000F000Fu) | 0x43004300u;
+                    A[4 * w + 2] = ((u >> 8) & 0x000F000Fu) | 0x43004300u;
+                    A[4 * w + 3] = ((u >> 12) & 0x000F000Fu) | 0x43004300u;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty + sidx);  // stage read by this warp
-                const int lc = i * cntp + s2;
-                {  // this block's scale and zero point, read when it is folded
+                // this half folds the block kLag blocks later: load its scale and
+                // zero point now (stored to the ring at the end of the iteration,
+                // so the loads' latency overlaps the block's TMEM traffic)
+                const bool folds = (bg & 1) == h;
+                uint32_t sz_new = 0u;  // rows beyond N: s = 0
+                {
                     const int n = (cid + i * ncl) * kRows + row;
-                    if (n < a.N) {
+                    if (folds && n < a.N) {
                         const size_t gi = static_cast<size_t>(n) * G + (((b0 + j) << 7) / a.g);
-                        prefetch_l1(a.scale + gi);
-                        prefetch_l1(a.zero + gi);
+                        sz_new = ldg_nc_u16(a.scale + gi) | (ldg_nc_u8(a.zero + gi) << 16);
                     }
                 }
-                if (lc >= 2)  // A slot free: the MMAs of block lc - 2 have completed
-                    tc_wait(done + 8 * par + ((lc - 2) & 7), ((lc - 2) >> 3) & 1, abort_flag);
+                if (bg >= kASlots)  // A slot free: the MMAs of block bg - 4 have completed
+                    tc_wait(done + (bg - kASlots) % kDSlots, ((bg - kASlots) / kDSlots) & 1,
+                            abort_flag);
                 tc_fence_after();
-                const int aslot = 2 * par + (lc & 1);
-                tmem_st_x32(lane_base + aslot * kACols, A0);
-                tmem_st_x32(lane_base + aslot * kACols + 32, A1);
+                tmem_st_x32(lane_base + (bg % kASlots) * kACols + h * 32, A);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(ready + aslot);
-                if (lc >= lag) fold(lc - lag);
-            } else {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty + sidx);  // odd block count: no block here
+                if (lane == 0) mbar_arrive(ready + bg % kASlots);
+                if (bg >= lag) fold_step(bg - lag);
+                if (folds) szr[(warp * kDSlots + bg % kDSlots) * 32 + lane] = sz_new;
+                ++bg;
             }
-            // no block of this parity in any tile: still meet the partner warp
-            // once per tile, in tile order
-            if (cntp == 0 && s2 == nss - 1) tile_end(i, acc_e);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + sidx);  // both blocks of the stage read
         }
-        if (cntp == 0 && nss == 0)
-            for (int i = 0; i < my_tiles; ++i) tile_end(i, acc_e);
-        for (int lcf = max(0, total_lc - lag); lcf < total_lc; ++lcf) fold(lcf);
+        for (int bf = max(0, total - lag); bf < total; ++bf) fold_step(bf);
     } else if (warp == kProducerWarp) {
         if (lane == 0) produce(total_st);
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             const uint32_t xs_addr = smem_addr(xs);
-            const int cnt0 = (nb + 1) >> 1, cnt1 = nb >> 1;  // blocks per tile of each parity
-            for (int i = 0; i < my_tiles; ++i)
-                for (int j = 0; j < nb; ++j) {
-                    const int par = j & 1;
-                    const int lc = i * (par ? cnt1 : cnt0) + (j >> 1);
-                    const int aslot = 2 * par + (lc & 1);
-                    const int dslot = 8 * par + (lc & 7);
-                    tc_wait(ready + aslot, (lc >> 1) & 1, abort_flag);
-                    tc_fence_after();
-                    const uint32_t a_t = tb + aslot * kACols;
-                    const uint32_t d_t = tb + kDCol0 + dslot * kDCols;
+            const int total = my_tiles * nb;
+            for (int bg = 0; bg < total; ++bg) {
+                const int j = bg % nb;
+                const int aslot = bg % kASlots;
+                const int dslot = bg % kDSlots;
+                tc_wait(ready + aslot, (bg / kASlots) & 1, abort_flag);
+                tc_fence_after();
+                const uint32_t a_t = tb + aslot * kACols;
+                const uint32_t d_t = tb + kDCol0 + dslot * kDCols;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t desc =
-                            smem_desc_kmajor(xs_addr + (j * 16 + 2 * kk) * kWordBytes, kWordBytes,
-                                             NTOK == 16 ? 128u : 0u);
-                        tc_mma_tmem_a(d_t, a_t + kk * 8, desc, kIdesc, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(done + dslot);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t desc =
+                        smem_desc_kmajor(xs_addr + (j * 16 + 2 * kk) * kWordBytes, kWordBytes,
+                                         NTOK == 16 ? 128u : 0u);
+                    tc_mma_tmem_a(d_t, a_t + kk * 8, desc, kIdesc, kk > 0 ? 1u : 0u);
                 }
+                tc_commit(done + dslot);
+            }
         }
     }
 
