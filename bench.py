@@ -325,6 +325,21 @@ def run_profile(args):
     import __graft_entry__
     __graft_entry__.build()
     from w4a16_int4_weight_gemv_gb300 import binding as w
+    if args.workload == "moe":
+        # the routed SwiGLU expert FFN (64 experts, H=2304, F=1024, top-8)
+        from w4a16_int4_weight_gemv_gb300 import synth
+        M = args.M or 1
+        p = synth.moe_problem(M=M, E=64, H=2304, F=1024, topk=8, g=128, seed=0)
+        b = dict(x=_dev(p["x"], torch), ids=_dev(p["ids"], torch), r=_dev(p["route_w"], torch),
+                 gate=tuple(_dev(a, torch) for a in p["gate"]),
+                 up=tuple(_dev(a, torch) for a in p["up"]),
+                 down=tuple(_dev(a, torch) for a in p["down"]))
+        for i in range(args.warmup + args.steps):
+            w.moe_ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_workload": "moe", "M": M, "launches_per_chain": 3,
+                          "chains": args.warmup + args.steps}))
+        return
     M, N, K, zmode, od = WORKLOADS[args.workload]
     M = args.M or M
     l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or 126 * 2**20
@@ -550,7 +565,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
                     help="plain launches of --workload for a profiler; prints no bench line")
-    ap.add_argument("--workload", default="square", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="square", choices=sorted(list(WORKLOADS) + ["moe"]))
     ap.add_argument("--M", type=int, default=0)
     ap.add_argument("--kernel-id", type=int, default=0)
     args = ap.parse_args()
