@@ -228,21 +228,23 @@ W4A16_API w4a16_status w4a16_moe_gemv_fixed_scratch(const uint16_t* x, int x_per
 
 /*
  * w4a16_moe_ffn_workspace_bytes -- workspace w4a16_moe_ffn needs: bf16 gate
- * and up outputs [M][topk][F] and fp32 partials [M][topk][H], each rounded
- * up to 256 bytes.
+ * and up outputs [M][topk][F], fp32 partials [M][topk][H] and one 32-bit
+ * counter per 64 rows of H, each part rounded up to 256 bytes.  Its contents
+ * need no initialisation.
  */
 W4A16_API size_t w4a16_moe_ffn_workspace_bytes(int M, int topk, int64_t H, int64_t F);
 
 /*
  * w4a16_moe_ffn -- the routed SwiGLU expert FFN of M tokens (README
  * technical-detail section: the grouped expert kernel; its kernel registry
- * names the SwiGLU op), in three launches:
+ * names the SwiGLU op), in two launches:
  *   1. gate and up products of every routed slot, both banks in one launch:
  *        G[t][j] = bf16(W^gate_e x[t]),  U[t][j] = bf16(W^up_e x[t]),
  *   2. down products of h[t][j] = bf16(silu(G[t][j]) * U[t][j]) (computed in
  *      fp32 exactly as w4a16_swiglu does, while staging the activations),
  *   3. y[t] = bf16(sum_j route_w[t][j] * (W^down_e h[t][j])) (fp32 sum, j
- *      ascending).
+ *      ascending), formed inside the down launch by the last CTA to finish
+ *      each row chunk.
  * Each distinct expert's three matrices are streamed once per call.
  *   x: bf16 [M][H]; expert_ids: int32 [M][topk]; route_w: fp32 [M][topk];
  *   gate, up: wq [E][F][H/8], scale and zero [E][F][H/g];

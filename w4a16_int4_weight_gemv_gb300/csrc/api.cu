@@ -322,7 +322,9 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 size_t w4a16_moe_ffn_workspace_bytes(int M, int topk, int64_t H, int64_t F) {
     if (M < 1 || topk < 1 || H < 1 || F < 1) return 0;
     const size_t S = static_cast<size_t>(M) * static_cast<size_t>(topk);
-    return 2 * align256(S * static_cast<size_t>(F) * 2) + align256(S * static_cast<size_t>(H) * 4);
+    const size_t chunks = static_cast<size_t>((H + 63) / 64);
+    return 2 * align256(S * static_cast<size_t>(F) * 2) + align256(S * static_cast<size_t>(H) * 4) +
+           align256(chunks * sizeof(unsigned));
 }
 
 w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const float* route_w,
@@ -360,6 +362,7 @@ w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const f
     uint16_t* g_out = reinterpret_cast<uint16_t*>(ws);
     uint16_t* u_out = reinterpret_cast<uint16_t*>(ws + align256(S * F * 2));
     float* part = reinterpret_cast<float*>(ws + 2 * align256(S * F * 2));
+    unsigned* counters = reinterpret_cast<unsigned*>(ws + 2 * align256(S * F * 2) + align256(S * H * 4));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // gate and up products of every slot: one launch over both banks
     MoeArgs a{};
@@ -368,6 +371,8 @@ w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const f
     a.bank[0] = MoeBank{gate_wq, gate_scale, gate_zero, g_out};
     a.bank[1] = MoeBank{up_wq, up_scale, up_zero, u_out};
     a.nbanks = 2;
+    a.zero_count = counters;  // for the down launch's in-launch routed sum
+    a.zero_n = moe_row_chunks(static_cast<int>(H));
     a.M = M;
     a.topk = topk;
     a.E = E;
@@ -377,7 +382,8 @@ w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const f
     a.err = dev->err;
     cudaError_t e = launch_moe(a, dev->info, s);
     if (e != cudaSuccess) return from_cuda(e);
-    // down products of h = silu(gate) * up (formed while staging) and the routed sum
+    // down products of h = silu(gate) * up (formed while staging); the last
+    // CTA of each row chunk forms that chunk's routed sums
     MoeArgs d{};
     d.sw_gate = g_out;
     d.sw_up = u_out;
@@ -388,6 +394,7 @@ w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const f
     d.early = 1;  // the gate/up launch signals its dependents only after its own wait
     d.y_routed = y;
     d.ws = part;
+    d.chunk_count = counters;  // routed sum by the last CTA of each row chunk
     d.M = M;
     d.topk = topk;
     d.E = E;

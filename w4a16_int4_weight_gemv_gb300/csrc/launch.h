@@ -141,6 +141,10 @@ struct MoeArgs {
                               // grid dependency wait (the predecessor is this chain's own)
     uint16_t* y_routed;       // bf16 [M][N]
     float* ws;                // fp32 [M*topk][N] partials of the routed sum
+    unsigned* chunk_count;    // non-null: the routed sum is formed inside the launch, per
+                              // 64/128-row chunk, by its last CTA (counters zero on entry)
+    unsigned* zero_count;     // counters this launch zeroes first (for the next launch)
+    int zero_n;
     int M;
     int topk;
     int E;
@@ -151,6 +155,8 @@ struct MoeArgs {
 };
 // Dynamic shared memory the expert kernel needs at least (two stages).
 int moe_smem_need(int M, int K, int g);
+// Number of row chunks (CTAs along x) of an expert launch for N rows.
+int moe_row_chunks(int N);
 cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s);
 
 cudaError_t launch_pack(const uint8_t* codes, uint32_t* wq, int64_t N, int64_t K, int sms,

@@ -64,6 +64,14 @@ struct MoeKernelArgs {
     int g;
     int stages;
     int early;  // ids, weights, scales may be read before the grid dependency wait
+    // Routed sum inside the launch (fused FFN chain): per 64-row chunk, the
+    // last CTA to finish its partials adds every token's slots in slot order.
+    unsigned* chunk_count;  // [gridDim.x] arrival counters (zero between calls)
+    const float* route_w;
+    uint16_t* y_routed;     // bf16 [M][N]
+    // zero these counters (the next launch's) before anything else
+    unsigned* zero_count;
+    int zero_n;
     uint32_t* err;
 };
 
@@ -81,6 +89,48 @@ __host__ __device__ inline MoeLayout moe_layout(int Mpad, int nblk, int G, int t
 }
 __host__ __device__ inline int moe_smem_bytes(int Mpad, int nblk, int G, int tiles, int ns) {
     return moe_layout(Mpad, nblk, G, tiles).base + 1024 + kWarps * ns * (kStageA + 8);
+}
+
+// y[t][n] = bf16(sum_j r[t][j] * ws[t][j][n]) over slots with a valid expert
+// id, for rows n in [n0, n1): fp32, j ascending (the same order as
+// k_moe_route_sum).
+__device__ __forceinline__ void moe_route_rows(const float* ws, const float* route_w,
+                                               const int* ids, uint16_t* y, int M, int topk,
+                                               int E, int N, int n0, int n1) {
+    const int rows = n1 - n0;
+    for (int i = threadIdx.x; i < M * rows; i += blockDim.x) {
+        const int t = i / rows;
+        const int n = n0 + (i - t * rows);
+        float v = 0.f;
+        for (int j = 0; j < topk; ++j) {
+            const int e = ids[t * topk + j];
+            if (e < 0 || e >= E) continue;
+            v = fmaf(route_w[t * topk + j], ws[(static_cast<size_t>(t) * topk + j) * N + n], v);
+        }
+        y[static_cast<size_t>(t) * N + n] = f32_to_bf16_rn(v);
+    }
+}
+
+// The chunk's partials of this CTA are written (or it has none): count it;
+// the CTA that completes the count forms the chunk's routed sums and resets
+// the counter for the next call.
+template <int ROWS>
+__device__ __forceinline__ void moe_chunk_done(const MoeKernelArgs& a, const int* ids) {
+    if (!a.chunk_count) return;
+    __shared__ unsigned s_last;
+    __threadfence();  // this CTA's partials are visible device-wide before it is counted
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned total = gridDim.y * gridDim.z;
+        s_last = (atomicAdd(a.chunk_count + blockIdx.x, 1u) == total - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();  // every counted CTA's partials are visible to this one
+    const int n0 = blockIdx.x * ROWS;
+    moe_route_rows(a.ws, a.route_w, ids, a.y_routed, a.M, a.topk, a.E, a.N, n0,
+                   min(a.N, n0 + ROWS));
+    if (threadIdx.x == 0) a.chunk_count[blockIdx.x] = 0u;
 }
 
 template <int NT, int TILES>
@@ -118,6 +168,8 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     // and scales -- inputs of the whole chain -- are read first and only the
     // activations and outputs wait.
     if (!a.early) grid_dependency_wait();
+    if (a.zero_count && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int i = threadIdx.x; i < a.zero_n; i += blockDim.x) a.zero_count[i] = 0u;
 
     // 1. which expert does this CTA serve?
     for (int i = threadIdx.x; i < S; i += blockDim.x) s_ids[i] = a.ids[i];
@@ -153,6 +205,10 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     }
     if (e < 0) {
         grid_dependents_launch();
+        if (a.chunk_count) {
+            grid_dependency_wait();  // the counters were zeroed by the preceding launch
+            moe_chunk_done<kRowsPerCta>(a, s_ids);
+        }
         return;
     }
 
@@ -363,6 +419,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
         __syncthreads();  // s_rowsel, xs and red are rewritten by the next pass
     }
     if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
+    moe_chunk_done<kRowsPerCta>(a, s_ids);
 }
 
 // y[t][n] = sum_j r[t][j] * ws[t][j][n] over slots with a valid expert id.
@@ -391,6 +448,8 @@ MoeKernel pick_moe_kernel(int Mpad, int tiles) {
 }
 
 }  // namespace
+
+int moe_row_chunks(int N) { return (N + 63) / 64; }
 
 int moe_smem_need(int M, int K, int g) {
     return moe_smem_bytes(M <= 8 ? 8 : 16, K / 128, K / g, 8, 2);
@@ -433,6 +492,11 @@ cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) 
         ++ns;
     k.stages = ns;
     k.early = a.early;
+    k.chunk_count = a.chunk_count;
+    k.route_w = a.route_w;
+    k.y_routed = a.y_routed;
+    k.zero_count = a.zero_count;
+    k.zero_n = a.zero_n;
     const int smem = moe_smem_bytes(Mpad, nblk, G, tiles, ns);
     if (smem > dev.max_smem_optin) return cudaErrorInvalidValue;
     CUtensorMap maps[2];
@@ -456,7 +520,7 @@ cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) 
     e = cudaLaunchKernelEx(&cfg, kern, k, maps[0], maps[1]);
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
-    if (e != cudaSuccess || !a.route_w) return e;
+    if (e != cudaSuccess || !a.route_w || a.chunk_count) return e;  // routed sum done in-launch
     const int total = a.M * a.N;
     int blocks = (total + 255) / 256;
     if (blocks > 4 * dev.sms) blocks = 4 * dev.sms;
