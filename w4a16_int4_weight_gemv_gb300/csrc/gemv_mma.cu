@@ -34,8 +34,10 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+// Warps per CTA: 12 when the tokens fit one 8-column MMA tile and the
+// activation slice is small (more warps to cover the MMA and dequant
+// latencies), else 8 (shared memory goes to the activations and the rings).
+int mma_warps_for(int M, int K) { return (M <= 8 && K <= 8192) ? 12 : 8; }
 constexpr int kSB = 4;           // 128-k blocks per step (512 k)
 constexpr int kHalfBytes = 2048;  // one tensor box: 16 rows x 128 bytes
 constexpr int kStageA = 2 * kHalfBytes;
@@ -79,17 +81,18 @@ __host__ __device__ inline int mma_base_bytes(int M, int NT, int upc, int tg, in
 
 // Whole dynamic shared memory for NS stages per warp; 1024 bytes of slack
 // let the A rings start on the 1024-byte boundary the swizzle needs.
-__host__ __device__ inline int mma_smem_bytes(int base, int ns) {
-    return base + 1024 + kWarps * ns * (kStageA + kStageSZ + 8) + 16;
+__host__ __device__ inline int mma_smem_bytes(int base, int ns, int warps) {
+    return base + 1024 + warps * ns * (kStageA + kStageSZ + 8) + 16;
 }
 
 // kFast: g == 128 and K % 512 == 0 -- a step's scales and zero points are
 // whole 8- and 4-byte pieces per row, copied with cp.async into the stage.
 // Otherwise the consumer loads the two rows' pair for each block itself.
-template <int NT, bool kFast>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NT, bool kFast, int W>
+__global__ void __launch_bounds__(W * 32, 1)
 k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
     constexpr int Mpad = 8 * NT;
+    constexpr int kWarps = W;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -350,10 +353,13 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
 
 using MmaKernel = void (*)(MmaKernelArgs, CUtensorMap);
 
-MmaKernel pick_mma_kernel(int M, int K, int g) {
+MmaKernel pick_mma_kernel(int M, int K, int g, int warps) {
     const bool fast = (g == 128) && (K % 512 == 0);
-    return (M <= 8) ? (fast ? k_gemv_mma<1, true> : k_gemv_mma<1, false>)
-                    : (fast ? k_gemv_mma<2, true> : k_gemv_mma<2, false>);
+    if (warps == 12)
+        return (M <= 8) ? (fast ? k_gemv_mma<1, true, 12> : k_gemv_mma<1, false, 12>)
+                        : (fast ? k_gemv_mma<2, true, 12> : k_gemv_mma<2, false, 12>);
+    return (M <= 8) ? (fast ? k_gemv_mma<1, true, 8> : k_gemv_mma<1, false, 8>)
+                    : (fast ? k_gemv_mma<2, true, 8> : k_gemv_mma<2, false, 8>);
 }
 
 }  // namespace
@@ -363,32 +369,33 @@ GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_
     const int units_all = (nblk + kSB - 1) / kSB;
     const int ntiles = (N + 15) / 16;
     const int NT = (M <= 8) ? 1 : 2;
-    const void* kern = reinterpret_cast<const void*>(pick_mma_kernel(M, K, g));
+    const int W = mma_warps_for(M, K);
+    const void* kern = reinterpret_cast<const void*>(pick_mma_kernel(M, K, g, W));
     // the launch fills the CTA's shared memory with stages, so co-residency of
     // clusters is queried at the full budget, not at the two-stage minimum
     const int budget = dev.max_smem_optin;
     const SplitChoice c = choose_split(
-        dev, ntiles, units_all, kWarps, 1, k_split_req,
-        [M, NT](int upc, int tg, int wpt, int tpg, int S) {
-            return mma_smem_bytes(mma_base_bytes(M, NT, upc, tg, wpt, tpg, S), 2);
+        dev, ntiles, units_all, W, 1, k_split_req,
+        [M, NT, W](int upc, int tg, int wpt, int tpg, int S) {
+            return mma_smem_bytes(mma_base_bytes(M, NT, upc, tg, wpt, tpg, S), 2, W);
         },
-        [kern, budget](int S, int) { return max_active_clusters(kern, kThreads, budget, S); });
+        [kern, budget, W](int S, int) { return max_active_clusters(kern, W * 32, budget, S); });
     GemvPlan p{};
     p.kernel_id = 2;
     p.k_split = c.S;
     p.wpt = c.wpt;
     p.units_per_cta = c.units_per_cta;
-    p.threads = kThreads;
+    p.threads = W * 32;
     p.ctas = c.ctas;
     p.tiles_per_cluster = c.tiles_per_group;
     if (c.ctas > 0) {
-        const int base = mma_base_bytes(M, NT, c.units_per_cta, kWarps / c.wpt, c.wpt,
+        const int base = mma_base_bytes(M, NT, c.units_per_cta, W / c.wpt, c.wpt,
                                         c.tiles_per_group, c.S);
         const int max_steps = c.tiles_per_group * ((c.units_per_cta + c.wpt - 1) / c.wpt);
         int ns = 2;
-        while (ns < kMaxStages && ns < max_steps && mma_smem_bytes(base, ns + 1) <= budget) ++ns;
+        while (ns < kMaxStages && ns < max_steps && mma_smem_bytes(base, ns + 1, W) <= budget) ++ns;
         p.stages = ns;
-        p.smem_bytes = mma_smem_bytes(base, ns);
+        p.smem_bytes = mma_smem_bytes(base, ns, W);
     }
     return p;
 }
@@ -413,7 +420,7 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s
     k.err = a.err;
     CUtensorMap wmap;
     if (!encode_weight_map(&wmap, a.wq, a.N, a.K, kBoxRows)) return cudaErrorInvalidValue;
-    MmaKernel kern = pick_mma_kernel(a.M, a.K, a.g);
+    MmaKernel kern = pick_mma_kernel(a.M, a.K, a.g, p.threads / 32);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          p.smem_bytes);
     if (e != cudaSuccess) return e;

@@ -70,7 +70,10 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
         if (forced_f > 0 && f != forced_f) continue;
         if (forced_f == 0 && f > units_all) break;
         // largest in-CTA share first: on equal cost the fewest CTAs per cluster
-        for (int wpt = (f < warps_per_cta ? f : warps_per_cta); wpt >= 1; wpt /= 2) {
+        // (wpt runs over the powers of two <= min(f, warps per CTA))
+        int wpt0 = 1;
+        while (wpt0 * 2 <= f && wpt0 * 2 <= warps_per_cta) wpt0 *= 2;
+        for (int wpt = wpt0; wpt >= 1; wpt /= 2) {
             const int S = f / wpt;
             if (S > 8 || wpt * S != f || warps_per_cta % wpt) continue;
             const int upc = (units_all + S - 1) / S;
