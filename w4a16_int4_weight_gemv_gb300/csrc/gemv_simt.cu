@@ -290,9 +290,12 @@ k_gemv_simt(const SimtKernelArgs a) {
     };
 
     // The activations gate all arithmetic: their loads are issued before the
-    // weight rings so they are not queued behind the weight stream.  With
-    // static weights one stage per warp is already requested while the
-    // preceding grid finishes.
+    // weight rings so they are not queued behind the weight stream, and only
+    // one stage per warp is requested before they are converted -- issuing a
+    // whole ring per warp here (tens of MB over the GPU) stalls the warps on
+    // memory back-pressure before they reach the conversion.  The rings are
+    // topped up once x' is staged.  With static weights that one stage is
+    // requested while the preceding grid finishes.
     if (a.weights_static && nss > 0) issue();
     grid_dependency_wait();
     constexpr int kXPre = 4;  // pieces per thread and token loaded ahead
@@ -302,7 +305,7 @@ k_gemv_simt(const SimtKernelArgs a) {
 #pragma unroll
         for (int j = 0; j < kXPre; ++j) xpre[m][j] = load_piece(m, threadIdx.x + j * blockDim.x);
     __syncthreads();
-    while (w_issued < NS && w_issued < nss) issue();
+    if (w_issued == 0 && nss > 0) issue();
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -313,6 +316,7 @@ k_gemv_simt(const SimtKernelArgs a) {
         for (int b = kXPre * blockDim.x; b < npieces; b += blockDim.x)
             store_piece(m, b + threadIdx.x, load_piece(m, b + threadIdx.x));
     __syncthreads();
+    while (w_issued < NS && w_issued < nss) issue();
 
     float acc[TR][MT];
 #pragma unroll
