@@ -196,11 +196,15 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
                           static_cast<uint32_t>(nb * 256), xbar);
     }
     __syncthreads();
-    while (w_issued < NS && w_issued < nss) issue();
+    // one stage per warp before the pairing pass, the rest after it: issuing
+    // whole rings here stalls the warps on memory back-pressure before they
+    // reach the pass
+    if (w_issued == 0 && nss > 0) issue();
 
     bool timed_out = !mbar_wait_bounded(xbar, 0);
     pair_x_in_place<NT>(a.M, nb, xs, xsum, tok_stride);
     __syncthreads();
+    while (w_issued < NS && w_issued < nss) issue();
 
     float acc[NT][4];
 #pragma unroll
