@@ -29,6 +29,8 @@
 // With route weights the per-slot results go to an fp32 workspace and a
 // second kernel forms y[t] = sum_j r[t][j] d[t][j] in slot order -- a fixed
 // order, so the result is deterministic (no floating-point atomics).
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 #include "mma_core.cuh"
@@ -47,6 +49,8 @@ constexpr unsigned kBoxRows = 16;
 constexpr int kMaxSlots = 256;
 constexpr int kMaxTableGroups = 64;      // scale/zero table in shared memory up to G = 64
 constexpr int kMaxStages = 4;
+constexpr int kTabBatch = 12;            // table entries per thread per load batch
+constexpr int kSwBatch = 2;              // gate/up pieces per thread per load batch
 
 struct MoeKernelArgs {
     const uint16_t* x;
@@ -82,7 +86,8 @@ __host__ __device__ inline MoeLayout moe_layout(int Mpad, int nblk, int G, int t
     MoeLayout L;
     L.xsum = Mpad * mma_token_stride(nblk);
     L.red = L.xsum + nblk * Mpad * 4;
-    L.tab = L.red + tiles * 16 * Mpad * 4;
+    // K-half partials only when two warps share a tile (4-tile CTAs)
+    L.tab = L.red + (kWarps / tiles > 1 ? tiles * 16 * Mpad * 4 : 0);
     const int end = L.tab + (G <= kMaxTableGroups ? tiles * 16 * G * 4 : 0);
     L.base = (end + 127) & ~127;
     return L;
@@ -143,11 +148,9 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     constexpr int kRowsPerCta = kTiles * 16;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ int s_ids[kMaxSlots];
-    __shared__ unsigned char s_first[kMaxSlots];
+    __shared__ unsigned char s_slots[kMaxSlots];
+    __shared__ unsigned s_mask[kWarps];
     __shared__ int s_expert;
-    __shared__ int s_nslots;
-    __shared__ int s_slots[kMaxSlots];
-    __shared__ int s_rowsel[Mpad];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -171,24 +174,32 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     if (a.zero_count && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
         for (int i = threadIdx.x; i < a.zero_n; i += blockDim.x) a.zero_count[i] = 0u;
 
-    // 1. which expert does this CTA serve?
-    for (int i = threadIdx.x; i < S; i += blockDim.x) s_ids[i] = a.ids[i];
+    // 1. which expert does this CTA serve?  One thread per routed slot
+    // (S <= kThreads): a slot is its expert's first if no earlier slot names
+    // the same expert; the first slots are counted in slot order by ballots.
+    const int si = threadIdx.x;
+    int my_id = -1;
+    if (si < S) {
+        my_id = a.ids[si];
+        s_ids[si] = my_id;
+    }
     if (threadIdx.x == 0) s_expert = -1;
     __syncthreads();
-    for (int i = threadIdx.x; i < S; i += blockDim.x) {
-        const int e = s_ids[i];
-        bool first = (e >= 0 && e < a.E);
+    bool first = false;
+    if (si < S) {
+        first = (my_id >= 0 && my_id < a.E);
         if (!first && blockIdx.x == 0 && blockIdx.y == 0 && z == 0)
             raise_device_error(a.err, W4A16_DEVERR_EXPERT_ID);
-        for (int j = 0; j < i && first; ++j) first = (s_ids[j] != e);
-        s_first[i] = first ? 1 : 0;
+        for (int j = 0; j < si && first; ++j) first = (s_ids[j] != my_id);
     }
+    const unsigned lt = (1u << lane) - 1u;
+    unsigned fm = __ballot_sync(0xFFFFFFFFu, first);
+    if (lane == 0) s_mask[warp] = fm;
     __syncthreads();
-    for (int i = threadIdx.x; i < S; i += blockDim.x) {
-        if (!s_first[i]) continue;
-        int ord = 0;
-        for (int j = 0; j < i; ++j) ord += s_first[j];
-        if (ord == static_cast<int>(blockIdx.y)) s_expert = s_ids[i];
+    if (first) {
+        int ord = __popc(fm & lt);
+        for (int w = 0; w < warp; ++w) ord += __popc(s_mask[w]);
+        if (ord == static_cast<int>(blockIdx.y)) s_expert = my_id;
     }
     __syncthreads();
     const int e = s_expert;
@@ -212,12 +223,10 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
         return;
     }
 
-    if (threadIdx.x == 0) {
-        int n = 0;
-        for (int i = 0; i < S; ++i)
-            if (s_ids[i] == e) s_slots[n++] = i;
-        s_nslots = n;
-    }
+    // the slots routed to e, in slot order
+    const bool mine = (si < S) && my_id == e;
+    fm = __ballot_sync(0xFFFFFFFFu, mine);
+    if (lane == 0) s_mask[warp] = fm;  // its earlier reads all precede the last barrier
 
     const MoeLayout lay = moe_layout(Mpad, nblk, G, kTiles);
     unsigned char* xs = smem_raw;
@@ -240,10 +249,60 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
         for (int i = 0; i < NS; ++i) mbar_init(bars + i, 1);
         mbar_init_fence();
     }
-    __syncthreads();  // s_nslots, barriers
-    const int nslots = s_nslots;
+    __syncthreads();  // s_mask, barriers
+    int nslots = 0;
+    if (mine) {
+        int pos = __popc(fm & lt);
+        for (int w = 0; w < warp; ++w) pos += __popc(s_mask[w]);
+        s_slots[pos] = static_cast<unsigned char>(si);
+    }
+    for (int w = 0; w < kWarps; ++w) nslots += __popc(s_mask[w]);
+    __syncthreads();  // s_slots
     const int npass = (nslots + Mpad - 1) / Mpad;
     const int total = npass * steps_mine;  // every pass streams the same weights
+
+    // 2. Loads issued before the weight copies, so that they are not queued
+    // behind this CTA's (and every other CTA's) weight stream: the first
+    // batch of the CTA's scales and zero points and, when they are plain
+    // inputs, the first pass's activation rows.
+    const uint16_t* escale = bank.scale + static_cast<size_t>(e) * a.N * G;
+    const uint8_t* ezero = bank.zero + static_cast<size_t>(e) * a.N * G;
+    const int nent = use_table ? kTiles * 16 * G : 0;  // scale | zero << 16 per (row, group)
+    uint32_t tv[kTabBatch];
+    auto tab_load = [&](int i0) {
+#pragma unroll
+        for (int j = 0; j < kTabBatch; ++j) {
+            const int i = i0 + j * kThreads + static_cast<int>(threadIdx.x);
+            const int rr = i / G;
+            const int n = blockIdx.x * kRowsPerCta + rr;
+            tv[j] = 0u;
+            if (i < nent && n < a.N) {
+                const size_t gi = static_cast<size_t>(n) * G + (i - rr * G);
+                tv[j] = ldg_nc_u16(escale + gi) | (ldg_nc_u8(ezero + gi) << 16);
+            }
+        }
+    };
+    auto tab_store = [&](int i0) {
+#pragma unroll
+        for (int j = 0; j < kTabBatch; ++j) {
+            const int i = i0 + j * kThreads + static_cast<int>(threadIdx.x);
+            if (i < nent) tab[i] = tv[j];
+        }
+    };
+    // activation rows of slots [base, base + m) to xs (natural order)
+    auto stage_x_async = [&](int base, int m) {
+        const int pieces = m * nblk * 16;  // 16-byte pieces of 8 values
+        for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+            const int n = i / (nblk * 16);
+            const int p = i - n * nblk * 16;
+            const int slot = s_slots[base + n];
+            const int row = a.x_per_slot ? slot : slot / a.topk;
+            cp_async_16(xs + n * tok_stride + p * 16, a.x + static_cast<size_t>(row) * a.K + p * 8);
+        }
+    };
+    const bool x_first = !a.sw_gate && !a.early;  // first pass's rows may be read now
+    if (nent > 0) tab_load(0);
+    if (x_first) stage_x_async(0, min(Mpad, nslots));
 
     // producer cursor over (pass, step); the weights do not depend on the pass
     int w_i = 0;
@@ -265,19 +324,11 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     };
     while (w_i < NS && w_i < total) issue();
 
-    // scale | zero << 16 of every (row, group) of this CTA's rows
-    const uint16_t* escale = bank.scale + static_cast<size_t>(e) * a.N * G;
-    const uint8_t* ezero = bank.zero + static_cast<size_t>(e) * a.N * G;
-    if (use_table) {
-        for (int i = threadIdx.x; i < kTiles * 16 * G; i += blockDim.x) {
-            const int rr = i / G;
-            const int n = blockIdx.x * kRowsPerCta + rr;
-            uint32_t v = 0u;
-            if (n < a.N) {
-                const size_t gi = static_cast<size_t>(n) * G + (i - rr * G);
-                v = ldg_nc_u16(escale + gi) | (ldg_nc_u8(ezero + gi) << 16);
-            }
-            tab[i] = v;
+    if (nent > 0) {
+        tab_store(0);
+        for (int i0 = kTabBatch * kThreads; i0 < nent; i0 += kTabBatch * kThreads) {
+            tab_load(i0);
+            tab_store(i0);
         }
     }
 
@@ -297,43 +348,45 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
 
     for (int base = 0; base < nslots; base += Mpad) {
         const int m = min(Mpad, nslots - base);
-        if (threadIdx.x < Mpad) {
-            int rs = -1;
-            if (static_cast<int>(threadIdx.x) < m) {
-                const int slot = s_slots[base + threadIdx.x];
-                rs = (a.x_per_slot || a.sw_gate) ? slot : slot / a.topk;
-            }
-            s_rowsel[threadIdx.x] = rs;
-        }
-        __syncthreads();
-        // 2. activations of the pass's slots, natural order, then paired in place
-        const int pieces = m * nblk * 16;  // 16-byte pieces of 8 values
+        // activations of the pass's slots, natural order, then paired in place
         if (a.sw_gate) {
-            for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
-                const int n = i / (nblk * 16);
-                const int p = i - n * nblk * 16;
-                const size_t src = static_cast<size_t>(s_rowsel[n]) * a.K + p * 8;
-                const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.sw_gate + src));
-                const uint4 uv = __ldg(reinterpret_cast<const uint4*>(a.sw_up + src));
-                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-                uint32_t hw[4];
+            // h = bf16(silu(gate) * up) of each slot; a batch's gate/up pieces
+            // are loaded before any is converted
+            const int pieces = m * nblk * 16;
+            for (int i0 = 0; i0 < pieces; i0 += kSwBatch * kThreads) {
+                uint4 gv[kSwBatch], uv[kSwBatch];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float h0 = silu_mul(bf16_to_f32(gw[q] & 0xFFFFu), bf16_to_f32(uw[q] & 0xFFFFu));
-                    const float h1 = silu_mul(bf16_to_f32(gw[q] >> 16), bf16_to_f32(uw[q] >> 16));
-                    hw[q] = f32_to_bf16_rn(h0) | (static_cast<uint32_t>(f32_to_bf16_rn(h1)) << 16);
+                for (int j = 0; j < kSwBatch; ++j) {
+                    const int i = i0 + j * kThreads + static_cast<int>(threadIdx.x);
+                    if (i < pieces) {
+                        const int n = i / (nblk * 16);
+                        const int p = i - n * nblk * 16;
+                        const size_t src = static_cast<size_t>(s_slots[base + n]) * a.K + p * 8;
+                        gv[j] = __ldg(reinterpret_cast<const uint4*>(a.sw_gate + src));
+                        uv[j] = __ldg(reinterpret_cast<const uint4*>(a.sw_up + src));
+                    }
                 }
-                *reinterpret_cast<uint4*>(xs + n * tok_stride + p * 16) =
-                    make_uint4(hw[0], hw[1], hw[2], hw[3]);
+#pragma unroll
+                for (int j = 0; j < kSwBatch; ++j) {
+                    const int i = i0 + j * kThreads + static_cast<int>(threadIdx.x);
+                    if (i >= pieces) continue;
+                    const int n = i / (nblk * 16);
+                    const int p = i - n * nblk * 16;
+                    const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+                    const uint32_t uw[4] = {uv[j].x, uv[j].y, uv[j].z, uv[j].w};
+                    uint32_t hw[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float h0 = silu_mul(bf16_to_f32(gw[q] & 0xFFFFu), bf16_to_f32(uw[q] & 0xFFFFu));
+                        const float h1 = silu_mul(bf16_to_f32(gw[q] >> 16), bf16_to_f32(uw[q] >> 16));
+                        hw[q] = f32_to_bf16_rn(h0) | (static_cast<uint32_t>(f32_to_bf16_rn(h1)) << 16);
+                    }
+                    *reinterpret_cast<uint4*>(xs + n * tok_stride + p * 16) =
+                        make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                }
             }
         } else {
-            for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
-                const int n = i / (nblk * 16);
-                const int p = i - n * nblk * 16;
-                cp_async_16(xs + n * tok_stride + p * 16,
-                            a.x + static_cast<size_t>(s_rowsel[n]) * a.K + p * 8);
-            }
+            if (!(x_first && base == 0)) stage_x_async(base, m);
             cp_async_wait_all();
         }
         __syncthreads();
@@ -416,7 +469,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
                     }
                 }
         }
-        __syncthreads();  // s_rowsel, xs and red are rewritten by the next pass
+        __syncthreads();  // xs and red are rewritten by the next pass
     }
     if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
     moe_chunk_done<kRowsPerCta>(a, s_ids);
@@ -445,6 +498,19 @@ using MoeKernel = void (*)(MoeKernelArgs, CUtensorMap, CUtensorMap);
 MoeKernel pick_moe_kernel(int Mpad, int tiles) {
     if (Mpad == 8) return tiles == 4 ? k_moe_tma<1, 4> : k_moe_tma<1, 8>;
     return tiles == 4 ? k_moe_tma<2, 4> : k_moe_tma<2, 8>;
+}
+
+// static shared memory of a kernel instance (queried once per instance)
+int moe_static_smem(MoeKernel k) {
+    static std::atomic<int> cached[4] = {{-1}, {-1}, {-1}, {-1}};
+    const int i = (k == k_moe_tma<1, 4>) ? 0 : (k == k_moe_tma<1, 8>) ? 1 : (k == k_moe_tma<2, 4>) ? 2 : 3;
+    int v = cached[i].load(std::memory_order_relaxed);
+    if (v < 0) {
+        cudaFuncAttributes fa{};
+        v = (cudaFuncGetAttributes(&fa, k) == cudaSuccess) ? static_cast<int>(fa.sharedSizeBytes) : 4096;
+        cached[i].store(v, std::memory_order_relaxed);
+    }
+    return v;
 }
 
 }  // namespace
@@ -484,8 +550,11 @@ cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) 
     // 64-row CTAs unless that takes more than one wave of two CTAs per SM
     const int tiles = (((a.N + 63) / 64) * dmax * nz > 2 * dev.sms) ? 8 : 4;
     const int rows = tiles * 16;
-    // stages: as many as leave room for two CTAs per SM (8-slot passes)
-    const int per_cta = dev.smem_per_sm / (Mpad == 8 ? 2 : 1) - 1024;
+    MoeKernel kern = pick_moe_kernel(Mpad, tiles);
+    // stages: as many as leave room for two CTAs per SM (8-slot passes),
+    // counting the kernel's static shared memory and the 1 KB the SM keeps
+    // per CTA
+    const int per_cta = dev.smem_per_sm / (Mpad == 8 ? 2 : 1) - 1024 - moe_static_smem(kern);
     int ns = 2;
     while (ns < kMaxStages && moe_smem_bytes(Mpad, nblk, G, tiles, ns + 1) <= per_cta &&
            moe_smem_bytes(Mpad, nblk, G, tiles, ns + 1) <= dev.max_smem_optin)
@@ -504,7 +573,6 @@ cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) 
         const MoeBank& bk = k.bank[b];
         if (!encode_weight_map(&maps[b], bk.wq, a.E * a.N, a.K, kBoxRows)) return cudaErrorInvalidValue;
     }
-    MoeKernel kern = pick_moe_kernel(Mpad, tiles);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
