@@ -344,6 +344,22 @@ def test_moe_gemv_per_slot(w, oracle, M):
     check_close(host_f64(ys), refs, "moe per slot, x per slot")
 
 
+@pytest.mark.parametrize("M,N,K,g", [(1, 100, 128, 128), (3, 70, 256, 256), (2, 130, 7168, 128),
+                                     (5, 40, 9216, 128), (1, 300, 4608, 256)])
+def test_moe_gemv_scale_table_edges(w, oracle, M, N, K, g):
+    # one group per row (G = 1), tables filled in several load batches
+    # (G = 56 over 64 rows), no table at all (G = 72: scales read in the
+    # loop), ragged row chunks
+    E, topk = 6, 2
+    wq, s, z = synth.expert_bank(66 + K, E, N, K, g)
+    ids, r = synth.routing(66 + K, M, topk, E)
+    x = synth.activations(66 + K, (M, K))
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g)
+    torch.cuda.synchronize()
+    check_close(host_f64(y), oracle.moe_gemv(x, ids, None, wq, s, z, g), "moe table edges")
+    assert w.w4a16_device_error(clear=True) == 0
+
+
 def test_moe_gemv_shared_experts_and_many_slots(w, oracle):
     # 12 tokens over 4 experts: every expert serves > 8 slots (two passes at
     # one n-tile for M <= 8 would not be enough)

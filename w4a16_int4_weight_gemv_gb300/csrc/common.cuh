@@ -170,6 +170,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Fetch a tensor map (a __grid_constant__ kernel parameter) into the TMA
+// unit's descriptor cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // Four 8x8 matrices of 16-bit elements from shared memory: lanes 8i..8i+7
 // give the 16-byte row addresses of matrix i; lane l receives, from each
 // matrix, the 32-bit word at row l / 4, bytes 4 * (l % 4) .. + 3.

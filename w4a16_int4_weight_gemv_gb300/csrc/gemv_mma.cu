@@ -139,6 +139,7 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
     const int my_steps = (nsteps_slice > kp) ? (nsteps_slice - kp + WPT - 1) / WPT : 0;
     const int nss = my_tiles * my_steps;
 
+    if (threadIdx.x == 0) prefetch_tensor_map(&wmap);
     grid_dependents_launch();
     if (lane == 0) {
         for (int i = 0; i < NS; ++i) mbar_init(bars + i, 1 + (kFast ? 32 : 0));

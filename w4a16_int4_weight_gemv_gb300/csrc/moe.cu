@@ -170,6 +170,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     // predecessor signalled only after its own wait) the routed ids, weights
     // and scales -- inputs of the whole chain -- are read first and only the
     // activations and outputs wait.
+    if (threadIdx.x == 0) prefetch_tensor_map(wmap);
     if (!a.early) grid_dependency_wait();
     if (a.zero_count && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
         for (int i = threadIdx.x; i < a.zero_n; i += blockDim.x) a.zero_count[i] = 0u;
@@ -261,19 +262,23 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     const int npass = (nslots + Mpad - 1) / Mpad;
     const int total = npass * steps_mine;  // every pass streams the same weights
 
-    // 2. Loads issued before the weight copies, so that they are not queued
-    // behind this CTA's (and every other CTA's) weight stream: the first
-    // batch of the CTA's scales and zero points and, when they are plain
-    // inputs, the first pass's activation rows.
+    // 2. The CTA's scales and zero points (first batch) and, when they are
+    // plain inputs, the first pass's activation rows are loaded before any
+    // weight copy is issued: issued after, they would wait behind every CTA's
+    // weight stream (several microseconds at launch, when all CTAs fill
+    // their rings at once), and compute cannot start without them.
     const uint16_t* escale = bank.scale + static_cast<size_t>(e) * a.N * G;
     const uint8_t* ezero = bank.zero + static_cast<size_t>(e) * a.N * G;
     const int nent = use_table ? kTiles * 16 * G : 0;  // scale | zero << 16 per (row, group)
     uint32_t tv[kTabBatch];
+    // i / G as a high multiply for G > 1: exact for i < 2^16 and G <= 64
+    // (the error term i * (gm - 2^32 / G) / 2^32 stays below 1 / G)
+    const uint32_t gm = (G > 1) ? 0xFFFFFFFFu / static_cast<uint32_t>(G) + 1u : 0u;
     auto tab_load = [&](int i0) {
 #pragma unroll
         for (int j = 0; j < kTabBatch; ++j) {
             const int i = i0 + j * kThreads + static_cast<int>(threadIdx.x);
-            const int rr = i / G;
+            const int rr = (G > 1) ? static_cast<int>(__umulhi(static_cast<uint32_t>(i), gm)) : i;
             const int n = blockIdx.x * kRowsPerCta + rr;
             tv[j] = 0u;
             if (i < nent && n < a.N) {
@@ -303,6 +308,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     const bool x_first = !a.sw_gate && !a.early;  // first pass's rows may be read now
     if (nent > 0) tab_load(0);
     if (x_first) stage_x_async(0, min(Mpad, nslots));
+    if (nent > 0) tab_store(0);  // waits for the batch
 
     // producer cursor over (pass, step); the weights do not depend on the pass
     int w_i = 0;
@@ -325,7 +331,6 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     while (w_i < NS && w_i < total) issue();
 
     if (nent > 0) {
-        tab_store(0);
         for (int i0 = kTabBatch * kThreads; i0 < nent; i0 += kTabBatch * kThreads) {
             tab_load(i0);
             tab_store(i0);
