@@ -49,7 +49,6 @@ constexpr unsigned kBoxRows = 16;
 constexpr int kMaxSlots = 256;
 constexpr int kMaxTableGroups = 64;      // scale/zero table in shared memory up to G = 64
 constexpr int kMaxStages = 4;
-constexpr int kTabBatch = 12;            // table entries per thread per load batch
 constexpr int kSwBatch = 2;              // gate/up pieces per thread per load batch
 
 struct MoeKernelArgs {
@@ -79,6 +78,17 @@ struct MoeKernelArgs {
     uint32_t* err;
 };
 
+// The CTA's scales and zero points, copied verbatim from the bank: its rows'
+// bf16 scales [rows][G], then (16-byte aligned) their u8 zero points, each
+// placed 0..15 bytes into its area so that it agrees with its source modulo
+// 16 (the copy then moves aligned 16-byte pieces).
+__host__ __device__ inline int moe_table_scale_bytes(int tiles, int G) {
+    return (tiles * 16 * G * 2 + 16 + 15) & ~15;
+}
+__host__ __device__ inline int moe_table_bytes(int tiles, int G) {
+    return moe_table_scale_bytes(tiles, G) + tiles * 16 * G + 16;
+}
+
 struct MoeLayout {
     int xsum, red, tab, base;
 };
@@ -88,12 +98,32 @@ __host__ __device__ inline MoeLayout moe_layout(int Mpad, int nblk, int G, int t
     L.red = L.xsum + nblk * Mpad * 4;
     // K-half partials only when two warps share a tile (4-tile CTAs)
     L.tab = L.red + (kWarps / tiles > 1 ? tiles * 16 * Mpad * 4 : 0);
-    const int end = L.tab + (G <= kMaxTableGroups ? tiles * 16 * G * 4 : 0);
+    const int end = L.tab + (G <= kMaxTableGroups ? moe_table_bytes(tiles, G) : 0);
     L.base = (end + 127) & ~127;
     return L;
 }
 __host__ __device__ inline int moe_smem_bytes(int Mpad, int nblk, int G, int tiles, int ns) {
     return moe_layout(Mpad, nblk, G, tiles).base + 1024 + kWarps * ns * (kStageA + 8);
+}
+
+// Bytes [src, src + n) of global memory to shared memory at dst, where dst
+// and src agree modulo 16: the aligned body by 16-byte cp.async, the ragged
+// head and tail by byte loads.  Before reading, the caller waits for its
+// cp.async groups and synchronises the CTA.
+__device__ __forceinline__ void copy_span_async(unsigned char* dst, const unsigned char* src,
+                                                int n) {
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
+    const uintptr_t a0 = (s0 + 15) & ~static_cast<uintptr_t>(15);
+    const uintptr_t a1 = (s0 + n) & ~static_cast<uintptr_t>(15);
+    const int head = (a0 < s0 + n) ? static_cast<int>(a0 - s0) : n;
+    const int body = (a0 < s0 + n && a1 > a0) ? static_cast<int>(a1 - a0) : 0;
+    for (int i = threadIdx.x; i < body / 16; i += blockDim.x)
+        cp_async_16(dst + head + 16 * i, src + head + 16 * i);
+    const int tail0 = head + body;
+    for (int i = threadIdx.x; i < head + (n - tail0); i += blockDim.x) {
+        const int o = i < head ? i : tail0 + (i - head);
+        dst[o] = static_cast<unsigned char>(ldg_nc_u8(src + o));
+    }
 }
 
 // y[t][n] = bf16(sum_j r[t][j] * ws[t][j][n]) over slots with a valid expert
@@ -233,7 +263,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     unsigned char* xs = smem_raw;
     float* xsum = reinterpret_cast<float*>(smem_raw + lay.xsum);
     float* red = reinterpret_cast<float*>(smem_raw + lay.red);
-    uint32_t* tab = reinterpret_cast<uint32_t*>(smem_raw + lay.tab);
+    unsigned char* tab = smem_raw + lay.tab;
     const uint32_t raw_addr = smem_addr(smem_raw);
     const int a_off = static_cast<int>(((raw_addr + lay.base + 1023u) & ~1023u) - raw_addr);
     unsigned char* ring = smem_raw + a_off + warp * NS * kStageA;
@@ -262,38 +292,26 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     const int npass = (nslots + Mpad - 1) / Mpad;
     const int total = npass * steps_mine;  // every pass streams the same weights
 
-    // 2. The CTA's scales and zero points (first batch) and, when they are
-    // plain inputs, the first pass's activation rows are loaded before any
-    // weight copy is issued: issued after, they would wait behind every CTA's
-    // weight stream (several microseconds at launch, when all CTAs fill
-    // their rings at once), and compute cannot start without them.
+    // 2. The CTA's scales and zero points and, when they are plain inputs,
+    // the first pass's activation rows are requested before any weight copy
+    // is issued: issued after, they would wait behind every CTA's weight
+    // stream (several microseconds at launch, when all CTAs fill their rings
+    // at once), and compute cannot start without them.  The table moves as
+    // two contiguous byte spans (this CTA's rows are consecutive), so a few
+    // hundred 16-byte copies replace a load per (row, group).
     const uint16_t* escale = bank.scale + static_cast<size_t>(e) * a.N * G;
     const uint8_t* ezero = bank.zero + static_cast<size_t>(e) * a.N * G;
-    const int nent = use_table ? kTiles * 16 * G : 0;  // scale | zero << 16 per (row, group)
-    uint32_t tv[kTabBatch];
-    // i / G as a high multiply for G > 1: exact for i < 2^16 and G <= 64
-    // (the error term i * (gm - 2^32 / G) / 2^32 stays below 1 / G)
-    const uint32_t gm = (G > 1) ? 0xFFFFFFFFu / static_cast<uint32_t>(G) + 1u : 0u;
-    auto tab_load = [&](int i0) {
-#pragma unroll
-        for (int j = 0; j < kTabBatch; ++j) {
-            const int i = i0 + j * kThreads + static_cast<int>(threadIdx.x);
-            const int rr = (G > 1) ? static_cast<int>(__umulhi(static_cast<uint32_t>(i), gm)) : i;
-            const int n = blockIdx.x * kRowsPerCta + rr;
-            tv[j] = 0u;
-            if (i < nent && n < a.N) {
-                const size_t gi = static_cast<size_t>(n) * G + (i - rr * G);
-                tv[j] = ldg_nc_u16(escale + gi) | (ldg_nc_u8(ezero + gi) << 16);
-            }
-        }
-    };
-    auto tab_store = [&](int i0) {
-#pragma unroll
-        for (int j = 0; j < kTabBatch; ++j) {
-            const int i = i0 + j * kThreads + static_cast<int>(threadIdx.x);
-            if (i < nent) tab[i] = tv[j];
-        }
-    };
+    const int n_base = blockIdx.x * kRowsPerCta;
+    const int rows_valid = min(kRowsPerCta, a.N - n_base);
+    const unsigned char* src_s = reinterpret_cast<const unsigned char*>(escale + static_cast<size_t>(n_base) * G);
+    const unsigned char* src_z = ezero + static_cast<size_t>(n_base) * G;
+    const unsigned char* tab_s = tab + (reinterpret_cast<uintptr_t>(src_s) & 15);
+    const unsigned char* tab_z =
+        tab + moe_table_scale_bytes(kTiles, G) + (reinterpret_cast<uintptr_t>(src_z) & 15);
+    if (use_table) {
+        copy_span_async(const_cast<unsigned char*>(tab_s), src_s, rows_valid * G * 2);
+        copy_span_async(const_cast<unsigned char*>(tab_z), src_z, rows_valid * G);
+    }
     // activation rows of slots [base, base + m) to xs (natural order)
     auto stage_x_async = [&](int base, int m) {
         const int pieces = m * nblk * 16;  // 16-byte pieces of 8 values
@@ -306,9 +324,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
         }
     };
     const bool x_first = !a.sw_gate && !a.early;  // first pass's rows may be read now
-    if (nent > 0) tab_load(0);
     if (x_first) stage_x_async(0, min(Mpad, nslots));
-    if (nent > 0) tab_store(0);  // waits for the batch
 
     // producer cursor over (pass, step); the weights do not depend on the pass
     int w_i = 0;
@@ -329,13 +345,6 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
         ++w_i;
     };
     while (w_i < NS && w_i < total) issue();
-
-    if (nent > 0) {
-        for (int i0 = kTabBatch * kThreads; i0 < nent; i0 += kTabBatch * kThreads) {
-            tab_load(i0);
-            tab_store(i0);
-        }
-    }
 
     if (a.early) grid_dependency_wait();
     // dependents may start now: everything this grid reads is complete
@@ -390,6 +399,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
                         make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 }
             }
+            cp_async_wait_all();  // the scale table's copies
         } else {
             if (!(x_first && base == 0)) stage_x_async(base, m);
             cp_async_wait_all();
@@ -424,8 +434,12 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
                     const int blk = lb0 + bb;
                     const int grp = (blk << 7) / a.g;
                     if (use_table) {
-                        L.sz0 = tab[(tl * 16 + r) * G + grp];
-                        L.sz1 = tab[(tl * 16 + r + 8) * G + grp];
+                        const int i0 = (tl * 16 + r) * G + grp;
+                        const int i1 = i0 + 8 * G;
+                        L.sz0 = *reinterpret_cast<const uint16_t*>(tab_s + 2 * i0) |
+                                (static_cast<uint32_t>(tab_z[i0]) << 16);
+                        L.sz1 = *reinterpret_cast<const uint16_t*>(tab_s + 2 * i1) |
+                                (static_cast<uint32_t>(tab_z[i1]) << 16);
                     } else {
                         L.sz0 = 0u;
                         L.sz1 = 0u;
