@@ -337,7 +337,7 @@ def run_profile(args):
         for i in range(args.warmup + args.steps):
             w.moe_ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128)
         torch.cuda.synchronize()
-        print(json.dumps({"profile_workload": "moe", "M": M, "launches_per_chain": 3,
+        print(json.dumps({"profile_workload": "moe", "M": M, "launches_per_chain": 2,
                           "chains": args.warmup + args.steps}))
         return
     M, N, K, zmode, od = WORKLOADS[args.workload]

@@ -373,6 +373,25 @@ def test_moe_gemv_shared_experts_and_many_slots(w, oracle):
     check_close(host_f64(y), ref, "routed sum")
 
 
+def test_moe_gemv_passes_with_several_tiles_per_warp(w, oracle):
+    # 64 distinct experts over 8 tokens make 128-row CTAs whose warps take two
+    # tiles in turn; expert 0 named twice by every token has 16 slots, so its
+    # CTAs stream their weights in two passes
+    M, E, N, K, g, topk = 8, 64, 1024, 1024, 128, 8
+    wq, s, z = synth.expert_bank(67, E, N, K, g)
+    ids, r = synth.routing(67, M, topk, E)
+    ids[:, 0] = 0
+    ids[:, 1] = 0
+    x = synth.activations(67, (M, K))
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g)
+    torch.cuda.synchronize()
+    check_close(host_f64(y), oracle.moe_gemv(x, ids, None, wq, s, z, g), "passes x tiles per warp")
+    yr = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, route_w=dev(r))
+    torch.cuda.synchronize()
+    check_close(host_f64(yr), oracle.moe_gemv(x, ids, r, wq, s, z, g), "routed, passes x tiles per warp")
+    assert w.w4a16_device_error(clear=True) == 0
+
+
 def test_moe_gemv_duplicate_ids_in_a_token(w, oracle):
     M, E, N, K, g, topk = 9, 3, 64, 1024, 128, 2
     wq, s, z = synth.expert_bank(64, E, N, K, g)

@@ -66,6 +66,7 @@ struct MoeKernelArgs {
     int K;
     int g;
     int stages;
+    int tpw;    // 16-row tiles per warp, one after another (8-tile CTAs only)
     int early;  // ids, weights, scales may be read before the grid dependency wait
     // Routed sum inside the launch (fused FFN chain): per 64-row chunk, the
     // last CTA to finish its partials adds every token's slots in slot order.
@@ -92,18 +93,19 @@ __host__ __device__ inline int moe_table_bytes(int tiles, int G) {
 struct MoeLayout {
     int xsum, red, tab, base;
 };
-__host__ __device__ inline MoeLayout moe_layout(int Mpad, int nblk, int G, int tiles) {
+__host__ __device__ inline MoeLayout moe_layout(int Mpad, int nblk, int G, int tiles, int tpw) {
     MoeLayout L;
     L.xsum = Mpad * mma_token_stride(nblk);
     L.red = L.xsum + nblk * Mpad * 4;
     // K-half partials only when two warps share a tile (4-tile CTAs)
     L.tab = L.red + (kWarps / tiles > 1 ? tiles * 16 * Mpad * 4 : 0);
-    const int end = L.tab + (G <= kMaxTableGroups ? moe_table_bytes(tiles, G) : 0);
+    const int end = L.tab + (G <= kMaxTableGroups ? moe_table_bytes(tiles * tpw, G) : 0);
     L.base = (end + 127) & ~127;
     return L;
 }
-__host__ __device__ inline int moe_smem_bytes(int Mpad, int nblk, int G, int tiles, int ns) {
-    return moe_layout(Mpad, nblk, G, tiles).base + 1024 + kWarps * ns * (kStageA + 8);
+__host__ __device__ inline int moe_smem_bytes(int Mpad, int nblk, int G, int tiles, int tpw,
+                                              int ns) {
+    return moe_layout(Mpad, nblk, G, tiles, tpw).base + 1024 + kWarps * ns * (kStageA + 8);
 }
 
 // Bytes [src, src + n) of global memory to shared memory at dst, where dst
@@ -149,8 +151,7 @@ __device__ __forceinline__ void moe_route_rows(const float* ws, const float* rou
 // The chunk's partials of this CTA are written (or it has none): count it;
 // the CTA that completes the count forms the chunk's routed sums and resets
 // the counter for the next call.
-template <int ROWS>
-__device__ __forceinline__ void moe_chunk_done(const MoeKernelArgs& a, const int* ids) {
+__device__ __forceinline__ void moe_chunk_done(const MoeKernelArgs& a, const int* ids, int rows) {
     if (!a.chunk_count) return;
     __shared__ unsigned s_last;
     __threadfence();  // this CTA's partials are visible device-wide before it is counted
@@ -162,9 +163,9 @@ __device__ __forceinline__ void moe_chunk_done(const MoeKernelArgs& a, const int
     __syncthreads();
     if (!s_last) return;
     __threadfence();  // every counted CTA's partials are visible to this one
-    const int n0 = blockIdx.x * ROWS;
+    const int n0 = blockIdx.x * rows;
     moe_route_rows(a.ws, a.route_w, ids, a.y_routed, a.M, a.topk, a.E, a.N, n0,
-                   min(a.N, n0 + ROWS));
+                   min(a.N, n0 + rows));
     if (threadIdx.x == 0) a.chunk_count[blockIdx.x] = 0u;
 }
 
@@ -175,7 +176,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     constexpr int Mpad = 8 * NT;
     constexpr int kTiles = TILES;
     constexpr int kWpt = kWarps / kTiles;  // warps sharing a tile (K halves)
-    constexpr int kRowsPerCta = kTiles * 16;
+    constexpr int kRowsPerTileSet = kTiles * 16;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ int s_ids[kMaxSlots];
     __shared__ unsigned char s_slots[kMaxSlots];
@@ -194,6 +195,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     const bool use_table = G <= kMaxTableGroups;
     const int tok_stride = mma_token_stride(nblk);
     const int NS = a.stages;
+    const int cta_rows = kRowsPerTileSet * a.tpw;  // rows of expert e this CTA covers
 
     // Programmatic dependent launch: without `early` everything waits for the
     // preceding grid; with it (a launch inside the FFN chain, whose
@@ -240,8 +242,8 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
         if (a.early) grid_dependency_wait();
         for (int i = 0; i < S; ++i) {
             if (s_ids[i] >= 0 && s_ids[i] < a.E) continue;
-            for (int row = blockIdx.x * kRowsPerCta + threadIdx.x;
-                 row < min(a.N, (blockIdx.x + 1) * kRowsPerCta); row += blockDim.x)
+            for (int row = blockIdx.x * cta_rows + threadIdx.x;
+                 row < min(a.N, (blockIdx.x + 1) * cta_rows); row += blockDim.x)
                 bank.y[static_cast<size_t>(i) * a.N + row] = 0;
         }
     }
@@ -249,7 +251,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
         grid_dependents_launch();
         if (a.chunk_count) {
             grid_dependency_wait();  // the counters were zeroed by the preceding launch
-            moe_chunk_done<kRowsPerCta>(a, s_ids);
+            moe_chunk_done(a, s_ids, cta_rows);
         }
         return;
     }
@@ -259,7 +261,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     fm = __ballot_sync(0xFFFFFFFFu, mine);
     if (lane == 0) s_mask[warp] = fm;  // its earlier reads all precede the last barrier
 
-    const MoeLayout lay = moe_layout(Mpad, nblk, G, kTiles);
+    const MoeLayout lay = moe_layout(Mpad, nblk, G, kTiles, a.tpw);
     unsigned char* xs = smem_raw;
     float* xsum = reinterpret_cast<float*>(smem_raw + lay.xsum);
     float* red = reinterpret_cast<float*>(smem_raw + lay.red);
@@ -269,12 +271,15 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     unsigned char* ring = smem_raw + a_off + warp * NS * kStageA;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + a_off + kWarps * NS * kStageA) + warp * NS;
 
-    const int tl = warp / kWpt;  // local tile
+    // warp (tl, kp) takes tiles tile0 + tp * kTiles, tp < ntl, of expert e
+    // (kp: its K part when kWpt warps share a tile)
+    const int tl = warp / kWpt;
     const int kp = warp - tl * kWpt;
-    const int tile = blockIdx.x * kTiles + tl;  // 16-row tile of expert e
-    const bool has_rows = tile * 16 < a.N;
-    const int steps_mine = (has_rows && nsteps > kp) ? (nsteps - kp + kWpt - 1) / kWpt : 0;
-    const int row0 = e * a.N + tile * 16;  // first row in the stacked bank
+    const int tile0 = blockIdx.x * kTiles * a.tpw + tl;
+    const int ntiles_all = (a.N + 15) >> 4;
+    const int ntl = tile0 < ntiles_all ? min(a.tpw, (ntiles_all - tile0 + kTiles - 1) / kTiles) : 0;
+    const int ms = (nsteps > kp) ? (nsteps - kp + kWpt - 1) / kWpt : 0;  // steps per tile
+    const int per_pass = ntl * ms;
 
     if (lane == 0) {
         for (int i = 0; i < NS; ++i) mbar_init(bars + i, 1);
@@ -290,7 +295,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     for (int w = 0; w < kWarps; ++w) nslots += __popc(s_mask[w]);
     __syncthreads();  // s_slots
     const int npass = (nslots + Mpad - 1) / Mpad;
-    const int total = npass * steps_mine;  // every pass streams the same weights
+    const int total = npass * per_pass;  // every pass streams the same weights
 
     // 2. The CTA's scales and zero points and, when they are plain inputs,
     // the first pass's activation rows are requested before any weight copy
@@ -301,13 +306,13 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     // hundred 16-byte copies replace a load per (row, group).
     const uint16_t* escale = bank.scale + static_cast<size_t>(e) * a.N * G;
     const uint8_t* ezero = bank.zero + static_cast<size_t>(e) * a.N * G;
-    const int n_base = blockIdx.x * kRowsPerCta;
-    const int rows_valid = min(kRowsPerCta, a.N - n_base);
+    const int n_base = blockIdx.x * cta_rows;
+    const int rows_valid = min(cta_rows, a.N - n_base);
     const unsigned char* src_s = reinterpret_cast<const unsigned char*>(escale + static_cast<size_t>(n_base) * G);
     const unsigned char* src_z = ezero + static_cast<size_t>(n_base) * G;
     const unsigned char* tab_s = tab + (reinterpret_cast<uintptr_t>(src_s) & 15);
     const unsigned char* tab_z =
-        tab + moe_table_scale_bytes(kTiles, G) + (reinterpret_cast<uintptr_t>(src_z) & 15);
+        tab + moe_table_scale_bytes(kTiles * a.tpw, G) + (reinterpret_cast<uintptr_t>(src_z) & 15);
     if (use_table) {
         copy_span_async(const_cast<unsigned char*>(tab_s), src_s, rows_valid * G * 2);
         copy_span_async(const_cast<unsigned char*>(tab_z), src_z, rows_valid * G);
@@ -326,13 +331,17 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     const bool x_first = !a.sw_gate && !a.early;  // first pass's rows may be read now
     if (x_first) stage_x_async(0, min(Mpad, nslots));
 
-    // producer cursor over (pass, step); the weights do not depend on the pass
+    // producer cursor over (pass, tile, step); the weights do not depend on
+    // the pass
     int w_i = 0;
     auto issue = [&]() {
         const int stg = w_i % NS;
         uint64_t* bar = bars + stg;
         unsigned char* dst = ring + stg * kStageA;
-        const int ks = kp + (w_i % steps_mine) * kWpt;
+        const int rr = w_i % per_pass;
+        const int tp = rr / ms;
+        const int ks = kp + (rr - tp * ms) * kWpt;
+        const int row0 = e * a.N + (tile0 + tp * kTiles) * 16;  // first row in the stacked bank
         const int blk0 = ks * kSB;
         const int nbs = min(kSB, nblk - blk0);
         const int nh = (nbs + 1) >> 1;
@@ -356,7 +365,6 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
     const uint32_t lbase = static_cast<uint32_t>(lrow * 128);
     const int lsw = lane & 7;
     const int lch = lane >> 4;
-    const int n0 = tile * 16 + r;
     bool timed_out = false;
     int c_i = 0;  // consumer cursor
 
@@ -408,13 +416,17 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
         pair_x_in_place<NT>(m, nblk, xs, xsum, tok_stride);
         __syncthreads();
 
-        // 3. stream this warp's K half of its tile against the pass's slots
+        // 3. stream this warp's K part of its tiles against the pass's slots
+        for (int tp = 0; tp < ntl; ++tp) {
+        const int tile = tile0 + tp * kTiles;  // 16-row tile of expert e
+        const int trow = (tp * kTiles + tl) * 16;  // its first row in the CTA's table
+        const int n0 = tile * 16 + r;
         float acc[NT][4];
 #pragma unroll
         for (int t = 0; t < NT; ++t)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
-        for (int s = 0; s < steps_mine; ++s) {
+        for (int s = 0; s < ms; ++s) {
             const int stg = c_i % NS;
             if (!mbar_wait_bounded(bars + stg, (c_i / NS) & 1)) timed_out = true;
             const uint32_t sa = smem_addr(ring + stg * kStageA);
@@ -434,7 +446,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
                     const int blk = lb0 + bb;
                     const int grp = (blk << 7) / a.g;
                     if (use_table) {
-                        const int i0 = (tl * 16 + r) * G + grp;
+                        const int i0 = (trow + r) * G + grp;
                         const int i1 = i0 + 8 * G;
                         L.sz0 = *reinterpret_cast<const uint16_t*>(tab_s + 2 * i0) |
                                 (static_cast<uint32_t>(tab_z[i0]) << 16);
@@ -460,7 +472,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
             if (w_i < total) issue();
         }
 
-        // 4. add the two K halves (fixed order) and store per-slot outputs
+        // 4. add the K parts (fixed order) and store per-slot outputs
         float* rb = red + tl * 16 * Mpad;
         if constexpr (kWpt > 1) {
             if (kp == 1) {
@@ -472,7 +484,7 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
             }
             named_barrier_sync(1 + tl, kWpt * 32);
         }
-        if (kp == 0 && has_rows) {
+        if (kp == 0) {
 #pragma unroll
             for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -488,10 +500,12 @@ k_moe_tma(const MoeKernelArgs a, const __grid_constant__ CUtensorMap map0,
                     }
                 }
         }
-        __syncthreads();  // xs and red are rewritten by the next pass
+        if constexpr (kWpt > 1) named_barrier_sync(1 + tl, kWpt * 32);  // rb is free again
+        }
+        __syncthreads();  // xs is rewritten by the next pass
     }
     if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
-    moe_chunk_done<kRowsPerCta>(a, s_ids);
+    moe_chunk_done(a, s_ids, cta_rows);
 }
 
 // y[t][n] = sum_j r[t][j] * ws[t][j][n] over slots with a valid expert id.
@@ -537,7 +551,8 @@ int moe_static_smem(MoeKernel k) {
 int moe_row_chunks(int N) { return (N + 63) / 64; }
 
 int moe_smem_need(int M, int K, int g) {
-    return moe_smem_bytes(M <= 8 ? 8 : 16, K / 128, K / g, 8, 2);
+    const int Mpad = M <= 8 ? 8 : 16;
+    return moe_smem_bytes(Mpad, K / 128, K / g, 8, 1, 2);
 }
 
 cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -566,26 +581,34 @@ cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) 
     const int Mpad = (a.M <= 8) ? 8 : 16;
     const int dmax = S < a.E ? S : a.E;
     const int nz = a.nbanks > 1 ? 2 : 1;
-    // 64-row CTAs unless that takes more than one wave of two CTAs per SM
+    // 64-row CTAs unless that takes more than one wave of two CTAs per SM;
+    // then 128-row CTAs, and a warp takes two or four tiles in turn while the
+    // grid would still need more than one wave
     const int tiles = (((a.N + 63) / 64) * dmax * nz > 2 * dev.sms) ? 8 : 4;
-    const int rows = tiles * 16;
     MoeKernel kern = pick_moe_kernel(Mpad, tiles);
     // stages: as many as leave room for two CTAs per SM (8-slot passes),
     // counting the kernel's static shared memory and the 1 KB the SM keeps
     // per CTA
     const int per_cta = dev.smem_per_sm / (Mpad == 8 ? 2 : 1) - 1024 - moe_static_smem(kern);
+    int tpw = 1;
+    if (tiles == 8)
+        while (tpw < 4 && ((a.N + tiles * 16 * tpw - 1) / (tiles * 16 * tpw)) * dmax * nz > 2 * dev.sms &&
+               moe_smem_bytes(Mpad, nblk, G, tiles, tpw * 2, 2) <= per_cta)
+            tpw *= 2;
+    const int rows = tiles * 16 * tpw;
     int ns = 2;
-    while (ns < kMaxStages && moe_smem_bytes(Mpad, nblk, G, tiles, ns + 1) <= per_cta &&
-           moe_smem_bytes(Mpad, nblk, G, tiles, ns + 1) <= dev.max_smem_optin)
+    while (ns < kMaxStages && moe_smem_bytes(Mpad, nblk, G, tiles, tpw, ns + 1) <= per_cta &&
+           moe_smem_bytes(Mpad, nblk, G, tiles, tpw, ns + 1) <= dev.max_smem_optin)
         ++ns;
     k.stages = ns;
+    k.tpw = tpw;
     k.early = a.early;
     k.chunk_count = a.chunk_count;
     k.route_w = a.route_w;
     k.y_routed = a.y_routed;
     k.zero_count = a.zero_count;
     k.zero_n = a.zero_n;
-    const int smem = moe_smem_bytes(Mpad, nblk, G, tiles, ns);
+    const int smem = moe_smem_bytes(Mpad, nblk, G, tiles, tpw, ns);
     if (smem > dev.max_smem_optin) return cudaErrorInvalidValue;
     CUtensorMap maps[2];
     for (int b = 0; b < 2; ++b) {
