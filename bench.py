@@ -259,6 +259,41 @@ def moe_chain_time(torch, w, M, steps, warmup, l2, fused=True):
     return t, float(np.mean(byts))
 
 
+def mlp_decode_chain_time(torch, w, M, steps, warmup, l2):
+    """One dense SwiGLU MLP of a decode step as the library chains it: gate
+    and up GEMVs (14336x4096), w4a16_swiglu, down GEMV (4096x14336), every
+    GEMV with programmatic dependent launch and the resident-weights flag,
+    so its first weight copies overlap the preceding kernel's tail.  Weight
+    sets rotate over copies > 2x L2; seconds per chain."""
+    from w4a16_int4_weight_gemv_gb300 import synth
+    F, H, g = 14336, 4096, 128
+    per = 2 * all_bytes(M, F, H, g) + all_bytes(M, H, F, g)
+    R = max(2, int(math.ceil(2.0 * l2 / per)))
+    sets = []
+    for r in range(R):
+        mats = []
+        for n_, k_, sub in ((F, H, 3 * r), (F, H, 3 * r + 1), (H, F, 3 * r + 2)):
+            p = synth.dense_problem(M, n_, k_, g, "uniform6to10", seed=5, sub=sub)
+            mats.append(tuple(_dev(p[k], torch) for k in ("wq", "scale", "zero")))
+        sets.append(mats)
+    x = _dev(synth.activations(5, (M, H)), torch)
+    go = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
+    uo = torch.empty_like(go)
+    h = torch.empty_like(go)
+    y = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+
+    def step(i):
+        gate, up, down = sets[i % R]
+        w.w4a16_gemv(x, *gate, g, out=go, weights_static=True)
+        w.w4a16_gemv(x, *up, g, out=uo, weights_static=True)
+        w.w4a16_swiglu(go, uo, out=h)
+        w.w4a16_gemv(h, *down, g, out=y, weights_static=True)
+
+    t = time_steps(torch, step, R, steps, warmup)
+    del sets
+    return t
+
+
 def e2e_gbs(torch, w, M, N, K, g, steps):
     """Public API with host buffers: per step copy x from pinned host memory,
     run w4a16_gemv on resident weights, read y back to host."""
@@ -443,6 +478,12 @@ def run_gpu(args):
             tu = sweep["up_M%d" % m]["us"]
             td = sweep["down_M%d" % m]["us"]
             sweep["mlp_chain_M%d_tokens_per_s" % m] = round(m / ((2 * tu + td) * 1e-6), 1)
+        for m in (1, 8):
+            t = mlp_decode_chain_time(torch, w, m, 200, 20, l2)
+            sweep["mlp_decode_chain_M%d" % m] = {
+                "us": round(t * 1e6, 3), "tokens_per_s": round(m / t, 1),
+                "sum_of_separate_gemvs_us": round(2 * sweep["up_M%d" % m]["us"] + sweep["down_M%d" % m]["us"], 3),
+                "note": "gate, up, SwiGLU, down chained in one graph (PDL, resident-weights flag)"}
         t = gpu_gemv_gbs(torch, w, 1, 163840, 4096, 128, "uniform6to10", l2, 200, 20,
                          out_dtype=torch.float32)
         sweep["vocab_M1"] = {"us": round(t * 1e6, 3),
