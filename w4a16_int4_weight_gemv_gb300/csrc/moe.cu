@@ -6,7 +6,7 @@
 // expert share one pass over that expert's weights: CTA (chunk, d, bank)
 // finds the d-th distinct expert among the routed slots (in order of first
 // appearance), gathers the activation rows of every slot routed to it into
-// shared memory and streams a 64-row chunk of W_e against all of them at
+// shared memory and streams a chunk of W_e's rows against all of them at
 // once.  The routed ids live on the device, so the grid is sized for the
 // worst case (min(E, M*topk) distinct experts) and CTAs beyond the actual
 // count exit at once.
@@ -15,10 +15,13 @@
 // (gemv_mma.cu, mma_core.cuh): one 2-D tensor map over the whole stacked
 // bank [E*N rows][K/8 words], per-warp rings of 16-row x 512-k stages filled
 // by two 128-byte-swizzled TMA boxes, ldmatrix fragments, mma.sync with the
-// 128 + code bf16 trick and the per-block zero-point/scale correction.  Two
-// warps share a 16-row tile (K halves, partials added in shared memory in a
-// fixed order).  A CTA's scales and zero points are gathered into a
-// shared-memory table once.
+// 128 + code bf16 trick and the per-block zero-point/scale correction.  A
+// chunk is 4 tiles of 16 rows with two warps per tile (K halves, partials
+// added in shared memory in a fixed order), or 8 tiles with a warp per tile
+// -- and then possibly two or four tiles per warp in turn -- when smaller
+// chunks would take more than one wave.  A CTA's scales and zero points (its
+// rows are consecutive, so two contiguous byte spans) are copied into
+// shared memory once, before its first weight box is issued.
 //
 // One launch can serve two banks of the same shape against the same
 // activations (grid z): the gate and up products of a SwiGLU expert FFN.
@@ -26,9 +29,11 @@
 // from per-slot gate and up outputs: the down product of that FFN, without a
 // separate SwiGLU pass.
 //
-// With route weights the per-slot results go to an fp32 workspace and a
-// second kernel forms y[t] = sum_j r[t][j] d[t][j] in slot order -- a fixed
-// order, so the result is deterministic (no floating-point atomics).
+// With route weights the per-slot results go to an fp32 workspace; y[t] =
+// sum_j r[t][j] d[t][j] is then formed in slot order -- a fixed order, so
+// the result is deterministic (no floating-point atomics) -- by a second
+// kernel, or, inside the FFN chain, by the last CTA to finish each row
+// chunk.
 #include <atomic>
 
 #include "common.cuh"
@@ -40,8 +45,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-// A CTA covers TILES 16-row tiles of one expert: 4 (two warps per tile,
-// K halves) or, when that would take more than one wave, 8 (a warp per tile).
 constexpr int kSB = 4;                   // 128-k blocks per step (512 k)
 constexpr int kHalfBytes = 2048;         // one TMA box: 16 rows x 128 bytes
 constexpr int kStageA = 2 * kHalfBytes;
