@@ -105,17 +105,31 @@ def _check(rc: int, where: str):
         raise W4A16Error(rc, where)
 
 
-def _stream(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+# The current stream's handle for a device index, without building a Stream
+# object (torch.cuda.current_stream() costs a few microseconds per call,
+# which a decode loop pays on every GEMV).
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device: int = None):
+    """Stream handle (an int) for a ctypes call: `stream`, or the current
+    stream of `device` (the current device if None)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_current_stream is not None and device is not None and device >= 0:
+        return _raw_current_stream(device)
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _ptr(t: torch.Tensor):
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _need(t: torch.Tensor, name: str, dtypes, shape=None):
+    # fast path: one expression over the properties a valid argument has
+    if (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype in dtypes and t.is_contiguous()
+            and (shape is None or t.shape == tuple(shape))):
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
     if not t.is_cuda:
@@ -140,7 +154,8 @@ def int4_pack(codes: torch.Tensor, out: torch.Tensor = None, stream=None) -> tor
     if out is None:
         out = torch.empty((N, K // 8), dtype=torch.int32, device=codes.device)
     _need(out, "out", _U32, (N, K // 8))
-    _check(load_library().int4_pack(_ptr(codes), _ptr(out), N, K, _stream(stream)), "int4_pack")
+    _check(load_library().int4_pack(_ptr(codes), _ptr(out), N, K, _stream(stream, codes.get_device())),
+           "int4_pack")
     return out
 
 
@@ -156,7 +171,7 @@ def int4_dequant(wq, scale, zero, g: int, out_dtype=torch.bfloat16, out=None, st
     _need(out, "out", (torch.bfloat16, torch.float32), (N, K))
     kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(load_library().int4_dequant(_ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
-                                       N, K, g, _stream(stream)), "int4_dequant")
+                                       N, K, g, _stream(stream, wq.get_device())), "int4_dequant")
     return out
 
 
@@ -200,16 +215,17 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
     _need(out, "out", (torch.bfloat16, torch.float32), (M, N))
     kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     lib = load_library()
+    sh = _stream(stream, x.get_device())
     if kernel_id == 0 and k_split == 0 and weights_static:
         rc = lib.w4a16_gemv_ex(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
-                               M, N, K, g, FLAG_WEIGHTS_STATIC, _stream(stream))
+                               M, N, K, g, FLAG_WEIGHTS_STATIC, sh)
     elif kernel_id == 0 and k_split == 0:
         rc = lib.w4a16_gemv(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
-                            M, N, K, g, None, 0, _stream(stream))
+                            M, N, K, g, None, 0, sh)
     else:
         rc = lib.w4a16_gemv_variant(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out),
                                     kind, M, N, K, g, kernel_id or (1 if M == 1 else 2),
-                                    k_split, _stream(stream))
+                                    k_split, sh)
     _check(rc, "w4a16_gemv")
     return out
 
@@ -248,7 +264,7 @@ def w4a16_moe_gemv(x, expert_ids, wq, scale, zero, g: int, route_w=None, x_per_s
     _need(out, "out", _BF16, shape)
     _check(lib.w4a16_moe_gemv(_ptr(x), int(bool(x_per_slot)), _ptr(expert_ids), rw, _ptr(wq),
                               _ptr(scale), _ptr(zero), _ptr(out), M, topk, E, N, K, g,
-                              ws_ptr, ws_bytes, _stream(stream)), "w4a16_moe_gemv")
+                              ws_ptr, ws_bytes, _stream(stream, x.get_device())), "w4a16_moe_gemv")
     return out
 
 
@@ -266,7 +282,8 @@ def w4a16_swiglu(gate, up, out=None, stream=None) -> torch.Tensor:
     if out.dim() != 2 or tuple(out.shape) != (rows, N) or out.stride(1) != 1:
         raise ValueError("out must be [rows, N] with unit column stride")
     _check(load_library().w4a16_swiglu(_ptr(gate), _ptr(up), gate.stride(0), _ptr(out),
-                                       out.stride(0), rows, N, _stream(stream)), "w4a16_swiglu")
+                                       out.stride(0), rows, N, _stream(stream, gate.get_device())),
+           "w4a16_swiglu")
     return out
 
 
@@ -302,7 +319,7 @@ def moe_ffn(x, expert_ids, route_w, gate, up, down, g: int, stream=None,
         _check(lib.w4a16_moe_ffn(_ptr(x), _ptr(expert_ids), _ptr(route_w), _ptr(gw), _ptr(gs),
                                  _ptr(gz), _ptr(uw), _ptr(us), _ptr(uz), _ptr(dw), _ptr(ds),
                                  _ptr(dz), _ptr(y), M, topk, E, H, F, g, _ptr(ws), nbytes,
-                                 _stream(stream)), "w4a16_moe_ffn")
+                                 _stream(stream, x.get_device())), "w4a16_moe_ffn")
         return y
     g_out = w4a16_moe_gemv(x, expert_ids, *gate, g, stream=stream)
     u_out = w4a16_moe_gemv(x, expert_ids, *up, g, stream=stream)

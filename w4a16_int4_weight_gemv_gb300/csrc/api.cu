@@ -92,11 +92,34 @@ w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, in
     if (st != W4A16_OK) return st;
     const int n = static_cast<int>(N), k = static_cast<int>(K);
     const int gg = static_cast<int>(g);
+    // plans depend only on the shape and the device: computed once each
+    struct Entry {
+        int device, kernel_id, M, N, K, g, k_split;
+        GemvPlan plan;
+    };
+    static std::mutex mu;
+    static Entry cache[256];
+    static int used = 0, next = 0;
+    const int d = static_cast<int>(*dev - g_dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i) {
+            const Entry& c = cache[i];
+            if (c.device == d && c.kernel_id == kernel_id && c.M == M && c.N == n && c.K == k &&
+                c.g == gg && c.k_split == k_split) {
+                *plan = c.plan;
+                return W4A16_OK;
+            }
+        }
+    }
     *plan = (kernel_id == 1)   ? plan_gemv_simt((*dev)->info, M, n, k, gg, k_split)
             : (kernel_id == 2) ? plan_gemv_mma((*dev)->info, M, n, k, gg, k_split)
                                : plan_gemv_tc((*dev)->info, M, n, k, gg, k_split);
     if (plan->ctas < 1 || plan->smem_bytes > (*dev)->info.max_smem_optin)
         return W4A16_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry& slot = (used < 256) ? cache[used++] : cache[next++ & 255];
+    slot = Entry{d, kernel_id, M, n, k, gg, k_split, *plan};
     return W4A16_OK;
 }
 
@@ -126,6 +149,29 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
 
 }  // namespace
 
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
+    struct Entry {
+        const void* kernel;
+        int device, bytes;
+    };
+    static std::mutex mu;
+    static Entry table[512];
+    static int used = 0;
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry* hit = nullptr;
+    for (int i = 0; i < used && !hit; ++i)
+        if (table[i].kernel == kernel && table[i].device == d) hit = &table[i];
+    if (hit && hit->bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (hit) hit->bytes = bytes;
+    else if (used < 512) table[used++] = Entry{kernel, d, bytes};
+    return cudaSuccess;
+}
+
 int max_active_clusters(const void* kernel, int threads, int smem, int S) {
     struct Entry {
         const void* kernel;
@@ -144,8 +190,7 @@ int max_active_clusters(const void* kernel, int threads, int smem, int S) {
             return e.value;
     }
     int n = 0;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess) {
+    if (ensure_dynamic_smem(kernel, smem) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }

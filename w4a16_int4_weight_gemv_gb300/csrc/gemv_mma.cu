@@ -426,8 +426,7 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s
     CUtensorMap wmap;
     if (!encode_weight_map(&wmap, a.wq, a.N, a.K, kBoxRows)) return cudaErrorInvalidValue;
     MmaKernel kern = pick_mma_kernel(a.M, a.K, a.g, p.threads / 32);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         p.smem_bytes);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), p.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.ctas);

@@ -597,8 +597,7 @@ cudaError_t launch_gemv_simt(const GemvArgs& a, const GemvPlan& p, cudaStream_t 
     k.weights_static = a.weights_static;
     k.err = a.err;
     SimtKernel kern = pick_simt_kernel(a.M, p.tile_rows, a.K, a.g);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         p.smem_bytes);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), p.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.ctas);

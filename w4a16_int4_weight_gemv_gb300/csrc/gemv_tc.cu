@@ -519,8 +519,7 @@ cudaError_t launch_gemv_tc(const GemvArgs& a, const GemvPlan& p, cudaStream_t s)
     CUtensorMap wmap;
     if (!encode_weight_map(&wmap, a.wq, a.N, a.K, kRows)) return cudaErrorInvalidValue;
     TcKernel kern = pick_tc_kernel(a.M);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         p.smem_bytes);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), p.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.ctas);

@@ -110,6 +110,12 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
     return best;
 }
 
+// Lets `kernel` run with `bytes` of dynamic shared memory on the current
+// device.  The limit persists per function and device, so it is raised only
+// when a launch needs more than every earlier one did (a host-side table
+// spares the driver call -- about a microsecond -- on every launch).
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
+
 // Number of clusters of S CTAs (threads each, smem bytes of dynamic shared
 // memory) of `kernel` the current device can run at once; cached.
 int max_active_clusters(const void* kernel, int threads, int smem, int S);

@@ -618,7 +618,7 @@ cudaError_t launch_moe(const MoeArgs& a, const DeviceInfo& dev, cudaStream_t s) 
         const MoeBank& bk = k.bank[b];
         if (!encode_weight_map(&maps[b], bk.wq, a.E * a.N, a.K, kBoxRows)) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((a.N + rows - 1) / rows, dmax, nz);
