@@ -323,6 +323,32 @@ def e2e_gbs(torch, w, M, N, K, g, steps):
             "us_per_step": dt * 1e6}
 
 
+def e2e_zero_copy_gbs(torch, w, M, N, K, g, steps):
+    """Public API with host buffers and no copy calls: x and y live in
+    page-locked host memory and the GEMV kernel reads x / writes y there
+    (over NVLink-C2C on a Grace-Blackwell node), then the stream is
+    synchronised and y is on the host.  M == 1 only."""
+    from w4a16_int4_weight_gemv_gb300 import synth
+    p = synth.dense_problem(M, N, K, g, "const8", seed=0)
+    wq, s, z = (_dev(p[k], torch) for k in ("wq", "scale", "zero"))
+    xs = [torch.from_numpy(synth.activations(0, (M, K), sub=i).view(np.int16)).pin_memory()
+          for i in range(8)]
+    y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream()
+    for i in range(20):
+        w.w4a16_gemv(xs[i % 8], wq, s, z, g, out=y_host)
+        stream.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        w.w4a16_gemv(xs[i % 8], wq, s, z, g, out=y_host)
+        stream.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": algo_bytes(M, N, K, g) / dt / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
+            "us_per_step": dt * 1e6,
+            "note": "x read and y written in page-locked host memory by the kernel (no copy calls)"}
+
+
 def cpu_baseline(seconds=10.0):
     """The CPU oracle as it stands, single-threaded, on full 4096x4096 GEMVs."""
     import oracle
@@ -514,6 +540,8 @@ def run_gpu(args):
                                          "note": "gate GEMV, up GEMV, SwiGLU, down GEMV + routed sum as separate calls"}
         extra["sweep"] = sweep
         extra["e2e"] = e2e_gbs(torch, w, M, N, K, g, min(args.steps, 3000))
+        if M == 1:
+            extra["e2e_zero_copy"] = e2e_zero_copy_gbs(torch, w, M, N, K, g, min(args.steps, 3000))
         if not args.no_cpu_baseline:
             extra["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:

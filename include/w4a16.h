@@ -125,6 +125,10 @@ W4A16_API size_t w4a16_gemv_workspace_bytes(int M, int64_t N, int64_t K, int64_t
  * The kernel is launched with programmatic dependent launch: it may begin
  * while the previous kernel on `stream` drains, but reads and writes no
  * global memory until that kernel has completed, so stream order is kept.
+ * Pointers are device-accessible addresses.  With M == 1 (the CUDA-core
+ * kernel, plain loads of x and stores of y), x and y may be page-locked
+ * host memory mapped into the device's address space: the kernel then reads
+ * and writes them in place, with no copies around the call.
  */
 W4A16_API w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
                         const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,
@@ -275,6 +279,14 @@ W4A16_API w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_id
  */
 W4A16_API w4a16_status w4a16_swiglu(const uint16_t* gate, const uint16_t* up, int64_t ld_in, uint16_t* h,
                           int64_t ld_out, int64_t rows, int64_t N, void* stream);
+
+/*
+ * w4a16_host_memory_mapped -- 1 if `p` is page-locked host memory that
+ * kernels on the current device address at the same pointer (so it may be
+ * passed as x or y of a one-token w4a16_gemv), else 0.  Host-side query, no
+ * stream work.
+ */
+W4A16_API int w4a16_host_memory_mapped(const void* p);
 
 /*
  * w4a16_device_error -- synchronise `stream`, then copy the current device's

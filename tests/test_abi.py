@@ -139,6 +139,9 @@ def test_other_entry_points_validate(lib):
     assert ffn(*ptrs, 1, 8, 64, 2304, 1024, 128, None, fneed, None) == Status.ERR_WORKSPACE
     assert ffn(*ptrs[:-1], MIS, 1, 8, 64, 2304, 1024, 128, A16, fneed, None) == Status.ERR_ALIGN
     assert lib.w4a16_gemv_workspace_bytes(1, 4096, 4096, 128) == 0
+    assert lib.w4a16_host_memory_mapped(None) == 0
+    buf = ctypes.create_string_buffer(64)   # ordinary host memory is never reported mapped
+    assert lib.w4a16_host_memory_mapped(ctypes.cast(buf, P)) == 0
     assert lib.w4a16_device_error(None, 0, None) == Status.ERR_NULL
 
 

@@ -297,6 +297,26 @@ def test_full_size_sampled_rows(w, oracle, name, M, N, K, zmode, out_dtype):
     assert torch.isfinite(y.float()).all()
 
 
+def test_gemv_with_page_locked_host_x_and_y(w, oracle):
+    # M == 1: the kernel reads x from and writes y to page-locked host memory;
+    # same kernel, same plan, so the result equals the device-buffer call bit
+    # for bit (and meets the oracle bar)
+    for N, K in ((4096, 4096), (300, 2304)):
+        p = synth.dense_problem(1, N, K, 128, "uniform6to10", seed=9100 + N)
+        x_dev, wq, s, z = dense_dev(p)
+        y_dev = w.w4a16_gemv(x_dev, wq, s, z, 128)
+        x_host = x_dev.cpu().pin_memory()
+        y_host = torch.empty((1, N), dtype=torch.bfloat16).pin_memory()
+        w.w4a16_gemv(x_host, wq, s, z, 128, out=y_host)
+        torch.cuda.synchronize()
+        assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
+        check_close(host_f64(y_host), oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 128),
+                    "host-resident x/y")
+    assert w.w4a16_device_error(clear=True) == 0
+    with pytest.raises(ValueError):   # more than one token: device buffers only
+        w.w4a16_gemv(torch.zeros((2, 4096), dtype=torch.bfloat16).pin_memory(), wq, s, z, 128)
+
+
 # ---- SwiGLU --------------------------------------------------------------
 
 def test_swiglu_matches_oracle(w, oracle):

@@ -90,6 +90,8 @@ def load_library():
     lib.w4a16_moe_ffn.argtypes = [P] * 13 + [I32, I32, I32, I64, I64, I64, P, SZ, P]
     lib.w4a16_swiglu.restype = I32
     lib.w4a16_swiglu.argtypes = [P, P, I64, P, I64, I64, I64, P]
+    lib.w4a16_host_memory_mapped.restype = I32
+    lib.w4a16_host_memory_mapped.argtypes = [P]
     lib.w4a16_device_error.restype = I32
     lib.w4a16_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), I32, P]
     _lib = lib
@@ -192,6 +194,28 @@ def gemv_plan(M: int, N: int, K: int, g: int) -> dict:
 FLAG_WEIGHTS_STATIC = 0x1
 
 
+def _host_side(x, out) -> bool:
+    return (isinstance(x, torch.Tensor) and not x.is_cuda) or \
+        (isinstance(out, torch.Tensor) and not out.is_cuda)
+
+
+# host addresses the library has confirmed kernels can use as they are
+_mapped_host = set()
+
+
+def _need_pinned(t, name, dtypes, shape=None):
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+        raise ValueError("%s: a page-locked host tensor is needed here (with the other of "
+                         "x/out on the host)" % name)
+    if t.dtype not in dtypes or not t.is_contiguous() or (shape is not None and t.shape != tuple(shape)):
+        raise ValueError("%s: dtype/shape/layout not accepted" % name)
+    p = t.data_ptr()
+    if p not in _mapped_host:
+        if not load_library().w4a16_host_memory_mapped(p):
+            raise ValueError("%s: this host memory is not mapped for the device" % name)
+        _mapped_host.add(p)
+
+
 def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
                kernel_id: int = 0, k_split: int = 0, weights_static: bool = False,
                stream=None) -> torch.Tensor:
@@ -201,21 +225,40 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
     CUDA-core, warp-MMA or tensor-core (tcgen05) kernel (measurement and
     tests).  weights_static declares that no
     kernel still running on the stream writes wq/scale/zero (resident
-    weights), so their loads may start before that kernel completes."""
-    _need(x, "x", _BF16)
-    M, K = x.shape
+    weights), so their loads may start before that kernel completes.
+
+    With M == 1, x and out may both be page-locked host tensors: the kernel
+    reads x and writes y there directly (over NVLink-C2C on a Grace-Blackwell
+    node), with no copies around the call; y is valid on the host once the
+    stream has been synchronised."""
     _need(wq, "wq", _U32)
     N = wq.shape[0]
-    if tuple(wq.shape) != (N, K // 8):
-        raise ValueError("wq shape %s does not match K=%d" % (tuple(wq.shape), K))
+    K = wq.shape[1] * 8
+    if _host_side(x, out):
+        # page-locked host x / y: read and written by the kernel in place
+        # (one token: the CUDA-core kernel, plain loads and stores)
+        _need_pinned(x, "x", _BF16)
+        M = x.shape[0]
+        if M != 1 or kernel_id not in (0, 1):
+            raise ValueError("page-locked host x/out: M == 1 and the CUDA-core kernel only")
+        if out is None:
+            out = torch.empty((M, N), dtype=out_dtype).pin_memory()
+        _need_pinned(out, "out", (torch.bfloat16, torch.float32), (M, N))
+        device = wq.get_device()
+    else:
+        _need(x, "x", _BF16)
+        M = x.shape[0]
+        if out is None:
+            out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+        _need(out, "out", (torch.bfloat16, torch.float32), (M, N))
+        device = x.get_device()
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x shape %s does not match wq %s" % (tuple(x.shape), tuple(wq.shape)))
     _need(scale, "scale", _BF16, (N, K // g))
     _need(zero, "zero", _U8, (N, K // g))
-    if out is None:
-        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
-    _need(out, "out", (torch.bfloat16, torch.float32), (M, N))
     kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     lib = load_library()
-    sh = _stream(stream, x.get_device())
+    sh = _stream(stream, device)
     if kernel_id == 0 and k_split == 0 and weights_static:
         rc = lib.w4a16_gemv_ex(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
                                M, N, K, g, FLAG_WEIGHTS_STATIC, sh)

@@ -467,6 +467,16 @@ w4a16_status w4a16_swiglu(const uint16_t* gate, const uint16_t* up, int64_t ld_i
                                    static_cast<cudaStream_t>(stream)));
 }
 
+int w4a16_host_memory_mapped(const void* p) {
+    if (!p) return 0;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return (at.type == cudaMemoryTypeHost && at.devicePointer == p) ? 1 : 0;
+}
+
 w4a16_status w4a16_device_error(uint32_t* bits_out, int clear, void* stream) {
     if (!bits_out) return W4A16_ERR_NULL;
     DeviceCache* dev = nullptr;
