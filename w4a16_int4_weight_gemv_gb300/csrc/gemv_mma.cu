@@ -380,7 +380,7 @@ GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_
     // clusters is queried at the full budget, not at the two-stage minimum
     const int budget = dev.max_smem_optin;
     const SplitChoice c = choose_split(
-        dev, ntiles, units_all, W, 1, k_split_req,
+        dev, ntiles, units_all, W, 1, k_split_req, 0,
         [M, NT, W](int upc, int tg, int wpt, int tpg, int S) {
             return mma_smem_bytes(mma_base_bytes(M, NT, upc, tg, wpt, tpg, S), 2, W);
         },

@@ -548,8 +548,10 @@ GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int g, int k
     // feasibility and residency with the minimum two stages per warp; the
     // launch fills the budget with stages, so cluster co-residency is queried
     // at the budget
+    // a split tile's reduction costs about a quarter of a 1024-k span: with
+    // tiles to spare (the vocabulary head) the unsplit plan wins (82 vs 85 us)
     const SplitChoice c = choose_split(
-        dev, ntiles, nspan_all, kWarps, kCtasPerSm, k_split_req,
+        dev, ntiles, nspan_all, kWarps, kCtasPerSm, k_split_req, 1,
         [M, TR, stage](int upc, int tg, int wpt, int tpg, int S) {
             return simt_base_bytes(M, TR, upc, tg, wpt, tpg, S) + kWarps * 2 * (stage + 8);
         },

@@ -60,9 +60,11 @@ struct DeviceInfo {
 struct SplitChoice {
     int wpt, S, ctas, tiles_per_group, units_per_cta, smem_bytes;
 };
+// split_cost_q: what a split's per-tile partial-sum reduction costs, in
+// quarters of a K unit (0: negligible next to a unit).
 template <class SmemFn, class ClusterFn>
 SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int warps_per_cta,
-                         int max_ctas_per_sm, int forced_f, SmemFn smem_fn,
+                         int max_ctas_per_sm, int forced_f, int split_cost_q, SmemFn smem_fn,
                          ClusterFn max_clusters) {
     SplitChoice best{};
     long best_cost = -1, best_work = 0;
@@ -97,8 +99,10 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
             const int tpg = (ntiles + clusters * tg - 1) / (clusters * tg);
             smem = smem_fn(upc, tg, wpt, tpg, S);
             if (smem > dev.max_smem_optin) continue;
-            // first the longest warp's steps, then the busiest CTA's steps
-            const long cost = static_cast<long>(tpg) * ((upc + wpt - 1) / wpt);
+            // first the longest warp's steps (plus its tiles' reductions when
+            // the tiles are split), then the busiest CTA's steps; in quarter units
+            const long cost = static_cast<long>(tpg) *
+                              (4L * ((upc + wpt - 1) / wpt) + (f > 1 ? split_cost_q : 0));
             const long cta_work = static_cast<long>((ntiles + clusters - 1) / clusters) * upc;
             if (best_cost < 0 || cost < best_cost || (cost == best_cost && cta_work < best_work)) {
                 best_cost = cost;
