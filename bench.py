@@ -550,9 +550,11 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "w4a16: int4 weights, bf16 activations/outputs, fp32 accumulate",
+            "dtype": "f32",
             "data": "synthetic (seeded: x~N(0,1) bf16, uniform 4-bit codes, scales~U[0.005,0.02], zero=8)",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "g": g,
+                       "operands": "int4 weights (bf16 scale, u8 zero per group), bf16 "
+                                   "activations and outputs; exact products, fp32 sums",
                        "l2_policy": "inputs larger than L2: %d rotating weight copies (codes, "
                                     "scales, zeros), %.0f MB total; the 8 KB activation vector "
                                     "is shared by all steps (L2-resident, as written by the "
