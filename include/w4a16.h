@@ -141,7 +141,11 @@ W4A16_API w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const u
  * has completed (x is still read, and y written, only after it completes).
  * Set it only when no kernel that may still be running on the stream writes
  * those three buffers -- the case of resident model weights in a decode loop.
- * Otherwise identical to w4a16_gemv (workspace is not needed).
+ * It is a permission, not a speed-up in itself: with the default plans (one
+ * CTA per SM, so a launch's CTAs become resident only as the previous
+ * launch's exit) back-to-back square GEMVs measured 5.3 us with it against
+ * 5.1 us without.  Otherwise identical to w4a16_gemv (workspace is not
+ * needed).
  */
 W4A16_API w4a16_status w4a16_gemv_ex(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
                                      const uint8_t* zero, void* y, w4a16_out_dtype out_dtype,
