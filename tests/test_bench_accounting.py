@@ -1,0 +1,39 @@
+"""The benchmark's byte accounting and its ncu-traffic lookup (no GPU).
+
+Algorithmic bytes of one GEMV are the packed codes (K/2 per row), the bf16
+scales (2 per row and group) and the bf16 activations (2 per token and k);
+the values below are that sum worked out for the five workloads."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_algorithmic_bytes_of_the_workloads():
+    assert bench.algo_bytes(1, 256, 512, 128) == 65536 + 2048 + 1024 == 68608
+    assert bench.algo_bytes(1, 4096, 4096, 128) == 8388608 + 262144 + 8192 == 8658944
+    assert bench.algo_bytes(1, 14336, 4096, 128) == 29360128 + 917504 + 8192 == 30285824
+    assert bench.algo_bytes(16, 14336, 4096, 128) == 29360128 + 917504 + 131072
+    assert bench.algo_bytes(1, 4096, 14336, 128) == 29360128 + 917504 + 28672
+    assert bench.algo_bytes(1, 163840, 4096, 128) == 335544320 + 10485760 + 8192 == 346038272
+
+
+def test_all_bytes_add_zero_points_and_outputs():
+    # zero points (1 byte per row and group) and the bf16 output
+    assert bench.all_bytes(1, 4096, 4096, 128) - bench.algo_bytes(1, 4096, 4096, 128) == 131072 + 8192
+
+
+def test_profiled_traffic_follows_the_kernel_source(monkeypatch):
+    t = bench.profiled_traffic()
+    text = open(os.path.join(ROOT, "profiles", "gemv_m1_square_4096.md")).read()
+    if "kernel_source_sha256_16: %s" % bench.kernel_source_hash() in text:
+        # captured on this source: DRAM traffic of a launch, at least its algorithmic bytes
+        assert t is not None and t >= bench.algo_bytes(1, 4096, 4096, 128)
+    else:
+        assert t is None
+    # a different kernel source: the stored counter no longer applies
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.profiled_traffic() is None
