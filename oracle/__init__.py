@@ -16,6 +16,7 @@ Parity status of each function (what pins it, in tests/test_oracle.py):
                      products, one-hot GEMV columns
   gemv / gemv_rows   pinned: closed form for constant codes, one-hot
                      activations, fp64 library matmul, brute force, invariants
+  gemv_parallel      pinned: equal to gemv element for element (same sums)
   swiglu             pinned: closed forms at 0 and large |v|, library silu
   moe_gemv, moe_ffn  pinned: one-hot routing reduces to a dense chain,
                      identical experts reduce to one chain, linearity in r
@@ -46,7 +47,10 @@ def build(force: bool = False) -> str:
         tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
                "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
-        subprocess.run(cmd, check=True)
+        # OpenMP only spreads oracle_gemv_parallel's rows over host threads;
+        # without it that function runs on one thread
+        if subprocess.run(cmd[:1] + ["-fopenmp"] + cmd[1:], capture_output=True).returncode != 0:
+            subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -92,6 +96,10 @@ def _bind(lib):
     lib.oracle_dequant.argtypes = [P, P, P, P, I, I, I]
     lib.oracle_gemv.argtypes = [P, P, P, P, P, I, I, I, I]
     lib.oracle_gemv_rows.argtypes = [P, P, P, P, P, I, P, I, I, I]
+    if hasattr(lib, "oracle_gemv_parallel"):
+        lib.oracle_gemv_parallel.argtypes = [P, P, P, P, P, I, I, I, I, I]
+        lib.oracle_max_threads.restype = I
+        lib.oracle_max_threads.argtypes = []
     lib.oracle_swiglu.argtypes = [P, P, P, I]
     lib.oracle_moe_gemv.restype = ctypes.c_int
     lib.oracle_moe_gemv.argtypes = [P, ctypes.c_int, P, P, P, P, P, P,
@@ -169,6 +177,28 @@ def gemv(x, wq, scale, zero, g: int) -> np.ndarray:
     assert wq.shape == (N, K // 8) and scale.shape == (N, K // g)
     y = np.empty((M, N), np.float64)
     lib.oracle_gemv(px, pw, ps, pz, y.ctypes.data_as(ctypes.c_void_p), M, N, K, g)
+    return y
+
+
+def max_threads() -> int:
+    """Host threads gemv(..., threads=) can use (1 if built without OpenMP)."""
+    return int(_load().oracle_max_threads())
+
+
+def gemv_parallel(x, wq, scale, zero, g: int, threads: int = 0) -> np.ndarray:
+    """gemv with the output rows shared among `threads` host threads (0: all
+    of them); element for element the same fp64 sums as gemv."""
+    lib = _load()
+    x, px = _c(x, np.uint16)
+    wq, pw = _c(wq, np.uint32)
+    scale, ps = _c(scale, np.uint16)
+    zero, pz = _c(zero, np.uint8)
+    M, K = x.shape
+    N = wq.shape[0]
+    assert wq.shape == (N, K // 8) and scale.shape == (N, K // g)
+    y = np.empty((M, N), np.float64)
+    lib.oracle_gemv_parallel(px, pw, ps, pz, y.ctypes.data_as(ctypes.c_void_p), M, N, K, g,
+                             int(threads) if threads else max_threads())
     return y
 
 

@@ -35,6 +35,9 @@
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ---- bf16 <-> double ---------------------------------------------------- */
 
@@ -156,6 +159,38 @@ void oracle_gemv(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
                        oracle_weight(wq, scale, zero, K, g, n, k);
             y[m * N + n] = acc;
         }
+}
+
+/* The same y[M][N] with the output rows shared among `threads` host threads
+ * (OpenMP when the library is built with it, else one thread).  Every
+ * element is the loop of oracle_gemv -- one fp64 sum in ascending k -- so the
+ * values are identical to it; only the rows' order of evaluation differs. */
+void oracle_gemv_parallel(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
+                          const uint8_t* zero, double* y, int64_t M, int64_t N, int64_t K,
+                          int64_t g, int64_t threads)
+{
+    (void)threads;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads((int)threads) schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += oracle_bf16_to_double(x[m * K + k]) *
+                       oracle_weight(wq, scale, zero, K, g, n, k);
+            y[m * N + n] = acc;
+        }
+}
+
+/* Host threads oracle_gemv_parallel can use (1 without OpenMP). */
+int64_t oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return (int64_t)omp_get_max_threads();
+#else
+    return 1;
+#endif
 }
 
 /* ---- SwiGLU ------------------------------------------------------------- */

@@ -23,11 +23,12 @@ def reg():
     return registry
 
 
-DENSE = [(1, 300, 1024, 128), (2, 257, 2304, 128), (5, 130, 4096, 128), (16, 64, 2048, 256)]
+DENSE = [(1, 300, 1024, 128), (2, 257, 2304, 128), (5, 130, 4096, 128), (16, 64, 2048, 256),
+         (8, 100, 3072, 128)]
 
 
 @pytest.mark.parametrize("M,N,K,g", DENSE)
-@pytest.mark.parametrize("variant", ["planned", "cuda_core", "warp_mma", "tcgen05"])
+@pytest.mark.parametrize("variant", ["planned", "cuda_core", "warp_mma", "tcgen05", "fp16_mma"])
 def test_dense_variants_match_the_reference(reg, oracle, variant, M, N, K, g):
     from w4a16_int4_weight_gemv_gb300 import binding
     p = synth.dense_problem(M, N, K, g, "uniform6to10", seed=8000 + M)
@@ -36,7 +37,7 @@ def test_dense_variants_match_the_reference(reg, oracle, variant, M, N, K, g):
         y = f(*dense_dev(p), g, out_dtype=torch.float32)
     except binding.W4A16Error as e:
         assert e.status == binding.Status.ERR_UNSUPPORTED, variant
-        assert variant in ("cuda_core", "tcgen05")
+        assert variant in ("cuda_core", "tcgen05", "fp16_mma")
         return
     torch.cuda.synchronize()
     check_close(host_f64(y), oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], g), variant)

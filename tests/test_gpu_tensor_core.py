@@ -13,7 +13,7 @@ import torch
 
 from w4a16_int4_weight_gemv_gb300 import synth
 
-from .test_gpu_parity import check_close, dense_dev, dev, host_f64, _sample_rows
+from .test_gpu_parity import check_close, dense_dev, dev, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -113,12 +113,10 @@ FULL = [("square", 1, 4096, 4096), ("vocab", 1, 163840, 4096)] + \
 
 
 @pytest.mark.parametrize("name,M,N,K", FULL, ids=["%s-M%d" % (f[0], f[1]) for f in FULL])
-def test_tensor_core_full_size_sampled_rows(w, oracle, name, M, N, K):
+def test_tensor_core_full_size_every_output(w, oracle, name, M, N, K):
     p = synth.dense_problem(M, N, K, 128, "uniform6to10", seed=1)
     y = w.w4a16_gemv(*dense_dev(p), 128, out_dtype=torch.bfloat16, kernel_id=TC)
     torch.cuda.synchronize()
-    rows = _sample_rows(N, seed=N + M + 3)
-    ref = oracle.gemv_rows(p["x"], p["wq"], p["scale"], p["zero"], 128, rows)
-    check_close(host_f64(y)[:, rows], ref, name)
-    assert torch.isfinite(y.float()).all()
+    ref = oracle.gemv_parallel(p["x"], p["wq"], p["scale"], p["zero"], 128)
+    check_close(host_f64(y), ref, name)
     assert w.w4a16_device_error(clear=True) == 0

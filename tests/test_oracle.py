@@ -258,6 +258,21 @@ def test_gemv_rows_matches_full(oracle):
     assert np.array_equal(part, full[:, rows])
 
 
+@pytest.mark.parametrize("threads", [1, 3, 0])
+def test_gemv_parallel_equals_gemv(oracle, threads):
+    # the threaded full-output GEMV evaluates each element with the same fp64
+    # sum, so it equals gemv bit for bit (0 threads = all host threads), and
+    # through it inherits gemv's pins (library matmul, closed forms, brute force)
+    p = synth.dense_problem(3, 301, 1024, 128, "uniform6to10", seed=12)
+    full = oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 128)
+    par = oracle.gemv_parallel(p["x"], p["wq"], p["scale"], p["zero"], 128, threads=threads)
+    assert np.array_equal(par, full)
+    W = torch.from_numpy(oracle.dequant(p["wq"], p["scale"], p["zero"], 128))
+    ref = torch.matmul(torch.from_numpy(oracle.bf16_to_f64(p["x"])), W.T).numpy()
+    np.testing.assert_allclose(par, ref, rtol=1e-12, atol=1e-10)
+    assert oracle.max_threads() >= 1
+
+
 # ---- SwiGLU --------------------------------------------------------------
 
 def test_swiglu_closed_forms(oracle):

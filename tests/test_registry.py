@@ -36,4 +36,5 @@ def test_unknown_names_are_rejected(text):
 
 
 def test_variants_list_matches_table():
-    assert registry.variants("w4a16_dense") == ["planned", "cuda_core", "warp_mma", "tcgen05"]
+    assert registry.variants("w4a16_dense") == ["planned", "cuda_core", "warp_mma", "tcgen05",
+                                                "fp16_mma"]

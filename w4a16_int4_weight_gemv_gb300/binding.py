@@ -221,9 +221,10 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
                stream=None) -> torch.Tensor:
     """y[M, N] = x[M, K] . dequant(wq, scale, zero)^T.
 
-    kernel_id 0 (default) lets the library choose; 1, 2 or 3 force the
-    CUDA-core, warp-MMA or tensor-core (tcgen05) kernel (measurement and
-    tests).  weights_static declares that no
+    kernel_id 0 (default) lets the library choose; 1, 2, 3 or 4 force the
+    CUDA-core, bf16 warp-MMA, tensor-core (tcgen05) or fp16 warp-MMA kernel
+    (measurement and tests); k_split forces the K split (for kernel 4, the
+    CTAs of a cluster).  weights_static declares that no
     kernel still running on the stream writes wq/scale/zero (resident
     weights), so their loads may start before that kernel completes.
 

@@ -80,13 +80,22 @@ w4a16_status check_gemv_shape(int M, int64_t N, int64_t K, int64_t g) {
 
 w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
                        GemvPlan* plan, DeviceCache** dev) {
-    // default: CUDA-core kernel for one token, and for two when the groups are
-    // finer than the warp-MMA kernel's 128-k blocks; warp MMA otherwise
-    if (kernel_id == 0) kernel_id = (M == 1 || (M == 2 && g % 128 != 0)) ? 1 : 2;
+    // default: the fp16 warp-MMA kernel for one token where it applies
+    // (g == 128, K % 512 == 0) and has a plan; otherwise the CUDA-core kernel
+    // for one token, and for two when the groups are finer than 128 k; the
+    // bf16 warp-MMA kernel for the rest
+    const int requested = kernel_id;
+    const bool automatic = kernel_id == 0;
+    if (automatic)
+        kernel_id = (M == 1 && hmma_supports(M, static_cast<int>(K), static_cast<int>(g))) ? 4
+                    : (M == 1 || (M == 2 && g % 128 != 0))                                 ? 1
+                                                                                           : 2;
     if (kernel_id == 1 && M > 2) return W4A16_ERR_UNSUPPORTED;
     if ((kernel_id == 2 || kernel_id == 3) && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
-    if (kernel_id < 1 || kernel_id > 3) return W4A16_ERR_UNSUPPORTED;
-    if (kernel_id == 3 && k_split > 8) return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id == 4 && !hmma_supports(M, static_cast<int>(K), static_cast<int>(g)))
+        return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id < 1 || kernel_id > 4) return W4A16_ERR_UNSUPPORTED;
+    if ((kernel_id == 3 || kernel_id == 4) && k_split > 8) return W4A16_ERR_UNSUPPORTED;
     if (k_split < 0 || k_split > 32 || (k_split & (k_split - 1))) return W4A16_ERR_UNSUPPORTED;
     w4a16_status st = current_device(dev);
     if (st != W4A16_OK) return st;
@@ -105,7 +114,7 @@ w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, in
         std::lock_guard<std::mutex> lock(mu);
         for (int i = 0; i < used; ++i) {
             const Entry& c = cache[i];
-            if (c.device == d && c.kernel_id == kernel_id && c.M == M && c.N == n && c.K == k &&
+            if (c.device == d && c.kernel_id == requested && c.M == M && c.N == n && c.K == k &&
                 c.g == gg && c.k_split == k_split) {
                 *plan = c.plan;
                 return W4A16_OK;
@@ -114,12 +123,19 @@ w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, in
     }
     *plan = (kernel_id == 1)   ? plan_gemv_simt((*dev)->info, M, n, k, gg, k_split)
             : (kernel_id == 2) ? plan_gemv_mma((*dev)->info, M, n, k, gg, k_split)
-                               : plan_gemv_tc((*dev)->info, M, n, k, gg, k_split);
+            : (kernel_id == 3) ? plan_gemv_tc((*dev)->info, M, n, k, gg, k_split)
+                               : plan_gemv_hmma((*dev)->info, M, n, k, gg, k_split);
+    if (automatic && kernel_id == 4 && plan->ctas < 1) {
+        // no fp16-MMA plan for this shape (activations too large for shared memory)
+        kernel_id = (M == 1) ? 1 : 2;
+        *plan = (kernel_id == 1) ? plan_gemv_simt((*dev)->info, M, n, k, gg, k_split)
+                                 : plan_gemv_mma((*dev)->info, M, n, k, gg, k_split);
+    }
     if (plan->ctas < 1 || plan->smem_bytes > (*dev)->info.max_smem_optin)
         return W4A16_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(mu);
     Entry& slot = (used < 256) ? cache[used++] : cache[next++ & 255];
-    slot = Entry{d, kernel_id, M, n, k, gg, k_split, *plan};
+    slot = Entry{d, requested, M, n, k, gg, k_split, *plan};
     return W4A16_OK;
 }
 
@@ -144,7 +160,8 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return from_cuda(plan.kernel_id == 1   ? launch_gemv_simt(a, plan, s)
                      : plan.kernel_id == 2 ? launch_gemv_mma(a, plan, s)
-                                           : launch_gemv_tc(a, plan, s));
+                     : plan.kernel_id == 3 ? launch_gemv_tc(a, plan, s)
+                                           : launch_gemv_hmma(a, plan, s));
 }
 
 }  // namespace
@@ -289,7 +306,7 @@ w4a16_status w4a16_gemv_variant(const uint16_t* x, const uint32_t* wq, const uin
                                 const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,
                                 int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
                                 void* stream) {
-    if (kernel_id < 1 || kernel_id > 3) return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id < 1 || kernel_id > 4) return W4A16_ERR_UNSUPPORTED;
     return gemv_impl(x, wq, scale, zero, y, out_dtype, M, N, K, g, kernel_id, k_split, 0u,
                      stream);
 }

@@ -201,6 +201,18 @@ __device__ __forceinline__ void cluster_barrier() {
             : "memory");
 }
 
+// The two halves of a cluster barrier.  A kernel that stores into a peer
+// CTA's shared memory arrives (relaxed) once its own shared memory is set up
+// and waits before its first remote store, so every peer has started; the
+// pair also makes one phase of the barrier, to be completed by every thread
+// before the next arrive.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Store into the shared memory of CTA `rank` of the cluster, at the offset
 // local_ptr has in this CTA (fire-and-forget; a cluster barrier makes it
 // visible to the owner).
@@ -210,6 +222,59 @@ __device__ __forceinline__ void st_dsmem_f32(float* local_ptr, uint32_t rank, fl
                  : "=r"(remote)
                  : "r"(smem_addr(local_ptr)), "r"(rank));
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+// Four floats into the shared memory of CTA `rank` of the cluster (16-byte
+// aligned offset), fire-and-forget like st_dsmem_f32.
+__device__ __forceinline__ void st_dsmem_f32x4(float* local_ptr, uint32_t rank, float4 v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(remote)
+                 : "r"(smem_addr(local_ptr)), "r"(rank));
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Warp MMA: D[16x8] (fp32) = A[16x16] (fp16, row) * B[16x8] (fp16, col) + D
+// (A operand: a0 rows r, a1 rows r + 8, k pairs 2c, 2c+1; a2/a3 the same at
+// k + 8; B: b0 k pairs 2c, 2c+1 of column r, b1 at k + 8; r = lane / 4,
+// c = lane % 4, lower k in the low half of each register)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same with a zero accumulator (the first product of a chain).
+__device__ __forceinline__ void mma_f16_16816_zero(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                   uint32_t a2, uint32_t a3, uint32_t b0,
+                                                   uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Two 4-bit codes of a packed word as an fp16 pair, by one LOP3 with the
+// exponent of 1024 (0x6400): (w & 0x000F000F) | 0x64006400 is
+// {1024 + code at bits 0..3, 1024 + code at bits 16..19}, and
+// (w & 0x00F000F0) | 0x64006400 is {1024 + 16 code(bits 4..7), 1024 + 16 code
+// (bits 20..23)} -- both exact, as fp16 has ten fraction bits.
+__device__ __forceinline__ uint32_t f16_codes_lo(uint32_t w) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(d) : "r"(w));
+    return d;
+}
+__device__ __forceinline__ uint32_t f16_codes_hi(uint32_t w) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(d) : "r"(w));
+    return d;
 }
 
 // ---------------------------------------------------------------------------

@@ -1,0 +1,529 @@
+// Dense W4A16 GEMV for 1..8 tokens on warp MMA with fp16 operands (sm_103a).
+//
+// The decode-time product of the local-kimi README, technical-detail section:
+// a true GEMV with K contiguous, every output row one fp32 accumulation.
+//
+// Why the tensor pipe for a GEMV.  On sm_103a the integer/logic pipe issues
+// at half rate (16 lanes per SMSP and clock): turning a packed word into
+// operands costs one LOP3 per code on the CUDA cores (each fp32 operand holds
+// one code), which alone needs ~85 % of that pipe at HBM speed.  An fp16 pair
+// holds two codes, so feeding the codes to the tensor pipe as the A operand of
+// mma.sync.m16n8k16 halves that work, and the multiply-adds leave the CUDA
+// cores altogether; the tokens are the B operand (8 columns, 1..8 used).
+//
+// Dequantisation.  (w & 0x000F000F) | 0x64006400 is the fp16 pair
+// {1024 + q0, 1024 + q4} and (w & 0x00F000F0) | 0x64006400 the pair
+// {1024 + 16 q1, 1024 + 16 q5}; the same two LOP3s on w >> 8 give codes 2, 6
+// and 3, 7 -- five logic instructions per word of eight codes.  The factor 16
+// of the odd codes is taken out of the activations (their B entries are x/16),
+// so every product A*B is 1024 B + q x' exactly, and for each 128-k block (one
+// quantisation group, g == 128)
+//     sum_k (q_k - z) x'_k = D - 1024 sum_k B_k - z sum_k x'_k,
+// with D the block's MMA sum; the scale multiplies that once per block.
+//
+// Activations.  Each CTA converts its K slice of x once, after the
+// grid-dependency wait, in one pass: every 128-k block of every token gets
+// its own power of two, x' = x * 2^sh with the block's largest |x| landing in
+// [2^14, 2^15) (fp16 holds it and every element within 2^24 of it exactly),
+// is rounded to fp16 and stored in the order the B fragments are read: one
+// 16-byte load per lane and chunk gives the four B registers of two MMAs.
+// Beside the fragments go the block sums of the rounded values (c1 = 1024
+// sum B, c2 = sum x') and 2^-sh, which multiplies the scale in the epilogue.
+//
+// Memory path.  A unit is one 16-row tile x 512 k.  Every warp streams its
+// own units through its own ring of `depth` stages with 16-byte cp.async
+// copies -- the 256 packed bytes of each row at a row pitch of 272 bytes, so
+// that ldmatrix reads the eight rows of a 16-byte chunk from eight bank
+// groups, then the tile's zero points and scales -- one commit group per
+// unit, waited for with cp.async.wait_group, so depth - 1 units are in
+// flight while the warp computes.  (The copy engine is not used: a bulk or
+// tensor copy costs its issuing warp tens of nanoseconds on sm_103a, and
+// with the weights split over many such copies the issue time outweighs the
+// arithmetic.)  Nothing waits on another thread except at named and
+// cluster barriers that every thread reaches.
+//
+// Work split.  The CTAs of a cluster share a range of 16-row tiles, rank r
+// taking the r-th K slice; inside the CTA, WPT warps share a tile, warp part
+// p taking K steps p, p + WPT, ...; tile groups take the CTA's tiles in turn.
+// Parts meet at a named barrier per tile and part 0 adds their partials in
+// part order; ranks push their tile sums into the owner's shared memory and
+// the owner adds them in rank order after a cluster barrier -- fixed orders,
+// so results are deterministic.
+//
+// Launch.  The rings are sized so that two CTAs fit on an SM where possible:
+// with programmatic dependent launch the next GEMV's CTA becomes resident
+// while this one runs, and with W4A16_FLAG_WEIGHTS_STATIC it requests its
+// first units before the grid-dependency wait.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kW = kHmmaWarps;
+constexpr int kThreads = 32 * kW;
+constexpr int kSZScales = 64;
+
+struct HmmaKernelArgs {
+    const uint16_t* x;
+    const unsigned char* wq;  // packed words as bytes, row pitch K / 2
+    const uint16_t* scale;
+    const uint8_t* zero;
+    void* y;
+    int out_f32;
+    int M;
+    int N;
+    int K;
+    int S;               // CTAs per cluster (K split)
+    int nclusters;       // tile ranges
+    int steps_per_rank;  // 512-k steps per K slice
+    int max_tiles;       // most tiles one cluster owns
+    int wpt;             // warps per tile
+    int depth;           // stages per warp
+    int weights_static;
+};
+
+// exact 2^e for any integer e in [-252, 254], as the product of two normal
+// powers of two (applied one after the other by the callers)
+__device__ __forceinline__ void pow2_pair(int e, float& f1, float& f2) {
+    const int e1 = e / 2;
+    f1 = exp2i(e1);
+    f2 = exp2i(e - e1);
+}
+
+// Shift of a block whose largest |x| has bf16 bits mb: the largest lands in
+// [2^14, 2^15); blocks of subnormals or zeros get 2^126 (their products are
+// below 2^-100 and exactness there is moot), so 2^-sh is a normal float.
+__device__ __forceinline__ int block_shift(uint32_t mb) {
+    int eb = static_cast<int>(mb >> 7);  // biased exponent of the largest |x|
+    if (eb > 254) eb = 254;              // Inf / NaN: any shift, the result is not finite
+    const int sh = 141 - eb;
+    return sh > 126 ? 126 : sh;
+}
+
+__device__ __forceinline__ float zero_point_f32(uint32_t bytes4, int b) {
+    // byte b of bytes4 placed under the exponent of 2^23, minus 2^23
+    return __uint_as_float(__byte_perm(bytes4, 0x4B000000u, 0x7540u + b)) - 8388608.f;
+}
+
+// Store the C-fragment values of lane l for 16-row tile `tile`: rows
+// 16 tile + l / 4 (x, y) and + 8 (z, w), tokens 2 (l % 4) (x, z) and + 1 (y, w).
+__device__ __forceinline__ void store_fragment(const HmmaKernelArgs& a, int tile, int l, float4 v) {
+    const int g = l >> 2, c = l & 3;
+    const int ra = (tile << 4) + g;
+    const int rb = ra + 8;
+    if (2 * c < a.M) {
+        const size_t o = static_cast<size_t>(2 * c) * a.N;
+        if (ra < a.N) store_out(a.y, a.out_f32, o + ra, v.x);
+        if (rb < a.N) store_out(a.y, a.out_f32, o + rb, v.z);
+    }
+    if (2 * c + 1 < a.M) {
+        const size_t o = static_cast<size_t>(2 * c + 1) * a.N;
+        if (ra < a.N) store_out(a.y, a.out_f32, o + ra, v.y);
+        if (rb < a.N) store_out(a.y, a.out_f32, o + rb, v.w);
+    }
+}
+
+// wait until at most n of this thread's cp.async commit groups are pending
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    }
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// MP: the token count rounded up to 1, 2, 4 or 8 -- the B fragments are
+// stored for MP tokens (the columns of tokens M..MP-1 are never stored, so
+// their contents do not matter)
+template <int MP>
+__global__ void __launch_bounds__(kThreads, 2) k_gemv_hmma(const HmmaKernelArgs a) {
+    constexpr int W = kW;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int S = a.S;
+    const int rank = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
+    const int cid = blockIdx.x / S;
+    const int ntiles = (a.N + 15) >> 4;
+    const int t0 = static_cast<int>(static_cast<long long>(ntiles) * cid / a.nclusters);
+    const int t1 = static_cast<int>(static_cast<long long>(ntiles) * (cid + 1) / a.nclusters);
+    const int nt = t1 - t0;
+    const int nsr = a.steps_per_rank;  // S divides K / 512: every rank has them all
+    const int s0 = rank * nsr;
+    const int M = a.M;
+    const int G = a.K >> 7;
+    const int WPT = a.wpt;
+    const int NG = W / WPT;
+    const int grp = warp / WPT;
+    const int part = warp - grp * WPT;
+    const int D = a.depth;
+
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char* base = smem_raw + (((raw + 127u) & ~127u) - raw);
+    const HmmaLayout L = hmma_layout(MP, nsr, S, a.max_tiles, D);
+    unsigned char* ring = base + L.ring + warp * D * kHmmaStage;
+    uint4* bfrag = reinterpret_cast<uint4*>(base + L.bfrag);
+    float* csum = reinterpret_cast<float*>(base + L.csum);
+    float4* red = reinterpret_cast<float4*>(base + L.red);
+    float4* cpart = reinterpret_cast<float4*>(base + L.cpart);
+
+    // this warp's units: tiles grp, grp + NG, ... of the CTA, K steps part,
+    // part + WPT, ... of the slice
+    const int my_tiles = (nt > grp) ? (nt - grp + NG - 1) / NG : 0;
+    const int my_steps = (nsr > part) ? (nsr - part + WPT - 1) / WPT : 0;
+    const int nu = my_tiles * my_steps;
+
+    grid_dependents_launch();
+    if (S > 1) cluster_arrive_relaxed();
+
+    // Producer side of this warp's ring: unit (i_tile, i_step) into stage
+    // i_slot as one commit group.  Lane l copies the 16-byte pieces
+    // (row 2 i + l / 16, column l % 16), i = 0..7, so each copy instruction
+    // reads two whole 256-byte row pieces; lanes 0..15 then copy the 4 zero
+    // points of row l, lanes 16..31 its 4 scales.
+    const size_t row_bytes = static_cast<size_t>(a.K) >> 1;
+    const size_t src_lane = static_cast<size_t>(lane >> 4) * row_bytes + (lane & 15) * 16;
+    const int dst_lane = (lane >> 4) * kHmmaRowPitch + (lane & 15) * 16;
+    const int rr = lane & 15;
+    int i_u = 0, i_slot = 0, i_tile = t0 + grp, i_step = part;
+    auto issue_next = [&]() {
+        if (i_u < nu) {
+            const int row0 = i_tile << 4;
+            const int rows = min(16, a.N - row0);
+            const int step = s0 + i_step;
+            unsigned char* stage = ring + i_slot * kHmmaStage;
+            const unsigned char* src = a.wq + static_cast<size_t>(row0) * row_bytes + step * 256 + src_lane;
+            unsigned char* dst = stage + dst_lane;
+            if (rows == 16) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cp_async_16(dst + i * 2 * kHmmaRowPitch, src + i * 2 * row_bytes);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (2 * i + (lane >> 4) < rows)
+                        cp_async_16(dst + i * 2 * kHmmaRowPitch, src + i * 2 * row_bytes);
+            }
+            if (rr < rows) {
+                const size_t gi = static_cast<size_t>(row0 + rr) * G + step * 4;
+                if (lane < 16) cp_async_4(stage + kHmmaUnitBytes + rr * 4, a.zero + gi);
+                else cp_async_8(stage + kHmmaUnitBytes + kSZScales + rr * 8, a.scale + gi);
+            }
+            ++i_u;
+            if (++i_slot == D) i_slot = 0;
+            i_step += WPT;
+            if (i_step >= nsr) {
+                i_step = part;
+                i_tile += NG;
+            }
+        }
+        cp_async_commit();  // one group per call, empty past the end
+    };
+    // with static weights the first units are requested before the
+    // preceding grid completes
+    if (a.weights_static)
+        for (int k = 0; k < D - 1; ++k) issue_next();
+    grid_dependency_wait();
+    if (!a.weights_static)
+        for (int k = 0; k < D - 1; ++k) issue_next();
+
+    {
+        // Activations: every (token, round) item of this thread; the loads of
+        // up to four items are issued before any is converted, so the L2
+        // latency is paid once per four.  The 16 pieces of a block are 16
+        // consecutive lanes (block max and sums by shuffles).
+        const int tid = threadIdx.x;
+        constexpr int T = kThreads;
+        const int nblk = nsr * 4;       // 128-k blocks of the slice
+        const int npieces = nblk * 16;  // 8-k pieces per token
+        const int nrounds = (npieces + T - 1) / T;
+        const int items = M * nrounds;
+        const uint16_t* xs = a.x + static_cast<size_t>(s0) * 512;
+        for (int it0 = 0; it0 < items; it0 += 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int it = it0 + b;
+                const int m = it / nrounds;
+                const int p = (it - m * nrounds) * T + tid;
+                v[b] = make_uint4(0u, 0u, 0u, 0u);
+                if (it < items && p < npieces)
+                    v[b] = __ldg(reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * a.K + p * 8));
+            }
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int it = it0 + b;
+                if (it >= items) break;  // the same for the whole CTA
+                const int m = it / nrounds;
+                const int p = (it - m * nrounds) * T + tid;
+                const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+                uint32_t mx = 0u;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    mx = max(mx, w[e] & 0x7FFFu);
+                    mx = max(mx, (w[e] >> 16) & 0x7FFFu);
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const int sh = block_shift(mx);
+                float fa, fb;
+                pow2_pair(sh, fa, fb);
+                const float fo = fb * 0.0625f;  // odd codes: B = x' / 16
+                uint32_t h[8];
+                float c1 = 0.f, c2 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t bits = (e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
+                    const float xv = __uint_as_float(bits) * fa;
+                    const __half hv = __float2half_rn((e & 1) ? xv * fo : xv * fb);
+                    h[e] = __half_as_ushort(hv);
+                    const float bv = __half2float(hv);
+                    c1 += bv;
+                    c2 += (e & 1) ? 16.f * bv : bv;
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    c1 += __shfl_xor_sync(0xffffffffu, c1, o);
+                    c2 += __shfl_xor_sync(0xffffffffu, c2, o);
+                }
+                if (p < npieces) {
+                    const int blk = p >> 4, j = (p >> 2) & 3, q = p & 3;
+                    uint4 o4;
+                    o4.x = h[0] | (h[4] << 16);  // MMA 1, b0: codes 0, 4
+                    o4.y = h[1] | (h[5] << 16);  // MMA 1, b1: codes 1, 5 (x/16)
+                    o4.z = h[2] | (h[6] << 16);  // MMA 2, b0: codes 2, 6
+                    o4.w = h[3] | (h[7] << 16);  // MMA 2, b1: codes 3, 7 (x/16)
+                    bfrag[((blk * 4 + j) * MP + m) * 4 + q] = o4;
+                    if ((p & 15) == 0) {
+                        float* cs = csum + (blk * 4 + (m >> 1)) * 8;
+                        cs[m & 1] = 1024.f * c1;
+                        cs[2 + (m & 1)] = c2;
+                        cs[4 + (m & 1)] = exp2i(-sh);
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (S > 1) cluster_wait();  // every peer CTA has started: remote stores are safe
+
+    const int g = lane >> 2, c = lane & 3;
+    // ldmatrix addressing: lane l supplies row (l & 7) + 8 ((l >> 3) & 1) of
+    // chunk (l >> 4) (+ 2 for the second load) of the block's four chunks; at
+    // the 272-byte pitch the eight rows of a matrix fall in eight bank groups
+    const int lrow = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int lch = lane >> 4;
+    const uint32_t ring_addr = smem_addr(ring) + static_cast<uint32_t>(lrow * kHmmaRowPitch + lch * 16);
+    // B fragments of token g (padding-token lanes read token 0's: their
+    // output columns are never stored) and the block sums of tokens 2c, 2c + 1
+    const uint4* bq_lane = bfrag + (g < M ? g : 0) * 4 + c;
+    const float* cs_lane = csum + c * 8;
+
+    float4 tacc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int c_slot = 0, c_step = part, c_tile = 0, ti = 0;  // c_tile: local tile of the group
+#pragma unroll 1
+    for (int k = 0; k < nu; ++k) {
+        issue_next();  // unit k + D - 1 into the stage consumed last iteration
+        cp_async_wait_pending(D - 1);
+        __syncwarp();  // every lane's copies of unit k have landed
+        const int slot = c_slot;
+        const int lstep = c_step;
+        if (++c_slot == D) c_slot = 0;
+        const uint32_t wst = ring_addr + static_cast<uint32_t>(slot * kHmmaStage);
+        const unsigned char* sz = ring + slot * kHmmaStage + kHmmaUnitBytes;
+        const uint32_t za = *reinterpret_cast<const uint32_t*>(sz + g * 4);
+        const uint32_t zb = *reinterpret_cast<const uint32_t*>(sz + (g + 8) * 4);
+        const uint2 sa = *reinterpret_cast<const uint2*>(sz + kSZScales + g * 8);
+        const uint2 sb = *reinterpret_cast<const uint2*>(sz + kSZScales + (g + 8) * 8);
+        const uint4* bqu = bq_lane + lstep * 16 * MP * 4;
+        const float* csu = cs_lane + lstep * 4 * 32;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+            const uint32_t hb = wst + static_cast<uint32_t>(bb * 64);
+            uint32_t q0[4], q1[4];
+            ldmatrix_x4(q0, hb);
+            ldmatrix_x4(q1, hb + 32u);
+            const uint32_t wa[4] = {q0[0], q0[2], q1[0], q1[2]};  // row g, chunks 0..3
+            const uint32_t wb[4] = {q0[1], q0[3], q1[1], q1[3]};  // row g + 8
+            uint4 bq[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) bq[j] = bqu[(bb * 4 + j) * MP * 4];
+            float d0[4], d1[4];
+            {
+                const uint32_t ta = wa[0] >> 8, tb = wb[0] >> 8;
+                mma_f16_16816_zero(d0, f16_codes_lo(wa[0]), f16_codes_lo(wb[0]), f16_codes_hi(wa[0]),
+                                   f16_codes_hi(wb[0]), bq[0].x, bq[0].y);
+                mma_f16_16816_zero(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
+                                   f16_codes_hi(tb), bq[0].z, bq[0].w);
+            }
+#pragma unroll
+            for (int j = 1; j < 4; ++j) {
+                const uint32_t ta = wa[j] >> 8, tb = wb[j] >> 8;
+                mma_f16_16816(d0, f16_codes_lo(wa[j]), f16_codes_lo(wb[j]), f16_codes_hi(wa[j]),
+                              f16_codes_hi(wb[j]), bq[j].x, bq[j].y);
+                mma_f16_16816(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
+                              f16_codes_hi(tb), bq[j].z, bq[j].w);
+            }
+            const float4 cs = *reinterpret_cast<const float4*>(csu + bb * 32);
+            const float2 fs = *reinterpret_cast<const float2*>(csu + bb * 32 + 4);
+            const float zfa = zero_point_f32(za, bb), zfb = zero_point_f32(zb, bb);
+            const uint32_t swa = (bb < 2) ? sa.x : sa.y, swb = (bb < 2) ? sb.x : sb.y;
+            const float sfa = __uint_as_float((bb & 1) ? (swa & 0xFFFF0000u) : (swa << 16));
+            const float sfb = __uint_as_float((bb & 1) ? (swb & 0xFFFF0000u) : (swb << 16));
+            acc[0] = fmaf(sfa * fs.x, (d0[0] + d1[0]) - fmaf(zfa, cs.z, cs.x), acc[0]);
+            acc[1] = fmaf(sfa * fs.y, (d0[1] + d1[1]) - fmaf(zfa, cs.w, cs.y), acc[1]);
+            acc[2] = fmaf(sfb * fs.x, (d0[2] + d1[2]) - fmaf(zfb, cs.z, cs.x), acc[2]);
+            acc[3] = fmaf(sfb * fs.y, (d0[3] + d1[3]) - fmaf(zfb, cs.w, cs.y), acc[3]);
+        }
+        __syncwarp();  // every lane is done with the stage before it is refilled
+        tacc.x += acc[0];
+        tacc.y += acc[1];
+        tacc.z += acc[2];
+        tacc.w += acc[3];
+        c_step += WPT;
+        if (c_step < nsr) continue;
+        c_step = part;
+        // the tile's part is complete: add the parts in order, then store or push
+        const int tile = t0 + grp + c_tile * NG;
+        if (WPT > 1) {
+            float4* rb = red + ((ti & 1) * W + grp * WPT) * 32;
+            rb[part * 32 + lane] = tacc;
+            named_barrier_sync(1 + grp, WPT * 32);
+            if (part == 0) {
+                tacc = rb[lane];
+                for (int q = 1; q < WPT; ++q) {
+                    const float4 v = rb[q * 32 + lane];
+                    tacc.x += v.x;
+                    tacc.y += v.y;
+                    tacc.z += v.z;
+                    tacc.w += v.w;
+                }
+            }
+        }
+        if (part == 0) {
+            if (S == 1) {
+                store_fragment(a, tile, lane, tacc);
+            } else {
+                const int tl = tile - t0;
+                st_dsmem_f32x4(reinterpret_cast<float*>(cpart + (tl * S + rank) * 32 + lane),
+                               static_cast<uint32_t>(tl % S), tacc);
+            }
+        }
+        tacc = make_float4(0.f, 0.f, 0.f, 0.f);
+        ++c_tile;
+        ++ti;
+    }
+    // a part with no K step still joins its group's per-tile barriers
+    if (WPT > 1 && my_steps == 0)
+        for (; ti < my_tiles; ++ti) {
+            float4* rb = red + ((ti & 1) * W + grp * WPT) * 32;
+            rb[part * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+            named_barrier_sync(1 + grp, WPT * 32);
+        }
+    cp_async_wait_pending(0);
+
+    // K split over the cluster: every rank pushed its tile sums into the owner
+    // (tile % S); after the barrier the owner adds them in rank order
+    if (S > 1) {
+        cluster_barrier();
+        for (int idx = threadIdx.x; idx < nt * 32; idx += blockDim.x) {
+            const int tl = idx >> 5, l = idx & 31;
+            if (tl % S != rank) continue;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int q = 0; q < S; ++q) {
+                const float4 pv = cpart[(tl * S + q) * 32 + l];
+                v.x += pv.x;
+                v.y += pv.y;
+                v.z += pv.z;
+                v.w += pv.w;
+            }
+            store_fragment(a, t0 + tl, l, v);
+        }
+    }
+}
+
+using HmmaKernel = void (*)(HmmaKernelArgs);
+HmmaKernel hmma_kernel(int M) {
+    return M <= 1 ? k_gemv_hmma<1> : M <= 2 ? k_gemv_hmma<2> : M <= 4 ? k_gemv_hmma<4> : k_gemv_hmma<8>;
+}
+// tokens rounded up to the instantiated count
+int hmma_mp(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+}  // namespace
+
+GemvPlan plan_gemv_hmma(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req) {
+    GemvPlan p{};
+    p.kernel_id = 4;
+    if (!hmma_supports(M, K, g)) return p;
+    const void* kern = reinterpret_cast<const void*>(hmma_kernel(M));
+    const HmmaChoice c = plan_hmma_split(dev, hmma_mp(M), N, K, k_split_req, [kern](int S, int smem) {
+        return max_active_clusters(kern, kThreads, smem, S);
+    });
+    if (c.nclusters < 1) return p;
+    p.k_split = c.S;
+    p.wpt = c.wpt;
+    p.units_per_cta = c.steps_per_rank;
+    p.threads = kThreads;
+    p.ctas = c.nclusters * c.S;
+    p.stages = c.depth;
+    p.smem_bytes = c.smem_bytes;
+    p.nclusters = c.nclusters;
+    p.max_tiles = c.max_tiles;
+    p.tiles_per_cluster = c.max_tiles;
+    p.tile_rows = 16;
+    return p;
+}
+
+cudaError_t launch_gemv_hmma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
+    HmmaKernelArgs k{};
+    k.x = a.x;
+    k.wq = reinterpret_cast<const unsigned char*>(a.wq);
+    k.scale = a.scale;
+    k.zero = a.zero;
+    k.y = a.y;
+    k.out_f32 = a.out_f32;
+    k.M = a.M;
+    k.N = a.N;
+    k.K = a.K;
+    k.S = p.k_split;
+    k.nclusters = p.nclusters;
+    k.steps_per_rank = p.units_per_cta;
+    k.max_tiles = p.max_tiles;
+    k.wpt = p.wpt;
+    k.depth = p.stages;
+    k.weights_static = a.weights_static;
+    const HmmaKernel kern = hmma_kernel(a.M);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(p.ctas);
+    cfg.blockDim = dim3(p.threads);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.k_split > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = p.k_split;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, k);
+}
+
+}  // namespace w4a16

@@ -147,6 +147,9 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
         mbar_init_fence();
     }
     __syncthreads();
+    // K split over a cluster: this CTA is running; the matching wait comes
+    // before the first store into a peer's shared memory
+    if (S > 1) cluster_arrive_relaxed();
 
     // producer cursor
     int w_tile = gid, w_step = kp, w_stage = 0, w_issued = 0;
@@ -206,6 +209,7 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
     pair_x_in_place<NT>(a.M, nb, xs, xsum, tok_stride);
     __syncthreads();
     while (w_issued < NS && w_issued < nss) issue();
+    if (S > 1) cluster_wait();  // every peer CTA has started
 
     float acc[NT][4];
 #pragma unroll

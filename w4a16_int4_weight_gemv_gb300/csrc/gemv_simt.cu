@@ -204,6 +204,9 @@ k_gemv_simt(const SimtKernelArgs a) {
         mbar_init_fence();
     }
     __syncwarp();
+    // K split over a cluster: this CTA is running; the matching wait comes
+    // before the first store into a peer's shared memory
+    if (S > 1) cluster_arrive_relaxed();
 
     // producer cursor: step (w_tile, w_span) goes to stage w_stage
     int w_tile = gid, w_span = kp, w_stage = 0, w_issued = 0;
@@ -317,6 +320,7 @@ k_gemv_simt(const SimtKernelArgs a) {
             store_piece(m, b + threadIdx.x, load_piece(m, b + threadIdx.x));
     __syncthreads();
     while (w_issued < NS && w_issued < nss) issue();
+    if (S > 1) cluster_wait();  // every peer CTA has started
 
     float acc[TR][MT];
 #pragma unroll

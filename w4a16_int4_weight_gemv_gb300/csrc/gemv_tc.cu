@@ -181,6 +181,9 @@ k_gemv_tc(const TcArgs a, const __grid_constant__ CUtensorMap wmap) {
     tc_fence_before();
     __syncthreads();  // barriers initialised, TMEM allocated, activation copies issued
     tc_fence_after();
+    // K split over a cluster: this CTA is running; the matching wait comes
+    // before the first store into a peer's shared memory
+    if (S > 1) cluster_arrive_relaxed();
     const uint32_t tb = *tmem_base;
 
     // producer: stage st holds blocks 2 s2, 2 s2 + 1 of tile i (st = i * nss + s2)
@@ -238,6 +241,7 @@ k_gemv_tc(const TcArgs a, const __grid_constant__ CUtensorMap wmap) {
     }
     fence_proxy_async_smem();  // B is read by the tensor cores (async proxy)
     __syncthreads();
+    if (S > 1) cluster_wait();  // every peer CTA has started
 
     if (warp < kDeqWarps) {
         // ------------------------------------------------------------------

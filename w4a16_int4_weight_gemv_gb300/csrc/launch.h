@@ -32,7 +32,8 @@ struct GemvArgs {
 };
 
 struct GemvPlan {
-    int kernel_id;  // 1 = CUDA-core kernel, 2 = warp-MMA kernel, 3 = tensor-core (tcgen05) kernel
+    int kernel_id;  // 1 = CUDA-core kernel, 2 = warp-MMA kernel, 3 = tensor-core (tcgen05) kernel,
+                    // 4 = fp16 warp-MMA kernel with a producer warp
     int ctas;
     int threads;
     int k_split;     // cluster size along K (1 = no split)
@@ -42,6 +43,8 @@ struct GemvPlan {
     int wpt;                // warps sharing one tile (K split inside the CTA)
     int stages;             // shared-memory stages per warp
     int tile_rows;          // rows per warp tile (CUDA-core kernel)
+    int nclusters;          // kernel 4: clusters (tile ranges)
+    int max_tiles;          // kernel 4: most tiles one cluster owns
 };
 
 struct DeviceInfo {
@@ -114,6 +117,102 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
     return best;
 }
 
+// ---------------------------------------------------------------------------
+// fp16 warp-MMA GEMV (kernel 4): 1..8 tokens, g == 128, K % 512 == 0.
+// A unit is one 16-row tile x 512 k: 16 rows of 256 packed bytes stored at a
+// padded pitch of 272 bytes, plus the tile's 16 x 4 zero points and 16 x 4
+// scales.  Every warp streams its own units through its own ring of
+// `depth` stages (cp.async); WPT warps of a CTA may share a tile (K steps
+// dealt round-robin, partials added behind a named barrier), and K may be
+// split over the S CTAs of a cluster (S | K/512).
+// ---------------------------------------------------------------------------
+constexpr int kHmmaWarps = 8;
+constexpr int kHmmaRowPitch = 272;                   // 256 bytes of a row + 16 of padding
+constexpr int kHmmaUnitBytes = 16 * kHmmaRowPitch;   // 4352
+constexpr int kHmmaUnitSZ = 192;   // zero points 16 x 4 bytes, then scales 16 x 8 bytes
+constexpr int kHmmaStage = kHmmaUnitBytes + kHmmaUnitSZ;
+constexpr int kHmmaMaxDepth = 6;
+
+struct HmmaLayout {
+    int ring, bfrag, csum, red, cpart, total;
+};
+// Byte offsets inside the CTA's shared memory (from a 128-aligned base; the
+// total includes the alignment slack) for M tokens (the count the B fragments
+// are stored for: 1, 2, 4 or 8), `steps` 512-k steps per
+// K slice, S CTAs per cluster, at most max_tiles tiles per cluster, `depth`
+// stages per warp.
+__host__ __device__ inline HmmaLayout hmma_layout(int M, int steps, int S, int max_tiles,
+                                                  int depth) {
+    HmmaLayout L;
+    int off = 0;
+    L.ring = off;  // [warp][depth] stages
+    off += kHmmaWarps * depth * kHmmaStage;
+    L.bfrag = off;  // activation fragments: [block][piece][token][lane % 4] x 16 bytes
+    off += steps * 4 * 4 * M * 4 * 16;
+    L.csum = off;  // per block and lane % 4: {c1[2c], c1[2c+1], c2[2c], c2[2c+1]},
+    off += steps * 4 * 4 * 32;  // then the block's 2^-shift of tokens 2c, 2c + 1
+    L.red = off;  // in-CTA K split: [2][warp][lane] float4 partials
+    off += 2 * kHmmaWarps * 32 * 16;
+    L.cpart = off;  // K split over the cluster: [tile][rank][lane] float4 pushed to the owner
+    off += (S > 1) ? max_tiles * S * 32 * 16 : 0;
+    L.total = off + 128;
+    return L;
+}
+
+struct HmmaChoice {
+    int S, nclusters, steps_per_rank, max_tiles, wpt, depth, smem_bytes, per_sm;
+};
+// Launch shape of kernel 4: the K split S over a cluster (a power of two
+// dividing K/512; forced_S > 0 forces it) and WPT warps per tile inside the
+// CTA, minimising the longest warp's units (tiles of its group x K steps of
+// its part), then preferring two CTAs per SM (so the next launch's CTA can
+// be resident beside this one), then the smallest S and WPT; then as many
+// stages per warp as fit that residency.  max_clusters(S, smem) is how many
+// clusters of S CTAs the device holds at once.  nclusters == 0: no plan.
+template <class ClusterFn>
+HmmaChoice plan_hmma_split(const DeviceInfo& dev, int M, int N, int K, int forced_S,
+                           ClusterFn max_clusters) {
+    HmmaChoice best{};
+    long best_t = -1;
+    const int ntiles = (N + 15) / 16;
+    const int nsteps = K / 512;
+    const int half = dev.smem_per_sm / 2 - 1024;
+    const int W = kHmmaWarps;
+    for (int S = 1; S <= 8; S *= 2) {
+        if (forced_S > 0 && S != forced_S) continue;
+        if (nsteps % S != 0) continue;
+        const int sps = nsteps / S;
+        int cap = dev.sms / S;
+        const int need_min = hmma_layout(M, sps, S, (ntiles + cap - 1) / cap, 2).total;
+        if (need_min > dev.max_smem_optin) continue;
+        if (S > 1) {
+            const int mc = max_clusters(S, need_min <= half ? half : dev.max_smem_optin);
+            if (mc < 1) continue;
+            if (cap > mc) cap = mc;
+        }
+        const int ncl = cap < ntiles ? cap : ntiles;
+        const int max_tiles = (ntiles + ncl - 1) / ncl;
+        for (int wpt = 1; wpt <= W; wpt *= 2) {
+            const int ng = W / wpt;
+            const long t = static_cast<long>((max_tiles + ng - 1) / ng) * ((sps + wpt - 1) / wpt);
+            const int units = static_cast<int>(t);
+            const int want = units < 3 ? (units < 2 ? 2 : units) : 3;
+            const int per_sm = hmma_layout(M, sps, S, max_tiles, want).total <= half ? 2 : 1;
+            if (best_t >= 0 && (t > best_t || (t == best_t && per_sm <= best.per_sm))) continue;
+            const int budget = per_sm == 2 ? half : dev.max_smem_optin;
+            int depth = 2;
+            while (depth < kHmmaMaxDepth && depth < units &&
+                   hmma_layout(M, sps, S, max_tiles, depth + 1).total <= budget)
+                ++depth;
+            const int smem = hmma_layout(M, sps, S, max_tiles, depth).total;
+            if (smem > dev.max_smem_optin) continue;
+            best_t = t;
+            best = HmmaChoice{S, ncl, sps, max_tiles, wpt, depth, smem, per_sm};
+        }
+    }
+    return best;
+}
+
 // Lets `kernel` run with `bytes` of dynamic shared memory on the current
 // device.  The limit persists per function and device, so it is raised only
 // when a launch needs more than every earlier one did (a host-side table
@@ -128,10 +227,14 @@ int max_active_clusters(const void* kernel, int threads, int smem, int S);
 GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
 GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
 GemvPlan plan_gemv_tc(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
+GemvPlan plan_gemv_hmma(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
+// True when kernel 4 serves this shape (1..8 tokens, g == 128, K % 512 == 0).
+inline bool hmma_supports(int M, int K, int g) { return M >= 1 && M <= 8 && g == 128 && K % 512 == 0; }
 
 cudaError_t launch_gemv_simt(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 cudaError_t launch_gemv_tc(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
+cudaError_t launch_gemv_hmma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 
 // One stacked expert bank: wq [E][N][K/8], scale and zero [E][N][K/g], and
 // its bf16 per-slot output [M*topk][N] (used when there is no routed sum).

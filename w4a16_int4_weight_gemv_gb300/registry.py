@@ -40,10 +40,11 @@ def _ffn(fused: bool):
 OPS = {
     # y[M, N] = x[M, K] . dequant(Wq, scale, zero)^T
     "w4a16_dense": {
-        "planned": _dense(0),    # the library's choice per shape (CUDA cores at M = 1, warp MMA above)
+        "planned": _dense(0),    # the library's choice per shape (fp16 warp MMA where it applies)
         "cuda_core": _dense(1),  # subnormal-float CUDA-core kernel, M <= 2
-        "warp_mma": _dense(2),   # mma.sync kernel, M <= 16
+        "warp_mma": _dense(2),   # bf16 mma.sync kernel, M <= 16
         "tcgen05": _dense(3),    # tensor-core (TMEM) kernel, g % 128 == 0
+        "fp16_mma": _dense(4),   # fp16 mma.sync kernel with a producer warp, M <= 8, g == 128
     },
     # per-slot products of the routed experts, or their routed sum
     "w4a16_grouped": {
