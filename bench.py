@@ -198,24 +198,52 @@ def capture(torch, fn, n):
     return g
 
 
+def _graph_events(torch):
+    """Two timing events that, recorded while a graph is captured, become
+    event-record nodes of the graph (None if this torch cannot do that)."""
+    try:
+        return (torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+    except TypeError:
+        return None
+
+
 class WarmGraphs:
-    """Exactly `steps` steps fn(0), fn(1), ... as replays of CUDA graphs: one
-    graph of `chunk` steps (a multiple of the R rotating copies, at most
-    ~2048 launches, or all the steps when there are fewer) replayed
-    steps // chunk times, plus a graph of the remainder.  warm() replays both
-    graphs untimed -- at least `warmup` steps and at least once each -- so the
-    timed replays only repeat graphs that have already run."""
+    """Exactly `steps` steps fn(0), fn(1), ... as replays of CUDA graphs.
+
+    Up to 2048 steps: one graph holding a start event, the steps and an end
+    event, so the measured interval is the steps' own device time from the
+    first launch to the last, without the host's graph-launch latency.  More
+    steps: a graph of `chunk` steps (a multiple of the R rotating copies,
+    ~2048 launches) replayed steps // chunk times plus a graph of the
+    remainder, timed by events around the replays.  warm() replays every
+    graph untimed -- at least `warmup` steps -- so the timed run only repeats
+    graphs that have already run."""
 
     def __init__(self, torch, fn, steps, R):
         self.torch = torch
-        if steps <= R:
-            chunk = steps
+        self.inner = _graph_events(torch) if steps <= 2048 else None
+        if self.inner is not None:
+            self.chunk = steps
+            self.reps, rem = 1, 0
+            ev0, ev1 = self.inner
+
+            def body(i):
+                if i == 0:
+                    ev0.record()
+                fn(i)
+                if i == steps - 1:
+                    ev1.record()
+            self.full = capture(torch, body, steps)
+            self.tail = None
+            self.timing = "event-record nodes inside the graph around the %d launches" % steps
         else:
-            chunk = R * max(1, min(steps // R, 2048 // R))
-        self.chunk = chunk
-        self.reps, rem = divmod(steps, chunk)
-        self.full = capture(torch, fn, chunk)
-        self.tail = capture(torch, fn, rem) if rem else None
+            chunk = steps if steps <= R else R * max(1, min(steps // R, 2048 // R))
+            self.chunk = chunk
+            self.reps, rem = divmod(steps, chunk)
+            self.full = capture(torch, fn, chunk)
+            self.tail = capture(torch, fn, rem) if rem else None
+            self.timing = "events on the stream around %d graph replays" % (self.reps + (rem > 0))
 
     def warm(self, warmup):
         for _ in range(max(1, int(math.ceil(warmup / self.chunk)))):
@@ -230,19 +258,27 @@ class WarmGraphs:
         if self.tail is not None:
             self.tail.replay()
 
+    def timed(self):
+        """Run the timed steps (caller synchronises around); seconds."""
+        if self.inner is not None:
+            self.run()
+            self.torch.cuda.synchronize()
+            return self.inner[0].elapsed_time(self.inner[1]) / 1e3
+        start = self.torch.cuda.Event(enable_timing=True)
+        end = self.torch.cuda.Event(enable_timing=True)
+        start.record()
+        self.run()
+        end.record()
+        self.torch.cuda.synchronize()
+        return start.elapsed_time(end) / 1e3
+
 
 def time_steps(torch, fn, R, steps, warmup):
     """Run at least `warmup` untimed steps, then exactly `steps` timed steps
     (warm graph replays); returns seconds per step."""
     g = WarmGraphs(torch, fn, steps, R)
     g.warm(warmup)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record()
-    g.run()
-    end.record()
-    torch.cuda.synchronize()
-    return start.elapsed_time(end) / 1e3 / steps
+    return g.timed() / steps
 
 
 def gpu_gemv_gbs(torch, w, M, N, K, g, zmode, l2, steps, warmup, out_dtype=None, kernel_id=0,
@@ -573,6 +609,7 @@ def run_gpu(args):
 
     graphs = WarmGraphs(torch, step, args.steps, R)
     chunk = graphs.chunk
+    timing = graphs.timing
     # warm-up: the graphs about to be timed, replayed untimed (>= W >= 3 steps)
     graphs.warm(max(3, args.warmup))
     clocks = ClockSampler(local)
@@ -580,20 +617,15 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.perf_counter()
-    start.record()
-    graphs.run()
-    end.record()
+    elapsed_dev = graphs.timed()
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     bytes_step = algo_bytes(M, N, K, g)
-    elapsed, per_step, value = replica_aggregate(torch, dist, world,
-                                                 start.elapsed_time(end) / 1e3, bytes_step,
+    elapsed, per_step, value = replica_aggregate(torch, dist, world, elapsed_dev, bytes_step,
                                                  args.steps)
     peak, peak_kind = measured_peak()
     achieved = bytes_step / per_step / 1e9
@@ -696,6 +728,7 @@ def run_gpu(args):
                        "launch": "CUDA graph of %d w4a16_gemv launches (weights rotating over %d "
                                  "copies), warmed by an untimed replay, replayed %d time(s)"
                                  % (chunk, R, args.steps // chunk),
+                       "timing": timing,
                        "plan": plan, "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
