@@ -60,6 +60,24 @@ def test_hmma_matches_oracle(w, oracle, M, N, K, out_dtype):
     assert w.w4a16_device_error(clear=True) == 0
 
 
+# shapes whose plan is a 16-warp CTA alone on its SM (long runs), one per
+# instantiated token count; the rest of this file runs 8-warp pairs
+WIDE = [(1, 28672, 4096), (2, 6000, 14336), (3, 8192, 8192), (8, 12000, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", WIDE)
+def test_hmma_wide_ctas_match_oracle(w, oracle, M, N, K):
+    if M == 1:  # the library's own choice for one token: kernel 4, 16 warps
+        plan = w.gemv_plan(M, N, K, 128)
+        assert (plan["kernel_id"], plan["threads"]) == (KID, 512)
+    p = synth.dense_problem(M, N, K, 128, "uniform6to10", seed=7050 + M)
+    y = w.w4a16_gemv(*dense_dev(p), 128, out_dtype=torch.float32, kernel_id=KID)
+    torch.cuda.synchronize()
+    ref = oracle.gemv_parallel(p["x"], p["wq"], p["scale"], p["zero"], 128)
+    check_close(host_f64(y), ref, "kernel 4, 16 warps, M=%d N=%d K=%d" % (M, N, K))
+    assert w.w4a16_device_error(clear=True) == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 64, 4096), (3, 48, 4096), (1, 40, 14336), (8, 33, 8192),
                                    (2, 4096, 4096)])
 @pytest.mark.parametrize("split", [1, 2, 4, 8])
@@ -130,16 +148,18 @@ def test_hmma_zero_activations(w):
     assert torch.count_nonzero(y).item() == 0
 
 
-@pytest.mark.parametrize("M", [1, 4])
-def test_hmma_weights_static_flag(w, oracle, M):
+@pytest.mark.parametrize("N", [4096, 28672])
+def test_hmma_weights_static_flag(w, oracle, N):
     # the flag only moves the weight copies ahead of the grid-dependency wait
-    p = synth.dense_problem(M, 4096, 4096, 128, "uniform6to10", seed=7600)
+    # (the library's own choice, kernel 4 for one token: 8- and 16-warp CTAs)
+    assert w.gemv_plan(1, N, 4096, 128)["kernel_id"] == KID
+    p = synth.dense_problem(1, N, 4096, 128, "uniform6to10", seed=7600)
     args = dense_dev(p)
-    a = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, kernel_id=KID)
-    b = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, kernel_id=KID, weights_static=True)
+    a = w.w4a16_gemv(*args, 128, out_dtype=torch.float32)
+    b = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, weights_static=True)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
-    check_close(host_f64(b), oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 128), "static")
+    check_close(host_f64(b), oracle.gemv_parallel(p["x"], p["wq"], p["scale"], p["zero"], 128), "static")
 
 
 @pytest.mark.parametrize("static", [False, True])

@@ -103,3 +103,106 @@ def test_infeasible_shared_memory_gives_no_plan(planner):
     # a K slice that can never fit one CTA's shared memory: no CTA at all
     p = planner(1024, 64, per_unit=1 << 20)
     assert p["ctas"] == 0
+
+
+# Kernel 4 (fp16 warp-MMA): choose_hmma_plan picks between 8-warp CTAs (two
+# per SM) and 16-warp CTAs (one per SM), each with its cluster K split, WPT
+# and ring depth.  Occupancy is modelled as the device does it: CTAs per SM
+# limited by shared memory (1 KB reserved per CTA) and by the register file
+# (16 warps of 124-register threads).
+HMMA_DRIVER = r'''
+#include <cstdio>
+#include "launch.h"
+using namespace w4a16;
+// args: M N K forced_S
+int main(int argc, char** argv) {
+    if (argc != 5) return 2;
+    const int M = atoi(argv[1]), N = atoi(argv[2]), K = atoi(argv[3]), forced = atoi(argv[4]);
+    DeviceInfo dev{152, 232448, 233472};
+    auto occ = [&](int warps) {
+        return [&dev, warps](int S, int smem) {
+            int per_sm = dev.smem_per_sm / (smem + 1024);
+            const int reg_cap = 16 / warps;
+            if (per_sm > reg_cap) per_sm = reg_cap;
+            return per_sm * dev.sms / S;
+        };
+    };
+    HmmaChoice c = choose_hmma_plan(dev, M, N, K, forced, occ(kHmmaWarpsPaired), occ(kHmmaWarpsWide));
+    const HmmaLayout L = hmma_layout(c.warps > 0 ? c.warps : 8, M, c.steps_per_rank > 0 ? c.steps_per_rank : 1,
+                                     c.S > 0 ? c.S : 1, c.max_tiles, c.depth > 0 ? c.depth : 2);
+    printf("{\"warps\": %d, \"S\": %d, \"nclusters\": %d, \"sps\": %d, \"max_tiles\": %d, \"wpt\": %d, "
+           "\"depth\": %d, \"smem\": %d, \"per_sm\": %d, \"layout_total\": %d}\n",
+           c.warps, c.S, c.nclusters, c.steps_per_rank, c.max_tiles, c.wpt, c.depth, c.smem_bytes,
+           c.per_sm, L.total);
+    return 0;
+}
+'''
+
+
+@pytest.fixture(scope="module")
+def hmma_planner(tmp_path_factory):
+    gxx = shutil.which("g++")
+    if gxx is None or not os.path.exists(os.path.join(CUDA_INC, "cuda_runtime.h")):
+        pytest.skip("g++ or the CUDA headers are missing")
+    d = tmp_path_factory.mktemp("hmma_planner")
+    src, exe = d / "driver.cpp", d / "driver"
+    src.write_text(HMMA_DRIVER)
+    r = subprocess.run([gxx, "-std=c++17", "-O1", "-I", CSRC, "-I", INCLUDE, "-I", CUDA_INC,
+                        str(src), "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+    def run(M, N, K, forced=0):
+        out = subprocess.run([str(exe), str(M), str(N), str(K), str(forced)],
+                             capture_output=True, text=True, check=True).stdout
+        return json.loads(out)
+    return run
+
+
+HMMA_SHAPES = [(1, 4096, 4096), (1, 14336, 4096), (1, 4096, 14336), (1, 163840, 4096),
+               (1, 28672, 4096), (1, 1, 512), (1, 17, 512), (2, 257, 2048), (8, 150, 4096),
+               (8, 14336, 4096), (4, 4096, 14336), (1, 64, 14336), (8, 33, 8192)]
+
+
+@pytest.mark.parametrize("M,N,K", HMMA_SHAPES)
+def test_hmma_plans_are_feasible_and_cover_the_work(hmma_planner, M, N, K):
+    p = hmma_planner(M, N, K)
+    assert p["warps"] in (8, 16) and p["nclusters"] >= 1
+    S, wpt = p["S"], p["wpt"]
+    assert S in (1, 2, 4, 8) and (K // 512) % S == 0 and p["sps"] * S == K // 512
+    assert wpt in (1, 2, 4, 8, 16) and p["warps"] % wpt == 0
+    assert 2 <= p["depth"] <= 6
+    ntiles = (N + 15) // 16
+    assert p["nclusters"] * p["max_tiles"] >= ntiles            # every tile has a cluster
+    assert p["nclusters"] <= ntiles
+    assert p["smem"] == p["layout_total"] <= 232448             # the layout the kernel uses
+    # the residency the plan claims is what the modelled occupancy gives
+    fit = min(233472 // (p["smem"] + 1024), 16 // p["warps"])
+    assert p["per_sm"] <= fit
+    assert p["nclusters"] * S <= 152 * fit
+
+
+def test_hmma_measured_width_choices(hmma_planner):
+    # measured on GB300, one token: 8-warp pairs for the short runs (square,
+    # MLP up and down), 16-warp CTAs for the 28672 x 4096 projection and the
+    # vocabulary head
+    for shape in ((1, 4096, 4096), (1, 14336, 4096), (1, 4096, 14336)):
+        p = hmma_planner(*shape)
+        assert p["warps"] == 8 and p["per_sm"] == 2, (shape, p)
+    for shape in ((1, 28672, 4096), (1, 163840, 4096)):
+        p = hmma_planner(*shape)
+        assert p["warps"] == 16 and p["per_sm"] == 1, (shape, p)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 28672, 4096), (2, 6000, 14336), (3, 8192, 8192),
+                                   (8, 12000, 4096)])
+def test_hmma_wide_parity_shapes_plan_16_warps(hmma_planner, M, N, K):
+    # the GPU parity cases of the 16-warp instantiations rely on these plans
+    assert hmma_planner(M, N, K)["warps"] == 16
+
+
+@pytest.mark.parametrize("forced", [1, 2, 4, 8])
+def test_hmma_forced_cluster_split(hmma_planner, forced):
+    p = hmma_planner(1, 4096, 8192, forced)
+    assert p["S"] == forced
+    # a split that does not divide K / 512 gives no plan
+    assert hmma_planner(1, 4096, 1536, 4)["nclusters"] == 0

@@ -226,7 +226,9 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
     (measurement and tests); k_split forces the K split (for kernel 4, the
     CTAs of a cluster).  weights_static declares that no
     kernel still running on the stream writes wq/scale/zero (resident
-    weights), so their loads may start before that kernel completes.
+    weights), so their loads may start before that kernel completes; it
+    goes with the library's own launch choice only (ValueError with a
+    forced kernel_id or k_split).
 
     With M == 1, x and out may both be page-locked host tensors: the kernel
     reads x and writes y there directly (over NVLink-C2C on a Grace-Blackwell
@@ -258,6 +260,9 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
     _need(scale, "scale", _BF16, (N, K // g))
     _need(zero, "zero", _U8, (N, K // g))
     kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    if weights_static and (kernel_id or k_split):
+        raise ValueError("weights_static applies to the library's own launch choice; "
+                         "it cannot be combined with kernel_id or k_split")
     lib = load_library()
     sh = _stream(stream, device)
     if kernel_id == 0 and k_split == 0 and weights_static:

@@ -35,8 +35,10 @@
 // copies -- the 256 packed bytes of each row at a row pitch of 272 bytes, so
 // that ldmatrix reads the eight rows of a 16-byte chunk from eight bank
 // groups, then the tile's zero points and scales -- one commit group per
-// unit, waited for with cp.async.wait_group, so depth - 1 units are in
-// flight while the warp computes.  (The copy engine is not used: a bulk or
+// unit, waited for with cp.async.wait_group.  The whole ring is filled
+// before the loop and a stage is refilled as soon as it is consumed, so a
+// warp with at most `depth` units has them all in flight at once and a
+// longer one keeps depth - 1 in flight while it computes.  (The copy engine is not used: a bulk or
 // tensor copy costs its issuing warp tens of nanoseconds on sm_103a, and
 // with the weights split over many such copies the issue time outweighs the
 // arithmetic.)  Nothing waits on another thread except at named and
@@ -62,8 +64,6 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kW = kHmmaWarps;
-constexpr int kThreads = 32 * kW;
 constexpr int kSZScales = 64;
 
 struct HmmaKernelArgs {
@@ -143,10 +143,11 @@ __device__ __forceinline__ void cp_async_commit() {
 
 // MP: the token count rounded up to 1, 2, 4 or 8 -- the B fragments are
 // stored for MP tokens (the columns of tokens M..MP-1 are never stored, so
-// their contents do not matter)
-template <int MP>
-__global__ void __launch_bounds__(kThreads, 2) k_gemv_hmma(const HmmaKernelArgs a) {
-    constexpr int W = kW;
+// their contents do not matter); W warps per CTA
+template <int MP, int W>
+__global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
+    k_gemv_hmma(const HmmaKernelArgs a) {
+    constexpr int kThreads = 32 * W;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_hmma(const HmmaKernelArgs 
 
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw + 127u) & ~127u) - raw);
-    const HmmaLayout L = hmma_layout(MP, nsr, S, a.max_tiles, D);
+    const HmmaLayout L = hmma_layout(W, MP, nsr, S, a.max_tiles, D);
     unsigned char* ring = base + L.ring + warp * D * kHmmaStage;
     uint4* bfrag = reinterpret_cast<uint4*>(base + L.bfrag);
     float* csum = reinterpret_cast<float*>(base + L.csum);
@@ -227,19 +228,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_hmma(const HmmaKernelArgs 
         }
         cp_async_commit();  // one group per call, empty past the end
     };
-    // with static weights the first units are requested before the
-    // preceding grid completes
+    // the ring is filled whole before the loop (a warp with few units has
+    // them all in flight at once); with static weights this happens before
+    // the preceding grid completes
     if (a.weights_static)
-        for (int k = 0; k < D - 1; ++k) issue_next();
+        for (int k = 0; k < D; ++k) issue_next();
     grid_dependency_wait();
-    if (!a.weights_static)
-        for (int k = 0; k < D - 1; ++k) issue_next();
 
     {
         // Activations: every (token, round) item of this thread; the loads of
-        // up to four items are issued before any is converted, so the L2
-        // latency is paid once per four.  The 16 pieces of a block are 16
-        // consecutive lanes (block max and sums by shuffles).
+        // up to four items are issued before any is converted, so the latency
+        // is paid once per four -- and the first four are issued before the
+        // weight copies.  The 16 pieces of a block are 16 consecutive lanes
+        // (block max and sums by shuffles).
         const int tid = threadIdx.x;
         constexpr int T = kThreads;
         const int nblk = nsr * 4;       // 128-k blocks of the slice
@@ -247,8 +248,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_hmma(const HmmaKernelArgs 
         const int nrounds = (npieces + T - 1) / T;
         const int items = M * nrounds;
         const uint16_t* xs = a.x + static_cast<size_t>(s0) * 512;
-        for (int it0 = 0; it0 < items; it0 += 4) {
-            uint4 v[4];
+        auto load_items = [&](int it0, uint4 (&v)[4]) {
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int it = it0 + b;
@@ -258,6 +258,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_hmma(const HmmaKernelArgs 
                 if (it < items && p < npieces)
                     v[b] = __ldg(reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * a.K + p * 8));
             }
+        };
+        uint4 v[4];
+        load_items(0, v);
+        if (!a.weights_static)
+            for (int k = 0; k < D; ++k) issue_next();
+        for (int it0 = 0; it0 < items; it0 += 4) {
+            if (it0 > 0) load_items(it0, v);
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int it = it0 + b;
@@ -331,8 +338,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_hmma(const HmmaKernelArgs 
     int c_slot = 0, c_step = part, c_tile = 0, ti = 0;  // c_tile: local tile of the group
 #pragma unroll 1
     for (int k = 0; k < nu; ++k) {
-        issue_next();  // unit k + D - 1 into the stage consumed last iteration
-        cp_async_wait_pending(D - 1);
+        cp_async_wait_pending(D - 1);  // units k + 1 .. k + D - 1 may be in flight
         __syncwarp();  // every lane's copies of unit k have landed
         const int slot = c_slot;
         const int lstep = c_step;
@@ -385,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_hmma(const HmmaKernelArgs 
             acc[3] = fmaf(sfb * fs.y, (d0[3] + d1[3]) - fmaf(zfb, cs.w, cs.y), acc[3]);
         }
         __syncwarp();  // every lane is done with the stage before it is refilled
+        issue_next();  // unit k + D into the stage just consumed
         tacc.x += acc[0];
         tacc.y += acc[1];
         tacc.z += acc[2];
@@ -452,8 +459,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_hmma(const HmmaKernelArgs 
 }
 
 using HmmaKernel = void (*)(HmmaKernelArgs);
-HmmaKernel hmma_kernel(int M) {
-    return M <= 1 ? k_gemv_hmma<1> : M <= 2 ? k_gemv_hmma<2> : M <= 4 ? k_gemv_hmma<4> : k_gemv_hmma<8>;
+template <int W>
+HmmaKernel hmma_kernel_w(int M) {
+    return M <= 1 ? k_gemv_hmma<1, W> : M <= 2 ? k_gemv_hmma<2, W> : M <= 4 ? k_gemv_hmma<4, W>
+                                                                      : k_gemv_hmma<8, W>;
+}
+HmmaKernel hmma_kernel(int M, int warps) {
+    return warps == kHmmaWarpsWide ? hmma_kernel_w<kHmmaWarpsWide>(M) : hmma_kernel_w<kHmmaWarpsPaired>(M);
 }
 // tokens rounded up to the instantiated count
 int hmma_mp(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
@@ -464,15 +476,17 @@ GemvPlan plan_gemv_hmma(const DeviceInfo& dev, int M, int N, int K, int g, int k
     GemvPlan p{};
     p.kernel_id = 4;
     if (!hmma_supports(M, K, g)) return p;
-    const void* kern = reinterpret_cast<const void*>(hmma_kernel(M));
-    const HmmaChoice c = plan_hmma_split(dev, hmma_mp(M), N, K, k_split_req, [kern](int S, int smem) {
-        return max_active_clusters(kern, kThreads, smem, S);
-    });
+    const void* k8 = reinterpret_cast<const void*>(hmma_kernel(M, kHmmaWarpsPaired));
+    const void* k16 = reinterpret_cast<const void*>(hmma_kernel(M, kHmmaWarpsWide));
+    const HmmaChoice c = choose_hmma_plan(
+        dev, hmma_mp(M), N, K, k_split_req,
+        [k8](int S, int smem) { return max_active_clusters(k8, 32 * kHmmaWarpsPaired, smem, S); },
+        [k16](int S, int smem) { return max_active_clusters(k16, 32 * kHmmaWarpsWide, smem, S); });
     if (c.nclusters < 1) return p;
     p.k_split = c.S;
     p.wpt = c.wpt;
     p.units_per_cta = c.steps_per_rank;
-    p.threads = kThreads;
+    p.threads = 32 * c.warps;
     p.ctas = c.nclusters * c.S;
     p.stages = c.depth;
     p.smem_bytes = c.smem_bytes;
@@ -501,7 +515,7 @@ cudaError_t launch_gemv_hmma(const GemvArgs& a, const GemvPlan& p, cudaStream_t 
     k.wpt = p.wpt;
     k.depth = p.stages;
     k.weights_static = a.weights_static;
-    const HmmaKernel kern = hmma_kernel(a.M);
+    const HmmaKernel kern = hmma_kernel(a.M, p.threads / 32);
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), p.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};

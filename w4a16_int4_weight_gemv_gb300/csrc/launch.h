@@ -126,7 +126,11 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
 // dealt round-robin, partials added behind a named barrier), and K may be
 // split over the S CTAs of a cluster (S | K/512).
 // ---------------------------------------------------------------------------
-constexpr int kHmmaWarps = 8;
+// warps per CTA: 8 (two CTAs per SM, so the next launch's CTA can be
+// resident beside this one) or 16 (one CTA per SM, twice the warps to hide
+// the arithmetic's latencies on long runs)
+constexpr int kHmmaWarpsPaired = 8;
+constexpr int kHmmaWarpsWide = 16;
 constexpr int kHmmaRowPitch = 272;                   // 256 bytes of a row + 16 of padding
 constexpr int kHmmaUnitBytes = 16 * kHmmaRowPitch;   // 4352
 constexpr int kHmmaUnitSZ = 192;   // zero points 16 x 4 bytes, then scales 16 x 8 bytes
@@ -137,22 +141,22 @@ struct HmmaLayout {
     int ring, bfrag, csum, red, cpart, total;
 };
 // Byte offsets inside the CTA's shared memory (from a 128-aligned base; the
-// total includes the alignment slack) for M tokens (the count the B fragments
-// are stored for: 1, 2, 4 or 8), `steps` 512-k steps per
-// K slice, S CTAs per cluster, at most max_tiles tiles per cluster, `depth`
-// stages per warp.
-__host__ __device__ inline HmmaLayout hmma_layout(int M, int steps, int S, int max_tiles,
-                                                  int depth) {
+// total includes the alignment slack) for `warps` warps per CTA, M tokens
+// (the count the B fragments are stored for: 1, 2, 4 or 8), `steps` 512-k
+// steps per K slice, S CTAs per cluster, at most max_tiles tiles per
+// cluster, `depth` stages per warp.
+__host__ __device__ inline HmmaLayout hmma_layout(int warps, int M, int steps, int S,
+                                                  int max_tiles, int depth) {
     HmmaLayout L;
     int off = 0;
     L.ring = off;  // [warp][depth] stages
-    off += kHmmaWarps * depth * kHmmaStage;
+    off += warps * depth * kHmmaStage;
     L.bfrag = off;  // activation fragments: [block][piece][token][lane % 4] x 16 bytes
     off += steps * 4 * 4 * M * 4 * 16;
     L.csum = off;  // per block and lane % 4: {c1[2c], c1[2c+1], c2[2c], c2[2c+1]},
     off += steps * 4 * 4 * 32;  // then the block's 2^-shift of tokens 2c, 2c + 1
     L.red = off;  // in-CTA K split: [2][warp][lane] float4 partials
-    off += 2 * kHmmaWarps * 32 * 16;
+    off += 2 * warps * 32 * 16;
     L.cpart = off;  // K split over the cluster: [tile][rank][lane] float4 pushed to the owner
     off += (S > 1) ? max_tiles * S * 32 * 16 : 0;
     L.total = off + 128;
@@ -160,30 +164,31 @@ __host__ __device__ inline HmmaLayout hmma_layout(int M, int steps, int S, int m
 }
 
 struct HmmaChoice {
-    int S, nclusters, steps_per_rank, max_tiles, wpt, depth, smem_bytes, per_sm;
+    int warps, S, nclusters, steps_per_rank, max_tiles, wpt, depth, smem_bytes, per_sm;
 };
-// Launch shape of kernel 4: the K split S over a cluster (a power of two
-// dividing K/512; forced_S > 0 forces it) and WPT warps per tile inside the
-// CTA, minimising the longest warp's units (tiles of its group x K steps of
-// its part), then preferring two CTAs per SM (so the next launch's CTA can
-// be resident beside this one), then the smallest S and WPT; then as many
-// stages per warp as fit that residency.  max_clusters(S, smem) is how many
-// clusters of S CTAs the device holds at once.  nclusters == 0: no plan.
+// Launch shape of kernel 4 with W warps per CTA: the K split S over a
+// cluster (a power of two dividing K/512; forced_S > 0 forces it) and WPT
+// warps per tile inside the CTA, minimising the longest warp's units (tiles
+// of its group x K steps of its part), then preferring two CTAs per SM (so
+// the next launch's CTA can be resident beside this one: a warp with at most
+// 8 units needs only two stages to qualify, a longer one three), then the
+// smallest S and WPT; then as many stages per warp as fit that residency.
+// max_clusters(S, smem) is how many clusters of S CTAs the device holds at
+// once.  nclusters == 0: no plan.
 template <class ClusterFn>
-HmmaChoice plan_hmma_split(const DeviceInfo& dev, int M, int N, int K, int forced_S,
+HmmaChoice plan_hmma_split(const DeviceInfo& dev, int W, int M, int N, int K, int forced_S,
                            ClusterFn max_clusters) {
     HmmaChoice best{};
     long best_t = -1;
     const int ntiles = (N + 15) / 16;
     const int nsteps = K / 512;
     const int half = dev.smem_per_sm / 2 - 1024;
-    const int W = kHmmaWarps;
     for (int S = 1; S <= 8; S *= 2) {
         if (forced_S > 0 && S != forced_S) continue;
         if (nsteps % S != 0) continue;
         const int sps = nsteps / S;
         int cap = dev.sms / S;
-        const int need_min = hmma_layout(M, sps, S, (ntiles + cap - 1) / cap, 2).total;
+        const int need_min = hmma_layout(W, M, sps, S, (ntiles + cap - 1) / cap, 2).total;
         if (need_min > dev.max_smem_optin) continue;
         if (S > 1) {
             const int mc = max_clusters(S, need_min <= half ? half : dev.max_smem_optin);
@@ -195,22 +200,41 @@ HmmaChoice plan_hmma_split(const DeviceInfo& dev, int M, int N, int K, int force
         for (int wpt = 1; wpt <= W; wpt *= 2) {
             const int ng = W / wpt;
             const long t = static_cast<long>((max_tiles + ng - 1) / ng) * ((sps + wpt - 1) / wpt);
+            // short runs (a few units per warp) gain most from the next
+            // launch's CTA being resident early: two stages per warp there;
+            // long runs want three to keep the stream deep
             const int units = static_cast<int>(t);
-            const int want = units < 3 ? (units < 2 ? 2 : units) : 3;
-            const int per_sm = hmma_layout(M, sps, S, max_tiles, want).total <= half ? 2 : 1;
+            const int want = units <= 8 ? 2 : 3;
+            const int per_sm = hmma_layout(W, M, sps, S, max_tiles, want).total <= half ? 2 : 1;
             if (best_t >= 0 && (t > best_t || (t == best_t && per_sm <= best.per_sm))) continue;
             const int budget = per_sm == 2 ? half : dev.max_smem_optin;
             int depth = 2;
             while (depth < kHmmaMaxDepth && depth < units &&
-                   hmma_layout(M, sps, S, max_tiles, depth + 1).total <= budget)
+                   hmma_layout(W, M, sps, S, max_tiles, depth + 1).total <= budget)
                 ++depth;
-            const int smem = hmma_layout(M, sps, S, max_tiles, depth).total;
+            const int smem = hmma_layout(W, M, sps, S, max_tiles, depth).total;
             if (smem > dev.max_smem_optin) continue;
             best_t = t;
-            best = HmmaChoice{S, ncl, sps, max_tiles, wpt, depth, smem, per_sm};
+            best = HmmaChoice{W, S, ncl, sps, max_tiles, wpt, depth, smem, per_sm};
         }
     }
     return best;
+}
+
+// The 8-warp plan where it puts two CTAs on an SM (short runs: the next
+// launch's CTA is resident early); otherwise the 16-warp plan, which has
+// twice the warps of an SM working (the register file holds 16 warps of
+// this kernel, so a 16-warp CTA is alone on its SM).  Measured on GB300 for
+// one token: 8 warps is ahead by 2-5 % on 4096 x 4096 .. 14336 x 4096 and
+// 4096 x 14336, 16 warps by 4-14 % from 28672 x 4096 up to the vocabulary
+// projection.
+template <class ClusterFn8, class ClusterFn16>
+HmmaChoice choose_hmma_plan(const DeviceInfo& dev, int M, int N, int K, int forced_S,
+                            ClusterFn8 max_clusters8, ClusterFn16 max_clusters16) {
+    const HmmaChoice paired = plan_hmma_split(dev, kHmmaWarpsPaired, M, N, K, forced_S, max_clusters8);
+    if (paired.nclusters > 0 && paired.per_sm == 2) return paired;
+    const HmmaChoice wide = plan_hmma_split(dev, kHmmaWarpsWide, M, N, K, forced_S, max_clusters16);
+    return wide.nclusters > 0 ? wide : paired;
 }
 
 // Lets `kernel` run with `bytes` of dynamic shared memory on the current
