@@ -83,6 +83,7 @@ struct HmmaKernelArgs {
     int wpt;             // warps per tile
     int depth;           // stages per warp
     int weights_static;
+    uint32_t* err;       // device error word (W4A16_DEVERR_TIMEOUT)
 };
 
 // exact 2^e for any integer e in [-252, 254], as the product of two normal
@@ -144,6 +145,23 @@ __device__ __forceinline__ void cp_async_commit() {
 // MP: the token count rounded up to 1, 2, 4 or 8 -- the B fragments are
 // stored for MP tokens (the columns of tokens M..MP-1 are never stored, so
 // their contents do not matter); W warps per CTA
+// Part `part` (> 0) of tile group `grp` (wpt parts) hands its partial of
+// the group's ti-th tile to part 0 through buffer ti % 2 of `red` (W warps
+// per CTA): it first waits until part 0 has read that buffer's previous
+// contents (tile ti - 2), then writes and arrives on the buffer's `full`
+// barrier.  False if the wait gave up.
+template <int W>
+__device__ __forceinline__ bool hand_partial(float4* red, uint64_t* gbar, int grp, int wpt, int part,
+                                             int ti, int lane, float4 v) {
+    const int b = ti & 1;
+    uint64_t* full = gbar + (grp * 2 + b) * 2;
+    bool ok = true;
+    if (ti >= 2) ok = mbar_wait_bounded(full + 1, ((ti >> 1) - 1) & 1);
+    red[(b * W + grp * wpt + part) * 32 + lane] = v;
+    mbar_arrive(full);
+    return ok;
+}
+
 template <int MP, int W>
 __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
     k_gemv_hmma(const HmmaKernelArgs a) {
@@ -176,6 +194,13 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
     float* csum = reinterpret_cast<float*>(base + L.csum);
     float4* red = reinterpret_cast<float4*>(base + L.red);
     float4* cpart = reinterpret_cast<float4*>(base + L.cpart);
+    uint64_t* gbar = reinterpret_cast<uint64_t*>(base + L.bars);
+    if (WPT > 1 && threadIdx.x < NG * 2) {
+        // buffer b of group g: `full` completes when the group's other parts
+        // have written their partials, `empty` when part 0 has read them
+        mbar_init(gbar + threadIdx.x * 2, (WPT - 1) * 32);
+        mbar_init(gbar + threadIdx.x * 2 + 1, 32);
+    }
 
     // this warp's units: tiles grp, grp + NG, ... of the CTA, K steps part,
     // part + WPT, ... of the slice
@@ -335,6 +360,7 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
     const float* cs_lane = csum + c * 8;
 
     float4 tacc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool timed_out = false;  // a bounded wait for a partner's partials expired
     int c_slot = 0, c_step = part, c_tile = 0, ti = 0;  // c_tile: local tile of the group
 #pragma unroll 1
     for (int k = 0; k < nu; ++k) {
@@ -363,6 +389,7 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
             uint4 bq[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) bq[j] = bqu[(bb * 4 + j) * MP * 4];
+            // two accumulator chains: codes 0/4 + 1/5 and codes 2/6 + 3/7
             float d0[4], d1[4];
             {
                 const uint32_t ta = wa[0] >> 8, tb = wb[0] >> 8;
@@ -385,28 +412,37 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
             const uint32_t swa = (bb < 2) ? sa.x : sa.y, swb = (bb < 2) ? sb.x : sb.y;
             const float sfa = __uint_as_float((bb & 1) ? (swa & 0xFFFF0000u) : (swa << 16));
             const float sfb = __uint_as_float((bb & 1) ? (swb & 0xFFFF0000u) : (swb << 16));
+            // token 2c in x/z, 2c + 1 in y/w; with one token only the former
             acc[0] = fmaf(sfa * fs.x, (d0[0] + d1[0]) - fmaf(zfa, cs.z, cs.x), acc[0]);
-            acc[1] = fmaf(sfa * fs.y, (d0[1] + d1[1]) - fmaf(zfa, cs.w, cs.y), acc[1]);
             acc[2] = fmaf(sfb * fs.x, (d0[2] + d1[2]) - fmaf(zfb, cs.z, cs.x), acc[2]);
-            acc[3] = fmaf(sfb * fs.y, (d0[3] + d1[3]) - fmaf(zfb, cs.w, cs.y), acc[3]);
+            if (MP > 1) {
+                acc[1] = fmaf(sfa * fs.y, (d0[1] + d1[1]) - fmaf(zfa, cs.w, cs.y), acc[1]);
+                acc[3] = fmaf(sfb * fs.y, (d0[3] + d1[3]) - fmaf(zfb, cs.w, cs.y), acc[3]);
+            }
         }
         __syncwarp();  // every lane is done with the stage before it is refilled
         issue_next();  // unit k + D into the stage just consumed
         tacc.x += acc[0];
-        tacc.y += acc[1];
         tacc.z += acc[2];
-        tacc.w += acc[3];
+        if (MP > 1) {
+            tacc.y += acc[1];
+            tacc.w += acc[3];
+        }
         c_step += WPT;
         if (c_step < nsr) continue;
         c_step = part;
-        // the tile's part is complete: add the parts in order, then store or push
+        // the tile's part is complete: the other parts hand their partials
+        // to part 0 and go on (they wait only to reuse a buffer part 0 has not
+        // read yet); part 0 adds them in part order, then stores or pushes
         const int tile = t0 + grp + c_tile * NG;
         if (WPT > 1) {
-            float4* rb = red + ((ti & 1) * W + grp * WPT) * 32;
-            rb[part * 32 + lane] = tacc;
-            named_barrier_sync(1 + grp, WPT * 32);
-            if (part == 0) {
-                tacc = rb[lane];
+            if (part != 0) {
+                timed_out |= !hand_partial<W>(red, gbar, grp, WPT, part, ti, lane, tacc);
+            } else {
+                const int b = ti & 1;
+                const float4* rb = red + (b * W + grp * WPT) * 32;
+                uint64_t* full = gbar + (grp * 2 + b) * 2;
+                timed_out |= !mbar_wait_bounded(full, (ti >> 1) & 1);
                 for (int q = 1; q < WPT; ++q) {
                     const float4 v = rb[q * 32 + lane];
                     tacc.x += v.x;
@@ -414,6 +450,7 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
                     tacc.z += v.z;
                     tacc.w += v.w;
                 }
+                mbar_arrive(full + 1);
             }
         }
         if (part == 0) {
@@ -429,14 +466,13 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
         ++c_tile;
         ++ti;
     }
-    // a part with no K step still joins its group's per-tile barriers
+    // a part with no K step still hands part 0 a (zero) partial per tile
     if (WPT > 1 && my_steps == 0)
-        for (; ti < my_tiles; ++ti) {
-            float4* rb = red + ((ti & 1) * W + grp * WPT) * 32;
-            rb[part * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-            named_barrier_sync(1 + grp, WPT * 32);
-        }
+        for (; ti < my_tiles; ++ti)
+            timed_out |= !hand_partial<W>(red, gbar, grp, WPT, part, ti, lane,
+                                             make_float4(0.f, 0.f, 0.f, 0.f));
     cp_async_wait_pending(0);
+    if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
 
     // K split over the cluster: every rank pushed its tile sums into the owner
     // (tile % S); after the barrier the owner adds them in rank order
@@ -515,6 +551,7 @@ cudaError_t launch_gemv_hmma(const GemvArgs& a, const GemvPlan& p, cudaStream_t 
     k.wpt = p.wpt;
     k.depth = p.stages;
     k.weights_static = a.weights_static;
+    k.err = a.err;
     const HmmaKernel kern = hmma_kernel(a.M, p.threads / 32);
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), p.smem_bytes);
     if (e != cudaSuccess) return e;

@@ -138,7 +138,7 @@ constexpr int kHmmaStage = kHmmaUnitBytes + kHmmaUnitSZ;
 constexpr int kHmmaMaxDepth = 6;
 
 struct HmmaLayout {
-    int ring, bfrag, csum, red, cpart, total;
+    int ring, bfrag, csum, red, bars, cpart, total;
 };
 // Byte offsets inside the CTA's shared memory (from a 128-aligned base; the
 // total includes the alignment slack) for `warps` warps per CTA, M tokens
@@ -157,6 +157,8 @@ __host__ __device__ inline HmmaLayout hmma_layout(int warps, int M, int steps, i
     off += steps * 4 * 4 * 32;  // then the block's 2^-shift of tokens 2c, 2c + 1
     L.red = off;  // in-CTA K split: [2][warp][lane] float4 partials
     off += 2 * warps * 32 * 16;
+    L.bars = off;  // their mbarriers: [tile group][buffer] {full, empty}
+    off += warps * 2 * 2 * 8;
     L.cpart = off;  // K split over the cluster: [tile][rank][lane] float4 pushed to the owner
     off += (S > 1) ? max_tiles * S * 32 * 16 : 0;
     L.total = off + 128;
