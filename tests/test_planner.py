@@ -193,6 +193,21 @@ def test_hmma_measured_width_choices(hmma_planner):
         assert p["warps"] == 16 and p["per_sm"] == 1, (shape, p)
 
 
+def test_hmma_measured_split_choices(hmma_planner):
+    # the K splits that timed fastest on GB300 for one token: in-CTA parts
+    # rather than clusters where K allows (square 4 parts; the vocabulary head
+    # and 81920 x 4096 two parts, where four or eight cost part 0 more adds
+    # than they save), and a cluster pair with two parts each for the MLP down
+    # projection (4096 x 14336), which keeps two CTAs per SM
+    def split(shape):
+        p = hmma_planner(*shape)
+        return p["S"], p["wpt"]
+    assert split((1, 4096, 4096)) == (1, 4)
+    assert split((1, 163840, 4096)) == (1, 2)
+    assert split((1, 81920, 4096)) == (1, 2)
+    assert split((1, 4096, 14336)) == (2, 2)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 28672, 4096), (2, 6000, 14336), (3, 8192, 8192),
                                    (8, 12000, 4096)])
 def test_hmma_wide_parity_shapes_plan_16_warps(hmma_planner, M, N, K):

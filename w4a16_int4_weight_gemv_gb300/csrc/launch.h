@@ -170,16 +170,18 @@ struct HmmaChoice {
 };
 // Launch shape of kernel 4 with W warps per CTA: the K split S over a
 // cluster (a power of two dividing K/512; forced_S > 0 forces it) and WPT
-// warps per tile inside the CTA, minimising the longest warp's units (tiles
-// of its group x K steps of its part), then preferring two CTAs per SM (so
-// the next launch's CTA can be resident beside this one: a warp with at most
-// 8 units needs only two stages to qualify, a longer one three), then the
-// smallest S and WPT; then as many stages per warp as fit that residency.
+// warps per tile inside the CTA, minimising a cost -- the longest warp's
+// units (tiles of its group x K steps of its part) plus what the splits add
+// -- then preferring two CTAs per SM (so the next launch's CTA can be
+// resident beside this one: a warp with at most 8 units needs only two
+// stages to qualify, a longer one three), then the smallest S and WPT; then
+// as many stages per warp as fit that residency.
 // max_clusters(S, smem) is how many clusters of S CTAs the device holds at
 // once.  nclusters == 0: no plan.
+// pair_only: consider only shapes with two CTAs per SM.
 template <class ClusterFn>
 HmmaChoice plan_hmma_split(const DeviceInfo& dev, int W, int M, int N, int K, int forced_S,
-                           ClusterFn max_clusters) {
+                           bool pair_only, ClusterFn max_clusters) {
     HmmaChoice best{};
     long best_t = -1;
     const int ntiles = (N + 15) / 16;
@@ -201,13 +203,20 @@ HmmaChoice plan_hmma_split(const DeviceInfo& dev, int W, int M, int N, int K, in
         const int max_tiles = (ntiles + ncl - 1) / ncl;
         for (int wpt = 1; wpt <= W; wpt *= 2) {
             const int ng = W / wpt;
-            const long t = static_cast<long>((max_tiles + ng - 1) / ng) * ((sps + wpt - 1) / wpt);
+            const int tpg = (max_tiles + ng - 1) / ng;  // tiles of the busiest group
+            const int units = tpg * ((sps + wpt - 1) / wpt);
+            // cost in eighths of a unit: the busiest warp's units, plus one
+            // eighth per partial part 0 of a split tile adds, plus a quarter
+            // per tile and extra rank of a cluster split (DSMEM push and
+            // cluster barrier) -- fitted to GB300 timings of one token
+            const long t = 8L * units + static_cast<long>(tpg) * (wpt - 1) +
+                           2L * (S - 1) * max_tiles;
             // short runs (a few units per warp) gain most from the next
             // launch's CTA being resident early: two stages per warp there;
             // long runs want three to keep the stream deep
-            const int units = static_cast<int>(t);
             const int want = units <= 8 ? 2 : 3;
             const int per_sm = hmma_layout(W, M, sps, S, max_tiles, want).total <= half ? 2 : 1;
+            if (pair_only && per_sm != 2) continue;
             if (best_t >= 0 && (t > best_t || (t == best_t && per_sm <= best.per_sm))) continue;
             const int budget = per_sm == 2 ? half : dev.max_smem_optin;
             int depth = 2;
@@ -223,20 +232,23 @@ HmmaChoice plan_hmma_split(const DeviceInfo& dev, int W, int M, int N, int K, in
     return best;
 }
 
-// The 8-warp plan where it puts two CTAs on an SM (short runs: the next
-// launch's CTA is resident early); otherwise the 16-warp plan, which has
-// twice the warps of an SM working (the register file holds 16 warps of
-// this kernel, so a 16-warp CTA is alone on its SM).  Measured on GB300 for
+// The best 8-warp plan with two CTAs on an SM, where there is one (short
+// runs: the next launch's CTA is resident early); otherwise the 16-warp
+// plan, which has twice the warps of an SM working (the register file holds
+// 16 warps of this kernel, so a 16-warp CTA is alone on its SM).  Measured on GB300 for
 // one token: 8 warps is ahead by 2-5 % on 4096 x 4096 .. 14336 x 4096 and
 // 4096 x 14336, 16 warps by 4-14 % from 28672 x 4096 up to the vocabulary
 // projection.
 template <class ClusterFn8, class ClusterFn16>
 HmmaChoice choose_hmma_plan(const DeviceInfo& dev, int M, int N, int K, int forced_S,
                             ClusterFn8 max_clusters8, ClusterFn16 max_clusters16) {
-    const HmmaChoice paired = plan_hmma_split(dev, kHmmaWarpsPaired, M, N, K, forced_S, max_clusters8);
-    if (paired.nclusters > 0 && paired.per_sm == 2) return paired;
-    const HmmaChoice wide = plan_hmma_split(dev, kHmmaWarpsWide, M, N, K, forced_S, max_clusters16);
-    return wide.nclusters > 0 ? wide : paired;
+    const HmmaChoice paired =
+        plan_hmma_split(dev, kHmmaWarpsPaired, M, N, K, forced_S, true, max_clusters8);
+    if (paired.nclusters > 0) return paired;
+    const HmmaChoice wide =
+        plan_hmma_split(dev, kHmmaWarpsWide, M, N, K, forced_S, false, max_clusters16);
+    if (wide.nclusters > 0) return wide;
+    return plan_hmma_split(dev, kHmmaWarpsPaired, M, N, K, forced_S, false, max_clusters8);
 }
 
 // Lets `kernel` run with `bytes` of dynamic shared memory on the current
