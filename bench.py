@@ -325,12 +325,14 @@ def moe_chain_time(torch, w, M, steps, warmup, l2, fused=True):
     return t, float(np.mean(byts))
 
 
-def mlp_decode_chain_time(torch, w, M, steps, warmup, l2):
-    """One dense SwiGLU MLP of a decode step as the library chains it: gate
-    and up GEMVs (14336x4096), w4a16_swiglu, down GEMV (4096x14336), every
-    GEMV with programmatic dependent launch and the resident-weights flag,
-    so its first weight copies overlap the preceding kernel's tail.  Weight
-    sets rotate over copies > 2x L2; seconds per chain."""
+def mlp_decode_chain_time(torch, w, M, steps, warmup, l2, fused=True):
+    """One dense SwiGLU MLP of a decode step (hidden 4096, intermediate
+    14336), every GEMV with programmatic dependent launch and the
+    resident-weights flag.  fused: gate and up as one GEMV over the two weight
+    matrices interleaved in 8-row blocks (28672x4096) whose epilogue stores
+    the SwiGLU, then the down GEMV (4096x14336): two launches; otherwise gate
+    GEMV, up GEMV, w4a16_swiglu, down GEMV (four launches).  Weight sets
+    rotate over copies > 2x L2; seconds per chain."""
     from w4a16_int4_weight_gemv_gb300 import synth
     F, H, g = 14336, 4096, 128
     per = 2 * all_bytes(M, F, H, g) + all_bytes(M, H, F, g)
@@ -338,7 +340,11 @@ def mlp_decode_chain_time(torch, w, M, steps, warmup, l2):
     sets = []
     for r in range(R):
         mats = []
-        for n_, k_, sub in ((F, H, 3 * r), (F, H, 3 * r + 1), (H, F, 3 * r + 2)):
+        if fused:
+            shapes = ((2 * F, H, 3 * r), (H, F, 3 * r + 2))
+        else:
+            shapes = ((F, H, 3 * r), (F, H, 3 * r + 1), (H, F, 3 * r + 2))
+        for n_, k_, sub in shapes:
             p = synth.dense_problem(M, n_, k_, g, "uniform6to10", seed=5, sub=sub)
             mats.append(tuple(_dev(p[k], torch) for k in ("wq", "scale", "zero")))
         sets.append(mats)
@@ -348,14 +354,19 @@ def mlp_decode_chain_time(torch, w, M, steps, warmup, l2):
     h = torch.empty_like(go)
     y = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
 
-    def step(i):
+    def step_fused(i):
+        gate_up, down = sets[i % R]
+        w.w4a16_gemv(x, *gate_up, g, out=h, weights_static=True, swiglu_output=True)
+        w.w4a16_gemv(h, *down, g, out=y, weights_static=True)
+
+    def step_unfused(i):
         gate, up, down = sets[i % R]
         w.w4a16_gemv(x, *gate, g, out=go, weights_static=True)
         w.w4a16_gemv(x, *up, g, out=uo, weights_static=True)
         w.w4a16_swiglu(go, uo, out=h)
         w.w4a16_gemv(h, *down, g, out=y, weights_static=True)
 
-    t = time_steps(torch, step, R, steps, warmup)
+    t = time_steps(torch, step_fused if fused else step_unfused, R, steps, warmup)
     del sets
     return t
 
@@ -650,10 +661,14 @@ def run_gpu(args):
             sweep["mlp_chain_M%d_tokens_per_s" % m] = round(m / ((2 * tu + td) * 1e-6), 1)
         for m in (1, 8):
             t = mlp_decode_chain_time(torch, w, m, 200, 20, l2)
+            tu = mlp_decode_chain_time(torch, w, m, 200, 20, l2, fused=False)
             sweep["mlp_decode_chain_M%d" % m] = {
                 "us": round(t * 1e6, 3), "tokens_per_s": round(m / t, 1),
                 "sum_of_separate_gemvs_us": round(2 * sweep["up_M%d" % m]["us"] + sweep["down_M%d" % m]["us"], 3),
-                "note": "gate, up, SwiGLU, down chained in one graph (PDL, resident-weights flag)"}
+                "unfused_chain_us": round(tu * 1e6, 3),
+                "note": "one GEMV over 8-row-interleaved gate|up weights with the SwiGLU in its "
+                        "epilogue, then the down GEMV (two launches, PDL, resident-weights flag); "
+                        "unfused: gate, up, w4a16_swiglu, down"}
         t = gpu_gemv_gbs(torch, w, 1, 163840, 4096, 128, "uniform6to10", l2, 200, 20,
                          out_dtype=torch.float32)
         sweep["vocab_M1"] = {"us": round(t * 1e6, 3),

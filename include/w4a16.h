@@ -73,6 +73,8 @@ typedef enum w4a16_out_dtype {
 /* Flags of w4a16_gemv_ex. */
 #define W4A16_FLAG_WEIGHTS_STATIC 0x1u /* wq, scale and zero are not written by work
                                           still running on the stream (see w4a16_gemv_ex) */
+#define W4A16_FLAG_SWIGLU_OUTPUT 0x2u  /* rows are gate/up pairs of 8-row blocks; y is
+                                          bf16(silu(gate) * up) (see w4a16_gemv_ex) */
 
 /* Bits of the per-device error word (see w4a16_device_error). */
 #define W4A16_DEVERR_EXPERT_ID 0x1u /* an expert id was outside [0, E) */
@@ -136,16 +138,28 @@ W4A16_API w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const u
                         void* stream);
 
 /*
- * w4a16_gemv_ex -- w4a16_gemv with flags.  W4A16_FLAG_WEIGHTS_STATIC lets the
- * kernel start loading wq/scale/zero before the previous kernel on `stream`
- * has completed (x is still read, and y written, only after it completes).
- * Set it only when no kernel that may still be running on the stream writes
- * those three buffers -- the case of resident model weights in a decode loop.
- * It is a permission, not a speed-up in itself: with the default plans (one
- * CTA per SM, so a launch's CTAs become resident only as the previous
- * launch's exit) back-to-back square GEMVs measured 5.3 us with it against
- * 5.1 us without.  Otherwise identical to w4a16_gemv (workspace is not
- * needed).
+ * w4a16_gemv_ex -- w4a16_gemv with flags.
+ *   W4A16_FLAG_WEIGHTS_STATIC lets the kernel start loading wq/scale/zero
+ *   before the previous kernel on `stream` has completed (x is still read,
+ *   and y written, only after it completes).  Set it only when no kernel that
+ *   may still be running on the stream writes those three buffers -- the
+ *   case of resident model weights in a decode loop.  It is a permission:
+ *   what it buys depends on the launch (measured on GB300, back-to-back
+ *   4096 x 4096 GEMVs: 4.51 us per call with it, 4.58 us without).
+ *   W4A16_FLAG_SWIGLU_OUTPUT fuses the SwiGLU of a decode MLP into the
+ *   gate/up projection (README technical-detail section: the kernel
+ *   registry's SwiGLU op; the expert FFN does the same inside
+ *   w4a16_moe_ffn).  The N rows of wq/scale/zero hold the gate and up
+ *   matrices (N/2 rows each) interleaved in blocks of 8: rows 16t..16t+7
+ *   are gate rows 8t..8t+7 and rows 16t+8..16t+15 are up rows 8t..8t+7.
+ *   y is then bf16 [M][N/2], y[m][i] = bf16(silu(gate) * up) with gate and
+ *   up the bf16-rounded products of row i of each matrix, computed in fp32
+ *   exactly as w4a16_swiglu computes it -- so the result equals that of the
+ *   plain GEMV followed by w4a16_swiglu, bit for bit, in one launch.
+ *   Requires N % 16 == 0, out_dtype W4A16_OUT_BF16 and a shape the fp16 or
+ *   bf16 warp-MMA kernel serves (w4a16_gemv_plan kernel id 4 or 2: g a
+ *   multiple of 128); otherwise W4A16_ERR_UNSUPPORTED.
+ * Otherwise identical to w4a16_gemv (workspace is not needed).
  */
 W4A16_API w4a16_status w4a16_gemv_ex(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
                                      const uint8_t* zero, void* y, w4a16_out_dtype out_dtype,

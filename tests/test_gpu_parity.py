@@ -264,14 +264,22 @@ def test_gemv_default_dispatch_is_pinned(w):
     for M in (2, 4, 8, 16):
         assert w.gemv_plan(M, 14336, 4096, 128)["kernel_id"] == 2
     assert w.gemv_plan(1, 4096, 4096, 64)["kernel_id"] == 1
-    p = synth.dense_problem(1, 512, 4096, 128, "const8", seed=49)
-    args = dense_dev(p)
-    plan = w.gemv_plan(1, 512, 4096, 128)
-    a = w.w4a16_gemv(*args, 128, out_dtype=torch.float32)
-    b = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, kernel_id=plan["kernel_id"],
-                     k_split=plan["k_split"])
-    torch.cuda.synchronize()
-    assert torch.equal(a, b)
+    # forcing the planned kernel (its own split) reproduces the default launch;
+    # for the CUDA-core and bf16 warp-MMA kernels so does forcing the reported
+    # split factor (warps per tile x CTAs per cluster)
+    for M, g in ((1, 128), (4, 128), (1, 64)):
+        p = synth.dense_problem(M, 512, 4096, g, "const8", seed=49)
+        args = dense_dev(p)
+        plan = w.gemv_plan(M, 512, 4096, g)
+        a = w.w4a16_gemv(*args, g, out_dtype=torch.float32)
+        b = w.w4a16_gemv(*args, g, out_dtype=torch.float32, kernel_id=plan["kernel_id"])
+        torch.cuda.synchronize()
+        assert torch.equal(a, b), (M, g, plan)
+        if plan["kernel_id"] in (1, 2):
+            c = w.w4a16_gemv(*args, g, out_dtype=torch.float32, kernel_id=plan["kernel_id"],
+                             k_split=plan["k_split"])
+            torch.cuda.synchronize()
+            assert torch.equal(a, c), (M, g, plan)
 
 
 # ---- full-size workloads, every output ------------------------------------

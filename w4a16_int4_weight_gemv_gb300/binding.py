@@ -192,6 +192,7 @@ def gemv_plan(M: int, N: int, K: int, g: int) -> dict:
 
 
 FLAG_WEIGHTS_STATIC = 0x1
+FLAG_SWIGLU_OUTPUT = 0x2
 
 
 def _host_side(x, out) -> bool:
@@ -218,7 +219,7 @@ def _need_pinned(t, name, dtypes, shape=None):
 
 def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
                kernel_id: int = 0, k_split: int = 0, weights_static: bool = False,
-               stream=None) -> torch.Tensor:
+               swiglu_output: bool = False, stream=None) -> torch.Tensor:
     """y[M, N] = x[M, K] . dequant(wq, scale, zero)^T.
 
     kernel_id 0 (default) lets the library choose; 1, 2, 3 or 4 force the
@@ -228,7 +229,10 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
     kernel still running on the stream writes wq/scale/zero (resident
     weights), so their loads may start before that kernel completes; it
     goes with the library's own launch choice only (ValueError with a
-    forced kernel_id or k_split).
+    forced kernel_id or k_split).  swiglu_output: the rows of wq are gate and
+    up rows interleaved in blocks of 8 (interleave_gate_up) and y is the
+    bf16 [M, N/2] SwiGLU of the two products, formed in the kernel's
+    epilogue (same restriction on forcing).
 
     With M == 1, x and out may both be page-locked host tensors: the kernel
     reads x and writes y there directly (over NVLink-C2C on a Grace-Blackwell
@@ -242,8 +246,9 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
         # (one token: the CUDA-core kernel, plain loads and stores)
         _need_pinned(x, "x", _BF16)
         M = x.shape[0]
-        if M != 1 or kernel_id not in (0, 1):
-            raise ValueError("page-locked host x/out: M == 1 and the CUDA-core kernel only")
+        if M != 1 or kernel_id not in (0, 1) or swiglu_output:
+            raise ValueError("page-locked host x/out: M == 1 and the CUDA-core kernel only "
+                             "(no SwiGLU input)")
         if out is None:
             out = torch.empty((M, N), dtype=out_dtype).pin_memory()
         _need_pinned(out, "out", (torch.bfloat16, torch.float32), (M, N))
@@ -251,23 +256,26 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
     else:
         _need(x, "x", _BF16)
         M = x.shape[0]
+        NO = N // 2 if swiglu_output else N
         if out is None:
-            out = torch.empty((M, N), dtype=out_dtype, device=x.device)
-        _need(out, "out", (torch.bfloat16, torch.float32), (M, N))
+            out = torch.empty((M, NO), dtype=torch.bfloat16 if swiglu_output else out_dtype,
+                              device=x.device)
+        _need(out, "out", (torch.bfloat16, torch.float32), (M, NO))
         device = x.get_device()
     if x.dim() != 2 or x.shape[1] != K:
         raise ValueError("x shape %s does not match wq %s" % (tuple(x.shape), tuple(wq.shape)))
     _need(scale, "scale", _BF16, (N, K // g))
     _need(zero, "zero", _U8, (N, K // g))
     kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
-    if weights_static and (kernel_id or k_split):
-        raise ValueError("weights_static applies to the library's own launch choice; "
-                         "it cannot be combined with kernel_id or k_split")
+    flags = (FLAG_WEIGHTS_STATIC if weights_static else 0) | (FLAG_SWIGLU_OUTPUT if swiglu_output else 0)
+    if flags and (kernel_id or k_split):
+        raise ValueError("weights_static and swiglu_output apply to the library's own launch "
+                         "choice; they cannot be combined with kernel_id or k_split")
     lib = load_library()
     sh = _stream(stream, device)
-    if kernel_id == 0 and k_split == 0 and weights_static:
+    if flags:
         rc = lib.w4a16_gemv_ex(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
-                               M, N, K, g, FLAG_WEIGHTS_STATIC, sh)
+                               M, N, K, g, flags, sh)
     elif kernel_id == 0 and k_split == 0:
         rc = lib.w4a16_gemv(_ptr(x), _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
                             M, N, K, g, None, 0, sh)
@@ -315,6 +323,18 @@ def w4a16_moe_gemv(x, expert_ids, wq, scale, zero, g: int, route_w=None, x_per_s
                               _ptr(scale), _ptr(zero), _ptr(out), M, topk, E, N, K, g,
                               ws_ptr, ws_bytes, _stream(stream, x.get_device())), "w4a16_moe_gemv")
     return out
+
+
+def interleave_gate_up(gate, up) -> torch.Tensor:
+    """The row layout W4A16_FLAG_SWIGLU_OUTPUT reads: two [I, ...] tensors
+    (packed weights, scales or zero points of the gate and up matrices, I a
+    multiple of 8) as one [2I, ...] tensor whose 16-row blocks hold 8 gate
+    rows, then the same 8 up rows.  A one-time copy at weight-load time."""
+    if gate.shape != up.shape or gate.dim() < 1 or gate.shape[0] % 8 != 0:
+        raise ValueError("gate and up must have the same shape, rows a multiple of 8")
+    rest = tuple(gate.shape[1:])
+    blocks = torch.stack((gate.reshape((-1, 8) + rest), up.reshape((-1, 8) + rest)), dim=1)
+    return blocks.reshape((2 * gate.shape[0],) + rest).contiguous()
 
 
 def w4a16_swiglu(gate, up, out=None, stream=None) -> torch.Tensor:

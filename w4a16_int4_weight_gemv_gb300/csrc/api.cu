@@ -143,7 +143,8 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
                        const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M, int64_t N,
                        int64_t K, int64_t g, int kernel_id, int k_split, unsigned flags,
                        void* stream) {
-    if (flags & ~static_cast<unsigned>(W4A16_FLAG_WEIGHTS_STATIC)) return W4A16_ERR_UNSUPPORTED;
+    if (flags & ~static_cast<unsigned>(W4A16_FLAG_WEIGHTS_STATIC | W4A16_FLAG_SWIGLU_OUTPUT))
+        return W4A16_ERR_UNSUPPORTED;
     if (!x || !wq || !scale || !zero || !y) return W4A16_ERR_NULL;
     w4a16_status st = check_gemv_shape(M, N, K, g);
     if (st != W4A16_OK) return st;
@@ -154,9 +155,15 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
     DeviceCache* dev = nullptr;
     st = make_plan(M, N, K, g, kernel_id, k_split, &plan, &dev);
     if (st != W4A16_OK) return st;
+    const int swiglu = (flags & W4A16_FLAG_SWIGLU_OUTPUT) ? 1 : 0;
+    // the fused SwiGLU lives in the epilogues of the two warp-MMA kernels,
+    // whose lanes hold rows r and r + 8 of a tile (a gate and its up row)
+    if (swiglu && ((plan.kernel_id != 2 && plan.kernel_id != 4) || N % 16 != 0 ||
+                   out_dtype != W4A16_OUT_BF16))
+        return W4A16_ERR_UNSUPPORTED;
     GemvArgs a{x, wq, scale, zero, y, out_dtype == W4A16_OUT_F32 ? 1 : 0, M,
                static_cast<int>(N), static_cast<int>(K), static_cast<int>(g), dev->err,
-               (flags & W4A16_FLAG_WEIGHTS_STATIC) ? 1 : 0};
+               (flags & W4A16_FLAG_WEIGHTS_STATIC) ? 1 : 0, swiglu};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return from_cuda(plan.kernel_id == 1   ? launch_gemv_simt(a, plan, s)
                      : plan.kernel_id == 2 ? launch_gemv_mma(a, plan, s)

@@ -34,6 +34,11 @@ __device__ __forceinline__ void store_out(void* y, int out_f32, size_t idx, floa
 __device__ __forceinline__ float silu_mul(float gte, float up) {
     return gte / (1.0f + expf(-gte)) * up;
 }
+// SwiGLU of a gate and an up product accumulated in fp32: both rounded to
+// bf16 first (as a GEMV storing them would), then bf16(silu(gate) * up)
+__device__ __forceinline__ uint16_t swiglu_of_sums(float gate, float up) {
+    return f32_to_bf16_rn(silu_mul(bf16_to_f32(f32_to_bf16_rn(gate)), bf16_to_f32(f32_to_bf16_rn(up))));
+}
 // exact power of two 2^e for a normal exponent e in [-126, 127]
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
 

@@ -83,6 +83,7 @@ struct HmmaKernelArgs {
     int wpt;             // warps per tile
     int depth;           // stages per warp
     int weights_static;
+    int swiglu_out;      // rows 16t..+7 gate, 16t+8..+15 up: y = bf16 SwiGLU [M][N/2]
     uint32_t* err;       // device error word (W4A16_DEVERR_TIMEOUT)
 };
 
@@ -111,7 +112,23 @@ __device__ __forceinline__ float zero_point_f32(uint32_t bytes4, int b) {
 
 // Store the C-fragment values of lane l for 16-row tile `tile`: rows
 // 16 tile + l / 4 (x, y) and + 8 (z, w), tokens 2 (l % 4) (x, z) and + 1 (y, w).
+// The SwiGLU form: rows g and g + 8 of the tile are gate and up row
+// 8 tile + g (every tile is whole: N % 16 == 0).  Kept out of line so that
+// its exponentials do not add to the main loop's register pressure.
+__device__ __noinline__ void store_swiglu_fragment(uint16_t* y, int M, int N, int tile, int l,
+                                                   float4 v) {
+    const int g = l >> 2, c = l & 3;
+    const size_t nh = static_cast<size_t>(N >> 1);
+    const size_t hr = static_cast<size_t>(tile) * 8 + g;
+    if (2 * c < M) y[2 * c * nh + hr] = swiglu_of_sums(v.x, v.z);
+    if (2 * c + 1 < M) y[(2 * c + 1) * nh + hr] = swiglu_of_sums(v.y, v.w);
+}
+
 __device__ __forceinline__ void store_fragment(const HmmaKernelArgs& a, int tile, int l, float4 v) {
+    if (a.swiglu_out) {
+        store_swiglu_fragment(static_cast<uint16_t*>(a.y), a.M, a.N, tile, l, v);
+        return;
+    }
     const int g = l >> 2, c = l & 3;
     const int ra = (tile << 4) + g;
     const int rb = ra + 8;
@@ -551,6 +568,7 @@ cudaError_t launch_gemv_hmma(const GemvArgs& a, const GemvPlan& p, cudaStream_t 
     k.wpt = p.wpt;
     k.depth = p.stages;
     k.weights_static = a.weights_static;
+    k.swiglu_out = a.swiglu_out;
     k.err = a.err;
     const HmmaKernel kern = hmma_kernel(a.M, p.threads / 32);
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), p.smem_bytes);

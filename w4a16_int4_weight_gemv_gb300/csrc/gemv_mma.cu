@@ -63,6 +63,7 @@ struct MmaKernelArgs {
     int tiles_per_group;
     int stages;
     int weights_static;
+    int swiglu_out;  // rows 16t..+7 gate, 16t+8..+15 up: y = bf16 SwiGLU [M][N/2]
     uint32_t* err;
 };
 
@@ -243,7 +244,20 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
                     }
             }
         }
-        if (kp == 0) {
+        if (kp == 0 && S == 1 && a.swiglu_out) {
+            // rows r and r + 8 of the tile are gate and up row 8 tile + r
+            const size_t nh = static_cast<size_t>(a.N >> 1);
+            uint16_t* y = static_cast<uint16_t*>(a.y);
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int tok = t * 8 + 2 * c + i;
+                    if (tok < a.M)
+                        y[tok * nh + static_cast<size_t>(c_tile) * 8 + r] =
+                            swiglu_of_sums(acc[t][i], acc[t][i + 2]);
+                }
+        } else if (kp == 0) {
 #pragma unroll
             for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -352,9 +366,18 @@ k_gemv_mma(const MmaKernelArgs a, const __grid_constant__ CUtensorMap wmap) {
             const int gid2 = g2 * ncl + cid;
             const int mt = (ntiles > gid2) ? (ntiles - gid2 + NG - 1) / NG : 0;
             if (t >= mt || (t % S) != rank) continue;
-            float v = 0.f;
+            if (a.swiglu_out && row >= 8) continue;  // the up row goes with its gate row
+            float v = 0.f, u = 0.f;
             for (int q = 0; q < S; ++q) v += part[(((t * S + q) * TG + g2) * 16 + row) * Mpad + tok];
             const int n = (gid2 + t * NG) * 16 + row;
+            if (a.swiglu_out) {
+                for (int q = 0; q < S; ++q)
+                    u += part[(((t * S + q) * TG + g2) * 16 + row + 8) * Mpad + tok];
+                static_cast<uint16_t*>(a.y)[static_cast<size_t>(tok) * (a.N >> 1) +
+                                            static_cast<size_t>(gid2 + t * NG) * 8 + row] =
+                    swiglu_of_sums(v, u);
+                continue;
+            }
             if (n < a.N) store_out(a.y, a.out_f32, static_cast<size_t>(tok) * a.N + n, v);
         }
     }
@@ -426,6 +449,7 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s
     k.tiles_per_group = p.tiles_per_cluster;
     k.stages = p.stages;
     k.weights_static = a.weights_static;
+    k.swiglu_out = a.swiglu_out;
     k.err = a.err;
     CUtensorMap wmap;
     if (!encode_weight_map(&wmap, a.wq, a.N, a.K, kBoxRows)) return cudaErrorInvalidValue;

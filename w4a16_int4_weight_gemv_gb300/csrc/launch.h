@@ -29,6 +29,7 @@ struct GemvArgs {
     int g;
     uint32_t* err;
     int weights_static;  // wq/scale/zero may be read before the preceding grid completes
+    int swiglu_out;      // rows are 8-row gate/up blocks; y is bf16(silu(gate) * up) [M][N/2]
 };
 
 struct GemvPlan {
