@@ -79,6 +79,9 @@ typedef enum w4a16_out_dtype {
 /* Bits of the per-device error word (see w4a16_device_error). */
 #define W4A16_DEVERR_EXPERT_ID 0x1u /* an expert id was outside [0, E) */
 #define W4A16_DEVERR_TIMEOUT 0x2u   /* a bounded wait for staged data expired */
+#define W4A16_DEVERR_RANGE 0x4u     /* an activation outside the CUDA-core kernel's
+                                       input range: |x| >= 2^43 or not finite
+                                       (see w4a16_gemv) */
 
 /* Version of this interface; bumped on any incompatible change. */
 W4A16_API int w4a16_abi_version(void);
@@ -97,7 +100,11 @@ W4A16_API const char* w4a16_status_string(w4a16_status status);
 W4A16_API w4a16_status int4_pack(const uint8_t* codes, uint32_t* wq, int64_t N, int64_t K, void* stream);
 
 /*
- * int4_dequant -- expand packed weights to W[n][k] = (code - zero) * scale.
+ * int4_dequant -- expand packed weights to W[n][k] = (code - zero) * scale,
+ * the group-quantised weights of the W4A16 kernels (README technical-detail
+ * section; the problem statement accompanying it writes the product as
+ * x . dequant(Wq, scale, zero) with one scale and zero point per g
+ * consecutive k of a row).
  *   w  [N][K] output, bf16 (the exact value rounded to nearest-even) or fp32
  *      (exact: |code - zero| <= 15 times an 8-bit significand fits in 24 bits).
  * Requires K % 32 == 0, g % 32 == 0, K % g == 0.
@@ -120,17 +127,30 @@ W4A16_API size_t w4a16_gemv_workspace_bytes(int M, int64_t N, int64_t K, int64_t
  * kernel).  Products are formed exactly and accumulated in fp32; y is stored
  * as bf16 (round to nearest-even) or fp32 per out_dtype.
  *   workspace/workspace_bytes: may be NULL/0 (none is needed; see above).
- * Kernel choice (fixed by M, N, K, g; see w4a16_gemv_plan): M == 1 runs the
- * CUDA-core kernel, 2 <= M <= 16 the warp-MMA kernel, which needs
- * g % 128 == 0 (M == 2 with finer groups runs the CUDA-core kernel; M > 2 with
- * finer groups is W4A16_ERR_UNSUPPORTED).
+ * Kernel choice (fixed by M, N, K, g; see w4a16_gemv_plan):
+ *   - M == 1, g == 128, K % 512 == 0: the fp16 warp-MMA kernel (id 4), which
+ *     takes any finite bf16 x (each 128-k block of x is scaled by a power of
+ *     two into fp16, exactly where the block's values lie within 2^24 of
+ *     its largest);
+ *   - otherwise, g % 128 == 0: the bf16 warp-MMA kernel (id 2), any M;
+ *   - otherwise (groups finer than 128 k), M <= 2: the CUDA-core kernel
+ *     (id 1); M > 2 is W4A16_ERR_UNSUPPORTED.
+ * Input range of the CUDA-core kernel (a precondition the call checks): it
+ * needs |x| < 2^43 -- a larger or non-finite activation sets
+ * W4A16_DEVERR_RANGE in the device error word (w4a16_device_error), and the
+ * outputs are then not to be used (an activation at a k that is a multiple
+ * of 8 overflows to infinity).  It forms products |code * x| >= 2^-62 exactly;
+ * smaller ones round to fp32's subnormal grid, so activations below about
+ * 2^-60 carry an absolute output error of up to (K + K/32) * 2^-86 *
+ * max|scale| * max|code - zero|.  The two warp-MMA kernels have neither
+ * limit beyond fp32's own range.
  * The kernel is launched with programmatic dependent launch: it may begin
  * while the previous kernel on `stream` drains, but reads and writes no
  * global memory until that kernel has completed, so stream order is kept.
- * Pointers are device-accessible addresses.  With M == 1 (the CUDA-core
- * kernel, plain loads of x and stores of y), x and y may be page-locked
- * host memory mapped into the device's address space: the kernel then reads
- * and writes them in place, with no copies around the call.
+ * Pointers are device-accessible addresses.  With M == 1, x and y may be
+ * page-locked host memory mapped into the device's address space (every
+ * kernel reads x and writes y with plain loads and stores): the kernel then
+ * reads and writes them in place, with no copies around the call.
  */
 W4A16_API w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,
                         const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M,
@@ -168,10 +188,10 @@ W4A16_API w4a16_status w4a16_gemv_ex(const uint16_t* x, const uint32_t* wq, cons
 
 /*
  * w4a16_gemv_plan -- describe the launch w4a16_gemv would make for a shape,
- * without launching: kernel id (1 = CUDA-core M=1 kernel, 2 = warp-MMA
- * kernel), CTAs, threads per CTA, K-split factor (how many warps share one
- * row tile, counting the CTAs of a thread-block cluster) and dynamic shared
- * memory bytes.  Any output pointer may be NULL.  Needs the current device's
+ * without launching: kernel id (1 = CUDA-core kernel, 2 = bf16 warp-MMA
+ * kernel, 4 = fp16 warp-MMA kernel), CTAs, threads per CTA, K-split factor
+ * (how many warps share one row tile, counting the CTAs of a thread-block
+ * cluster) and dynamic shared memory bytes.  Any output pointer may be NULL.  Needs the current device's
  * properties (W4A16_ERR_CUDA without a device).
  */
 W4A16_API w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, int* kernel_id, int* ctas,
@@ -179,11 +199,12 @@ W4A16_API w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, i
 
 /*
  * w4a16_gemv_variant -- w4a16_gemv with the kernel forced (for measurement):
- * kernel_id 1 (CUDA-core, M <= 2), 2 (warp-MMA, any M, g % 128 == 0) or 3
- * (tensor-core tcgen05, any M, g % 128 == 0); k_split 0 = automatic, else
- * the K-split factor, a power of two: for kernels 1 and 2, 1..32 (warps of a
- * CTA first, then up to 8 CTAs of a cluster); for kernel 3, 1..8 CTAs of a
- * cluster.  A split the shape cannot use (a CTA's activation slice too large
+ * kernel_id 1 (CUDA-core, M <= 2), 2 (bf16 warp-MMA, any M, g % 128 == 0),
+ * 3 (tensor-core tcgen05, any M, g % 128 == 0) or 4 (fp16 warp-MMA,
+ * M <= 8, g == 128, K % 512 == 0); k_split 0 = automatic, else the K-split
+ * factor, a power of two: for kernels 1 and 2, 1..32 (warps of a CTA first,
+ * then up to 8 CTAs of a cluster); for kernels 3 and 4, 1..8 CTAs of a
+ * cluster (kernel 4 then chooses its warps per tile itself).  A split the shape cannot use (a CTA's activation slice too large
  * for shared memory, or a CTA left without K range) is
  * W4A16_ERR_UNSUPPORTED.  Same contract as w4a16_gemv.
  */
@@ -225,18 +246,19 @@ W4A16_API w4a16_status w4a16_moe_gemv(const uint16_t* x, int x_per_slot, const i
 
 /*
  * w4a16_moe_gemv_fixed_scratch -- w4a16_moe_gemv for callers that cannot
- * allocate device memory or lend a workspace: code that runs while a CUDA
- * graph is being captured, engines whose device memory is split into fixed
- * pools, plug-ins whose host runtime owns the allocator.  (The README has no
- * counterpart; this is an integration convenience of this library.)
- * Same arguments and results as w4a16_moe_gemv, minus the workspace: the
- * fp32 partials of the routed sum go to a buffer of
+ * allocate device memory or lend a workspace: engines whose device memory is
+ * split into fixed pools, plug-ins whose host runtime owns the allocator.
+ * (The README has no counterpart; this is an integration convenience of
+ * this library.)  Same arguments and results as w4a16_moe_gemv, minus the
+ * workspace: the fp32 partials of the routed sum go to a buffer of
  * W4A16_FIXED_SCRATCH_BYTES compiled into the library, one per device, held
  * until the process exits.  Nothing is allocated by the call.
+ *   - Only calls with route_w use the buffer; calls without it need none.
  *   - Requests needing more than W4A16_FIXED_SCRATCH_BYTES
  *     (M * topk * N * 4 bytes with route_w) return W4A16_ERR_WORKSPACE.
- *   - The first call on a device looks the buffer up (cudaGetSymbolAddress);
- *     make that first call before any stream capture.
+ *   - The first routed call on a device looks the buffer up
+ *     (cudaGetSymbolAddress) and caches its address for the life of the
+ *     process: do not use the call after cudaDeviceReset.
  *   - All calls on a device share the buffer: calls whose kernels can overlap
  *     on the GPU race on it; calls ordered on one stream are safe.  Nothing
  *     left in it by an earlier call is read.

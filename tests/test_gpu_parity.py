@@ -254,16 +254,72 @@ def test_gemv_large_activation_range(w, oracle):
     check_close(host_f64(y), ref, "wide range")
 
 
+def _range_problem(seed, lo, hi, M=1, N=64, K=1024, g=64):
+    # one token with 64-wide groups: the CUDA-core kernel; |x| = 2^e, e
+    # uniform in [lo, hi], random signs
+    p = synth.dense_problem(M, N, K, g, "uniform6to10", seed=seed)
+    r = synth.rng(seed, "misc")
+    mag = np.ldexp(1.0, r.integers(lo, hi + 1, size=(M, K))) * r.choice([-1.0, 1.0], size=(M, K))
+    p["x"] = synth.f32_to_bf16_bits(mag.astype(np.float32))
+    return p
+
+
+def test_cuda_core_kernel_input_range_edges(w, oracle):
+    # the CUDA-core kernel (groups finer than 128) stages x * 2^(85 - p): it
+    # is exact up to |x| < 2^43 and flags anything larger.  At the edge:
+    # magnitudes up to the largest bf16 below 2^43, no flag, within tolerance
+    assert w.gemv_plan(1, 64, 1024, 64)["kernel_id"] == 1
+    w.w4a16_device_error(clear=True)
+    p = _range_problem(51, 20, 42)
+    p["x"][0, :4] = [0x54FF, 0xD4FF, 0x54FF, 0xD4FF]  # +-(2^43 - 2^35)
+    y = w.w4a16_gemv(*dense_dev(p), 64, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert w.w4a16_device_error(clear=True) == 0
+    check_close(host_f64(y), oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 64), "x < 2^43")
+    # beyond it: one 2^43 flags W4A16_DEVERR_RANGE; at a k that is a
+    # multiple of 8 (the lowest nibble, staged times 2^85) it overflows
+    p["x"][0, 96] = 0x5500
+    y = w.w4a16_gemv(*dense_dev(p), 64, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert w.w4a16_device_error(clear=True) & w.DEVERR_RANGE
+    assert not np.all(np.isfinite(host_f64(y)))
+
+
+def test_cuda_core_kernel_small_activations(w, oracle):
+    # products |code * x| >= 2^-62 are exact: activations down to 2^-58
+    # meet the tolerance
+    p = _range_problem(52, -58, -40)
+    y = w.w4a16_gemv(*dense_dev(p), 64, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    check_close(host_f64(y), oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 64), "x >= 2^-58")
+    # below that, products and chunk sums round to fp32's subnormal grid
+    # (2^-149, restored by 2^64): each output is off by at most
+    # (K + K / 32) * 2^-150 * 2^64 * max scale * max |code - zero| -- here
+    # that bound, not the relative tolerance, holds
+    p = _range_problem(53, -100, -90)
+    y = host_f64(w.w4a16_gemv(*dense_dev(p), 64, out_dtype=torch.float32))
+    torch.cuda.synchronize()
+    assert w.w4a16_device_error(clear=True) == 0
+    ref = oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 64)
+    smax = synth.bf16_bits_to_f32(p["scale"]).max()
+    bound = (1024 + 1024 / 32) * 2.0 ** -86 * smax * 16
+    assert np.abs(y - ref).max() <= bound, (np.abs(y - ref).max(), bound)
+
+
 def test_gemv_default_dispatch_is_pinned(w):
     # the dispatch the benchmark times is the library default; pin it: the
     # fp16 warp-MMA kernel for one token on the square, wide-MLP and
-    # vocabulary shapes, the bf16 warp-MMA kernel for 2..16 tokens, the
-    # CUDA-core kernel for one token with groups of 64
+    # vocabulary shapes, the bf16 warp-MMA kernel for 2..16 tokens and for
+    # one token where kernel 4 does not apply (groups of 256, K % 512 != 0),
+    # the CUDA-core kernel for one or two tokens with groups of 64
     for N, K in ((4096, 4096), (14336, 4096), (4096, 14336), (163840, 4096)):
         assert w.gemv_plan(1, N, K, 128)["kernel_id"] == 4
     for M in (2, 4, 8, 16):
         assert w.gemv_plan(M, 14336, 4096, 128)["kernel_id"] == 2
+    assert w.gemv_plan(1, 4096, 4096, 256)["kernel_id"] == 2
+    assert w.gemv_plan(1, 4096, 2304, 128)["kernel_id"] == 2
     assert w.gemv_plan(1, 4096, 4096, 64)["kernel_id"] == 1
+    assert w.gemv_plan(2, 4096, 4096, 64)["kernel_id"] == 1
     # forcing the planned kernel (its own split) reproduces the default launch;
     # for the CUDA-core and bf16 warp-MMA kernels so does forcing the reported
     # split factor (warps per tile x CTAs per cluster)

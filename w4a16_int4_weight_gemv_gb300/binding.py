@@ -32,6 +32,7 @@ class Status(enum.IntEnum):
 
 
 DEVERR_EXPERT_ID = 0x1
+DEVERR_RANGE = 0x4
 DEVERR_TIMEOUT = 0x2
 OUT_BF16 = 0
 OUT_F32 = 1

@@ -81,15 +81,15 @@ w4a16_status check_gemv_shape(int M, int64_t N, int64_t K, int64_t g) {
 w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
                        GemvPlan* plan, DeviceCache** dev) {
     // default: the fp16 warp-MMA kernel for one token where it applies
-    // (g == 128, K % 512 == 0) and has a plan; otherwise the CUDA-core kernel
-    // for one token, and for two when the groups are finer than 128 k; the
-    // bf16 warp-MMA kernel for the rest
+    // (g == 128, K % 512 == 0) and has a plan; otherwise the bf16 warp-MMA
+    // kernel where the groups are multiples of 128 k; the CUDA-core kernel
+    // for one or two tokens with finer groups
     const int requested = kernel_id;
     const bool automatic = kernel_id == 0;
     if (automatic)
         kernel_id = (M == 1 && hmma_supports(M, static_cast<int>(K), static_cast<int>(g))) ? 4
-                    : (M == 1 || (M == 2 && g % 128 != 0))                                 ? 1
-                                                                                           : 2;
+                    : (g % 128 == 0)                                                       ? 2
+                                                                                           : 1;
     if (kernel_id == 1 && M > 2) return W4A16_ERR_UNSUPPORTED;
     if ((kernel_id == 2 || kernel_id == 3) && g % 128 != 0) return W4A16_ERR_UNSUPPORTED;
     if (kernel_id == 4 && !hmma_supports(M, static_cast<int>(K), static_cast<int>(g)))
@@ -127,9 +127,8 @@ w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, in
                                : plan_gemv_hmma((*dev)->info, M, n, k, gg, k_split);
     if (automatic && kernel_id == 4 && plan->ctas < 1) {
         // no fp16-MMA plan for this shape (activations too large for shared memory)
-        kernel_id = (M == 1) ? 1 : 2;
-        *plan = (kernel_id == 1) ? plan_gemv_simt((*dev)->info, M, n, k, gg, k_split)
-                                 : plan_gemv_mma((*dev)->info, M, n, k, gg, k_split);
+        kernel_id = 2;
+        *plan = plan_gemv_mma((*dev)->info, M, n, k, gg, k_split);
     }
     if (plan->ctas < 1 || plan->smem_bytes > (*dev)->info.max_smem_optin)
         return W4A16_ERR_UNSUPPORTED;

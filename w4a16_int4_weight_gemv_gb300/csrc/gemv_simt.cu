@@ -25,7 +25,8 @@
 // folded into the staged activations and the 2^64 is restored on the output.
 // The FMAs keep subnormal operands (the library is built without
 // flush-to-zero); the exact product of a bf16 x and a 4-bit code stays normal
-// unless |code * x| < 2^-62.  Inputs need |x| < 2^40 so x * 2^85 stays finite.
+// unless |code * x| < 2^-62.  Inputs need |x| < 2^43 so x * 2^85 stays finite;
+// a larger (or non-finite) activation sets W4A16_DEVERR_RANGE.
 //
 // Work split.  One persistent CTA of 16 warps per SM.  Warps own tiles of TR
 // rows (4, or 8 when rows are plentiful); a step of a warp is one span of its
@@ -267,6 +268,7 @@ k_gemv_simt(const SimtKernelArgs a) {
         return v;
     };
     // all lanes of the warp take part (chunk sums are 4-lane shuffles)
+    bool out_of_range = false;  // some |x| >= 2^43: x' would overflow
     auto store_piece = [&](int m, int i, const uint4 v) {
         const int k0 = i << 3;   // local k
         const int cl = k0 >> 5;  // local chunk
@@ -276,6 +278,8 @@ k_gemv_simt(const SimtKernelArgs a) {
         float sum = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
+            // bf16 magnitude bits >= those of 2^43 (biased exponent 170)
+            out_of_range |= (wv[e] & 0x7FFFu) >= 0x5500u || (wv[e] & 0x7FFF0000u) >= 0x55000000u;
             const float lo = bf16_to_f32(wv[e] & 0xFFFFu);
             const float hi = bf16_to_f32(wv[e] >> 16);
             sum += lo + hi;
@@ -318,7 +322,8 @@ k_gemv_simt(const SimtKernelArgs a) {
     for (int m = 0; m < MT; ++m)
         for (int b = kXPre * blockDim.x; b < npieces; b += blockDim.x)
             store_piece(m, b + threadIdx.x, load_piece(m, b + threadIdx.x));
-    __syncthreads();
+    if (__syncthreads_or(out_of_range) && threadIdx.x == 0)
+        raise_device_error(a.err, W4A16_DEVERR_RANGE);
     while (w_issued < NS && w_issued < nss) issue();
     if (S > 1) cluster_wait();  // every peer CTA has started
 
