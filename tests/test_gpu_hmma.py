@@ -62,7 +62,7 @@ def test_hmma_matches_oracle(w, oracle, M, N, K, out_dtype):
 
 # shapes whose plan is a 16-warp CTA alone on its SM (long runs), one per
 # instantiated token count; the rest of this file runs 8-warp pairs
-WIDE = [(1, 28672, 4096), (2, 6000, 14336), (3, 8192, 8192), (8, 12000, 4096)]
+WIDE = [(1, 28672, 4096), (2, 6000, 14336), (3, 28672, 4096), (8, 12000, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", WIDE)

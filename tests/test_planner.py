@@ -208,7 +208,7 @@ def test_hmma_measured_split_choices(hmma_planner):
     assert split((1, 4096, 14336)) == (2, 2)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 28672, 4096), (2, 6000, 14336), (3, 8192, 8192),
+@pytest.mark.parametrize("M,N,K", [(1, 28672, 4096), (2, 6000, 14336), (3, 28672, 4096),
                                    (8, 12000, 4096)])
 def test_hmma_wide_parity_shapes_plan_16_warps(hmma_planner, M, N, K):
     # the GPU parity cases of the 16-warp instantiations rely on these plans

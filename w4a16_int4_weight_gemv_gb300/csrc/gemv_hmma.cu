@@ -32,13 +32,16 @@
 //
 // Memory path.  A unit is one 16-row tile x 512 k.  Every warp streams its
 // own units through its own ring of `depth` stages with 16-byte cp.async
-// copies -- the 256 packed bytes of each row at a row pitch of 272 bytes, so
-// that ldmatrix reads the eight rows of a 16-byte chunk from eight bank
-// groups, then the tile's zero points and scales -- one commit group per
-// unit, waited for with cp.async.wait_group.  The whole ring is filled
-// before the loop and a stage is refilled as soon as it is consumed, so a
-// warp with at most `depth` units has them all in flight at once and a
-// longer one keeps depth - 1 in flight while it computes.  (The copy engine is not used: a bulk or
+// copies -- the 256 packed bytes of each row as one aligned 256-byte block,
+// its 16-byte chunks XOR-swizzled by the row so that ldmatrix reads the
+// eight rows of a chunk from eight bank groups (measured 3-8 % faster than
+// a padded 272-byte pitch, whose rows split every copied line across two
+// lines of shared memory), then the tile's zero points and scales -- one
+// commit group per unit, waited for with cp.async.wait_group.  The whole
+// ring is filled before the loop and a stage is refilled as soon as it is
+// consumed, so a warp with at most `depth` units has them all in flight at
+// once and a longer one keeps depth - 1 in flight while it computes.  (The
+// copy engine is not used: a bulk or
 // tensor copy costs its issuing warp tens of nanoseconds on sm_103a, and
 // with the weights split over many such copies the issue time outweighs the
 // arithmetic.)  Nothing waits on another thread except at named and
@@ -229,13 +232,25 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
     if (S > 1) cluster_arrive_relaxed();
 
     // Producer side of this warp's ring: unit (i_tile, i_step) into stage
-    // i_slot as one commit group.  Lane l copies the 16-byte pieces
-    // (row 2 i + l / 16, column l % 16), i = 0..7, so each copy instruction
+    // i_slot as one commit group.  Lane l copies the 16-byte chunks
+    // (row 2 i + l / 16, chunk l % 16), i = 0..7, so each copy instruction
     // reads two whole 256-byte row pieces; lanes 0..15 then copy the 4 zero
-    // points of row l, lanes 16..31 its 4 scales.
+    // points of row l, lanes 16..31 its 4 scales.  In the stage, chunk c of
+    // row r sits at chunk c ^ (r & 7) of the row's 256 bytes: every row is
+    // one aligned 256-byte block (a copy instruction fills two of them, with
+    // no line of the copy split across two lines of shared memory), and the
+    // eight rows an ldmatrix phase reads for one chunk fall in eight bank
+    // groups.  For row 2 i + h the swizzle is (c ^ h) ^ 2 (i & 3), so four
+    // lane offsets serve the eight copies.
     const size_t row_bytes = static_cast<size_t>(a.K) >> 1;
     const size_t src_lane = static_cast<size_t>(lane >> 4) * row_bytes + (lane & 15) * 16;
-    const int dst_lane = (lane >> 4) * kHmmaRowPitch + (lane & 15) * 16;
+    const int sw_h = lane >> 4, sw_c = ((lane & 15) ^ sw_h) << 4;
+    const int dl0 = sw_h * kHmmaRowPitch + sw_c, dl1 = sw_h * kHmmaRowPitch + (sw_c ^ 32);
+    const int dl2 = sw_h * kHmmaRowPitch + (sw_c ^ 64), dl3 = sw_h * kHmmaRowPitch + (sw_c ^ 96);
+    auto dst_off = [&](int i) {  // copy i (compile-time): row 2 i + h
+        return ((i & 3) == 0 ? dl0 : (i & 3) == 1 ? dl1 : (i & 3) == 2 ? dl2 : dl3) +
+               i * 2 * kHmmaRowPitch;
+    };
     const int rr = lane & 15;
     int i_u = 0, i_slot = 0, i_tile = t0 + grp, i_step = part;
     auto issue_next = [&]() {
@@ -245,15 +260,13 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
             const int step = s0 + i_step;
             unsigned char* stage = ring + i_slot * kHmmaStage;
             const unsigned char* src = a.wq + static_cast<size_t>(row0) * row_bytes + step * 256 + src_lane;
-            unsigned char* dst = stage + dst_lane;
             if (rows == 16) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) cp_async_16(dst + i * 2 * kHmmaRowPitch, src + i * 2 * row_bytes);
+                for (int i = 0; i < 8; ++i) cp_async_16(stage + dst_off(i), src + i * 2 * row_bytes);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    if (2 * i + (lane >> 4) < rows)
-                        cp_async_16(dst + i * 2 * kHmmaRowPitch, src + i * 2 * row_bytes);
+                    if (2 * i + (lane >> 4) < rows) cp_async_16(stage + dst_off(i), src + i * 2 * row_bytes);
             }
             if (rr < rows) {
                 const size_t gi = static_cast<size_t>(row0 + rr) * G + step * 4;
@@ -366,11 +379,19 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
 
     const int g = lane >> 2, c = lane & 3;
     // ldmatrix addressing: lane l supplies row (l & 7) + 8 ((l >> 3) & 1) of
-    // chunk (l >> 4) (+ 2 for the second load) of the block's four chunks; at
-    // the 272-byte pitch the eight rows of a matrix fall in eight bank groups
+    // chunk 4 bb + t + (l >> 4) (t = 0, then 2 for the second load); with
+    // s = l & 7 (the row's swizzle), bits 0..2 of that chunk index flip with
+    // those of s and bit 3 (bb >> 1) is left alone, so four lane offsets
+    // lv[t / 2 + 2 (bb & 1)] plus 128 (bb >> 1) cover the eight loads
     const int lrow = (lane & 7) + (((lane >> 3) & 1) << 3);
     const int lch = lane >> 4;
-    const uint32_t ring_addr = smem_addr(ring) + static_cast<uint32_t>(lrow * kHmmaRowPitch + lch * 16);
+    const int sw_s = lane & 7;
+    const uint32_t ring_addr = smem_addr(ring) + static_cast<uint32_t>(lrow * kHmmaRowPitch);
+    const uint32_t lve = (lch ^ (sw_s & 1)) << 4;
+    const uint32_t lv0 = lve + ((0 ^ (sw_s & 2)) << 4) + ((0 ^ (sw_s & 4)) << 4);
+    const uint32_t lv1 = lve + ((2 ^ (sw_s & 2)) << 4) + ((0 ^ (sw_s & 4)) << 4);
+    const uint32_t lv2 = lve + ((0 ^ (sw_s & 2)) << 4) + ((4 ^ (sw_s & 4)) << 4);
+    const uint32_t lv3 = lve + ((2 ^ (sw_s & 2)) << 4) + ((4 ^ (sw_s & 4)) << 4);
     // B fragments of token g (padding-token lanes read token 0's: their
     // output columns are never stored) and the block sums of tokens 2c, 2c + 1
     const uint4* bq_lane = bfrag + (g < M ? g : 0) * 4 + c;
@@ -397,10 +418,10 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
-            const uint32_t hb = wst + static_cast<uint32_t>(bb * 64);
+            const uint32_t hb = wst + static_cast<uint32_t>((bb >> 1) * 128);
             uint32_t q0[4], q1[4];
-            ldmatrix_x4(q0, hb);
-            ldmatrix_x4(q1, hb + 32u);
+            ldmatrix_x4(q0, hb + ((bb & 1) ? lv2 : lv0));
+            ldmatrix_x4(q1, hb + ((bb & 1) ? lv3 : lv1));
             const uint32_t wa[4] = {q0[0], q0[2], q1[0], q1[2]};  // row g, chunks 0..3
             const uint32_t wb[4] = {q0[1], q0[3], q1[1], q1[3]};  // row g + 8
             uint4 bq[4];

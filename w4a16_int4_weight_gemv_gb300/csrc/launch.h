@@ -120,20 +120,20 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
 
 // ---------------------------------------------------------------------------
 // fp16 warp-MMA GEMV (kernel 4): 1..8 tokens, g == 128, K % 512 == 0.
-// A unit is one 16-row tile x 512 k: 16 rows of 256 packed bytes stored at a
-// padded pitch of 272 bytes, plus the tile's 16 x 4 zero points and 16 x 4
+// A unit is one 16-row tile x 512 k: 16 rows of 256 packed bytes (16-byte
+// chunks XOR-swizzled by row), plus the tile's 16 x 4 zero points and 16 x 4
 // scales.  Every warp streams its own units through its own ring of
 // `depth` stages (cp.async); WPT warps of a CTA may share a tile (K steps
-// dealt round-robin, partials added behind a named barrier), and K may be
-// split over the S CTAs of a cluster (S | K/512).
+// dealt round-robin, partials handed to part 0 through shared memory), and
+// K may be split over the S CTAs of a cluster (S | K/512).
 // ---------------------------------------------------------------------------
 // warps per CTA: 8 (two CTAs per SM, so the next launch's CTA can be
 // resident beside this one) or 16 (one CTA per SM, twice the warps to hide
 // the arithmetic's latencies on long runs)
 constexpr int kHmmaWarpsPaired = 8;
 constexpr int kHmmaWarpsWide = 16;
-constexpr int kHmmaRowPitch = 272;                   // 256 bytes of a row + 16 of padding
-constexpr int kHmmaUnitBytes = 16 * kHmmaRowPitch;   // 4352
+constexpr int kHmmaRowPitch = 256;                   // a row's 256 bytes, chunks XOR-swizzled
+constexpr int kHmmaUnitBytes = 16 * kHmmaRowPitch;   // 4096
 constexpr int kHmmaUnitSZ = 192;   // zero points 16 x 4 bytes, then scales 16 x 8 bytes
 constexpr int kHmmaStage = kHmmaUnitBytes + kHmmaUnitSZ;
 constexpr int kHmmaMaxDepth = 6;
