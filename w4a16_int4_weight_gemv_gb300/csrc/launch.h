@@ -218,6 +218,9 @@ HmmaChoice plan_hmma_split(const DeviceInfo& dev, int W, int M, int N, int K, in
             const int want = units <= 8 ? 2 : 3;
             const int per_sm = hmma_layout(W, M, sps, S, max_tiles, want).total <= half ? 2 : 1;
             if (pair_only && per_sm != 2) continue;
+            // clusters of four or more CTAs that could pair up on an SM were
+            // placed unevenly (measured 30-60 % slower than S <= 2)
+            if (per_sm == 2 && S > 2 && forced_S == 0) continue;
             if (best_t >= 0 && (t > best_t || (t == best_t && per_sm <= best.per_sm))) continue;
             const int budget = per_sm == 2 ? half : dev.max_smem_optin;
             int depth = 2;
