@@ -208,17 +208,46 @@ def _graph_events(torch):
         return None
 
 
-class WarmGraphs:
-    """Exactly `steps` steps fn(0), fn(1), ... as replays of CUDA graphs.
+def capture_lead_timed(torch, fn, n, ev0, ev1):
+    """CUDA graph of one untimed lead-in step fn(-1), then n steps fn(0..n-1)
+    timed by ev0 (recorded on a side branch once the lead-in step has
+    completed, so the launches keep their programmatic-dependent-launch
+    edges) and ev1 (after the last step)."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn(0)  # make sure nothing lazy happens inside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.graph(g):
+        main = torch.cuda.current_stream()
+        fn(-1)
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            ev0.record()
+        for i in range(n):
+            fn(i)
+        ev1.record()
+        main.wait_stream(side)
+    return g
 
-    Up to 2048 steps: one graph holding a start event, the steps and an end
-    event, so the measured interval is the steps' own device time from the
-    first launch to the last, without the host's graph-launch latency.  More
-    steps: a graph of `chunk` steps (a multiple of the R rotating copies,
-    ~2048 launches) replayed steps // chunk times plus a graph of the
-    remainder, timed by events around the replays.  warm() replays every
-    graph untimed -- at least `warmup` steps -- so the timed run only repeats
-    graphs that have already run."""
+
+class WarmGraphs:
+    """Exactly `steps` timed steps fn(0), fn(1), ... as replays of CUDA graphs.
+
+    Up to 2048 steps: one graph holding an untimed lead-in step, a start
+    event on a side branch that fires when the lead-in step completes, the
+    steps and an end event -- so the measured interval is exactly the steps'
+    own device time in steady state (each launch overlapping its predecessor
+    as in a decode loop), without the host's graph-launch latency or the
+    first launch's start-up.  More steps: a graph of `chunk` steps (a
+    multiple of the R rotating copies, ~2048 launches) replayed
+    steps // chunk times plus a graph of the remainder, timed by events
+    around the replays.  warm() replays every graph untimed -- at least
+    `warmup` steps -- so the timed run only repeats graphs that have already
+    run."""
 
     def __init__(self, torch, fn, steps, R):
         self.torch = torch
@@ -226,17 +255,10 @@ class WarmGraphs:
         if self.inner is not None:
             self.chunk = steps
             self.reps, rem = 1, 0
-            ev0, ev1 = self.inner
-
-            def body(i):
-                if i == 0:
-                    ev0.record()
-                fn(i)
-                if i == steps - 1:
-                    ev1.record()
-            self.full = capture(torch, body, steps)
+            self.full = capture_lead_timed(torch, fn, steps, *self.inner)
             self.tail = None
-            self.timing = "event-record nodes inside the graph around the %d launches" % steps
+            self.timing = ("events inside the graph: the start on a side branch after one "
+                           "untimed lead-in launch, the end after the %d timed launches" % steps)
         else:
             chunk = steps if steps <= R else R * max(1, min(steps // R, 2048 // R))
             self.chunk = chunk
@@ -621,6 +643,7 @@ def run_gpu(args):
     graphs = WarmGraphs(torch, step, args.steps, R)
     chunk = graphs.chunk
     timing = graphs.timing
+    lead_in = graphs.inner is not None
     # warm-up: the graphs about to be timed, replayed untimed (>= W >= 3 steps)
     graphs.warm(max(3, args.warmup))
     clocks = ClockSampler(local)
@@ -740,9 +763,10 @@ def run_gpu(args):
                                     "is shared by all steps (L2-resident, as written by the "
                                     "preceding op; HBM-cold x: sweep.square_M1_x_cold)"
                                     % (R, R * all_bytes(M, N, K, g) / 1e6),
-                       "launch": "CUDA graph of %d w4a16_gemv launches (weights rotating over %d "
-                                 "copies), warmed by an untimed replay, replayed %d time(s)"
-                                 % (chunk, R, args.steps // chunk),
+                       "launch": "CUDA graph of %d timed w4a16_gemv launches%s (weights rotating "
+                                 "over %d copies), warmed by an untimed replay, replayed %d time(s)"
+                                 % (chunk, " after one untimed lead-in launch"
+                                    if lead_in else "", R, args.steps // chunk),
                        "timing": timing,
                        "plan": plan, "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
