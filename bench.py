@@ -68,7 +68,7 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_hmma_m1_square_4096.md")
 def kernel_source_hash():
     """Hash of the sources of the one-token kernel the headline times."""
     h = hashlib.sha256()
-    for name in ("gemv_hmma.cu", "common.cuh", "launch.h"):
+    for name in ("gemv_hmma.cu", "hmma_core.cuh", "common.cuh", "launch.h"):
         with open(os.path.join(ROOT, "w4a16_int4_weight_gemv_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -28,7 +28,7 @@ def test_all_bytes_add_zero_points_and_outputs():
 
 def test_profiled_traffic_follows_the_kernel_source(monkeypatch):
     t = bench.profiled_traffic()
-    text = open(os.path.join(ROOT, "profiles", "gemv_m1_square_4096.md")).read()
+    text = open(bench.PROFILE_SUMMARY).read()
     if "kernel_source_sha256_16: %s" % bench.kernel_source_hash() in text:
         # captured on this source: DRAM traffic of a launch, at least its algorithmic bytes
         assert t is not None and t >= bench.algo_bytes(1, 4096, 4096, 128)
