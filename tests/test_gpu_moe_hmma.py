@@ -1,0 +1,103 @@
+"""The routed SwiGLU expert FFN on the fp16 warp-MMA path (w4a16_moe_ffn with
+1..8 tokens, at most 32 routed slots, g = 128): against the oracle's chain
+(gate and up GEMVs, bf16 SwiGLU, down GEMVs, routed sum in fp64), over
+shapes whose K needs a partial last 512-k step, token and slot counts up to
+the path's limits, experts shared by several tokens and by several slots of
+one token (more than 8 slots on one expert), invalid ids, and repeated calls
+(the routed-sum counters reset themselves).  Bar: relative L2 <= 5e-3 and
+max |err| <= 1e-2 * max |y_ref|."""
+import numpy as np
+import pytest
+import torch
+
+from w4a16_int4_weight_gemv_gb300 import synth
+
+from .test_gpu_parity import check_close, dev, host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from w4a16_int4_weight_gemv_gb300 import build_ext
+    build_ext.build()
+    from w4a16_int4_weight_gemv_gb300 import binding
+    binding.w4a16_device_error(clear=True)
+    return binding
+
+
+def bank(b):
+    return tuple(dev(a) for a in b)
+
+
+def run(w, p, ids=None, route_w=None):
+    ids = p["ids"] if ids is None else ids
+    route_w = p["route_w"] if route_w is None else route_w
+    y = w.moe_ffn(dev(p["x"]), dev(ids), dev(route_w), bank(p["gate"]), bank(p["up"]),
+                  bank(p["down"]), 128)
+    torch.cuda.synchronize()
+    return y
+
+
+@pytest.mark.parametrize("M,E,H,F,topk", [
+    (1, 64, 2304, 1024, 8),    # the MoE workload, one token
+    (4, 64, 2304, 1024, 8),    # 32 slots: the path's limit
+    (8, 16, 1024, 512, 4),     # eight tokens
+    (5, 8, 640, 256, 3),       # H = 5 blocks: one whole and one partial step
+    (3, 12, 384, 384, 2),      # 3 blocks: a single partial step in both launches
+    (2, 4, 128, 128, 2),       # one block each way, four experts
+])
+def test_moe_hmma_matches_oracle(w, oracle, M, E, H, F, topk):
+    p = synth.moe_problem(M=M, E=E, H=H, F=F, topk=topk, g=128, seed=9000 + M * 7 + E)
+    y = run(w, p)
+    ref = oracle.moe_ffn(p["x"], p["ids"], p["route_w"], p["gate"], p["up"], p["down"], 128)
+    check_close(host_f64(y), ref["out"], "moe hmma M=%d E=%d H=%d F=%d topk=%d" % (M, E, H, F, topk))
+    assert w.w4a16_device_error(clear=True) == 0
+
+
+def test_moe_hmma_shared_and_repeated_experts(w, oracle):
+    # every token routes slot 0 to expert 3, token 1 routes three more slots
+    # to it (same token, same expert: identical products), and token 3 routes
+    # all its slots to expert 5: expert 3 then has 7 slots, expert 5 eight
+    # plus one more from token 0 -- more than one group of 8
+    p = synth.moe_problem(M=4, E=16, H=1024, F=512, topk=8, g=128, seed=9100)
+    ids = p["ids"].copy()
+    ids[:, 0] = 3
+    ids[1, 1:4] = 3
+    ids[3, :] = 5
+    ids[0, 7] = 5
+    y = run(w, p, ids=ids)
+    ref = oracle.moe_ffn(p["x"], ids, p["route_w"], p["gate"], p["up"], p["down"], 128)
+    check_close(host_f64(y), ref["out"], "shared experts")
+    assert w.w4a16_device_error(clear=True) == 0
+
+
+def test_moe_hmma_invalid_ids_are_skipped_and_flagged(w, oracle):
+    p = synth.moe_problem(M=3, E=16, H=1024, F=512, topk=4, g=128, seed=9200)
+    ids = p["ids"].copy()
+    ids[0, 1] = -1
+    ids[2, 3] = 16
+    w.w4a16_device_error(clear=True)
+    y = run(w, p, ids=ids)
+    assert w.w4a16_device_error(clear=True) & w.DEVERR_EXPERT_ID
+    ref_ids = ids.copy()
+    ref_rw = p["route_w"].copy()
+    for t, j in ((0, 1), (2, 3)):
+        ref_ids[t, j] = 0
+        ref_rw[t, j] = 0.0
+    ref = oracle.moe_ffn(p["x"], ref_ids, ref_rw, p["gate"], p["up"], p["down"], 128)
+    check_close(host_f64(y), ref["out"], "invalid ids")
+
+
+def test_moe_hmma_repeated_calls_are_identical(w):
+    # the per-chunk counters of the routed sum are cleared by the first
+    # launch and reset by the last arrival: calls in a row agree bit for bit
+    p = synth.moe_problem(M=2, E=64, H=2304, F=1024, topk=8, g=128, seed=9300)
+    args = (dev(p["x"]), dev(p["ids"]), dev(p["route_w"]), bank(p["gate"]), bank(p["up"]),
+            bank(p["down"]), 128)
+    outs = [w.moe_ffn(*args) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert w.w4a16_device_error(clear=True) == 0

@@ -434,6 +434,17 @@ w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const f
     float* part = reinterpret_cast<float*>(ws + 2 * align256(S * F * 2));
     unsigned* counters = reinterpret_cast<unsigned*>(ws + 2 * align256(S * F * 2) + align256(S * H * 4));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (moe_hmma_supports(M, topk, H, F, g) && moe_hmma_fits(dev->info, M, topk, E, H, F)) {
+        // the fp16 warp-MMA path: h = SwiGLU of the gate/up products in the
+        // first launch's epilogue (into the gate-output part of the
+        // workspace), the down products and routed sums in the second (in
+        // shared memory: the rest of the workspace is not used)
+        MoeHmmaArgs m{x,     expert_ids, route_w, gate_wq, gate_scale, gate_zero,
+                      up_wq, up_scale,   up_zero, down_wq, down_scale, down_zero,
+                      g_out, y,          M,       topk,    E,          H,
+                      F,     dev->err};
+        return from_cuda(launch_moe_hmma(m, dev->info, s));
+    }
     // gate and up products of every slot: one launch over both banks
     MoeArgs a{};
     a.x = x;

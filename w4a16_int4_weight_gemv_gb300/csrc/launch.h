@@ -278,6 +278,33 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s
 cudaError_t launch_gemv_tc(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 cudaError_t launch_gemv_hmma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 
+// Routed SwiGLU expert FFN on the fp16 warp-MMA path (moe_hmma.cu): 1..8
+// tokens, M * topk <= 32 slots, g == 128, H and F multiples of 128.  h is
+// the bf16 [M*topk][F] intermediate.
+constexpr int kMoeHmmaMaxSlots = 32;
+struct MoeHmmaArgs {
+    const uint16_t* x;
+    const int32_t* ids;
+    const float* route_w;
+    const uint32_t* gate_wq;
+    const uint16_t* gate_scale;
+    const uint8_t* gate_zero;
+    const uint32_t* up_wq;
+    const uint16_t* up_scale;
+    const uint8_t* up_zero;
+    const uint32_t* down_wq;
+    const uint16_t* down_scale;
+    const uint8_t* down_zero;
+    uint16_t* h;
+    uint16_t* y;
+    int M, topk, E;
+    int64_t H, F;
+    uint32_t* err;
+};
+bool moe_hmma_supports(int M, int topk, int64_t H, int64_t F, int64_t g);
+bool moe_hmma_fits(const DeviceInfo& dev, int M, int topk, int E, int64_t H, int64_t F);
+cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStream_t s);
+
 // One stacked expert bank: wq [E][N][K/8], scale and zero [E][N][K/g], and
 // its bf16 per-slot output [M*topk][N] (used when there is no routed sum).
 struct MoeBank {

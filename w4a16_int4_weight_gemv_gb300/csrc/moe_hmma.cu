@@ -1,0 +1,798 @@
+// Routed SwiGLU expert FFN of 1..8 tokens on the fp16 warp-MMA path (g ==
+// 128): the grouped expert kernel of the local-kimi README (technical-detail
+// section), as two launches.
+//
+//   1. gate/up: for every distinct routed expert e, the gate and up products
+//      of all tokens, h[t][j] = bf16(silu(bf16(W^gate_e x[t])) *
+//      bf16(W^up_e x[t])) stored for every slot (t, j) routed to e.
+//   2. down: a CTA owns 16-row tiles of the output and computes, for every
+//      routed slot, d[t][j] = W^down_e h[t][j] on them (fp32, in shared
+//      memory), then y[t] = bf16(sum_j route_w[t][j] d[t][j]) (j ascending,
+//      invalid ids skipped) -- no partials leave the CTA.
+//
+// Both launches share one design with the dense fp16 warp-MMA GEMV: a 16-row
+// tile of weights is the A operand of mma.sync m16n8k16, the codes become
+// fp16 with one LOP3 per two (1024 + code, the 16x scaling of odd codes
+// folded into B), the activations are staged per CTA as fp16 B fragments
+// with each 128-k block scaled by a power of two, units of 16 rows x 512 k
+// stream through per-warp cp.async rings, and parts of a split tile hand
+// their partials to part 0.  What differs:
+//
+// Tiles.  Warp 0 routes once per CTA: the distinct valid experts in order
+// of first appearance among the M * topk slots (<= 32).  A launch-1 tile
+// pairs gate rows 8r..8r+7 (tile rows 0..7) with the same up rows (tile rows
+// 8..15) of one expert, so a lane holds a gate and its up row and forms h in
+// the epilogue; its B columns are the M tokens.  A launch-2 tile is 16 rows
+// of one expert's down matrix; its B columns are that expert's routed slots
+// (an "entry": up to 8 slots; an expert with more slots has several
+// entries), and a CTA's warps take the entries of its row tiles in turn,
+// each entry's K steps in one warp.  Every tile column the MMA computes
+// beyond the real ones is free.
+//
+// Partial steps.  K need not be a multiple of 512 (the FFN's H = 2304 is
+// 4.5 steps): the last unit of a row carries 1..3 blocks, copied and used
+// block by block.  The zero points and scales of a unit are copied from the
+// 4-byte-aligned words around them (their rows start at any byte, g = 128
+// giving K / 128 groups per row), zero-filled past the end of the arrays,
+// and picked out with funnel shifts.
+//
+// Launch.  Launch 2 reads the routing and its weights before its
+// grid-dependency wait; launch 1 signals its dependents only after its own
+// wait, so everything launch 2 reads early was complete before launch 1 ran.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "hmma_core.cuh"
+#include "launch.h"
+
+namespace w4a16 {
+namespace {
+
+// warps per CTA: 8 (two CTAs fit an SM) or 16 (launch 1 with long runs)
+constexpr int kMWPaired = 8;
+constexpr int kMWWide = 16;
+constexpr int kMZero = kHmmaUnitBytes;          // 16 rows x 8 zero-point bytes
+constexpr int kMScale = kHmmaUnitBytes + 128;   // 16 rows x 16 scale bytes
+constexpr int kMStage = kHmmaUnitBytes + 384;
+constexpr int kMMaxDepth = 4;
+
+struct MoeHK {
+    int phase;                 // 1: gate/up -> h; 2: down -> routed sums
+    const uint16_t* x;         // launch 1: x [M][K]; launch 2: h [M*topk][K]
+    const int32_t* ids;        // [M][topk]
+    const float* route_w;      // [M][topk] (launch 2)
+    const unsigned char* wq_a;  // launch 1: gate bank, launch 2: down bank
+    const uint16_t* scale_a;
+    const uint8_t* zero_a;
+    const unsigned char* wq_b;  // launch 1: up bank
+    const uint16_t* scale_b;
+    const uint8_t* zero_b;
+    uint16_t* h;               // launch 1 output [M*topk][N]
+    uint16_t* y;               // launch 2 output [M][N]
+    int M, topk, E, N, K;      // N, K: rows and columns of one expert matrix
+    int ents;                  // staged B columns: M (launch 1) or M * topk
+    int max_rt;                // launch 2: most 16-row output tiles a CTA owns
+    int wpt, depth;
+    uint32_t* err;
+};
+
+struct MoeHLayout {
+    int ring, bfrag, csum, red, bars, ids, ent_e, ent_n, ent_col, ybuf, nent, total;
+};
+__host__ __device__ inline MoeHLayout moeh_layout(int W, int ents, int kblocks, int depth, int max_rt) {
+    MoeHLayout L;
+    int off = 0;
+    L.ring = off;  // [warp][depth] stages
+    off += W * depth * kMStage;
+    L.bfrag = off;  // [block][piece][column entity][lane % 4] x 16 bytes
+    off += kblocks * 4 * ents * 4 * 16;
+    L.csum = off;  // [block][column entity] {1024 sum B, sum x', 2^-sh, 0}
+    off += kblocks * ents * 16;
+    L.red = off;  // [2][warp][lane] float4 partials of split tiles
+    off += 2 * W * 32 * 16;
+    L.bars = off;  // [tile group][buffer] {full, empty}
+    off += W * 2 * 2 * 8;
+    L.ids = off;  // routed expert of each slot (-1: invalid)
+    off += kMoeHmmaMaxSlots * 4;
+    L.ent_e = off;  // expert of each entry
+    off += kMoeHmmaMaxSlots * 4;
+    L.ent_n = off;  // slots of each entry (launch 2)
+    off += kMoeHmmaMaxSlots * 4;
+    L.ent_col = off;  // [entry][8] slots (launch 2)
+    off += kMoeHmmaMaxSlots * 8 * 4;
+    L.ybuf = off;  // launch 2: [row tile][slot][16 rows] fp32 products
+    off += max_rt * ents * 16 * 4;
+    L.nent = off;
+    off += 16;
+    L.total = off + 128;
+    return L;
+}
+
+// cp.async of the 4 bytes at src, of which only the first n (0..4) are read
+// (the rest of the destination is zero-filled)
+__device__ __forceinline__ void cp_async_4_fill(void* dst, const void* src, int n) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "r"(n)
+                 : "memory");
+}
+
+__device__ __forceinline__ int clamp4(long long v) { return v < 0 ? 0 : (v > 4 ? 4 : static_cast<int>(v)); }
+
+template <int W>
+__global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(const MoeHK a) {
+    constexpr int T = 32 * W;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int S = a.M * a.topk;
+    const int kblocks = a.K >> 7;
+    const int nsteps = (kblocks + 3) >> 2;
+    const int G = kblocks;  // zero points and scales per row (g == 128)
+    const int WPT = a.wpt;
+    const int NG = W / WPT;
+    const int grp = warp / WPT;
+    const int part = warp - grp * WPT;
+    const int D = a.depth;
+    const int ENTS = a.ents;
+    const bool p1 = a.phase == 1;
+
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char* base = smem_raw + (((raw + 127u) & ~127u) - raw);
+    const MoeHLayout L = moeh_layout(W, ENTS, kblocks, D, a.max_rt);
+    unsigned char* ring = base + L.ring + warp * D * kMStage;
+    uint4* bfrag = reinterpret_cast<uint4*>(base + L.bfrag);
+    float4* csum = reinterpret_cast<float4*>(base + L.csum);
+    float4* red = reinterpret_cast<float4*>(base + L.red);
+    uint64_t* gbar = reinterpret_cast<uint64_t*>(base + L.bars);
+    int* s_ids = reinterpret_cast<int*>(base + L.ids);
+    int* ent_e = reinterpret_cast<int*>(base + L.ent_e);
+    int* ent_n = reinterpret_cast<int*>(base + L.ent_n);
+    int* ent_col = reinterpret_cast<int*>(base + L.ent_col);
+    int* s_nent = reinterpret_cast<int*>(base + L.nent);
+    float* ybuf = reinterpret_cast<float*>(base + L.ybuf);
+
+    if (WPT > 1 && threadIdx.x < NG * 2) {
+        mbar_init(gbar + threadIdx.x * 2, (WPT - 1) * 32);
+        mbar_init(gbar + threadIdx.x * 2 + 1, 32);
+    }
+    if (!p1) grid_dependents_launch();
+
+    // Routing (warp 0): slot s = lane.  Entries: launch 1, one per distinct
+    // valid expert; launch 2, one per group of up to 8 of an expert's slots;
+    // both in order of the expert's first appearance.
+    auto route = [&]() {
+        if (warp != 0) return;
+        const int e = lane < S ? a.ids[lane] : -1;
+        const bool valid = lane < S && e >= 0 && e < a.E;
+        if (p1 && lane < S && !valid) raise_device_error(a.err, W4A16_DEVERR_EXPERT_ID);
+        int first = lane, pos = 0, cnt = 0;
+        for (int q = 0; q < 32; ++q) {
+            const int eq = __shfl_sync(0xffffffffu, valid ? e : -1, q);
+            if (valid && eq == e) {
+                first = min(first, q);
+                pos += q < lane ? 1 : 0;
+                ++cnt;
+            }
+        }
+        const bool is_first = valid && first == lane;
+        const int nsub = is_first ? (p1 ? 1 : (cnt + 7) >> 3) : 0;
+        int incl = nsub;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int ebase = __shfl_sync(0xffffffffu, incl - nsub, valid ? first : 0);
+        if (valid) {
+            if (p1) {
+                if (is_first) ent_e[ebase] = e;
+            } else {
+                const int en = ebase + (pos >> 3);
+                ent_col[en * 8 + (pos & 7)] = lane;
+                if ((pos & 7) == 0) {
+                    ent_e[en] = e;
+                    ent_n[en] = min(8, cnt - pos);
+                }
+            }
+        }
+        if (lane < kMoeHmmaMaxSlots) s_ids[lane] = valid ? e : -1;
+        if (lane == 31) *s_nent = incl;
+    };
+    if (!p1) route();
+    __syncthreads();  // barriers initialised, routing of launch 2 published
+
+    // Tiles.  Launch 1: the CTA's range of the (entry, 8-row pair) tiles,
+    // entry-major.  Launch 2: for each of the CTA's 16-row output tiles, one
+    // tile per entry.  A tile is walked as (outer, inner): launch 1 (entry,
+    // pair), launch 2 (output tile of the CTA, entry).
+    const int tpe = p1 ? (a.N >> 3) : (a.N >> 4);  // pair / row tiles per expert matrix
+    int nent = 0, isz = 1, t0 = 0, nt = 0, rt0 = 0, nrt = 0;
+    auto set_range = [&](int ne) {
+        nent = ne;
+        if (p1) {
+            const long long tt = static_cast<long long>(ne) * tpe;
+            t0 = static_cast<int>(tt * blockIdx.x / gridDim.x);
+            nt = static_cast<int>(tt * (blockIdx.x + 1) / gridDim.x) - t0;
+            isz = tpe;
+        } else {
+            rt0 = static_cast<int>(static_cast<long long>(tpe) * blockIdx.x / gridDim.x);
+            nrt = static_cast<int>(static_cast<long long>(tpe) * (blockIdx.x + 1) / gridDim.x) - rt0;
+            t0 = 0;
+            nt = nrt * ne;
+            isz = ne > 0 ? ne : 1;
+        }
+    };
+    if (!p1) set_range(*s_nent);
+
+    const size_t row_bytes = static_cast<size_t>(a.K) >> 1;
+    const int sw_h = lane >> 4, sw_c = ((lane & 15) ^ sw_h) << 4;
+    const int dl0 = sw_h * kHmmaRowPitch + sw_c, dl1 = sw_h * kHmmaRowPitch + (sw_c ^ 32);
+    const int dl2 = sw_h * kHmmaRowPitch + (sw_c ^ 64), dl3 = sw_h * kHmmaRowPitch + (sw_c ^ 96);
+    auto dst_off = [&](int i) {
+        return ((i & 3) == 0 ? dl0 : (i & 3) == 1 ? dl1 : (i & 3) == 2 ? dl2 : dl3) +
+               i * 2 * kHmmaRowPitch;
+    };
+    const int rr = lane & 15;
+    const bool zlane = lane < 16;
+    const long long zend = static_cast<long long>(a.E) * a.N * G;  // zero-point bytes per bank
+    // tile t of the range -> entry and row block, advanced without division
+    int my_tiles = 0, my_steps = 0, nu = 0;
+    auto set_units = [&]() {
+        my_tiles = (nt > grp) ? (nt - grp + NG - 1) / NG : 0;
+        my_steps = (nsteps > part) ? (nsteps - part + WPT - 1) / WPT : 0;
+        nu = my_tiles * my_steps;
+    };
+    if (!p1) set_units();
+    int i_u = 0, i_slot = 0, i_step = part, i_o = 0, i_i = 0;
+    auto start_cursor = [&](int& o, int& in) {
+        const int t = t0 + grp;
+        o = t / isz;  // once per warp
+        in = t - o * isz;
+    };
+    auto next_tile = [&](int& o, int& in) {
+        in += NG;
+        while (in >= isz) {
+            in -= isz;
+            ++o;
+        }
+    };
+    // entry and row tile of the expert matrix of the tile at (o, in)
+    auto tile_of = [&](int o, int in, int& en, int& r) {
+        if (p1) {
+            en = o;
+            r = in;
+        } else {
+            en = in;
+            r = rt0 + o;
+        }
+    };
+    // first weight byte of tile rows 0 and 8, and the global row index of
+    // rows 0 and 8 (launch 1: gate rows in bank a, the same up rows in bank b)
+    auto tile_rows = [&](int o, int in, const unsigned char*& w0, const unsigned char*& w8,
+                         long long& z0, long long& z8) {
+        int en, r;
+        tile_of(o, in, en, r);
+        const long long e = ent_e[en];
+        if (p1) {
+            z0 = e * a.N + 8LL * r;
+            z8 = z0;
+            w0 = a.wq_a + z0 * static_cast<long long>(row_bytes);
+            w8 = a.wq_b + z8 * static_cast<long long>(row_bytes);
+        } else {
+            z0 = e * a.N + 16LL * r;
+            z8 = z0 + 8;
+            w0 = a.wq_a + z0 * static_cast<long long>(row_bytes);
+            w8 = w0 + 8 * row_bytes;
+        }
+    };
+    // the producer's tile: this lane's first weight byte of tile rows sw_h
+    // and 8 + sw_h, and the first group of its zero-point / scale row
+    const bool bank_b = p1 && rr >= 8;  // launch 1: tile rows 8..15 are up rows
+    const unsigned char* i_w0 = nullptr;
+    const unsigned char* i_w8 = nullptr;
+    long long i_zg = 0;
+    auto producer_tile = [&]() {
+        const unsigned char *w0, *w8;
+        long long z0, z8;
+        tile_rows(i_o, i_i, w0, w8, z0, z8);
+        const size_t lane_b = sw_h * row_bytes + (lane & 15) * 16;
+        i_w0 = w0 + lane_b;
+        i_w8 = w8 + lane_b;
+        i_zg = (rr < 8 ? z0 + rr : z8 + (rr - 8)) * G;
+    };
+    auto issue_next = [&]() {
+        if (i_u < nu) {
+            const int step = i_step;
+            const int nbs = min(4, kblocks - 4 * step);
+            unsigned char* stage = ring + i_slot * kMStage;
+            if ((lane & 15) < nbs * 4) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const unsigned char* src =
+                        (i < 4 ? i_w0 + 2 * i * row_bytes : i_w8 + (2 * i - 8) * row_bytes) + step * 256;
+                    cp_async_16(stage + dst_off(i), src);
+                }
+            }
+            // zero points (lanes 0..15) or scales (16..31) of tile row rr,
+            // from the 4-byte words around them
+            const long long gi = i_zg + 4LL * step;  // first group of the unit
+            if (zlane) {
+                const uint8_t* zb = bank_b ? a.zero_b : a.zero_a;
+                const long long w4 = gi & ~3LL;
+                unsigned char* dz = stage + kMZero + rr * 8;
+                if (w4 + 8 <= zend) {
+                    cp_async_4(dz, zb + w4);
+                    cp_async_4(dz + 4, zb + w4 + 4);
+                } else {  // the last bytes of the array: read no further
+                    const int n0 = clamp4(zend - w4), n1 = clamp4(zend - w4 - 4);
+                    cp_async_4_fill(dz, zb + w4, n0);
+                    cp_async_4_fill(dz + 4, zb + (n1 > 0 ? w4 + 4 : w4), n1);
+                }
+            } else {
+                const unsigned char* sb =
+                    reinterpret_cast<const unsigned char*>(bank_b ? a.scale_b : a.scale_a);
+                const long long b = gi * 2, w4 = b & ~3LL, send = zend * 2;
+                unsigned char* ds = stage + kMScale + rr * 16;
+                if (w4 + 12 <= send) {
+                    cp_async_4(ds, sb + w4);
+                    cp_async_4(ds + 4, sb + w4 + 4);
+                    cp_async_4(ds + 8, sb + w4 + 8);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) {
+                        const int n = clamp4(send - w4 - 4 * q);
+                        cp_async_4_fill(ds + 4 * q, sb + (n > 0 ? w4 + 4 * q : w4), n);
+                    }
+                }
+            }
+            ++i_u;
+            if (++i_slot == D) i_slot = 0;
+            i_step += WPT;
+            if (i_step >= nsteps) {
+                i_step = part;
+                next_tile(i_o, i_i);
+                if (i_u < nu) producer_tile();
+            }
+        }
+        cp_async_commit();
+    };
+    // launch 2: routing and weights are inputs of the whole chain
+    if (!p1) {
+        if (nu > 0) {
+            start_cursor(i_o, i_i);
+            producer_tile();
+        }
+        for (int k = 0; k < D; ++k) issue_next();
+    }
+    grid_dependency_wait();
+    if (p1) grid_dependents_launch();
+
+    {
+        // B columns: the K range of every column entity (token or slot), in
+        // fragment order, each 128-k block scaled by a power of two
+        // pieces (8 k of one column) are dealt flat over the CTA's threads:
+        // piece f of the (column, piece) sequence goes to thread f % T of
+        // item f / T; a column has a multiple of 16 pieces, so the 16 pieces
+        // of a block are always 16 consecutive lanes
+        const int tid = threadIdx.x;
+        const int npieces = kblocks * 16;
+        const int cols = p1 ? a.M : S;  // staged B columns: tokens or slots
+        const int nflat = cols * npieces;
+        const int items = (nflat + T - 1) / T;
+        auto load_items = [&](int it0, uint4 (&v)[4]) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int f = (it0 + b) * T + tid;
+                v[b] = make_uint4(0u, 0u, 0u, 0u);
+                if (it0 + b < items && f < nflat) {
+                    const int m = f / npieces, p = f - m * npieces;
+                    v[b] = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * a.K + p * 8));
+                }
+            }
+        };
+        uint4 v[4];
+        load_items(0, v);
+        if (p1) {
+            // launch 1 routes while its first activation loads are in flight,
+            // then requests its first units
+            route();
+            __syncthreads();
+            set_range(*s_nent);
+            set_units();
+            if (nu > 0) {
+                start_cursor(i_o, i_i);
+                producer_tile();
+            }
+            for (int k = 0; k < D; ++k) issue_next();
+        }
+        for (int it0 = 0; it0 < items; it0 += 4) {
+            if (it0 > 0) load_items(it0, v);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int it = it0 + b;
+                if (it >= items) break;  // the same for the whole CTA
+                const int f = it * T + tid;
+                const int m = f / npieces, p = f - m * npieces;
+                const uint32_t wv[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+                uint32_t mx = 0u;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    mx = max(mx, wv[e] & 0x7FFFu);
+                    mx = max(mx, (wv[e] >> 16) & 0x7FFFu);
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const int sh = block_shift(mx);
+                float fa, fb;
+                pow2_pair(sh, fa, fb);
+                const float fo = fb * 0.0625f;  // odd codes: B = x' / 16
+                uint32_t hq[8];
+                float c1 = 0.f, c2 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t bits = (e & 1) ? (wv[e >> 1] & 0xFFFF0000u) : (wv[e >> 1] << 16);
+                    const float xv = __uint_as_float(bits) * fa;
+                    const __half hv = __float2half_rn((e & 1) ? xv * fo : xv * fb);
+                    hq[e] = __half_as_ushort(hv);
+                    const float bv = __half2float(hv);
+                    c1 += bv;
+                    c2 += (e & 1) ? 16.f * bv : bv;
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    c1 += __shfl_xor_sync(0xffffffffu, c1, o);
+                    c2 += __shfl_xor_sync(0xffffffffu, c2, o);
+                }
+                if (f < nflat) {
+                    const int blk = p >> 4, j = (p >> 2) & 3, q = p & 3;
+                    uint4 o4;
+                    o4.x = hq[0] | (hq[4] << 16);
+                    o4.y = hq[1] | (hq[5] << 16);
+                    o4.z = hq[2] | (hq[6] << 16);
+                    o4.w = hq[3] | (hq[7] << 16);
+                    bfrag[((blk * 4 + j) * cols + m) * 4 + q] = o4;
+                    if ((p & 15) == 0) csum[blk * cols + m] = make_float4(1024.f * c1, c2, exp2i(-sh), 0.f);
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    const int g = lane >> 2, c = lane & 3;
+    const int CS = p1 ? a.M : S;  // B column stride of the staged fragments
+    const int lrow = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int lch = lane >> 4;
+    const int sw_s = lane & 7;
+    const uint32_t ring_addr = smem_addr(ring) + static_cast<uint32_t>(lrow * kHmmaRowPitch);
+    const uint32_t lve = (lch ^ (sw_s & 1)) << 4;
+    const uint32_t lv0 = lve + ((0 ^ (sw_s & 2)) << 4) + ((0 ^ (sw_s & 4)) << 4);
+    const uint32_t lv1 = lve + ((2 ^ (sw_s & 2)) << 4) + ((0 ^ (sw_s & 4)) << 4);
+    const uint32_t lv2 = lve + ((0 ^ (sw_s & 2)) << 4) + ((4 ^ (sw_s & 4)) << 4);
+    const uint32_t lv3 = lve + ((2 ^ (sw_s & 2)) << 4) + ((4 ^ (sw_s & 4)) << 4);
+
+    float4 tacc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool timed_out = false;
+    int c_slot = 0, c_step = part, ti = 0, c_o = 0, c_i = 0, c_ent = 0, c_r = 0;
+    if (nu > 0) {
+        start_cursor(c_o, c_i);
+        tile_of(c_o, c_i, c_ent, c_r);
+    }
+    // per tile: B column entity of lane g, C column entities 2c, 2c + 1
+    int col_g = 0, col0 = 0, col1 = 0;
+    bool use0 = false, use1 = false, two = false;
+    int subz_a = 0, subz_b = 0, subs_a = 0, subs_b = 0;
+    auto set_tile = [&]() {
+        if (p1) {
+            col_g = g < a.M ? g : 0;
+            use0 = 2 * c < a.M;
+            use1 = 2 * c + 1 < a.M;
+            col0 = use0 ? 2 * c : 0;
+            col1 = use1 ? 2 * c + 1 : 0;
+            two = a.M > 1;
+        } else {
+            const int n = ent_n[c_ent];
+            const int* cl = ent_col + c_ent * 8;
+            col_g = cl[g < n ? g : 0];
+            use0 = 2 * c < n;
+            use1 = 2 * c + 1 < n;
+            col0 = cl[use0 ? 2 * c : 0];
+            col1 = cl[use1 ? 2 * c + 1 : 0];
+            two = n > 1;
+        }
+        const unsigned char *w0, *w8;
+        long long z0, z8;
+        tile_rows(c_o, c_i, w0, w8, z0, z8);
+        subz_a = static_cast<int>(((z0 + g) * G) & 3);
+        subz_b = static_cast<int>(((z8 + g) * G) & 3);
+        subs_a = static_cast<int>(((z0 + g) * G * 2) & 3);
+        subs_b = static_cast<int>(((z8 + g) * G * 2) & 3);
+    };
+    if (nu > 0) set_tile();
+#pragma unroll 1
+    for (int k = 0; k < nu; ++k) {
+        cp_async_wait_pending(D - 1);
+        __syncwarp();
+        const int slot = c_slot;
+        const int lstep = c_step;
+        if (++c_slot == D) c_slot = 0;
+        const int nbs = min(4, kblocks - 4 * lstep);
+        const uint32_t wst = ring_addr + static_cast<uint32_t>(slot * kMStage);
+        const unsigned char* sz = ring + slot * kMStage;
+        const uint2 zwa = *reinterpret_cast<const uint2*>(sz + kMZero + g * 8);
+        const uint2 zwb = *reinterpret_cast<const uint2*>(sz + kMZero + (g + 8) * 8);
+        const uint4 swa = *reinterpret_cast<const uint4*>(sz + kMScale + g * 16);
+        const uint4 swb = *reinterpret_cast<const uint4*>(sz + kMScale + (g + 8) * 16);
+        const uint32_t za = __funnelshift_r(zwa.x, zwa.y, 8 * subz_a);
+        const uint32_t zb = __funnelshift_r(zwb.x, zwb.y, 8 * subz_b);
+        const uint32_t sa01 = __funnelshift_r(swa.x, swa.y, 8 * subs_a);
+        const uint32_t sa23 = __funnelshift_r(swa.y, swa.z, 8 * subs_a);
+        const uint32_t sb01 = __funnelshift_r(swb.x, swb.y, 8 * subs_b);
+        const uint32_t sb23 = __funnelshift_r(swb.y, swb.z, 8 * subs_b);
+        const uint4* bqu = bfrag + static_cast<size_t>(4 * lstep) * 4 * CS * 4 + col_g * 4 + c;
+        const float4* csu = csum + static_cast<size_t>(4 * lstep) * CS;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+            if (bb >= nbs) break;  // the same for the whole warp
+            const uint32_t hb = wst + static_cast<uint32_t>((bb >> 1) * 128);
+            uint32_t q0[4], q1[4];
+            ldmatrix_x4(q0, hb + ((bb & 1) ? lv2 : lv0));
+            ldmatrix_x4(q1, hb + ((bb & 1) ? lv3 : lv1));
+            const uint32_t wa[4] = {q0[0], q0[2], q1[0], q1[2]};
+            const uint32_t wb[4] = {q0[1], q0[3], q1[1], q1[3]};
+            uint4 bq[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) bq[j] = bqu[(bb * 4 + j) * CS * 4];
+            float d0[4], d1[4];
+            {
+                const uint32_t ta = wa[0] >> 8, tb = wb[0] >> 8;
+                mma_f16_16816_zero(d0, f16_codes_lo(wa[0]), f16_codes_lo(wb[0]), f16_codes_hi(wa[0]),
+                                   f16_codes_hi(wb[0]), bq[0].x, bq[0].y);
+                mma_f16_16816_zero(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
+                                   f16_codes_hi(tb), bq[0].z, bq[0].w);
+            }
+#pragma unroll
+            for (int j = 1; j < 4; ++j) {
+                const uint32_t ta = wa[j] >> 8, tb = wb[j] >> 8;
+                mma_f16_16816(d0, f16_codes_lo(wa[j]), f16_codes_lo(wb[j]), f16_codes_hi(wa[j]),
+                              f16_codes_hi(wb[j]), bq[j].x, bq[j].y);
+                mma_f16_16816(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
+                              f16_codes_hi(tb), bq[j].z, bq[j].w);
+            }
+            const float zfa = zero_point_f32(za, bb), zfb = zero_point_f32(zb, bb);
+            const uint32_t pa = bb < 2 ? sa01 : sa23, pb = bb < 2 ? sb01 : sb23;
+            const float sfa = __uint_as_float((bb & 1) ? (pa & 0xFFFF0000u) : (pa << 16));
+            const float sfb = __uint_as_float((bb & 1) ? (pb & 0xFFFF0000u) : (pb << 16));
+            const float4 cs0 = csu[bb * CS + col0];
+            acc[0] = fmaf(sfa * cs0.z, (d0[0] + d1[0]) - fmaf(zfa, cs0.y, cs0.x), acc[0]);
+            acc[2] = fmaf(sfb * cs0.z, (d0[2] + d1[2]) - fmaf(zfb, cs0.y, cs0.x), acc[2]);
+            if (two) {
+                const float4 cs1 = csu[bb * CS + col1];
+                acc[1] = fmaf(sfa * cs1.z, (d0[1] + d1[1]) - fmaf(zfa, cs1.y, cs1.x), acc[1]);
+                acc[3] = fmaf(sfb * cs1.z, (d0[3] + d1[3]) - fmaf(zfb, cs1.y, cs1.x), acc[3]);
+            }
+        }
+        __syncwarp();
+        issue_next();
+        tacc.x += acc[0];
+        tacc.y += acc[1];
+        tacc.z += acc[2];
+        tacc.w += acc[3];
+        c_step += WPT;
+        if (c_step < nsteps) continue;
+        c_step = part;
+        // the tile is complete: partials to part 0, which stores
+        if (WPT > 1) {
+            if (part != 0) {
+                timed_out |= !hand_partial<W>(red, gbar, grp, WPT, part, ti, lane, tacc);
+            } else {
+                const int b = ti & 1;
+                const float4* rb = red + (b * W + grp * WPT) * 32;
+                uint64_t* full = gbar + (grp * 2 + b) * 2;
+                timed_out |= !mbar_wait_bounded(full, (ti >> 1) & 1);
+                for (int q = 1; q < WPT; ++q) {
+                    const float4 pv = rb[q * 32 + lane];
+                    tacc.x += pv.x;
+                    tacc.y += pv.y;
+                    tacc.z += pv.z;
+                    tacc.w += pv.w;
+                }
+                mbar_arrive(full + 1);
+            }
+        }
+        if (part == 0) {
+            const int e = ent_e[c_ent];
+            if (p1) {
+                // rows g, g + 8: gate and up row 8 r + g of expert e
+                const size_t hr = static_cast<size_t>(c_r) * 8 + g;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int t = 2 * c + q;
+                    if (t >= a.M) continue;
+                    const uint16_t hv = swiglu_of_sums(q ? tacc.y : tacc.x, q ? tacc.w : tacc.z);
+                    for (int j = 0; j < a.topk; ++j)
+                        if (s_ids[t * a.topk + j] == e)
+                            a.h[static_cast<size_t>(t * a.topk + j) * a.N + hr] = hv;
+                }
+            } else {
+                // the entry's slot columns of output tile c_r, to shared memory
+                float* yb = ybuf + static_cast<size_t>(c_r - rt0) * S * 16;
+                if (use0) {
+                    yb[col0 * 16 + g] = tacc.x;
+                    yb[col0 * 16 + g + 8] = tacc.z;
+                }
+                if (use1) {
+                    yb[col1 * 16 + g] = tacc.y;
+                    yb[col1 * 16 + g + 8] = tacc.w;
+                }
+            }
+        }
+        tacc = make_float4(0.f, 0.f, 0.f, 0.f);
+        ++ti;
+        if (k + 1 < nu) {
+            next_tile(c_o, c_i);
+            tile_of(c_o, c_i, c_ent, c_r);
+            set_tile();
+        }
+    }
+    if (WPT > 1 && my_steps == 0)
+        for (; ti < my_tiles; ++ti)
+            timed_out |= !hand_partial<W>(red, gbar, grp, WPT, part, ti, lane,
+                                          make_float4(0.f, 0.f, 0.f, 0.f));
+    cp_async_wait_pending(0);
+    if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
+    if (!p1) {
+        // routed sums of the CTA's output tiles: every slot's product is in
+        // shared memory; slots in order, invalid ids skipped
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < nrt * a.M * 16; idx += T) {
+            const int rl = idx / (a.M * 16);
+            const int rem = idx - rl * a.M * 16;
+            const int t = rem >> 4, row = rem & 15;
+            const float* yb = ybuf + static_cast<size_t>(rl) * S * 16;
+            float v = 0.f;
+            for (int j = 0; j < a.topk; ++j) {
+                const int sl = t * a.topk + j;
+                if (s_ids[sl] >= 0) v += a.route_w[sl] * yb[sl * 16 + row];
+            }
+            a.y[static_cast<size_t>(t) * a.N + (rt0 + rl) * 16 + row] = f32_to_bf16_rn(v);
+        }
+    }
+}
+
+struct MoeHPlan {
+    int warps, ctas, wpt, depth, smem, max_rt;
+};
+// launch 1 runs 16-warp CTAs (twice the warps on an SM for its long unit
+// runs), launch 2 8-warp CTAs (short runs; two fit an SM)
+constexpr int kMPhase1Warps = kMWWide;
+// CTAs, warps per tile and ring depth for one launch, at most one CTA per SM
+// (two fit where shared memory allows, for the next launch's).  Launch 1:
+// tiles_max (entry, pair) tiles, the split of K steps over warps that
+// minimises the busiest warp's units.  Launch 2: row_tiles output tiles over
+// the CTAs, each entry's K steps in one warp.
+MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int kblocks, long long tiles_max,
+                       int row_tiles) {
+    MoeHPlan p{};
+    p.warps = phase == 1 ? kMPhase1Warps : kMWPaired;
+    const int nsteps = (kblocks + 3) / 4;
+    if (phase == 1) {
+        if (tiles_max < 1) return p;
+        p.ctas = static_cast<int>(tiles_max < dev.sms ? tiles_max : dev.sms);
+        const long long max_tiles = (tiles_max + p.ctas - 1) / p.ctas;
+        long long best = -1;
+        for (int wpt = 1; wpt <= p.warps; wpt *= 2) {
+            const int ng = p.warps / wpt;
+            const long long u = ((max_tiles + ng - 1) / ng) * ((nsteps + wpt - 1) / wpt);
+            const long long cost = 8 * u + ((max_tiles + ng - 1) / ng) * (wpt - 1);
+            if (best < 0 || cost < best) {
+                best = cost;
+                p.wpt = wpt;
+            }
+        }
+        p.max_rt = 0;
+    } else {
+        if (row_tiles < 1) return p;
+        p.ctas = row_tiles < dev.sms ? row_tiles : dev.sms;
+        p.wpt = 1;
+        p.max_rt = (row_tiles + p.ctas - 1) / p.ctas;
+    }
+    const int half = dev.smem_per_sm / 2 - 1024;
+    const int budget = p.warps == kMWPaired && moeh_layout(p.warps, ents, kblocks, 2, p.max_rt).total <= half
+                           ? half
+                           : dev.max_smem_optin;
+    p.depth = 2;
+    while (p.depth < kMMaxDepth && moeh_layout(p.warps, ents, kblocks, p.depth + 1, p.max_rt).total <= budget)
+        ++p.depth;
+    p.smem = moeh_layout(p.warps, ents, kblocks, p.depth, p.max_rt).total;
+    if (p.smem > dev.max_smem_optin) p.ctas = 0;
+    return p;
+}
+
+}  // namespace
+
+bool moe_hmma_supports(int M, int topk, int64_t H, int64_t F, int64_t g) {
+    return g == 128 && M >= 1 && M <= 8 && topk >= 1 && M * topk <= kMoeHmmaMaxSlots &&
+           H % 128 == 0 && F % 128 == 0 && H >= 128 && F >= 128;
+}
+
+bool moe_hmma_fits(const DeviceInfo& dev, int M, int topk, int E, int64_t H, int64_t F) {
+    const int S = M * topk;
+    const long long d = E < S ? E : S;
+    return plan_moe_hmma(dev, 1, M, static_cast<int>(H / 128), d * (F / 8), 0).ctas > 0 &&
+           plan_moe_hmma(dev, 2, S, static_cast<int>(F / 128), 0, static_cast<int>(H / 16)).ctas > 0;
+}
+
+cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+    const int S = a.M * a.topk;
+    for (int phase = 1; phase <= 2; ++phase) {
+        MoeHK k{};
+        k.phase = phase;
+        k.ids = a.ids;
+        k.route_w = a.route_w;
+        k.M = a.M;
+        k.topk = a.topk;
+        k.E = a.E;
+        k.err = a.err;
+        k.h = a.h;
+        k.y = a.y;
+        long long tiles_max = 0;
+        int row_tiles = 0;
+        if (phase == 1) {
+            k.x = a.x;
+            k.wq_a = reinterpret_cast<const unsigned char*>(a.gate_wq);
+            k.scale_a = a.gate_scale;
+            k.zero_a = a.gate_zero;
+            k.wq_b = reinterpret_cast<const unsigned char*>(a.up_wq);
+            k.scale_b = a.up_scale;
+            k.zero_b = a.up_zero;
+            k.N = static_cast<int>(a.F);
+            k.K = static_cast<int>(a.H);
+            k.ents = a.M;
+            tiles_max = static_cast<long long>(a.E < S ? a.E : S) * (a.F / 8);
+        } else {
+            k.x = a.h;
+            k.wq_a = reinterpret_cast<const unsigned char*>(a.down_wq);
+            k.scale_a = a.down_scale;
+            k.zero_a = a.down_zero;
+            k.N = static_cast<int>(a.H);
+            k.K = static_cast<int>(a.F);
+            k.ents = S;
+            row_tiles = static_cast<int>(a.H / 16);
+        }
+        const MoeHPlan p = plan_moe_hmma(dev, phase, k.ents, k.K / 128, tiles_max, row_tiles);
+        if (p.ctas < 1) return cudaErrorInvalidConfiguration;
+        k.max_rt = p.max_rt;
+        k.wpt = p.wpt;
+        k.depth = p.depth;
+        const void* kern = p.warps == kMWWide ? reinterpret_cast<const void*>(k_moe_hmma<kMWWide>)
+                                              : reinterpret_cast<const void*>(k_moe_hmma<kMWPaired>);
+        cudaError_t e = ensure_dynamic_smem(kern, p.smem);
+        if (e != cudaSuccess) return e;
+        // the two launches ask for different shared memory: with the largest
+        // carve-out for both, a launch-2 CTA can be resident beside a
+        // launch-1 CTA (an SM whose carve-out must change waits to drain)
+        static bool carveout_set[2] = {false, false};
+        if (!carveout_set[phase - 1]) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
+            carveout_set[phase - 1] = true;
+        }
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(p.ctas);
+        cfg.blockDim = dim3(32 * p.warps);
+        cfg.dynamicSmemBytes = p.smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = p.warps == kMWWide ? cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWWide>, k)
+                               : cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWPaired>, k);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace w4a16
