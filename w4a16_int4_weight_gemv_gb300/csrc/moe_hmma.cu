@@ -662,9 +662,15 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
 struct MoeHPlan {
     int warps, ctas, wpt, depth, smem, max_rt;
 };
-// launch 1 runs 16-warp CTAs (twice the warps on an SM for its long unit
-// runs), launch 2 8-warp CTAs (short runs; two fit an SM)
-constexpr int kMPhase1Warps = kMWWide;
+// Warps per CTA.  Launch 1 runs 16-warp CTAs (twice the warps on an SM for
+// its long unit runs).  Launch 2 does too for up to 16 slots; with more, the
+// 16 x 512 k activations of every slot fill shared memory and 8-warp CTAs
+// are faster.  Measured, MoE chain of 64 experts (2304 x 1024), top-8:
+// 8/8 warps 20.1 / 34.4 / 56.6 us at M = 1 / 2 / 4; 16/8 18.4 / 27.0 / 49.3;
+// 16/16 16.4 / 23.3 / 54.0.
+int moe_warps(int phase, int slots) {
+    return (phase == 1 || slots <= 16) ? kMWWide : kMWPaired;
+}
 // CTAs, warps per tile and ring depth for one launch, at most one CTA per SM
 // (two fit where shared memory allows, for the next launch's).  Launch 1:
 // tiles_max (entry, pair) tiles, the split of K steps over warps that
@@ -673,7 +679,7 @@ constexpr int kMPhase1Warps = kMWWide;
 MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int kblocks, long long tiles_max,
                        int row_tiles) {
     MoeHPlan p{};
-    p.warps = phase == 1 ? kMPhase1Warps : kMWPaired;
+    p.warps = moe_warps(phase, ents);
     const int nsteps = (kblocks + 3) / 4;
     if (phase == 1) {
         if (tiles_max < 1) return p;
