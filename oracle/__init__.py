@@ -20,6 +20,15 @@ Parity status of each function (what pins it, in tests/test_oracle.py):
   swiglu             pinned: closed forms at 0 and large |v|, library silu
   moe_gemv, moe_ffn  pinned: one-hot routing reduces to a dense chain,
                      identical experts reduce to one chain, linearity in r
+
+The ~3-bit expert weights (``int3_oracle.c``: the format is this library's
+reading, stated in that file's header), pinned in tests/test_oracle_int3.py:
+  pack3 / unpack3    pinned: hand-derived chunk words, every code bit owning
+                     one distinct bit of its block, random round trip
+  dequant3, gemv3    pinned: equal to the INT4 oracle on the same codes (all
+                     codes 0..7 are INT4 codes), closed form, one-hot
+                     activations, fp64 library matmul
+  moe_ffn3           pinned: equal to the INT4 chain on the same codes
 """
 from __future__ import annotations
 
@@ -32,6 +41,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "w4a16_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "int3_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lock = threading.Lock()
@@ -41,12 +51,12 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the C oracle with gcc (portable flags: x86_64 and aarch64)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
-    stale = (not os.path.exists(_LIB_PATH)) or (
-        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    stale = (not os.path.exists(_LIB_PATH)) or any(
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(src) for src in _SRCS)
     if force or stale:
         tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
-               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+               "-ffp-contract=off"] + _SRCS + ["-o", tmp, "-lm"]
         # OpenMP only spreads oracle_gemv_parallel's rows over host threads;
         # without it that function runs on one thread
         if subprocess.run(cmd[:1] + ["-fopenmp"] + cmd[1:], capture_output=True).returncode != 0:
@@ -106,6 +116,12 @@ def _bind(lib):
                                     I, I, I, I, I, I]
     lib.oracle_moe_ffn.restype = ctypes.c_int
     lib.oracle_moe_ffn.argtypes = [P] * 17 + [I] * 6
+    lib.oracle3_pack.argtypes = [P, P, I, I]
+    lib.oracle3_unpack.argtypes = [P, P, I, I]
+    lib.oracle3_dequant.argtypes = [P, P, P, P, I, I, I]
+    lib.oracle3_gemv.argtypes = [P, P, P, P, P, I, I, I, I]
+    lib.oracle3_moe_ffn.restype = ctypes.c_int
+    lib.oracle3_moe_ffn.argtypes = [P] * 17 + [I] * 6
     return lib
 
 
@@ -284,6 +300,98 @@ def moe_ffn(x, ids, route_w, gate, up, down, g: int):
                             d.ctypes.data_as(ctypes.c_void_p),
                             out.ctypes.data_as(ctypes.c_void_p),
                             M, topk, E, H, F, g)
+    if rc != 0:
+        raise ValueError("expert id out of range")
+    return {"out": out, "gate": gate_bf, "up": up_bf, "h": h_bf, "d": d}
+
+
+# ---- ~3-bit expert weights (int3_oracle.c) ---------------------------------
+
+def int3_row_words(K: int) -> int:
+    """32-bit words per packed INT3 row of K codes (K % 128 == 0)."""
+    if K % 128:
+        raise ValueError("INT3 rows need K % 128 == 0")
+    return K // 128 * 12
+
+
+def pack3(codes) -> np.ndarray:
+    """codes uint8 [N, K] (0..7) -> INT3 words uint32 [N, 3K/32]."""
+    lib = _load()
+    codes, pc = _c(codes, np.uint8)
+    N, K = codes.shape
+    wq3 = np.empty((N, int3_row_words(K)), np.uint32)
+    lib.oracle3_pack(pc, wq3.ctypes.data_as(ctypes.c_void_p), N, K)
+    return wq3
+
+
+def unpack3(wq3, K: int) -> np.ndarray:
+    lib = _load()
+    wq3, pw = _c(wq3, np.uint32)
+    N = wq3.shape[0]
+    assert wq3.shape[1] == int3_row_words(K)
+    codes = np.empty((N, K), np.uint8)
+    lib.oracle3_unpack(pw, codes.ctypes.data_as(ctypes.c_void_p), N, K)
+    return codes
+
+
+def dequant3(wq3, scale, zero, g: int) -> np.ndarray:
+    """fp64 [N, K] = (code - zero) * scale for INT3 words [N, 3K/32]."""
+    lib = _load()
+    wq3, pw = _c(wq3, np.uint32)
+    scale, ps = _c(scale, np.uint16)
+    zero, pz = _c(zero, np.uint8)
+    N = wq3.shape[0]
+    K = wq3.shape[1] // 12 * 128
+    w = np.empty((N, K), np.float64)
+    lib.oracle3_dequant(pw, ps, pz, w.ctypes.data_as(ctypes.c_void_p), N, K, g)
+    return w
+
+
+def gemv3(x, wq3, scale, zero, g: int) -> np.ndarray:
+    """fp64 y [M, N] = x [M, K] (bf16 bits) times the INT3 matrix."""
+    lib = _load()
+    x, px = _c(x, np.uint16)
+    wq3, pw = _c(wq3, np.uint32)
+    scale, ps = _c(scale, np.uint16)
+    zero, pz = _c(zero, np.uint8)
+    M, K = x.shape
+    N = wq3.shape[0]
+    assert wq3.shape[1] == int3_row_words(K)
+    y = np.empty((M, N), np.float64)
+    lib.oracle3_gemv(px, pw, ps, pz, y.ctypes.data_as(ctypes.c_void_p), M, N, K, g)
+    return y
+
+
+def moe_ffn3(x, ids, route_w, gate, up, down, g: int):
+    """Routed SwiGLU FFN chain over INT3 experts: gate/up wq [E, F, 3H/32],
+    down wq [E, H, 3F/32]; the same result dict as moe_ffn."""
+    lib = _load()
+    x, px = _c(x, np.uint16)
+    ids, pi = _c(ids, np.int32)
+    route_w, pr = _c(route_w, np.float32)
+    arrs = []
+    ptrs = []
+    for (wq, s, z) in (gate, up, down):
+        for a, dt in ((wq, np.uint32), (s, np.uint16), (z, np.uint8)):
+            a, p = _c(a, dt)
+            arrs.append(a)
+            ptrs.append(p)
+    E, F, _ = arrs[0].shape
+    M, H = x.shape
+    assert arrs[0].shape[2] == int3_row_words(H) and arrs[6].shape == (E, H, int3_row_words(F))
+    topk = ids.shape[1]
+    gate_bf = np.empty((M, topk, F), np.uint16)
+    up_bf = np.empty((M, topk, F), np.uint16)
+    h_bf = np.empty((M, topk, F), np.uint16)
+    d = np.empty((M, topk, H), np.float64)
+    out = np.empty((M, H), np.float64)
+    rc = lib.oracle3_moe_ffn(px, pi, pr, *ptrs,
+                             gate_bf.ctypes.data_as(ctypes.c_void_p),
+                             up_bf.ctypes.data_as(ctypes.c_void_p),
+                             h_bf.ctypes.data_as(ctypes.c_void_p),
+                             d.ctypes.data_as(ctypes.c_void_p),
+                             out.ctypes.data_as(ctypes.c_void_p),
+                             M, topk, E, H, F, g)
     if rc != 0:
         raise ValueError("expert id out of range")
     return {"out": out, "gate": gate_bf, "up": up_bf, "h": h_bf, "d": d}

@@ -13,8 +13,10 @@ import pytest
 
 import oracle as oracle_mod
 from tests import test_oracle as pins
+from tests import test_oracle_int3 as pins3
 
 SRC = os.path.join(os.path.dirname(oracle_mod.__file__), "w4a16_oracle.c")
+SRC3 = os.path.join(os.path.dirname(oracle_mod.__file__), "int3_oracle.c")
 
 # (name, text to replace, replacement, how many occurrences must exist)
 MUTANTS = [
@@ -45,9 +47,24 @@ MUTANTS = [
 ]
 
 
+# slips in the ~3-bit format and its chain (int3_oracle.c)
+MUTANTS3 = [
+    ("int3_halves_swapped", [("16 * (r / 5) + 3 * (r % 5)", "16 * (1 - r / 5) + 3 * (r % 5)")]),
+    ("int3_field_width_4", [("16 * (r / 5) + 3 * (r % 5)", "16 * (r / 5) + 4 * (r % 5) - (r % 5 == 4)")]),
+    ("int3_leftover_bits_swapped", [("(i == 30) ? 15 : 31", "(i == 30) ? 31 : 15")]),
+    ("int3_leftover_bit_order", [("*word = first + j;", "*word = first + 2 - j;")]),
+    ("int3_chunk_stride", [("int64_t first = 12 * b + 3 * c;", "int64_t first = 12 * b + 3 * (3 - c);")]),
+    ("int3_words_of_a_chunk", [("*word = first + i / 10;", "*word = first + (i / 10 + 1) % 3;")]),
+    ("int3_zero_dropped", [("((double)oracle3_code(wq3, K, n, k) - z) * s", "((double)oracle3_code(wq3, K, n, k)) * s")]),
+    ("int3_group_index", [("scale[n * G + k / g]", "scale[n * G + (k / 128) % G]")]),
+    ("int3_expert_stride", [("wq_down + e * H * wf", "wq_down + e * H * wh")]),
+    ("int3_chain_route_weight", [("(double)route_w[t * topk + j] * acc", "(double)route_w[j] * acc")]),
+]
+
+
 def _pin_functions():
     out = []
-    for name, fn in sorted(vars(pins).items()):
+    for name, fn in sorted(list(vars(pins).items()) + list(vars(pins3).items()), key=lambda kv: kv[0]):
         if not name.startswith("test_") or not callable(fn):
             continue
         params = inspect.signature(fn).parameters
@@ -79,17 +96,23 @@ def _run_pins():
     return failed
 
 
-@pytest.mark.parametrize("name,edits", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_mutant(tmp_path, name, edits):
-    src = open(SRC).read()
-    for old, new in edits:
-        assert old in src, "mutation site not found: %r" % old
-        src = src.replace(old, new)
-    path = tmp_path / "mutant.c"
-    path.write_text(src)
+@pytest.mark.parametrize("name,edits,target",
+                         [(n, e, SRC) for n, e in MUTANTS] + [(n, e, SRC3) for n, e in MUTANTS3],
+                         ids=[m[0] for m in MUTANTS] + [m[0] for m in MUTANTS3])
+def test_pins_catch_mutant(tmp_path, name, edits, target):
+    sources = []
+    for i, path in enumerate((SRC, SRC3)):
+        src = open(path).read()
+        if path == target:
+            for old, new in edits:
+                assert old in src, "mutation site not found: %r" % old
+                src = src.replace(old, new)
+        out = tmp_path / ("mutant%d.c" % i)
+        out.write_text(src)
+        sources.append(str(out))
     lib = tmp_path / "libmutant.so"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-                    str(path), "-o", str(lib), "-lm"], check=True)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off"] + sources +
+                   ["-o", str(lib), "-lm"], check=True)
     oracle_mod.build()
     with oracle_mod.using_library(str(lib)):
         failed = _run_pins()

@@ -11,6 +11,11 @@ Recipe (the workload descriptions the library is measured on):
           weights are drawn directly as uniform uint32 words
   scale   bf16 ~ U[0.005, 0.02], one per (row, group)
   zero    uint8, either the constant 8 or uniform integers 6..10
+  int3    (~3-bit expert weights) codes uniform 0..7; every bit of a packed
+          INT3 chunk belongs to exactly one code, so packed words are again
+          uniform uint32 (3 K / 32 words per row); zero points the constant 4
+          or uniform integers 2..6 (the INT4 spread of five values around the
+          middle of the 3-bit range); scales as for INT4
   routing per token, top-k expert ids uniform without replacement, and
           route weights = softmax of top-k N(0, 1) logits (fp32)
 Every tensor has its own stream: numpy PCG64 seeded with (seed, tag).
@@ -61,6 +66,10 @@ def zeros(seed: int, N: int, G: int, mode: str = "const8", sub: int = 0) -> np.n
         return np.full((N, G), 8, np.uint8)
     if mode == "uniform6to10":
         return rng(seed, "zero", sub).integers(6, 11, size=(N, G), dtype=np.uint8)
+    if mode == "const4":
+        return np.full((N, G), 4, np.uint8)
+    if mode == "uniform2to6":
+        return rng(seed, "zero", sub).integers(2, 7, size=(N, G), dtype=np.uint8)
     raise ValueError(mode)
 
 
@@ -108,5 +117,39 @@ def moe_problem(M: int, E: int = 64, H: int = 2304, F: int = 1024, topk: int = 8
         "gate": expert_bank(seed, E, F, H, g, sub=1),
         "up": expert_bank(seed, E, F, H, g, sub=2),
         "down": expert_bank(seed, E, H, F, g, sub=3),
+        "M": M, "E": E, "H": H, "F": F, "topk": topk, "g": g,
+    }
+
+
+def packed_weights3(seed: int, N: int, K: int, sub: int = 0) -> np.ndarray:
+    """Uniform INT3 words [N, 3K/32] (uniform 3-bit codes)."""
+    assert K % 128 == 0
+    return rng(seed, "wq", sub).integers(0, 2**32, size=(N, 3 * K // 32), dtype=np.uint32)
+
+
+def codes3(seed: int, N: int, K: int, sub: int = 0) -> np.ndarray:
+    return rng(seed, "codes", sub).integers(0, 8, size=(N, K), dtype=np.uint8)
+
+
+def expert_bank3(seed: int, E: int, N: int, K: int, g: int = 128,
+                 zero_mode: str = "uniform2to6", sub: int = 0):
+    """E stacked INT3 expert matrices: wq [E,N,3K/32], scale/zero [E,N,K/g]."""
+    G = K // g
+    wq = packed_weights3(seed, E * N, K, sub).reshape(E, N, 3 * K // 32)
+    s = scales(seed, E * N, G, sub).reshape(E, N, G)
+    z = zeros(seed, E * N, G, zero_mode, sub).reshape(E, N, G)
+    return wq, s, z
+
+
+def moe_problem3(M: int, E: int = 64, H: int = 2304, F: int = 1024, topk: int = 8,
+                 g: int = 128, seed: int = 0) -> dict:
+    """Routed SwiGLU FFN over INT3 experts (shapes as moe_problem)."""
+    ids, route_w = routing(seed, M, topk, E)
+    return {
+        "x": activations(seed, (M, H)),
+        "ids": ids, "route_w": route_w,
+        "gate": expert_bank3(seed, E, F, H, g, sub=1),
+        "up": expert_bank3(seed, E, F, H, g, sub=2),
+        "down": expert_bank3(seed, E, H, F, g, sub=3),
         "M": M, "E": E, "H": H, "F": F, "topk": topk, "g": g,
     }
