@@ -48,6 +48,11 @@ def algo_bytes(M, N, K, g):
     return N * K // 2 + N * (K // g) * 2 + M * K * 2
 
 
+def algo_bytes3(M, N, K, g):
+    """The same for INT3 (~3-bit) weights: 3 bits per weight."""
+    return N * K * 3 // 8 + N * (K // g) * 2 + M * K * 2
+
+
 def all_bytes(M, N, K, g, out_bytes=2):
     return algo_bytes(M, N, K, g) + N * (K // g) + M * N * out_bytes
 
@@ -319,29 +324,35 @@ def gpu_gemv_gbs(torch, w, M, N, K, g, zmode, l2, steps, warmup, out_dtype=None,
     return t
 
 
-def moe_chain_time(torch, w, M, steps, warmup, l2, fused=True):
+def moe_chain_time(torch, w, M, steps, warmup, l2, fused=True, bits=4):
     """Routed SwiGLU expert chain (64 experts, gate/up [1024, 2304], down
     [2304, 1024], top-8) over rotated expert banks; seconds per chain and
-    the distinct-expert weight bytes it streams."""
+    the distinct-expert weight bytes it streams.  bits=3: INT3 (~3-bit)
+    expert banks through w3a16_moe_ffn."""
     from w4a16_int4_weight_gemv_gb300 import synth
-    per_bank = 64 * (2 * 1024 * 2304 + 2304 * 1024) * (0.5 + 2.0 / 128)
+    per_bank = 64 * (2 * 1024 * 2304 + 2304 * 1024) * (bits / 8.0 + 2.0 / 128)
     R = max(2, int(math.ceil(2.0 * l2 / per_bank)))
     banks = []
     byts = []
+    ab = algo_bytes if bits == 4 else algo_bytes3
     for r in range(R):
-        p = synth.moe_problem(M=M, E=64, H=2304, F=1024, topk=8, g=128, seed=r)
+        gen = synth.moe_problem if bits == 4 else synth.moe_problem3
+        p = gen(M=M, E=64, H=2304, F=1024, topk=8, g=128, seed=r)
         banks.append(dict(x=_dev(p["x"], torch), ids=_dev(p["ids"], torch),
                           r=_dev(p["route_w"], torch),
                           gate=tuple(_dev(a, torch) for a in p["gate"]),
                           up=tuple(_dev(a, torch) for a in p["up"]),
                           down=tuple(_dev(a, torch) for a in p["down"])))
         distinct = len(np.unique(p["ids"]))
-        byts.append(distinct * (2 * algo_bytes(0, 1024, 2304, 128) + algo_bytes(0, 2304, 1024, 128))
+        byts.append(distinct * (2 * ab(0, 1024, 2304, 128) + ab(0, 2304, 1024, 128))
                     + 2 * M * 2304 * 2 + M * 8 * 1024 * 2)
 
     def step(i):
         b = banks[i % R]
-        w.moe_ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128, fused=fused)
+        if bits == 3:
+            w.w3a16_moe_ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128)
+        else:
+            w.moe_ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128, fused=fused)
 
     t = time_steps(torch, step, R, steps, warmup)
     return t, float(np.mean(byts))

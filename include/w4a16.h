@@ -114,6 +114,40 @@ W4A16_API w4a16_status int4_dequant(const uint32_t* wq, const uint16_t* scale, c
                           void* stream);
 
 /*
+ * ~3-bit expert weights.  The README's hardware-requirements paragraph says
+ * that fitting a 24 GB card needs the expert weights near three bits and
+ * gives no format; this library's INT3 format (exactly three bits per code):
+ *   codes 0..7, W[n][k] = (code - zero[n][k/g]) * scale[n][k/g] with the bf16
+ *   scale and uint8 zero point of the INT4 path;
+ *   a row of K codes (K % 128 == 0) is 3K/32 uint32 words; the 32 codes
+ *   k = 32j .. 32j + 31 of a row (a chunk) are words 3j, 3j + 1, 3j + 2;
+ *   code i < 30 of a chunk is the 3-bit field (lowest bit first) of word
+ *   3j + i/10 at bit 16 * ((i % 10) / 5) + 3 * (i % 5): five codes in bits
+ *   0..14 of each 16-bit half;
+ *   bit b (b = 0, 1, 2) of code 30 is bit 15, and of code 31 bit 31, of word
+ *   3j + b.
+ * Uniform codes make uniform words: the 96 bits of a chunk hold its 32 codes.
+ */
+
+/*
+ * int3_pack -- pack 3-bit codes into the INT3 layout above.
+ *   codes  uint8 [N][K], each 0..7 (only the low three bits are used)
+ *   wq3    uint32 [N][3K/32] output
+ * Requires K % 128 == 0.  Bit-exact integer work.
+ */
+W4A16_API w4a16_status int3_pack(const uint8_t* codes, uint32_t* wq3, int64_t N, int64_t K, void* stream);
+
+/*
+ * int3_dequant -- expand INT3 weights to W[n][k] = (code - zero) * scale,
+ * as int4_dequant does for INT4 (bf16: the exact value rounded to
+ * nearest-even; fp32: exact).
+ * Requires K % 128 == 0, g % 32 == 0, K % g == 0.
+ */
+W4A16_API w4a16_status int3_dequant(const uint32_t* wq3, const uint16_t* scale, const uint8_t* zero,
+                                    void* w, w4a16_out_dtype out_dtype, int64_t N, int64_t K, int64_t g,
+                                    void* stream);
+
+/*
  * w4a16_gemv_workspace_bytes -- device workspace w4a16_gemv needs for this
  * shape.  The dense GEMV needs none (0): split-K partials are combined
  * on chip through thread-block-cluster shared memory.  Kept so callers can
@@ -303,6 +337,39 @@ W4A16_API w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_id
                                      const uint16_t* gate_scale, const uint8_t* gate_zero,
                                      const uint32_t* up_wq, const uint16_t* up_scale,
                                      const uint8_t* up_zero, const uint32_t* down_wq,
+                                     const uint16_t* down_scale, const uint8_t* down_zero,
+                                     uint16_t* y, int M, int topk, int E, int64_t H, int64_t F,
+                                     int64_t g, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
+ * w3a16_moe_ffn_workspace_bytes -- workspace w3a16_moe_ffn needs: the bf16
+ * intermediate h [M][topk][F], rounded up to 256 bytes.  Its contents need
+ * no initialisation.
+ */
+W4A16_API size_t w3a16_moe_ffn_workspace_bytes(int M, int topk, int64_t H, int64_t F);
+
+/*
+ * w3a16_moe_ffn -- the routed SwiGLU expert FFN of w4a16_moe_ffn over INT3
+ * expert banks (the ~3-bit expert weights above):
+ *   y[t] = bf16(sum_j route_w[t][j] * (W^down_e h[t][j])),
+ *   h[t][j] = bf16(silu(bf16(W^gate_e x[t])) * bf16(W^up_e x[t])), e = ids[t][j],
+ * in two launches on the fp16 warp-MMA path (gate/up with the SwiGLU in the
+ * epilogue, then the down products and routed sums).
+ *   x: bf16 [M][H]; expert_ids: int32 [M][topk]; route_w: fp32 [M][topk];
+ *   gate, up: wq3 [E][F][3H/32], scale and zero [E][F][H/g];
+ *   down: wq3 [E][H][3F/32], scale and zero [E][H][F/g]; y: bf16 [M][H];
+ *   workspace: >= w3a16_moe_ffn_workspace_bytes(M, topk, H, F) bytes,
+ *   caller-owned, 16-byte aligned (W4A16_ERR_WORKSPACE if smaller).
+ * Limits: 1 <= M <= 8, M * topk <= 32, g == 128, H and F multiples of 128
+ * (W4A16_ERR_UNSUPPORTED otherwise).  Expert ids outside [0, E) are skipped
+ * and flagged with W4A16_DEVERR_EXPERT_ID.
+ */
+W4A16_API w4a16_status w3a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids,
+                                     const float* route_w, const uint32_t* gate_wq3,
+                                     const uint16_t* gate_scale, const uint8_t* gate_zero,
+                                     const uint32_t* up_wq3, const uint16_t* up_scale,
+                                     const uint8_t* up_zero, const uint32_t* down_wq3,
                                      const uint16_t* down_scale, const uint8_t* down_zero,
                                      uint16_t* y, int M, int topk, int E, int64_t H, int64_t F,
                                      int64_t g, void* workspace, size_t workspace_bytes,

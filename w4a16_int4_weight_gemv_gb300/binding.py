@@ -95,6 +95,14 @@ def load_library():
     lib.w4a16_host_memory_mapped.argtypes = [P]
     lib.w4a16_device_error.restype = I32
     lib.w4a16_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), I32, P]
+    lib.int3_pack.restype = I32
+    lib.int3_pack.argtypes = [P, P, I64, I64, P]
+    lib.int3_dequant.restype = I32
+    lib.int3_dequant.argtypes = [P, P, P, P, I32, I64, I64, I64, P]
+    lib.w3a16_moe_ffn_workspace_bytes.restype = SZ
+    lib.w3a16_moe_ffn_workspace_bytes.argtypes = [I32, I32, I64, I64]
+    lib.w3a16_moe_ffn.restype = I32
+    lib.w3a16_moe_ffn.argtypes = [P] * 13 + [I32, I32, I32, I64, I64, I64, P, SZ, P]
     _lib = lib
     return lib
 
@@ -175,6 +183,35 @@ def int4_dequant(wq, scale, zero, g: int, out_dtype=torch.bfloat16, out=None, st
     kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(load_library().int4_dequant(_ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), kind,
                                        N, K, g, _stream(stream, wq.get_device())), "int4_dequant")
+    return out
+
+
+def int3_pack(codes: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """codes uint8 [N, K] (0..7, K % 128 == 0) -> INT3 words int32 [N, 3K/32]
+    (uint32 bit patterns; the format is stated in include/w4a16.h)."""
+    _need(codes, "codes", _U8)
+    N, K = codes.shape
+    if out is None:
+        out = torch.empty((N, 3 * K // 32), dtype=torch.int32, device=codes.device)
+    _need(out, "out", _U32, (N, 3 * K // 32))
+    _check(load_library().int3_pack(_ptr(codes), _ptr(out), N, K, _stream(stream, codes.get_device())),
+           "int3_pack")
+    return out
+
+
+def int3_dequant(wq3, scale, zero, g: int, out_dtype=torch.bfloat16, out=None, stream=None):
+    """INT3 words [N, 3K/32] -> W [N, K] = (code - zero) * scale, bf16 or fp32."""
+    _need(wq3, "wq3", _U32)
+    N, W3 = wq3.shape
+    K = W3 // 3 * 32
+    _need(scale, "scale", _BF16, (N, K // g))
+    _need(zero, "zero", _U8, (N, K // g))
+    if out is None:
+        out = torch.empty((N, K), dtype=out_dtype, device=wq3.device)
+    _need(out, "out", (torch.bfloat16, torch.float32), (N, K))
+    kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(load_library().int3_dequant(_ptr(wq3), _ptr(scale), _ptr(zero), _ptr(out), kind,
+                                       N, K, g, _stream(stream, wq3.get_device())), "int3_dequant")
     return out
 
 
@@ -369,8 +406,9 @@ def moe_ffn(x, expert_ids, route_w, gate, up, down, g: int, stream=None,
     """Routed SwiGLU FFN for M tokens.  gate/up/down are (wq, scale, zero)
     triples with gate/up [E, F, H] and down [E, H, F].  Returns bf16 [M, H].
 
-    fused (default): w4a16_moe_ffn -- gate and up in one launch, SwiGLU formed
-    while the down product stages its activations, then the routed sum.
+    fused (default): w4a16_moe_ffn -- two launches: the gate and up products
+    with the SwiGLU formed in their epilogue, then the down products and the
+    routed sums (older expert kernels outside the fp16 path's limits).
     fused=False: the same chain from the single-purpose calls (one
     expert-indexed GEMV each for gate and up, w4a16_swiglu, the down GEMV
     with the routed sum)."""
@@ -397,6 +435,28 @@ def moe_ffn(x, expert_ids, route_w, gate, up, down, g: int, stream=None,
     h = w4a16_swiglu(g_out.view(M * topk, F), u_out.view(M * topk, F), stream=stream)
     return w4a16_moe_gemv(h.view(M, topk, F), expert_ids, *down, g, route_w=route_w,
                           x_per_slot=True, stream=stream)
+
+
+def w3a16_moe_ffn(x, expert_ids, route_w, gate, up, down, g: int, stream=None) -> torch.Tensor:
+    """Routed SwiGLU FFN over INT3 (~3-bit) expert banks.  gate/up/down are
+    (wq3, scale, zero) triples: gate/up wq3 [E, F, 3H/32], down [E, H, 3F/32],
+    scale/zero as for INT4.  Returns bf16 [M, H]."""
+    M, topk = expert_ids.shape
+    _need(x, "x", _BF16)
+    _need(expert_ids, "expert_ids", (torch.int32,))
+    _need(route_w, "route_w", (torch.float32,), (M, topk))
+    (gw, gs, gz), (uw, us, uz), (dw, ds, dz) = gate, up, down
+    E, F, H3 = gw.shape
+    H = H3 // 3 * 32
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    lib = load_library()
+    nbytes = int(lib.w3a16_moe_ffn_workspace_bytes(M, topk, H, F))
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    _check(lib.w3a16_moe_ffn(_ptr(x), _ptr(expert_ids), _ptr(route_w), _ptr(gw), _ptr(gs),
+                             _ptr(gz), _ptr(uw), _ptr(us), _ptr(uz), _ptr(dw), _ptr(ds),
+                             _ptr(dz), _ptr(y), M, topk, E, H, F, g, _ptr(ws), nbytes,
+                             _stream(stream, x.get_device())), "w3a16_moe_ffn")
+    return y
 
 
 load_library()

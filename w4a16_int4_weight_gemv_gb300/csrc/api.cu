@@ -287,6 +287,34 @@ w4a16_status int4_dequant(const uint32_t* wq, const uint16_t* scale, const uint8
                                     g, dev->info.sms, static_cast<cudaStream_t>(stream)));
 }
 
+w4a16_status int3_pack(const uint8_t* codes, uint32_t* wq3, int64_t N, int64_t K, void* stream) {
+    if (!codes || !wq3) return W4A16_ERR_NULL;
+    if (N < 0 || K < 0 || K % 128 != 0) return W4A16_ERR_SHAPE;
+    if (!aligned16(codes) || !aligned16(wq3)) return W4A16_ERR_ALIGN;
+    if (N == 0 || K == 0) return W4A16_OK;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    return from_cuda(launch_pack3(codes, wq3, N, K, dev->info.sms, static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status int3_dequant(const uint32_t* wq3, const uint16_t* scale, const uint8_t* zero, void* w,
+                          w4a16_out_dtype out_dtype, int64_t N, int64_t K, int64_t g,
+                          void* stream) {
+    if (!wq3 || !scale || !zero || !w) return W4A16_ERR_NULL;
+    if (N < 0 || K < 0 || g < 32 || K % 128 != 0 || g % 32 != 0 || K % g != 0)
+        return W4A16_ERR_SHAPE;
+    if (out_dtype != W4A16_OUT_BF16 && out_dtype != W4A16_OUT_F32) return W4A16_ERR_UNSUPPORTED;
+    if (!aligned16(wq3) || !aligned16(scale) || !aligned16(zero) || !aligned16(w))
+        return W4A16_ERR_ALIGN;
+    if (N == 0 || K == 0) return W4A16_OK;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    return from_cuda(launch_dequant3(wq3, scale, zero, w, out_dtype == W4A16_OUT_F32 ? 1 : 0, N, K,
+                                     g, dev->info.sms, static_cast<cudaStream_t>(stream)));
+}
+
 size_t w4a16_gemv_workspace_bytes(int M, int64_t N, int64_t K, int64_t g) {
     (void)M;
     (void)N;
@@ -434,7 +462,7 @@ w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const f
     float* part = reinterpret_cast<float*>(ws + 2 * align256(S * F * 2));
     unsigned* counters = reinterpret_cast<unsigned*>(ws + 2 * align256(S * F * 2) + align256(S * H * 4));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (moe_hmma_supports(M, topk, H, F, g) && moe_hmma_fits(dev->info, M, topk, E, H, F)) {
+    if (moe_hmma_supports(M, topk, H, F, g) && moe_hmma_fits(dev->info, M, topk, E, H, F, 4)) {
         // the fp16 warp-MMA path: h = SwiGLU of the gate/up products in the
         // first launch's epilogue (into the gate-output part of the
         // workspace), the down products and routed sums in the second (in
@@ -442,7 +470,7 @@ w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const f
         MoeHmmaArgs m{x,     expert_ids, route_w, gate_wq, gate_scale, gate_zero,
                       up_wq, up_scale,   up_zero, down_wq, down_scale, down_zero,
                       g_out, y,          M,       topk,    E,          H,
-                      F,     dev->err};
+                      F,     dev->err,   4};
         return from_cuda(launch_moe_hmma(m, dev->info, s));
     }
     // gate and up products of every slot: one launch over both banks
@@ -484,6 +512,44 @@ w4a16_status w4a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const f
     d.g = static_cast<int>(g);
     d.err = dev->err;
     return from_cuda(launch_moe(d, dev->info, s));
+}
+
+size_t w3a16_moe_ffn_workspace_bytes(int M, int topk, int64_t H, int64_t F) {
+    (void)H;
+    if (M < 1 || topk < 1 || F < 1) return 0;
+    return align256(static_cast<size_t>(M) * static_cast<size_t>(topk) * static_cast<size_t>(F) * 2);
+}
+
+w4a16_status w3a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const float* route_w,
+                           const uint32_t* gate_wq3, const uint16_t* gate_scale,
+                           const uint8_t* gate_zero, const uint32_t* up_wq3,
+                           const uint16_t* up_scale, const uint8_t* up_zero,
+                           const uint32_t* down_wq3, const uint16_t* down_scale,
+                           const uint8_t* down_zero, uint16_t* y, int M, int topk, int E,
+                           int64_t H, int64_t F, int64_t g, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    if (!x || !expert_ids || !route_w || !gate_wq3 || !gate_scale || !gate_zero || !up_wq3 ||
+        !up_scale || !up_zero || !down_wq3 || !down_scale || !down_zero || !y)
+        return W4A16_ERR_NULL;
+    if (M < 1 || topk < 1 || E < 1 || H < 128 || F < 128 || g < 32) return W4A16_ERR_SHAPE;
+    if (g % 32 != 0 || H % 128 != 0 || F % 128 != 0 || H % g != 0 || F % g != 0) return W4A16_ERR_SHAPE;
+    if (!moe_hmma_supports(M, topk, H, F, g) || H > 65536 || F > 65536) return W4A16_ERR_UNSUPPORTED;
+    const void* ptrs[] = {x,        expert_ids, route_w,  gate_wq3,   gate_scale, gate_zero, up_wq3,
+                          up_scale, up_zero,    down_wq3, down_scale, down_zero,  y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return W4A16_ERR_ALIGN;
+    const size_t need = w3a16_moe_ffn_workspace_bytes(M, topk, H, F);
+    if (!workspace || workspace_bytes < need) return W4A16_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return W4A16_ERR_ALIGN;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    if (!moe_hmma_fits(dev->info, M, topk, E, H, F, 3)) return W4A16_ERR_UNSUPPORTED;
+    MoeHmmaArgs m{x,      expert_ids, route_w, gate_wq3, gate_scale, gate_zero,
+                  up_wq3, up_scale,   up_zero, down_wq3, down_scale, down_zero,
+                  static_cast<uint16_t*>(workspace), y, M, topk, E, H,
+                  F,      dev->err,   3};
+    return from_cuda(launch_moe_hmma(m, dev->info, static_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_swiglu(const uint16_t* gate, const uint16_t* up, int64_t ld_in, uint16_t* h,

@@ -280,7 +280,8 @@ cudaError_t launch_gemv_hmma(const GemvArgs& a, const GemvPlan& p, cudaStream_t 
 
 // Routed SwiGLU expert FFN on the fp16 warp-MMA path (moe_hmma.cu): 1..8
 // tokens, M * topk <= 32 slots, g == 128, H and F multiples of 128.  h is
-// the bf16 [M*topk][F] intermediate.
+// the bf16 [M*topk][F] intermediate.  bits: 4 (INT4 banks, K/8 words per
+// row) or 3 (INT3 banks, 3K/32 words per row).
 constexpr int kMoeHmmaMaxSlots = 32;
 struct MoeHmmaArgs {
     const uint16_t* x;
@@ -300,9 +301,10 @@ struct MoeHmmaArgs {
     int M, topk, E;
     int64_t H, F;
     uint32_t* err;
+    int bits;
 };
 bool moe_hmma_supports(int M, int topk, int64_t H, int64_t F, int64_t g);
-bool moe_hmma_fits(const DeviceInfo& dev, int M, int topk, int E, int64_t H, int64_t F);
+bool moe_hmma_fits(const DeviceInfo& dev, int M, int topk, int E, int64_t H, int64_t F, int bits);
 cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStream_t s);
 
 // One stacked expert bank: wq [E][N][K/8], scale and zero [E][N][K/g], and
@@ -351,5 +353,11 @@ cudaError_t launch_dequant(const uint32_t* wq, const uint16_t* scale, const uint
                            cudaStream_t s);
 cudaError_t launch_swiglu(const uint16_t* gate, const uint16_t* up, int64_t ld_in, uint16_t* h,
                           int64_t ld_out, int64_t rows, int64_t N, int sms, cudaStream_t s);
+// INT3 codes <-> words (K % 128 == 0; 3K/32 words per row) and dequant
+cudaError_t launch_pack3(const uint8_t* codes, uint32_t* wq3, int64_t N, int64_t K, int sms,
+                         cudaStream_t s);
+cudaError_t launch_dequant3(const uint32_t* wq3, const uint16_t* scale, const uint8_t* zero,
+                            void* w, int out_f32, int64_t N, int64_t K, int64_t g, int sms,
+                            cudaStream_t s);
 
 }  // namespace w4a16

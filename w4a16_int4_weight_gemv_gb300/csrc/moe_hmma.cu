@@ -39,6 +39,21 @@
 // Launch.  Launch 2 reads the routing and its weights before its
 // grid-dependency wait; launch 1 signals its dependents only after its own
 // wait, so everything launch 2 reads early was complete before launch 1 ran.
+//
+// ~3-bit experts (BITS == 3; the README's hardware-requirements paragraph
+// asks for expert weights near three bits, the INT3 format is this
+// library's: a chunk of 32 codes in three words, five 3-bit fields in each
+// 16-bit half at bits 0, 3, 6, 9, 12, codes 30 and 31 in the spare bits 15
+// and 31).  The same kernel with another unit format: a row of a unit is
+// 192 bytes (4 groups x 48), staged at a 208-byte pitch so that the 32-bit
+// reads of 8 rows x 4 chunks hit 32 different banks; lane (g, c) reads
+// chunk c of each 128-k block of rows g and g + 8 (three words each) and
+// makes the 16 fp16 pairs of a row with one LOP3 each -- fields at bits 0,
+// 3, 6 of a word give 1024 + q, 1024 + 8q, 1024 + 64q, the same masks on
+// the word shifted right by 9 give the fields at 9 and 12, and three LOP3s
+// gather the spare bits into {1024 + q30, 1024 + q31}: 24 ALU operations per
+// 32 codes.  B holds x / 1, x / 8 or x / 64 to match; the eight MMAs of a
+// block take pairs (2m, 2m + 1) as their two k halves.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -51,10 +66,16 @@ namespace {
 // warps per CTA: 8 (two CTAs fit an SM) or 16 (launch 1 with long runs)
 constexpr int kMWPaired = 8;
 constexpr int kMWWide = 16;
-constexpr int kMZero = kHmmaUnitBytes;          // 16 rows x 8 zero-point bytes
-constexpr int kMScale = kHmmaUnitBytes + 128;   // 16 rows x 16 scale bytes
-constexpr int kMStage = kHmmaUnitBytes + 384;
 constexpr int kMMaxDepth = 4;
+// A stage holds one unit (16 rows x 512 k): the weight rows at m_pitch
+// bytes each, then 16 rows x 8 zero-point bytes and 16 rows x 16 scale
+// bytes.  INT4: 256-byte rows, 16-byte chunks XOR-swizzled by the row; INT3:
+// 192-byte rows at a 208-byte pitch.
+__host__ __device__ constexpr int m_pitch(int bits) { return bits == 4 ? kHmmaRowPitch : 208; }
+__host__ __device__ constexpr int m_zero(int bits) { return 16 * m_pitch(bits); }
+__host__ __device__ constexpr int m_scale(int bits) { return m_zero(bits) + 128; }
+__host__ __device__ constexpr int m_stage(int bits) { return m_zero(bits) + 384; }
+static_assert(m_zero(4) == kHmmaUnitBytes && m_stage(3) % 16 == 0, "stage layout");
 
 struct MoeHK {
     int phase;                 // 1: gate/up -> h; 2: down -> routed sums
@@ -79,11 +100,12 @@ struct MoeHK {
 struct MoeHLayout {
     int ring, bfrag, csum, red, bars, ids, ent_e, ent_n, ent_col, ybuf, nent, total;
 };
-__host__ __device__ inline MoeHLayout moeh_layout(int W, int ents, int kblocks, int depth, int max_rt) {
+__host__ __device__ inline MoeHLayout moeh_layout(int W, int ents, int kblocks, int depth, int max_rt,
+                                                  int bits) {
     MoeHLayout L;
     int off = 0;
     L.ring = off;  // [warp][depth] stages
-    off += W * depth * kMStage;
+    off += W * depth * m_stage(bits);
     L.bfrag = off;  // [block][piece][column entity][lane % 4] x 16 bytes
     off += kblocks * 4 * ents * 4 * 16;
     L.csum = off;  // [block][column entity] {1024 sum B, sum x', 2^-sh, 0}
@@ -118,9 +140,48 @@ __device__ __forceinline__ void cp_async_4_fill(void* dst, const void* src, int 
 
 __device__ __forceinline__ int clamp4(long long v) { return v < 0 ? 0 : (v > 4 ? 4 : static_cast<int>(v)); }
 
-template <int W>
+// 3-bit pairs: (a & MASK) | C by one LOP3
+template <uint32_t MASK, uint32_t C>
+__device__ __forceinline__ uint32_t and_or(uint32_t a) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "n"(C));
+    return d;
+}
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or_r(uint32_t a, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+    return d;
+}
+// The 16 fp16 pairs of one INT3 chunk (words w0, w1, w2).  Pair P < 15:
+// word P / 5, field f = P % 5, codes 10 (P / 5) + f (low half) and
+// 10 (P / 5) + 5 + f (high half), times 1, 8, 64, 1, 8 for f = 0..4; pair 15:
+// codes 30 and 31, times 1.  Each value is 1024 + code * factor.
+__device__ __forceinline__ void int3_pairs(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t (&p)[16]) {
+    constexpr uint32_t E = 0x64006400u;
+    const uint32_t w[3] = {w0, w1, w2};
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const uint32_t t = w[i] >> 9;
+        p[5 * i + 0] = and_or<0x00070007u, E>(w[i]);
+        p[5 * i + 1] = and_or<0x00380038u, E>(w[i]);
+        p[5 * i + 2] = and_or<0x01C001C0u, E>(w[i]);
+        p[5 * i + 3] = and_or<0x00070007u, E>(t);
+        p[5 * i + 4] = and_or<0x00380038u, E>(t);
+    }
+    p[15] = and_or_r<0x00040004u>(w2 >> 13, and_or_r<0x00020002u>(w1 >> 14, and_or<0x00010001u, E>(w0 >> 15)));
+}
+// x' factor of pair P (the inverse of its code factor) and its two codes
+__host__ __device__ constexpr int int3_pair_shift(int P) {  // log2 of the code factor
+    return P == 15 ? 0 : ((P % 5) == 1 || (P % 5) == 4) ? 3 : (P % 5) == 2 ? 6 : 0;
+}
+__host__ __device__ constexpr int int3_pair_lo(int P) { return P == 15 ? 30 : 10 * (P / 5) + P % 5; }
+
+template <int W, int BITS>
 __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(const MoeHK a) {
     constexpr int T = 32 * W;
+    constexpr int kPitch = m_pitch(BITS), kStage = m_stage(BITS);
+    constexpr int kZero = m_zero(BITS), kScale = m_scale(BITS);
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -138,8 +199,8 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
 
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw + 127u) & ~127u) - raw);
-    const MoeHLayout L = moeh_layout(W, ENTS, kblocks, D, a.max_rt);
-    unsigned char* ring = base + L.ring + warp * D * kMStage;
+    const MoeHLayout L = moeh_layout(W, ENTS, kblocks, D, a.max_rt, BITS);
+    unsigned char* ring = base + L.ring + warp * D * kStage;
     uint4* bfrag = reinterpret_cast<uint4*>(base + L.bfrag);
     float4* csum = reinterpret_cast<float4*>(base + L.csum);
     float4* red = reinterpret_cast<float4*>(base + L.red);
@@ -223,8 +284,11 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
     };
     if (!p1) set_range(*s_nent);
 
-    const size_t row_bytes = static_cast<size_t>(a.K) >> 1;
+    const size_t row_bytes = BITS == 4 ? static_cast<size_t>(a.K) >> 1 : static_cast<size_t>(a.K) / 128 * 48;
     const int sw_h = lane >> 4, sw_c = ((lane & 15) ^ sw_h) << 4;
+    // INT3 copies: lanes 0..23 copy 16-byte chunk col3 of row 2 i + h3
+    const int h3 = lane >= 12 ? 1 : 0;
+    const int col3 = lane - 12 * h3;
     const int dl0 = sw_h * kHmmaRowPitch + sw_c, dl1 = sw_h * kHmmaRowPitch + (sw_c ^ 32);
     const int dl2 = sw_h * kHmmaRowPitch + (sw_c ^ 64), dl3 = sw_h * kHmmaRowPitch + (sw_c ^ 96);
     auto dst_off = [&](int i) {
@@ -294,7 +358,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         const unsigned char *w0, *w8;
         long long z0, z8;
         tile_rows(i_o, i_i, w0, w8, z0, z8);
-        const size_t lane_b = sw_h * row_bytes + (lane & 15) * 16;
+        const size_t lane_b = BITS == 4 ? sw_h * row_bytes + (lane & 15) * 16 : h3 * row_bytes + col3 * 16;
         i_w0 = w0 + lane_b;
         i_w8 = w8 + lane_b;
         i_zg = (rr < 8 ? z0 + rr : z8 + (rr - 8)) * G;
@@ -303,13 +367,24 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         if (i_u < nu) {
             const int step = i_step;
             const int nbs = min(4, kblocks - 4 * step);
-            unsigned char* stage = ring + i_slot * kMStage;
-            if ((lane & 15) < nbs * 4) {
+            unsigned char* stage = ring + i_slot * kStage;
+            if constexpr (BITS == 4) {
+                if ((lane & 15) < nbs * 4) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const unsigned char* src =
-                        (i < 4 ? i_w0 + 2 * i * row_bytes : i_w8 + (2 * i - 8) * row_bytes) + step * 256;
-                    cp_async_16(stage + dst_off(i), src);
+                    for (int i = 0; i < 8; ++i) {
+                        const unsigned char* src =
+                            (i < 4 ? i_w0 + 2 * i * row_bytes : i_w8 + (2 * i - 8) * row_bytes) + step * 256;
+                        cp_async_16(stage + dst_off(i), src);
+                    }
+                }
+            } else {
+                if (lane < 24 && col3 < nbs * 3) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const unsigned char* src =
+                            (i < 4 ? i_w0 + 2 * i * row_bytes : i_w8 + (2 * i - 8) * row_bytes) + step * 192;
+                        cp_async_16(stage + (2 * i + h3) * kPitch + col3 * 16, src);
+                    }
                 }
             }
             // zero points (lanes 0..15) or scales (16..31) of tile row rr,
@@ -318,7 +393,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
             if (zlane) {
                 const uint8_t* zb = bank_b ? a.zero_b : a.zero_a;
                 const long long w4 = gi & ~3LL;
-                unsigned char* dz = stage + kMZero + rr * 8;
+                unsigned char* dz = stage + kZero + rr * 8;
                 if (w4 + 8 <= zend) {
                     cp_async_4(dz, zb + w4);
                     cp_async_4(dz + 4, zb + w4 + 4);
@@ -331,7 +406,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
                 const unsigned char* sb =
                     reinterpret_cast<const unsigned char*>(bank_b ? a.scale_b : a.scale_a);
                 const long long b = gi * 2, w4 = b & ~3LL, send = zend * 2;
-                unsigned char* ds = stage + kMScale + rr * 16;
+                unsigned char* ds = stage + kScale + rr * 16;
                 if (w4 + 12 <= send) {
                     cp_async_4(ds, sb + w4);
                     cp_async_4(ds + 4, sb + w4 + 4);
@@ -366,7 +441,21 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
     grid_dependency_wait();
     if (p1) grid_dependents_launch();
 
-    {
+    // launch 1 routes while its first activation loads are in flight, then
+    // requests its first units
+    auto start_launch1 = [&]() {
+        if (!p1) return;
+        route();
+        __syncthreads();
+        set_range(*s_nent);
+        set_units();
+        if (nu > 0) {
+            start_cursor(i_o, i_i);
+            producer_tile();
+        }
+        for (int k = 0; k < D; ++k) issue_next();
+    };
+    if constexpr (BITS == 4) {
         // B columns: the K range of every column entity (token or slot), in
         // fragment order, each 128-k block scaled by a power of two
         // pieces (8 k of one column) are dealt flat over the CTA's threads:
@@ -391,19 +480,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         };
         uint4 v[4];
         load_items(0, v);
-        if (p1) {
-            // launch 1 routes while its first activation loads are in flight,
-            // then requests its first units
-            route();
-            __syncthreads();
-            set_range(*s_nent);
-            set_units();
-            if (nu > 0) {
-                start_cursor(i_o, i_i);
-                producer_tile();
-            }
-            for (int k = 0; k < D; ++k) issue_next();
-        }
+        start_launch1();
         for (int it0 = 0; it0 < items; it0 += 4) {
             if (it0 > 0) load_items(it0, v);
 #pragma unroll
@@ -453,6 +530,78 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
                     if ((p & 15) == 0) csum[blk * cols + m] = make_float4(1024.f * c1, c2, exp2i(-sh), 0.f);
                 }
             }
+        }
+    } else {
+        // B columns for INT3 units: one item is 32 k (a chunk) of one column
+        // entity; the 4 chunks of a 128-k block are 4 consecutive lanes.
+        // An item's 16 B registers are the pairs of its chunk (int3_pairs
+        // order), x scaled by the block's power of two and divided by the
+        // pair's code factor.
+        const int tid = threadIdx.x;
+        const int cpc = kblocks * 4;    // chunks per column
+        const int cols = p1 ? a.M : S;  // staged B columns: tokens or slots
+        const int nflat = cols * cpc;
+        const int items = (nflat + T - 1) / T;
+        auto load_item = [&](int it, uint4 (&v)[4]) {
+            const int f = it * T + tid;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) v[b] = make_uint4(0u, 0u, 0u, 0u);
+            if (it < items && f < nflat) {
+                const int m = f / cpc, r = f - m * cpc;
+                const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * a.K + r * 32);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) v[b] = __ldg(src + b);
+            }
+        };
+        uint4 v[4], vn[4];
+        load_item(0, v);
+        start_launch1();
+        for (int it = 0; it < items; ++it) {  // the same count for the whole CTA
+            load_item(it + 1, vn);
+            const int f = it * T + tid;
+            const uint32_t wv[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                                     v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
+            uint32_t mx2 = 0u;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) mx2 = __vmaxu2(mx2, wv[e] & 0x7FFF7FFFu);
+            uint32_t mx = max(mx2 & 0xFFFFu, mx2 >> 16);
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const int sh = block_shift(mx);
+            float fa, fb;
+            pow2_pair(sh, fa, fb);
+            auto xs = [&](int i) {  // x of code i of the chunk, times 2^sh / fb
+                const uint32_t w = wv[i >> 1];
+                return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16)) * fa;
+            };
+            uint32_t breg[16];
+            float c1 = 0.f, c2 = 0.f;
+#pragma unroll
+            for (int P = 0; P < 16; ++P) {
+                const int lo = int3_pair_lo(P), hi = P == 15 ? 31 : lo + 5;
+                const float fac = fb * (1.f / static_cast<float>(1 << int3_pair_shift(P)));
+                const __half2 h2 = __floats2half2_rn(xs(lo) * fac, xs(hi) * fac);
+                breg[P] = *reinterpret_cast<const uint32_t*>(&h2);
+                const float2 bf = __half22float2(h2);
+                const float ps = bf.x + bf.y;
+                c1 += ps;
+                c2 = fmaf(static_cast<float>(1 << int3_pair_shift(P)), ps, c2);
+            }
+            c1 += __shfl_xor_sync(0xffffffffu, c1, 1);
+            c2 += __shfl_xor_sync(0xffffffffu, c2, 1);
+            c1 += __shfl_xor_sync(0xffffffffu, c1, 2);
+            c2 += __shfl_xor_sync(0xffffffffu, c2, 2);
+            if (f < nflat) {
+                const int m = f / cpc, r = f - m * cpc;
+                const int blk = r >> 2, ch = r & 3;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    bfrag[((blk * 4 + u) * cols + m) * 4 + ch] =
+                        make_uint4(breg[4 * u], breg[4 * u + 1], breg[4 * u + 2], breg[4 * u + 3]);
+                if (ch == 0) csum[blk * cols + m] = make_float4(1024.f * c1, c2, exp2i(-sh), 0.f);
+            }
+#pragma unroll
+            for (int b = 0; b < 4; ++b) v[b] = vn[b];
         }
     }
     __syncthreads();
@@ -515,12 +664,12 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         const int lstep = c_step;
         if (++c_slot == D) c_slot = 0;
         const int nbs = min(4, kblocks - 4 * lstep);
-        const uint32_t wst = ring_addr + static_cast<uint32_t>(slot * kMStage);
-        const unsigned char* sz = ring + slot * kMStage;
-        const uint2 zwa = *reinterpret_cast<const uint2*>(sz + kMZero + g * 8);
-        const uint2 zwb = *reinterpret_cast<const uint2*>(sz + kMZero + (g + 8) * 8);
-        const uint4 swa = *reinterpret_cast<const uint4*>(sz + kMScale + g * 16);
-        const uint4 swb = *reinterpret_cast<const uint4*>(sz + kMScale + (g + 8) * 16);
+        const uint32_t wst = ring_addr + static_cast<uint32_t>(slot * kStage);
+        const unsigned char* sz = ring + slot * kStage;
+        const uint2 zwa = *reinterpret_cast<const uint2*>(sz + kZero + g * 8);
+        const uint2 zwb = *reinterpret_cast<const uint2*>(sz + kZero + (g + 8) * 8);
+        const uint4 swa = *reinterpret_cast<const uint4*>(sz + kScale + g * 16);
+        const uint4 swb = *reinterpret_cast<const uint4*>(sz + kScale + (g + 8) * 16);
         const uint32_t za = __funnelshift_r(zwa.x, zwa.y, 8 * subz_a);
         const uint32_t zb = __funnelshift_r(zwb.x, zwb.y, 8 * subz_b);
         const uint32_t sa01 = __funnelshift_r(swa.x, swa.y, 8 * subs_a);
@@ -533,30 +682,48 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
             if (bb >= nbs) break;  // the same for the whole warp
-            const uint32_t hb = wst + static_cast<uint32_t>((bb >> 1) * 128);
-            uint32_t q0[4], q1[4];
-            ldmatrix_x4(q0, hb + ((bb & 1) ? lv2 : lv0));
-            ldmatrix_x4(q1, hb + ((bb & 1) ? lv3 : lv1));
-            const uint32_t wa[4] = {q0[0], q0[2], q1[0], q1[2]};
-            const uint32_t wb[4] = {q0[1], q0[3], q1[1], q1[3]};
             uint4 bq[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) bq[j] = bqu[(bb * 4 + j) * CS * 4];
             float d0[4], d1[4];
-            {
-                const uint32_t ta = wa[0] >> 8, tb = wb[0] >> 8;
-                mma_f16_16816_zero(d0, f16_codes_lo(wa[0]), f16_codes_lo(wb[0]), f16_codes_hi(wa[0]),
-                                   f16_codes_hi(wb[0]), bq[0].x, bq[0].y);
-                mma_f16_16816_zero(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
-                                   f16_codes_hi(tb), bq[0].z, bq[0].w);
-            }
+            if constexpr (BITS == 4) {
+                const uint32_t hb = wst + static_cast<uint32_t>((bb >> 1) * 128);
+                uint32_t q0[4], q1[4];
+                ldmatrix_x4(q0, hb + ((bb & 1) ? lv2 : lv0));
+                ldmatrix_x4(q1, hb + ((bb & 1) ? lv3 : lv1));
+                const uint32_t wa[4] = {q0[0], q0[2], q1[0], q1[2]};
+                const uint32_t wb[4] = {q0[1], q0[3], q1[1], q1[3]};
+                {
+                    const uint32_t ta = wa[0] >> 8, tb = wb[0] >> 8;
+                    mma_f16_16816_zero(d0, f16_codes_lo(wa[0]), f16_codes_lo(wb[0]), f16_codes_hi(wa[0]),
+                                       f16_codes_hi(wb[0]), bq[0].x, bq[0].y);
+                    mma_f16_16816_zero(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
+                                       f16_codes_hi(tb), bq[0].z, bq[0].w);
+                }
 #pragma unroll
-            for (int j = 1; j < 4; ++j) {
-                const uint32_t ta = wa[j] >> 8, tb = wb[j] >> 8;
-                mma_f16_16816(d0, f16_codes_lo(wa[j]), f16_codes_lo(wb[j]), f16_codes_hi(wa[j]),
-                              f16_codes_hi(wb[j]), bq[j].x, bq[j].y);
-                mma_f16_16816(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
-                              f16_codes_hi(tb), bq[j].z, bq[j].w);
+                for (int j = 1; j < 4; ++j) {
+                    const uint32_t ta = wa[j] >> 8, tb = wb[j] >> 8;
+                    mma_f16_16816(d0, f16_codes_lo(wa[j]), f16_codes_lo(wb[j]), f16_codes_hi(wa[j]),
+                                  f16_codes_hi(wb[j]), bq[j].x, bq[j].y);
+                    mma_f16_16816(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
+                                  f16_codes_hi(tb), bq[j].z, bq[j].w);
+                }
+            } else {
+                // chunk c of block bb of rows g and g + 8: three words each
+                const uint32_t* ra = reinterpret_cast<const uint32_t*>(sz + g * kPitch + bb * 48 + c * 12);
+                const uint32_t* rb = ra + 2 * kPitch;  // 8 rows on
+                uint32_t pa[16], pb[16];
+                int3_pairs(ra[0], ra[1], ra[2], pa);
+                int3_pairs(rb[0], rb[1], rb[2], pb);
+                // MMA m: pairs 2m (k slots 2c, 2c + 1) and 2m + 1 (2c + 8, 2c + 9)
+                mma_f16_16816_zero(d0, pa[0], pb[0], pa[1], pb[1], bq[0].x, bq[0].y);
+                mma_f16_16816_zero(d1, pa[2], pb[2], pa[3], pb[3], bq[0].z, bq[0].w);
+#pragma unroll
+                for (int j = 1; j < 4; ++j) {
+                    mma_f16_16816(d0, pa[4 * j], pb[4 * j], pa[4 * j + 1], pb[4 * j + 1], bq[j].x, bq[j].y);
+                    mma_f16_16816(d1, pa[4 * j + 2], pb[4 * j + 2], pa[4 * j + 3], pb[4 * j + 3], bq[j].z,
+                                  bq[j].w);
+                }
             }
             const float zfa = zero_point_f32(za, bb), zfb = zero_point_f32(zb, bb);
             const uint32_t pa = bb < 2 ? sa01 : sa23, pb = bb < 2 ? sb01 : sb23;
@@ -677,7 +844,7 @@ int moe_warps(int phase, int slots) {
 // minimises the busiest warp's units.  Launch 2: row_tiles output tiles over
 // the CTAs, each entry's K steps in one warp.
 MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int kblocks, long long tiles_max,
-                       int row_tiles) {
+                       int row_tiles, int bits) {
     MoeHPlan p{};
     p.warps = moe_warps(phase, ents);
     const int nsteps = (kblocks + 3) / 4;
@@ -703,13 +870,15 @@ MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int kblocks, 
         p.max_rt = (row_tiles + p.ctas - 1) / p.ctas;
     }
     const int half = dev.smem_per_sm / 2 - 1024;
-    const int budget = p.warps == kMWPaired && moeh_layout(p.warps, ents, kblocks, 2, p.max_rt).total <= half
-                           ? half
-                           : dev.max_smem_optin;
+    const int budget =
+        p.warps == kMWPaired && moeh_layout(p.warps, ents, kblocks, 2, p.max_rt, bits).total <= half
+            ? half
+            : dev.max_smem_optin;
     p.depth = 2;
-    while (p.depth < kMMaxDepth && moeh_layout(p.warps, ents, kblocks, p.depth + 1, p.max_rt).total <= budget)
+    while (p.depth < kMMaxDepth &&
+           moeh_layout(p.warps, ents, kblocks, p.depth + 1, p.max_rt, bits).total <= budget)
         ++p.depth;
-    p.smem = moeh_layout(p.warps, ents, kblocks, p.depth, p.max_rt).total;
+    p.smem = moeh_layout(p.warps, ents, kblocks, p.depth, p.max_rt, bits).total;
     if (p.smem > dev.max_smem_optin) p.ctas = 0;
     return p;
 }
@@ -721,11 +890,11 @@ bool moe_hmma_supports(int M, int topk, int64_t H, int64_t F, int64_t g) {
            H % 128 == 0 && F % 128 == 0 && H >= 128 && F >= 128;
 }
 
-bool moe_hmma_fits(const DeviceInfo& dev, int M, int topk, int E, int64_t H, int64_t F) {
+bool moe_hmma_fits(const DeviceInfo& dev, int M, int topk, int E, int64_t H, int64_t F, int bits) {
     const int S = M * topk;
     const long long d = E < S ? E : S;
-    return plan_moe_hmma(dev, 1, M, static_cast<int>(H / 128), d * (F / 8), 0).ctas > 0 &&
-           plan_moe_hmma(dev, 2, S, static_cast<int>(F / 128), 0, static_cast<int>(H / 16)).ctas > 0;
+    return plan_moe_hmma(dev, 1, M, static_cast<int>(H / 128), d * (F / 8), 0, bits).ctas > 0 &&
+           plan_moe_hmma(dev, 2, S, static_cast<int>(F / 128), 0, static_cast<int>(H / 16), bits).ctas > 0;
 }
 
 cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -765,24 +934,28 @@ cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStr
             k.ents = S;
             row_tiles = static_cast<int>(a.H / 16);
         }
-        const MoeHPlan p = plan_moe_hmma(dev, phase, k.ents, k.K / 128, tiles_max, row_tiles);
+        const MoeHPlan p = plan_moe_hmma(dev, phase, k.ents, k.K / 128, tiles_max, row_tiles, a.bits);
         if (p.ctas < 1) return cudaErrorInvalidConfiguration;
         k.max_rt = p.max_rt;
         k.wpt = p.wpt;
         k.depth = p.depth;
-        const void* kern = p.warps == kMWWide ? reinterpret_cast<const void*>(k_moe_hmma<kMWWide>)
-                                              : reinterpret_cast<const void*>(k_moe_hmma<kMWPaired>);
+        const bool wide = p.warps == kMWWide, b3 = a.bits == 3;
+        const void* kern = b3 ? (wide ? reinterpret_cast<const void*>(k_moe_hmma<kMWWide, 3>)
+                                      : reinterpret_cast<const void*>(k_moe_hmma<kMWPaired, 3>))
+                              : (wide ? reinterpret_cast<const void*>(k_moe_hmma<kMWWide, 4>)
+                                      : reinterpret_cast<const void*>(k_moe_hmma<kMWPaired, 4>));
         cudaError_t e = ensure_dynamic_smem(kern, p.smem);
         if (e != cudaSuccess) return e;
         // the two launches ask for different shared memory: with the largest
         // carve-out for both, a launch-2 CTA can be resident beside a
         // launch-1 CTA (an SM whose carve-out must change waits to drain)
-        static bool carveout_set[2] = {false, false};
-        if (!carveout_set[phase - 1]) {
+        static bool carveout_set[4] = {false, false, false, false};
+        const int ck = (b3 ? 2 : 0) + (wide ? 1 : 0);
+        if (!carveout_set[ck]) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
             if (e != cudaSuccess) return e;
-            carveout_set[phase - 1] = true;
+            carveout_set[ck] = true;
         }
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(p.ctas);
@@ -794,8 +967,10 @@ cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStr
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = p.warps == kMWWide ? cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWWide>, k)
-                               : cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWPaired>, k);
+        e = b3 ? (wide ? cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWWide, 3>, k)
+                       : cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWPaired, 3>, k))
+               : (wide ? cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWWide, 4>, k)
+                       : cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWPaired, 4>, k));
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
