@@ -746,6 +746,12 @@ def run_gpu(args):
         t, byts = moe_chain_time(torch, w, 1, 200, 20, l2, fused=False)
         sweep["moe_chain_M1_unfused"] = {"us": round(t * 1e6, 3), "GB/s": round(byts / t / 1e9, 1),
                                          "note": "gate GEMV, up GEMV, SwiGLU, down GEMV + routed sum as separate calls"}
+        for m in (1, 2, 4):
+            t, byts = moe_chain_time(torch, w, m, 200, 20, l2, bits=3)
+            sweep["moe3_chain_M%d" % m] = {"us": round(t * 1e6, 3), "GB/s": round(byts / t / 1e9, 1),
+                                           "frac_measured_peak": round(byts / t / 1e9 / peak, 4),
+                                           "tokens_per_s": round(m / t, 1),
+                                           "note": "INT3 (~3-bit) expert banks, w3a16_moe_ffn; bytes at 3 bits per weight"}
         extra["sweep"] = sweep
         e2e_steps = max(200, min(args.steps, 3000))
         cabi = e2e_cabi_gbs(torch, w, M, N, K, g, e2e_steps)

@@ -21,6 +21,14 @@ def test_algorithmic_bytes_of_the_workloads():
     assert bench.algo_bytes(1, 163840, 4096, 128) == 335544320 + 10485760 + 8192 == 346038272
 
 
+def test_int3_algorithmic_bytes_of_the_expert_matrices():
+    # INT3: three bits per weight (3K/8 bytes per row), same scales and activations;
+    # one MoE gate/up expert matrix is 1024 x 2304, the down matrix 2304 x 1024
+    assert bench.algo_bytes3(0, 1024, 2304, 128) == 884736 + 36864
+    assert bench.algo_bytes3(0, 2304, 1024, 128) == 884736 + 36864
+    assert bench.algo_bytes3(1, 1024, 2304, 128) - bench.algo_bytes3(0, 1024, 2304, 128) == 4608
+
+
 def test_all_bytes_add_zero_points_and_outputs():
     # zero points (1 byte per row and group) and the bf16 output
     assert bench.all_bytes(1, 4096, 4096, 128) - bench.algo_bytes(1, 4096, 4096, 128) == 131072 + 8192

@@ -70,3 +70,16 @@ def test_ffn_variants_match_the_reference(reg, oracle, M):
         torch.cuda.synchronize()
         check_close(host_f64(y), ref["out"], variant)
     assert binding.w4a16_device_error(clear=True) == 0
+
+
+def test_int3_ffn_variants_match_the_reference(reg, oracle):
+    from w4a16_int4_weight_gemv_gb300 import binding
+    p = synth.moe_problem3(M=2, E=16, H=1024, F=512, topk=4, g=128, seed=83)
+    ref = oracle.moe_ffn3(p["x"], p["ids"], p["route_w"], p["gate"], p["up"], p["down"], 128)
+    bank = lambda b: tuple(dev(a) for a in b)
+    for variant, f in reg.OPS["w3a16_ffn"].items():
+        y = f(dev(p["x"]), dev(p["ids"]), dev(p["route_w"]), bank(p["gate"]), bank(p["up"]),
+              bank(p["down"]), 128)
+        torch.cuda.synchronize()
+        check_close(host_f64(y), ref["out"], variant)
+    assert binding.w4a16_device_error(clear=True) == 0

@@ -9,7 +9,7 @@ def test_shipped_defaults_are_pinned(monkeypatch):
     # an ordinary run (no selection in the environment) gets the fast paths
     monkeypatch.delenv(registry.ENV, raising=False)
     assert registry.selection() == {"w4a16_dense": "planned", "w4a16_grouped": "tma",
-                                    "w4a16_ffn": "fused"}
+                                    "w4a16_ffn": "fused", "w3a16_ffn": "fp16_mma"}
     for op, var in registry.DEFAULTS.items():
         assert registry.get(op) is registry.OPS[op][var]
 

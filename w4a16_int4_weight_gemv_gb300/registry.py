@@ -52,8 +52,12 @@ OPS = {
     },
     # routed SwiGLU expert FFN
     "w4a16_ffn": {
-        "fused": _ffn(True),     # w4a16_moe_ffn: gate+up launch, down launch with SwiGLU and routed sum
+        "fused": _ffn(True),     # w4a16_moe_ffn: gate/up launch with the SwiGLU epilogue, down launch with routed sums
         "chain": _ffn(False),    # single-purpose calls: gate, up, SwiGLU, down with routed sum
+    },
+    # the same FFN over ~3-bit (INT3) expert banks
+    "w3a16_ffn": {
+        "fp16_mma": binding.w3a16_moe_ffn,
     },
 }
 
@@ -62,6 +66,7 @@ DEFAULTS = {
     "w4a16_dense": "planned",
     "w4a16_grouped": "tma",
     "w4a16_ffn": "fused",
+    "w3a16_ffn": "fp16_mma",
 }
 
 ENV = "W4A16_KERNELS"
