@@ -239,84 +239,156 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
     grid_dependency_wait();
 
     {
-        // Activations: every (token, round) item of this thread; the loads of
-        // up to four items are issued before any is converted, so the latency
-        // is paid once per four -- and the first four are issued before the
-        // weight copies.  The 16 pieces of a block are 16 consecutive lanes
-        // (block max and sums by shuffles).
-        const int tid = threadIdx.x;
-        constexpr int T = kThreads;
-        const int nblk = nsr * 4;       // 128-k blocks of the slice
-        const int npieces = nblk * 16;  // 8-k pieces per token
-        const int nrounds = (npieces + T - 1) / T;
-        const int items = M * nrounds;
-        const uint16_t* xs = a.x + static_cast<size_t>(s0) * 512;
-        auto load_items = [&](int it0, uint4 (&v)[4]) {
+        if constexpr (MP == 1) {
+            // Activations of one token (measured 2 % faster on the 4096 x 4096
+            // GEMV than the 16-k items below): every (token, round) item of
+            // this thread is one 8-k piece; the loads of
+            // up to four items are issued before any is converted, so the latency
+            // is paid once per four -- and the first four are issued before the
+            // weight copies.  The 16 pieces of a block are 16 consecutive lanes
+            // (block max and sums by shuffles).
+            const int tid = threadIdx.x;
+            constexpr int T = kThreads;
+            const int nblk = nsr * 4;       // 128-k blocks of the slice
+            const int npieces = nblk * 16;  // 8-k pieces per token
+            const int nrounds = (npieces + T - 1) / T;
+            const int items = M * nrounds;
+            const uint16_t* xs = a.x + static_cast<size_t>(s0) * 512;
+            auto load_items = [&](int it0, uint4 (&v)[4]) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int it = it0 + b;
-                const int m = it / nrounds;
-                const int p = (it - m * nrounds) * T + tid;
-                v[b] = make_uint4(0u, 0u, 0u, 0u);
-                if (it < items && p < npieces)
-                    v[b] = __ldg(reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * a.K + p * 8));
+                for (int b = 0; b < 4; ++b) {
+                    const int it = it0 + b;
+                    const int m = it / nrounds;
+                    const int p = (it - m * nrounds) * T + tid;
+                    v[b] = make_uint4(0u, 0u, 0u, 0u);
+                    if (it < items && p < npieces)
+                        v[b] = __ldg(reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * a.K + p * 8));
+                }
+            };
+            uint4 v[4];
+            load_items(0, v);
+            if (!a.weights_static)
+                for (int k = 0; k < D; ++k) issue_next();
+            for (int it0 = 0; it0 < items; it0 += 4) {
+                if (it0 > 0) load_items(it0, v);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int it = it0 + b;
+                    if (it >= items) break;  // the same for the whole CTA
+                    const int m = it / nrounds;
+                    const int p = (it - m * nrounds) * T + tid;
+                    const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+                    uint32_t mx = 0u;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        mx = max(mx, w[e] & 0x7FFFu);
+                        mx = max(mx, (w[e] >> 16) & 0x7FFFu);
+                    }
+#pragma unroll
+                    for (int o = 1; o < 16; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    const int sh = block_shift(mx);
+                    float fa, fb;
+                    pow2_pair(sh, fa, fb);
+                    const float fo = fb * 0.0625f;  // odd codes: B = x' / 16
+                    uint32_t h[8];
+                    float c1 = 0.f, c2 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t bits = (e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
+                        const float xv = __uint_as_float(bits) * fa;
+                        const __half hv = __float2half_rn((e & 1) ? xv * fo : xv * fb);
+                        h[e] = __half_as_ushort(hv);
+                        const float bv = __half2float(hv);
+                        c1 += bv;
+                        c2 += (e & 1) ? 16.f * bv : bv;
+                    }
+#pragma unroll
+                    for (int o = 1; o < 16; o <<= 1) {
+                        c1 += __shfl_xor_sync(0xffffffffu, c1, o);
+                        c2 += __shfl_xor_sync(0xffffffffu, c2, o);
+                    }
+                    if (p < npieces) {
+                        const int blk = p >> 4, j = (p >> 2) & 3, q = p & 3;
+                        uint4 o4;
+                        o4.x = h[0] | (h[4] << 16);  // MMA 1, b0: codes 0, 4
+                        o4.y = h[1] | (h[5] << 16);  // MMA 1, b1: codes 1, 5 (x/16)
+                        o4.z = h[2] | (h[6] << 16);  // MMA 2, b0: codes 2, 6
+                        o4.w = h[3] | (h[7] << 16);  // MMA 2, b1: codes 3, 7 (x/16)
+                        bfrag[((blk * 4 + j) * MP + m) * 4 + q] = o4;
+                        if ((p & 15) == 0) {
+                            float* cs = csum + (blk * 4 + (m >> 1)) * 8;
+                            cs[m & 1] = 1024.f * c1;
+                            cs[2 + (m & 1)] = c2;
+                            cs[4 + (m & 1)] = exp2i(-sh);
+                        }
+                    }
+                }
             }
-        };
-        uint4 v[4];
-        load_items(0, v);
-        if (!a.weights_static)
-            for (int k = 0; k < D; ++k) issue_next();
-        for (int it0 = 0; it0 < items; it0 += 4) {
-            if (it0 > 0) load_items(it0, v);
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int it = it0 + b;
-                if (it >= items) break;  // the same for the whole CTA
-                const int m = it / nrounds;
-                const int p = (it - m * nrounds) * T + tid;
-                const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
-                uint32_t mx = 0u;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    mx = max(mx, w[e] & 0x7FFFu);
-                    mx = max(mx, (w[e] >> 16) & 0x7FFFu);
+        } else {
+            // Activations: one item is two 8-k pieces (16 k) of one token's K
+            // slice (pieces l and l + 8 of a 128-k block, l = 0..7); the 8 items
+            // of a block are 8 consecutive lanes, which share the block's maximum
+            // and sums by shuffles.  Four items per
+            // thread are in flight: the first four are loaded before the weight
+            // copies are issued (loads issued after them wait behind the weight
+            // stream), and each item's slot is refilled four items ahead as soon
+            // as it is converted.
+            const int tid = threadIdx.x;
+            constexpr int T = kThreads;
+            const int nit = nsr * 32;  // items per token of the slice
+            const int nflat = M * nit;
+            const int items = (nflat + T - 1) / T;
+            const uint16_t* xs = a.x + static_cast<size_t>(s0) * 512;
+            auto load_item = [&](int it, uint4 (&v)[2]) {
+                const int f = it * T + tid;
+                v[0] = v[1] = make_uint4(0u, 0u, 0u, 0u);
+                if (it < items && f < nflat) {
+                    const int m = f / nit, r = f - m * nit;
+                    // pieces l and l + 8 of block r / 8 (l = r % 8)
+                    const uint4* src = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(m) * a.K) +
+                                       (r >> 3) * 16 + (r & 7);
+                    v[0] = __ldg(src);
+                    v[1] = __ldg(src + 8);
                 }
+            };
+            uint4 v[4][2];
 #pragma unroll
-                for (int o = 1; o < 16; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                const int sh = block_shift(mx);
-                float fa, fb;
-                pow2_pair(sh, fa, fb);
-                const float fo = fb * 0.0625f;  // odd codes: B = x' / 16
-                uint32_t h[8];
-                float c1 = 0.f, c2 = 0.f;
+            for (int b = 0; b < 4; ++b) load_item(b, v[b]);
+            if (!a.weights_static)
+                for (int k = 0; k < D; ++k) issue_next();
+            for (int it0 = 0; it0 < items; it0 += 4) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t bits = (e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
-                    const float xv = __uint_as_float(bits) * fa;
-                    const __half hv = __float2half_rn((e & 1) ? xv * fo : xv * fb);
-                    h[e] = __half_as_ushort(hv);
-                    const float bv = __half2float(hv);
-                    c1 += bv;
-                    c2 += (e & 1) ? 16.f * bv : bv;
-                }
+                for (int b = 0; b < 4; ++b) {
+                    const int it = it0 + b;
+                    if (it >= items) break;  // the same for the whole CTA
+                    const int f = it * T + tid;
+                    uint32_t mx = pieces_absmax<2>(v[b]);
 #pragma unroll
-                for (int o = 1; o < 16; o <<= 1) {
-                    c1 += __shfl_xor_sync(0xffffffffu, c1, o);
-                    c2 += __shfl_xor_sync(0xffffffffu, c2, o);
-                }
-                if (p < npieces) {
-                    const int blk = p >> 4, j = (p >> 2) & 3, q = p & 3;
-                    uint4 o4;
-                    o4.x = h[0] | (h[4] << 16);  // MMA 1, b0: codes 0, 4
-                    o4.y = h[1] | (h[5] << 16);  // MMA 1, b1: codes 1, 5 (x/16)
-                    o4.z = h[2] | (h[6] << 16);  // MMA 2, b0: codes 2, 6
-                    o4.w = h[3] | (h[7] << 16);  // MMA 2, b1: codes 3, 7 (x/16)
-                    bfrag[((blk * 4 + j) * MP + m) * 4 + q] = o4;
-                    if ((p & 15) == 0) {
-                        float* cs = csum + (blk * 4 + (m >> 1)) * 8;
-                        cs[m & 1] = 1024.f * c1;
-                        cs[2 + (m & 1)] = c2;
-                        cs[4 + (m & 1)] = exp2i(-sh);
+                    for (int o = 1; o < 8; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    const int sh = block_shift(mx);
+                    float fa, fb;
+                    pow2_pair(sh, fa, fb);
+                    uint4 o2[2];
+                    float c1 = 0.f, c2 = 0.f;
+                    int4_piece_fragments<2>(v[b], fa, fb, o2, c1, c2);
+                    load_item(it + 4, v[b]);
+#pragma unroll
+                    for (int o = 1; o < 8; o <<= 1) {
+                        c1 += __shfl_xor_sync(0xffffffffu, c1, o);
+                        c2 += __shfl_xor_sync(0xffffffffu, c2, o);
+                    }
+                    if (f < nflat) {
+                        const int m = f / nit, r = f - m * nit;
+                        // piece p = 16 blk + l: chunk l / 4 of the block, word l % 4
+                        const int blk = r >> 3, l = r & 7;
+                        bfrag[((blk * 4 + (l >> 2)) * MP + m) * 4 + (l & 3)] = o2[0];
+                        bfrag[((blk * 4 + (l >> 2) + 2) * MP + m) * 4 + (l & 3)] = o2[1];
+                        if (l == 0) {
+                            float* cs = csum + (blk * 4 + (m >> 1)) * 8;
+                            cs[m & 1] = 1024.f * c1;
+                            cs[2 + (m & 1)] = c2;
+                            cs[4 + (m & 1)] = exp2i(-sh);
+                        }
                     }
                 }
             }

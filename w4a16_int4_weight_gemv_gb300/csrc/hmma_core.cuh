@@ -3,6 +3,8 @@
 // control and the hand-off of a split tile's partials.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace w4a16 {
@@ -24,6 +26,52 @@ __device__ __forceinline__ int block_shift(uint32_t mb) {
     if (eb > 254) eb = 254;              // Inf / NaN: any shift, the result is not finite
     const int sh = 141 - eb;
     return sh > 126 ? 126 : sh;
+}
+
+// Largest |x| bits (bf16, sign cleared) of NP 8-k pieces of activations.
+template <int NP>
+__device__ __forceinline__ uint32_t pieces_absmax(const uint4 (&v)[NP]) {
+    uint32_t m2 = 0u;
+#pragma unroll
+    for (int b = 0; b < NP; ++b) {
+        m2 = __vmaxu2(m2, v[b].x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v[b].y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v[b].z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v[b].w & 0x7FFF7FFFu);
+    }
+    return max(m2 & 0xFFFFu, m2 >> 16);
+}
+
+// B fragments of an INT4 unit for NP consecutive 8-k pieces of one column
+// (v[q] = the piece's x, bf16): a piece becomes the fp16 pairs
+// {(x0, x4), (x1, x5) / 16, (x2, x6), (x3, x7) / 16} times 2^sh = fa * fb --
+// the k order and scaling of the codes one LOP3 per two makes (odd codes
+// carry a factor 16).  c1 and c2 gain the pieces' sum of B and of B times
+// its code factor.
+template <int NP>
+__device__ __forceinline__ void int4_piece_fragments(const uint4 (&v)[NP], float fa, float fb, uint4 (&o)[NP],
+                                                     float& c1, float& c2) {
+    const float fo = fb * 0.0625f;
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            x[e] = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16)) * fa;
+        const __half2 h0 = __floats2half2_rn(x[0] * fb, x[4] * fb);
+        const __half2 h1 = __floats2half2_rn(x[1] * fo, x[5] * fo);
+        const __half2 h2 = __floats2half2_rn(x[2] * fb, x[6] * fb);
+        const __half2 h3 = __floats2half2_rn(x[3] * fo, x[7] * fo);
+        o[q] = make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
+                          *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
+        const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+        const float2 f2 = __half22float2(h2), f3 = __half22float2(h3);
+        const float ev = (f0.x + f0.y) + (f2.x + f2.y);
+        const float od = (f1.x + f1.y) + (f3.x + f3.y);
+        c1 += ev + od;
+        c2 += fmaf(16.f, od, ev);
+    }
 }
 
 __device__ __forceinline__ float zero_point_f32(uint32_t bytes4, int b) {

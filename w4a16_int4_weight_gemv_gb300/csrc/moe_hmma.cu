@@ -457,77 +457,59 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
     };
     if constexpr (BITS == 4) {
         // B columns: the K range of every column entity (token or slot), in
-        // fragment order, each 128-k block scaled by a power of two
-        // pieces (8 k of one column) are dealt flat over the CTA's threads:
-        // piece f of the (column, piece) sequence goes to thread f % T of
-        // item f / T; a column has a multiple of 16 pieces, so the 16 pieces
-        // of a block are always 16 consecutive lanes
+        // fragment order, each 128-k block scaled by a power of two.  One
+        // item is two 8-k pieces (16 k) of one column, pieces l and l + 8 of
+        // a 128-k block; the 8 items of a block are 8 consecutive lanes (they
+        // share the block's maximum and sums by shuffles).  Four items per thread are in flight, each slot
+        // refilled four items ahead as soon as it is converted.
         const int tid = threadIdx.x;
-        const int npieces = kblocks * 16;
+        const int ipc = kblocks * 8;    // items per column
         const int cols = p1 ? a.M : S;  // staged B columns: tokens or slots
-        const int nflat = cols * npieces;
+        const int nflat = cols * ipc;
         const int items = (nflat + T - 1) / T;
-        auto load_items = [&](int it0, uint4 (&v)[4]) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int f = (it0 + b) * T + tid;
-                v[b] = make_uint4(0u, 0u, 0u, 0u);
-                if (it0 + b < items && f < nflat) {
-                    const int m = f / npieces, p = f - m * npieces;
-                    v[b] = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * a.K + p * 8));
-                }
+        auto load_item = [&](int it, uint4 (&v)[2]) {
+            const int f = it * T + tid;
+            v[0] = v[1] = make_uint4(0u, 0u, 0u, 0u);
+            if (it < items && f < nflat) {
+                const int m = f / ipc, r = f - m * ipc;
+                // pieces l and l + 8 of block r / 8 (l = r % 8)
+                const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * a.K) +
+                                   (r >> 3) * 16 + (r & 7);
+                v[0] = __ldg(src);
+                v[1] = __ldg(src + 8);
             }
         };
-        uint4 v[4];
-        load_items(0, v);
+        uint4 v[4][2];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) load_item(b, v[b]);
         start_launch1();
         for (int it0 = 0; it0 < items; it0 += 4) {
-            if (it0 > 0) load_items(it0, v);
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int it = it0 + b;
                 if (it >= items) break;  // the same for the whole CTA
                 const int f = it * T + tid;
-                const int m = f / npieces, p = f - m * npieces;
-                const uint32_t wv[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
-                uint32_t mx = 0u;
+                uint32_t mx = pieces_absmax<2>(v[b]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    mx = max(mx, wv[e] & 0x7FFFu);
-                    mx = max(mx, (wv[e] >> 16) & 0x7FFFu);
-                }
-#pragma unroll
-                for (int o = 1; o < 16; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                for (int o = 1; o < 8; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                 const int sh = block_shift(mx);
                 float fa, fb;
                 pow2_pair(sh, fa, fb);
-                const float fo = fb * 0.0625f;  // odd codes: B = x' / 16
-                uint32_t hq[8];
+                uint4 o2[2];
                 float c1 = 0.f, c2 = 0.f;
+                int4_piece_fragments<2>(v[b], fa, fb, o2, c1, c2);
+                load_item(it + 4, v[b]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t bits = (e & 1) ? (wv[e >> 1] & 0xFFFF0000u) : (wv[e >> 1] << 16);
-                    const float xv = __uint_as_float(bits) * fa;
-                    const __half hv = __float2half_rn((e & 1) ? xv * fo : xv * fb);
-                    hq[e] = __half_as_ushort(hv);
-                    const float bv = __half2float(hv);
-                    c1 += bv;
-                    c2 += (e & 1) ? 16.f * bv : bv;
-                }
-#pragma unroll
-                for (int o = 1; o < 16; o <<= 1) {
+                for (int o = 1; o < 8; o <<= 1) {
                     c1 += __shfl_xor_sync(0xffffffffu, c1, o);
                     c2 += __shfl_xor_sync(0xffffffffu, c2, o);
                 }
                 if (f < nflat) {
-                    const int blk = p >> 4, j = (p >> 2) & 3, q = p & 3;
-                    uint4 o4;
-                    o4.x = hq[0] | (hq[4] << 16);
-                    o4.y = hq[1] | (hq[5] << 16);
-                    o4.z = hq[2] | (hq[6] << 16);
-                    o4.w = hq[3] | (hq[7] << 16);
-                    bfrag[((blk * 4 + j) * cols + m) * 4 + q] = o4;
-                    if ((p & 15) == 0) csum[blk * cols + m] = make_float4(1024.f * c1, c2, exp2i(-sh), 0.f);
+                    const int m = f / ipc, r = f - m * ipc;
+                    const int blk = r >> 3, l = r & 7;  // pieces 16 blk + l and 16 blk + l + 8
+                    bfrag[((blk * 4 + (l >> 2)) * cols + m) * 4 + (l & 3)] = o2[0];
+                    bfrag[((blk * 4 + (l >> 2) + 2) * cols + m) * 4 + (l & 3)] = o2[1];
+                    if (l == 0) csum[blk * cols + m] = make_float4(1024.f * c1, c2, exp2i(-sh), 0.f);
                 }
             }
         }
