@@ -586,19 +586,22 @@ def run_profile(args):
     import __graft_entry__
     __graft_entry__.build()
     from w4a16_int4_weight_gemv_gb300 import binding as w
-    if args.workload == "moe":
-        # the routed SwiGLU expert FFN (64 experts, H=2304, F=1024, top-8)
+    if args.workload in ("moe", "moe3"):
+        # the routed SwiGLU expert FFN (64 experts, H=2304, F=1024, top-8);
+        # moe3: over INT3 (~3-bit) expert banks
         from w4a16_int4_weight_gemv_gb300 import synth
         M = args.M or 1
-        p = synth.moe_problem(M=M, E=64, H=2304, F=1024, topk=8, g=128, seed=0)
+        gen = synth.moe_problem3 if args.workload == "moe3" else synth.moe_problem
+        p = gen(M=M, E=64, H=2304, F=1024, topk=8, g=128, seed=0)
         b = dict(x=_dev(p["x"], torch), ids=_dev(p["ids"], torch), r=_dev(p["route_w"], torch),
                  gate=tuple(_dev(a, torch) for a in p["gate"]),
                  up=tuple(_dev(a, torch) for a in p["up"]),
                  down=tuple(_dev(a, torch) for a in p["down"]))
+        ffn = w.w3a16_moe_ffn if args.workload == "moe3" else w.moe_ffn
         for i in range(args.warmup + args.steps):
-            w.moe_ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128)
+            ffn(b["x"], b["ids"], b["r"], b["gate"], b["up"], b["down"], 128)
         torch.cuda.synchronize()
-        print(json.dumps({"profile_workload": "moe", "M": M, "launches_per_chain": 2,
+        print(json.dumps({"profile_workload": args.workload, "M": M, "launches_per_chain": 2,
                           "chains": args.warmup + args.steps}))
         return
     M, N, K, zmode, od = WORKLOADS[args.workload]
@@ -877,7 +880,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
                     help="plain launches of --workload for a profiler; prints no bench line")
-    ap.add_argument("--workload", default="square", choices=sorted(list(WORKLOADS) + ["moe"]))
+    ap.add_argument("--workload", default="square", choices=sorted(list(WORKLOADS) + ["moe", "moe3"]))
     ap.add_argument("--M", type=int, default=0)
     ap.add_argument("--kernel-id", type=int, default=0)
     args = ap.parse_args()

@@ -226,15 +226,11 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         const int e = lane < S ? a.ids[lane] : -1;
         const bool valid = lane < S && e >= 0 && e < a.E;
         if (p1 && lane < S && !valid) raise_device_error(a.err, W4A16_DEVERR_EXPERT_ID);
-        int first = lane, pos = 0, cnt = 0;
-        for (int q = 0; q < 32; ++q) {
-            const int eq = __shfl_sync(0xffffffffu, valid ? e : -1, q);
-            if (valid && eq == e) {
-                first = min(first, q);
-                pos += q < lane ? 1 : 0;
-                ++cnt;
-            }
-        }
+        // the lanes routed to this lane's expert (an invalid slot matches none)
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);
+        const int first = __ffs(peers) - 1;
+        const int pos = __popc(peers & ((1u << lane) - 1u));  // earlier slots of the expert
+        const int cnt = __popc(peers);
         const bool is_first = valid && first == lane;
         const int nsub = is_first ? (p1 ? 1 : (cnt + 7) >> 3) : 0;
         int incl = nsub;
@@ -824,7 +820,7 @@ int moe_warps(int phase, int slots) {
 // (two fit where shared memory allows, for the next launch's).  Launch 1:
 // tiles_max (entry, pair) tiles, the split of K steps over warps that
 // minimises the busiest warp's units.  Launch 2: row_tiles output tiles over
-// the CTAs, each entry's K steps in one warp.
+// the CTAs, tiles_max entries at most.
 MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int kblocks, long long tiles_max,
                        int row_tiles, int bits) {
     MoeHPlan p{};
@@ -848,8 +844,13 @@ MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int kblocks, 
     } else {
         if (row_tiles < 1) return p;
         p.ctas = row_tiles < dev.sms ? row_tiles : dev.sms;
-        p.wpt = 1;
         p.max_rt = (row_tiles + p.ctas - 1) / p.ctas;
+        // tiles_max: at most this many entries.  Each entry's K steps go to
+        // one warp, or to a power of two of warps while the CTA's tiles
+        // leave warps idle (one token: 8 entries on 16 warps, two each)
+        const long long tiles = static_cast<long long>(p.max_rt) * tiles_max;
+        p.wpt = 1;
+        while (p.wpt * 2 <= nsteps && tiles * p.wpt * 2 <= p.warps) p.wpt *= 2;
     }
     const int half = dev.smem_per_sm / 2 - 1024;
     const int budget =
@@ -872,11 +873,19 @@ bool moe_hmma_supports(int M, int topk, int64_t H, int64_t F, int64_t g) {
            H % 128 == 0 && F % 128 == 0 && H >= 128 && F >= 128;
 }
 
+// Entries of launch 2 (groups of up to 8 slots of one expert): at most one
+// per slot, and at most one per expert plus one per 8 slots.
+static long long moe_entries_bound(int S, int E) {
+    const long long b = static_cast<long long>(E) + S / 8;
+    return b < S ? b : S;
+}
+
 bool moe_hmma_fits(const DeviceInfo& dev, int M, int topk, int E, int64_t H, int64_t F, int bits) {
     const int S = M * topk;
     const long long d = E < S ? E : S;
     return plan_moe_hmma(dev, 1, M, static_cast<int>(H / 128), d * (F / 8), 0, bits).ctas > 0 &&
-           plan_moe_hmma(dev, 2, S, static_cast<int>(F / 128), 0, static_cast<int>(H / 16), bits).ctas > 0;
+           plan_moe_hmma(dev, 2, S, static_cast<int>(F / 128), moe_entries_bound(S, E),
+                         static_cast<int>(H / 16), bits).ctas > 0;
 }
 
 cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStream_t s) {
@@ -915,6 +924,7 @@ cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStr
             k.K = static_cast<int>(a.F);
             k.ents = S;
             row_tiles = static_cast<int>(a.H / 16);
+            tiles_max = moe_entries_bound(S, a.E);
         }
         const MoeHPlan p = plan_moe_hmma(dev, phase, k.ents, k.K / 128, tiles_max, row_tiles, a.bits);
         if (p.ctas < 1) return cudaErrorInvalidConfiguration;
