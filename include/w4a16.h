@@ -163,9 +163,10 @@ W4A16_API size_t w4a16_gemv_workspace_bytes(int M, int64_t N, int64_t K, int64_t
  *   workspace/workspace_bytes: may be NULL/0 (none is needed; see above).
  * Kernel choice (fixed by M, N, K, g; see w4a16_gemv_plan):
  *   - g == 128, K % 512 == 0 and either M <= 2, or M <= 8 with
- *     N * K >= 2^25: the fp16 warp-MMA kernel (id 4), which takes any finite
- *     bf16 x (each 128-k block of x is scaled by a power of two into fp16,
- *     exactly where the block's values lie within 2^24 of its largest);
+ *     N * K >= 2^25: the fp16 warp-MMA kernel (id 4; it serves up to 16
+ *     tokens when forced), which takes any finite bf16 x (each 128-k block
+ *     of x is scaled by a power of two into fp16, exactly where the block's
+ *     values lie within 2^24 of its largest);
  *   - otherwise, g % 128 == 0: the bf16 warp-MMA kernel (id 2), any M;
  *   - otherwise (groups finer than 128 k), M <= 2: the CUDA-core kernel
  *     (id 1); M > 2 is W4A16_ERR_UNSUPPORTED.
@@ -235,7 +236,7 @@ W4A16_API w4a16_status w4a16_gemv_plan(int M, int64_t N, int64_t K, int64_t g, i
  * w4a16_gemv_variant -- w4a16_gemv with the kernel forced (for measurement):
  * kernel_id 1 (CUDA-core, M <= 2), 2 (bf16 warp-MMA, any M, g % 128 == 0),
  * 3 (tensor-core tcgen05, any M, g % 128 == 0) or 4 (fp16 warp-MMA,
- * M <= 8, g == 128, K % 512 == 0); k_split 0 = automatic, else the K-split
+ * M <= 16, g == 128, K % 512 == 0); k_split 0 = automatic, else the K-split
  * factor, a power of two: for kernels 1 and 2, 1..32 (warps of a CTA first,
  * then up to 8 CTAs of a cluster); for kernels 3 and 4, 1..8 CTAs of a
  * cluster (kernel 4 then chooses its warps per tile itself).  A split the shape cannot use (a CTA's activation slice too large

@@ -1,5 +1,6 @@
 """Parity of the fp16 warp-MMA GEMV (kernel 4) with the oracle, through the C
-ABI: ragged row counts, every token count 1..8, K from one 512-k unit to the
+ABI: ragged row counts, token counts 1..16 (9..16 as two 8-token MMA tiles),
+K from one 512-k unit to the
 wide-MLP down projection, cluster K splits, both output types, the
 resident-weights flag, dependent launches, determinism, activations across
 the bf16 range (the kernel scales each 128-k block by a power of two), and
@@ -46,6 +47,11 @@ CASES = [
     (8, 150, 4096),
     (1, 64, 14336),     # wide-MLP down-projection K
     (2, 40, 14336),
+    (9, 77, 1024),      # two MMA tiles, the second with one token
+    (12, 130, 2048),
+    (13, 17, 512),
+    (16, 200, 4096),
+    (16, 33, 14336),
 ]
 
 
@@ -62,7 +68,7 @@ def test_hmma_matches_oracle(w, oracle, M, N, K, out_dtype):
 
 # shapes whose plan is a 16-warp CTA alone on its SM (long runs), one per
 # instantiated token count; the rest of this file runs 8-warp pairs
-WIDE = [(1, 28672, 4096), (2, 6000, 14336), (3, 28672, 4096), (8, 12000, 4096)]
+WIDE = [(1, 28672, 4096), (2, 6000, 14336), (3, 28672, 4096), (8, 12000, 4096), (16, 12000, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", WIDE)
@@ -79,7 +85,7 @@ def test_hmma_wide_ctas_match_oracle(w, oracle, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 64, 4096), (3, 48, 4096), (1, 40, 14336), (8, 33, 8192),
-                                   (2, 4096, 4096)])
+                                   (2, 4096, 4096), (16, 48, 4096), (11, 300, 8192)])
 @pytest.mark.parametrize("split", [1, 2, 4, 8])
 def test_hmma_cluster_k_split(w, oracle, M, N, K, split):
     # K split over the CTAs of a cluster (partials pushed to the owner's
@@ -90,6 +96,14 @@ def test_hmma_cluster_k_split(w, oracle, M, N, K, split):
             w.w4a16_gemv(*dense_dev(p), 128, kernel_id=KID, k_split=split)
         assert ei.value.status == w.Status.ERR_UNSUPPORTED
         return
+    if M > 8 and K // split >= 4096:
+        # 16 tokens' fp16 fragments of a 4096-k slice (128 KB) plus the
+        # rings need more shared memory than a CTA has: refused, not run
+        try:
+            w.w4a16_gemv(*dense_dev(p), 128, kernel_id=KID, k_split=split)
+        except w.W4A16Error as e:
+            assert e.status == w.Status.ERR_UNSUPPORTED
+            return
     y = w.w4a16_gemv(*dense_dev(p), 128, out_dtype=torch.float32, kernel_id=KID, k_split=split)
     torch.cuda.synchronize()
     check_close(host_f64(y), oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 128),
@@ -99,21 +113,21 @@ def test_hmma_cluster_k_split(w, oracle, M, N, K, split):
 
 def test_hmma_refuses_unsupported_shapes(w):
     # nine tokens, groups other than 128, K not a multiple of 512
-    for M, K, g in ((9, 1024, 128), (1, 1024, 64), (1, 1024, 256), (1, 768, 128)):
+    for M, K, g in ((17, 1024, 128), (1, 1024, 64), (1, 1024, 256), (1, 768, 128)):
         p = synth.dense_problem(M, 32, K, g, "const8", seed=7200)
         with pytest.raises(w.W4A16Error) as ei:
             w.w4a16_gemv(*dense_dev(p), g, kernel_id=KID)
         assert ei.value.status == w.Status.ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("M", [1, 2, 8])
+@pytest.mark.parametrize("M", [1, 2, 8, 16])
 def test_hmma_one_hot_is_bit_exact(w, oracle, M):
     # x = e_k0 per token: D - c1 - z c2 = (q - z) x' exactly, so y is
     # RNE_bf16(W[n][k0]) bit for bit -- at even and odd code positions
     N, K = 48, 2048
     p = synth.dense_problem(M, N, K, 128, "uniform6to10", seed=7300)
     W = oracle.dequant(p["wq"], p["scale"], p["zero"], 128)
-    ks = [0, 1, 7, 130, 1023, 1500, 2046, 2047][:M]
+    ks = [0, 1, 7, 130, 1023, 1500, 2046, 2047, 3, 64, 511, 512, 777, 1024, 1999, 2040][:M]
     x = np.zeros((M, K), np.uint16)
     for m, k0 in enumerate(ks):
         x[m, k0] = 0x3F80

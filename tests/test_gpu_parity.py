@@ -324,6 +324,7 @@ def test_gemv_default_dispatch_is_pinned(w):
         assert w.gemv_plan(M, 8191, 4096, 128)["kernel_id"] == 2
     for M in (9, 16):
         assert w.gemv_plan(M, 14336, 4096, 128)["kernel_id"] == 2
+        assert w.gemv_plan(M, 8192, 8192, 128)["kernel_id"] == 2
     assert w.gemv_plan(1, 4096, 4096, 256)["kernel_id"] == 2
     assert w.gemv_plan(1, 4096, 2304, 128)["kernel_id"] == 2
     assert w.gemv_plan(1, 4096, 4096, 64)["kernel_id"] == 1

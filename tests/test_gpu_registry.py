@@ -24,7 +24,7 @@ def reg():
 
 
 DENSE = [(1, 300, 1024, 128), (2, 257, 2304, 128), (5, 130, 4096, 128), (16, 64, 2048, 256),
-         (8, 100, 3072, 128)]
+         (8, 100, 3072, 128), (12, 96, 2048, 128)]
 
 
 @pytest.mark.parametrize("M,N,K,g", DENSE)

@@ -1,4 +1,4 @@
-// Dense W4A16 GEMV for 1..8 tokens on warp MMA with fp16 operands (sm_103a).
+// Dense W4A16 GEMV for 1..16 tokens on warp MMA with fp16 operands (sm_103a).
 //
 // The decode-time product of the local-kimi README, technical-detail section:
 // a true GEMV with K contiguous, every output row one fp32 accumulation.
@@ -98,42 +98,47 @@ struct HmmaKernelArgs {
 // 8 tile + g (every tile is whole: N % 16 == 0).  Kept out of line so that
 // its exponentials do not add to the main loop's register pressure.
 __device__ __noinline__ void store_swiglu_fragment(uint16_t* y, int M, int N, int tile, int l,
-                                                   float4 v) {
-    const int g = l >> 2, c = l & 3;
+                                                   float4 v, int tok0) {
+    const int g = l >> 2, c = tok0 + 2 * (l & 3);
     const size_t nh = static_cast<size_t>(N >> 1);
     const size_t hr = static_cast<size_t>(tile) * 8 + g;
-    if (2 * c < M) y[2 * c * nh + hr] = swiglu_of_sums(v.x, v.z);
-    if (2 * c + 1 < M) y[(2 * c + 1) * nh + hr] = swiglu_of_sums(v.y, v.w);
+    if (c < M) y[c * nh + hr] = swiglu_of_sums(v.x, v.z);
+    if (c + 1 < M) y[(c + 1) * nh + hr] = swiglu_of_sums(v.y, v.w);
 }
 
-__device__ __forceinline__ void store_fragment(const HmmaKernelArgs& a, int tile, int l, float4 v) {
+// tok0: the first token of the 8-token MMA tile the fragment belongs to
+__device__ __forceinline__ void store_fragment(const HmmaKernelArgs& a, int tile, int l, float4 v,
+                                               int tok0) {
     if (a.swiglu_out) {
-        store_swiglu_fragment(static_cast<uint16_t*>(a.y), a.M, a.N, tile, l, v);
+        store_swiglu_fragment(static_cast<uint16_t*>(a.y), a.M, a.N, tile, l, v, tok0);
         return;
     }
-    const int g = l >> 2, c = l & 3;
+    const int g = l >> 2, c = tok0 + 2 * (l & 3);
     const int ra = (tile << 4) + g;
     const int rb = ra + 8;
-    if (2 * c < a.M) {
-        const size_t o = static_cast<size_t>(2 * c) * a.N;
+    if (c < a.M) {
+        const size_t o = static_cast<size_t>(c) * a.N;
         if (ra < a.N) store_out(a.y, a.out_f32, o + ra, v.x);
         if (rb < a.N) store_out(a.y, a.out_f32, o + rb, v.z);
     }
-    if (2 * c + 1 < a.M) {
-        const size_t o = static_cast<size_t>(2 * c + 1) * a.N;
+    if (c + 1 < a.M) {
+        const size_t o = static_cast<size_t>(c + 1) * a.N;
         if (ra < a.N) store_out(a.y, a.out_f32, o + ra, v.y);
         if (rb < a.N) store_out(a.y, a.out_f32, o + rb, v.w);
     }
 }
 
 
-// MP: the token count rounded up to 1, 2, 4 or 8 -- the B fragments are
+// MP: the token count rounded up to 1, 2, 4, 8 or 16 -- the B fragments are
 // stored for MP tokens (the columns of tokens M..MP-1 are never stored, so
-// their contents do not matter); W warps per CTA
+// their contents do not matter); 16 tokens are two 8-column MMA tiles that
+// share every A operand.  W warps per CTA
 template <int MP, int W>
-__global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
+__global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired && MP <= 8 ? 2 : 1)
     k_gemv_hmma(const HmmaKernelArgs a) {
     constexpr int kThreads = 32 * W;
+    constexpr int NT = MP > 8 ? 2 : 1;       // 8-token MMA tiles
+    constexpr int CSP = MP > 8 ? MP / 2 : 4;  // token pairs per block in the sums
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -316,7 +321,7 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
                         o4.w = h[3] | (h[7] << 16);  // MMA 2, b1: codes 3, 7 (x/16)
                         bfrag[((blk * 4 + j) * MP + m) * 4 + q] = o4;
                         if ((p & 15) == 0) {
-                            float* cs = csum + (blk * 4 + (m >> 1)) * 8;
+                            float* cs = csum + (blk * CSP + (m >> 1)) * 8;
                             cs[m & 1] = 1024.f * c1;
                             cs[2 + (m & 1)] = c2;
                             cs[4 + (m & 1)] = exp2i(-sh);
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
                         bfrag[((blk * 4 + (l >> 2)) * MP + m) * 4 + (l & 3)] = o2[0];
                         bfrag[((blk * 4 + (l >> 2) + 2) * MP + m) * 4 + (l & 3)] = o2[1];
                         if (l == 0) {
-                            float* cs = csum + (blk * 4 + (m >> 1)) * 8;
+                            float* cs = csum + (blk * CSP + (m >> 1)) * 8;
                             cs[m & 1] = 1024.f * c1;
                             cs[2 + (m & 1)] = c2;
                             cs[4 + (m & 1)] = exp2i(-sh);
@@ -412,12 +417,20 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
     const uint32_t lv1 = lve + ((2 ^ (sw_s & 2)) << 4) + ((0 ^ (sw_s & 4)) << 4);
     const uint32_t lv2 = lve + ((0 ^ (sw_s & 2)) << 4) + ((4 ^ (sw_s & 4)) << 4);
     const uint32_t lv3 = lve + ((2 ^ (sw_s & 2)) << 4) + ((4 ^ (sw_s & 4)) << 4);
-    // B fragments of token g (padding-token lanes read token 0's: their
-    // output columns are never stored) and the block sums of tokens 2c, 2c + 1
-    const uint4* bq_lane = bfrag + (g < M ? g : 0) * 4 + c;
-    const float* cs_lane = csum + c * 8;
+    // B fragments of token g (+ 8 t for MMA tile t; padding-token lanes read
+    // token 0's: their output columns are never stored) and the block sums of
+    // tokens 2c, 2c + 1 (+ 8 t)
+    const uint4* bq_lane[NT];
+    const float* cs_lane[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        bq_lane[t] = bfrag + (g + 8 * t < M ? g + 8 * t : 0) * 4 + c;
+        cs_lane[t] = csum + (c + 4 * t) * 8;
+    }
 
-    float4 tacc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 tacc[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) tacc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
     bool timed_out = false;  // a bounded wait for a partner's partials expired
     int c_slot = 0, c_step = part, c_tile = 0, ti = 0;  // c_tile: local tile of the group
 #pragma unroll 1
@@ -433,9 +446,9 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
         const uint32_t zb = *reinterpret_cast<const uint32_t*>(sz + (g + 8) * 4);
         const uint2 sa = *reinterpret_cast<const uint2*>(sz + kSZScales + g * 8);
         const uint2 sb = *reinterpret_cast<const uint2*>(sz + kSZScales + (g + 8) * 8);
-        const uint4* bqu = bq_lane + lstep * 16 * MP * 4;
-        const float* csu = cs_lane + lstep * 4 * 32;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
             const uint32_t hb = wst + static_cast<uint32_t>((bb >> 1) * 128);
@@ -444,47 +457,56 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
             ldmatrix_x4(q1, hb + ((bb & 1) ? lv3 : lv1));
             const uint32_t wa[4] = {q0[0], q0[2], q1[0], q1[2]};  // row g, chunks 0..3
             const uint32_t wb[4] = {q0[1], q0[3], q1[1], q1[3]};  // row g + 8
-            uint4 bq[4];
+            // two accumulator chains per MMA tile: codes 0/4 + 1/5 and codes
+            // 2/6 + 3/7; the A operands of a chunk serve every tile
+            float d0[NT][4], d1[NT][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) bq[j] = bqu[(bb * 4 + j) * MP * 4];
-            // two accumulator chains: codes 0/4 + 1/5 and codes 2/6 + 3/7
-            float d0[4], d1[4];
-            {
-                const uint32_t ta = wa[0] >> 8, tb = wb[0] >> 8;
-                mma_f16_16816_zero(d0, f16_codes_lo(wa[0]), f16_codes_lo(wb[0]), f16_codes_hi(wa[0]),
-                                   f16_codes_hi(wb[0]), bq[0].x, bq[0].y);
-                mma_f16_16816_zero(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
-                                   f16_codes_hi(tb), bq[0].z, bq[0].w);
-            }
-#pragma unroll
-            for (int j = 1; j < 4; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 const uint32_t ta = wa[j] >> 8, tb = wb[j] >> 8;
-                mma_f16_16816(d0, f16_codes_lo(wa[j]), f16_codes_lo(wb[j]), f16_codes_hi(wa[j]),
-                              f16_codes_hi(wb[j]), bq[j].x, bq[j].y);
-                mma_f16_16816(d1, f16_codes_lo(ta), f16_codes_lo(tb), f16_codes_hi(ta),
-                              f16_codes_hi(tb), bq[j].z, bq[j].w);
+                const uint32_t a0 = f16_codes_lo(wa[j]), a1 = f16_codes_lo(wb[j]);
+                const uint32_t a2 = f16_codes_hi(wa[j]), a3 = f16_codes_hi(wb[j]);
+                const uint32_t e0 = f16_codes_lo(ta), e1 = f16_codes_lo(tb);
+                const uint32_t e2 = f16_codes_hi(ta), e3 = f16_codes_hi(tb);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const uint4 bq = bq_lane[t][((lstep * 16) + bb * 4 + j) * MP * 4];
+                    if (j == 0) {
+                        mma_f16_16816_zero(d0[t], a0, a1, a2, a3, bq.x, bq.y);
+                        mma_f16_16816_zero(d1[t], e0, e1, e2, e3, bq.z, bq.w);
+                    } else {
+                        mma_f16_16816(d0[t], a0, a1, a2, a3, bq.x, bq.y);
+                        mma_f16_16816(d1[t], e0, e1, e2, e3, bq.z, bq.w);
+                    }
+                }
             }
-            const float4 cs = *reinterpret_cast<const float4*>(csu + bb * 32);
-            const float2 fs = *reinterpret_cast<const float2*>(csu + bb * 32 + 4);
             const float zfa = zero_point_f32(za, bb), zfb = zero_point_f32(zb, bb);
             const uint32_t swa = (bb < 2) ? sa.x : sa.y, swb = (bb < 2) ? sb.x : sb.y;
             const float sfa = __uint_as_float((bb & 1) ? (swa & 0xFFFF0000u) : (swa << 16));
             const float sfb = __uint_as_float((bb & 1) ? (swb & 0xFFFF0000u) : (swb << 16));
-            // token 2c in x/z, 2c + 1 in y/w; with one token only the former
-            acc[0] = fmaf(sfa * fs.x, (d0[0] + d1[0]) - fmaf(zfa, cs.z, cs.x), acc[0]);
-            acc[2] = fmaf(sfb * fs.x, (d0[2] + d1[2]) - fmaf(zfb, cs.z, cs.x), acc[2]);
-            if (MP > 1) {
-                acc[1] = fmaf(sfa * fs.y, (d0[1] + d1[1]) - fmaf(zfa, cs.w, cs.y), acc[1]);
-                acc[3] = fmaf(sfb * fs.y, (d0[3] + d1[3]) - fmaf(zfb, cs.w, cs.y), acc[3]);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const float* csb = cs_lane[t] + (lstep * 4 + bb) * CSP * 8;
+                const float4 cs = *reinterpret_cast<const float4*>(csb);
+                const float2 fs = *reinterpret_cast<const float2*>(csb + 4);
+                // token 2c in x/z, 2c + 1 in y/w; with one token only the former
+                acc[t][0] = fmaf(sfa * fs.x, (d0[t][0] + d1[t][0]) - fmaf(zfa, cs.z, cs.x), acc[t][0]);
+                acc[t][2] = fmaf(sfb * fs.x, (d0[t][2] + d1[t][2]) - fmaf(zfb, cs.z, cs.x), acc[t][2]);
+                if (MP > 1) {
+                    acc[t][1] = fmaf(sfa * fs.y, (d0[t][1] + d1[t][1]) - fmaf(zfa, cs.w, cs.y), acc[t][1]);
+                    acc[t][3] = fmaf(sfb * fs.y, (d0[t][3] + d1[t][3]) - fmaf(zfb, cs.w, cs.y), acc[t][3]);
+                }
             }
         }
         __syncwarp();  // every lane is done with the stage before it is refilled
         issue_next();  // unit k + D into the stage just consumed
-        tacc.x += acc[0];
-        tacc.z += acc[2];
-        if (MP > 1) {
-            tacc.y += acc[1];
-            tacc.w += acc[3];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            tacc[t].x += acc[t][0];
+            tacc[t].z += acc[t][2];
+            if (MP > 1) {
+                tacc[t].y += acc[t][1];
+                tacc[t].w += acc[t][3];
+            }
         }
         c_step += WPT;
         if (c_step < nsr) continue;
@@ -495,40 +517,46 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
         const int tile = t0 + grp + c_tile * NG;
         if (WPT > 1) {
             if (part != 0) {
-                timed_out |= !hand_partial<W>(red, gbar, grp, WPT, part, ti, lane, tacc);
+                timed_out |= !hand_partials<W, NT>(red, gbar, grp, WPT, part, ti, lane, tacc);
             } else {
                 const int b = ti & 1;
-                const float4* rb = red + (b * W + grp * WPT) * 32;
                 uint64_t* full = gbar + (grp * 2 + b) * 2;
                 timed_out |= !mbar_wait_bounded(full, (ti >> 1) & 1);
-                for (int q = 1; q < WPT; ++q) {
-                    const float4 v = rb[q * 32 + lane];
-                    tacc.x += v.x;
-                    tacc.y += v.y;
-                    tacc.z += v.z;
-                    tacc.w += v.w;
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const float4* rb = red + t * 2 * W * 32 + (b * W + grp * WPT) * 32;
+                    for (int q = 1; q < WPT; ++q) {
+                        const float4 v = rb[q * 32 + lane];
+                        tacc[t].x += v.x;
+                        tacc[t].y += v.y;
+                        tacc[t].z += v.z;
+                        tacc[t].w += v.w;
+                    }
                 }
                 mbar_arrive(full + 1);
             }
         }
         if (part == 0) {
-            if (S == 1) {
-                store_fragment(a, tile, lane, tacc);
-            } else {
-                const int tl = tile - t0;
-                st_dsmem_f32x4(reinterpret_cast<float*>(cpart + (tl * S + rank) * 32 + lane),
-                               static_cast<uint32_t>(tl % S), tacc);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                if (S == 1) {
+                    store_fragment(a, tile, lane, tacc[t], 8 * t);
+                } else {
+                    const int tl = tile - t0;
+                    st_dsmem_f32x4(reinterpret_cast<float*>(cpart + ((t * a.max_tiles + tl) * S + rank) * 32 + lane),
+                                   static_cast<uint32_t>(tl % S), tacc[t]);
+                }
             }
         }
-        tacc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) tacc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
         ++c_tile;
         ++ti;
     }
     // a part with no K step still hands part 0 a (zero) partial per tile
     if (WPT > 1 && my_steps == 0)
         for (; ti < my_tiles; ++ti)
-            timed_out |= !hand_partial<W>(red, gbar, grp, WPT, part, ti, lane,
-                                             make_float4(0.f, 0.f, 0.f, 0.f));
+            timed_out |= !hand_partials<W, NT>(red, gbar, grp, WPT, part, ti, lane, tacc);
     cp_async_wait_pending(0);
     if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
 
@@ -536,18 +564,19 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
     // (tile % S); after the barrier the owner adds them in rank order
     if (S > 1) {
         cluster_barrier();
-        for (int idx = threadIdx.x; idx < nt * 32; idx += blockDim.x) {
-            const int tl = idx >> 5, l = idx & 31;
+        for (int idx = threadIdx.x; idx < NT * nt * 32; idx += blockDim.x) {
+            const int t = idx / (nt * 32);
+            const int tl = (idx >> 5) - t * nt, l = idx & 31;
             if (tl % S != rank) continue;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int q = 0; q < S; ++q) {
-                const float4 pv = cpart[(tl * S + q) * 32 + l];
+                const float4 pv = cpart[((t * a.max_tiles + tl) * S + q) * 32 + l];
                 v.x += pv.x;
                 v.y += pv.y;
                 v.z += pv.z;
                 v.w += pv.w;
             }
-            store_fragment(a, t0 + tl, l, v);
+            store_fragment(a, t0 + tl, l, v, 8 * t);
         }
     }
 }
@@ -555,14 +584,17 @@ __global__ void __launch_bounds__(32 * W, W == kHmmaWarpsPaired ? 2 : 1)
 using HmmaKernel = void (*)(HmmaKernelArgs);
 template <int W>
 HmmaKernel hmma_kernel_w(int M) {
-    return M <= 1 ? k_gemv_hmma<1, W> : M <= 2 ? k_gemv_hmma<2, W> : M <= 4 ? k_gemv_hmma<4, W>
-                                                                      : k_gemv_hmma<8, W>;
+    return M <= 1 ? k_gemv_hmma<1, W>
+           : M <= 2 ? k_gemv_hmma<2, W>
+           : M <= 4 ? k_gemv_hmma<4, W>
+           : M <= 8 ? k_gemv_hmma<8, W>
+                    : k_gemv_hmma<16, W>;
 }
 HmmaKernel hmma_kernel(int M, int warps) {
     return warps == kHmmaWarpsWide ? hmma_kernel_w<kHmmaWarpsWide>(M) : hmma_kernel_w<kHmmaWarpsPaired>(M);
 }
 // tokens rounded up to the instantiated count
-int hmma_mp(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+int hmma_mp(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
 
 }  // namespace
 

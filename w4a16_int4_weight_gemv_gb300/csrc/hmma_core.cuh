@@ -99,16 +99,24 @@ __device__ __forceinline__ void cp_async_commit() {
 // per CTA): it first waits until part 0 has read that buffer's previous
 // contents (tile ti - 2), then writes and arrives on the buffer's `full`
 // barrier.  False if the wait gave up.
-template <int W>
-__device__ __forceinline__ bool hand_partial(float4* red, uint64_t* gbar, int grp, int wpt, int part,
-                                             int ti, int lane, float4 v) {
+// With NT 8-token MMA tiles the partials of tile t go to red + t * 2 * W * 32.
+template <int W, int NT>
+__device__ __forceinline__ bool hand_partials(float4* red, uint64_t* gbar, int grp, int wpt, int part,
+                                              int ti, int lane, const float4 (&v)[NT]) {
     const int b = ti & 1;
     uint64_t* full = gbar + (grp * 2 + b) * 2;
     bool ok = true;
     if (ti >= 2) ok = mbar_wait_bounded(full + 1, ((ti >> 1) - 1) & 1);
-    red[(b * W + grp * wpt + part) * 32 + lane] = v;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) red[t * 2 * W * 32 + (b * W + grp * wpt + part) * 32 + lane] = v[t];
     mbar_arrive(full);
     return ok;
+}
+template <int W>
+__device__ __forceinline__ bool hand_partial(float4* red, uint64_t* gbar, int grp, int wpt, int part,
+                                             int ti, int lane, float4 v) {
+    const float4 one[1] = {v};
+    return hand_partials<W, 1>(red, gbar, grp, wpt, part, ti, lane, one);
 }
 
 }  // namespace

@@ -143,25 +143,28 @@ struct HmmaLayout {
 };
 // Byte offsets inside the CTA's shared memory (from a 128-aligned base; the
 // total includes the alignment slack) for `warps` warps per CTA, M tokens
-// (the count the B fragments are stored for: 1, 2, 4 or 8), `steps` 512-k
+// (the count the B fragments are stored for: 1, 2, 4, 8 or 16 -- 16 tokens
+// are two 8-column MMA tiles, which double the partials), `steps` 512-k
 // steps per K slice, S CTAs per cluster, at most max_tiles tiles per
 // cluster, `depth` stages per warp.
 __host__ __device__ inline HmmaLayout hmma_layout(int warps, int M, int steps, int S,
                                                   int max_tiles, int depth) {
+    const int nt = M > 8 ? 2 : 1;            // 8-token MMA tiles
+    const int pairs = M > 8 ? M / 2 : 4;     // token pairs per block in the sums
     HmmaLayout L;
     int off = 0;
     L.ring = off;  // [warp][depth] stages
     off += warps * depth * kHmmaStage;
     L.bfrag = off;  // activation fragments: [block][piece][token][lane % 4] x 16 bytes
     off += steps * 4 * 4 * M * 4 * 16;
-    L.csum = off;  // per block and lane % 4: {c1[2c], c1[2c+1], c2[2c], c2[2c+1]},
-    off += steps * 4 * 4 * 32;  // then the block's 2^-shift of tokens 2c, 2c + 1
-    L.red = off;  // in-CTA K split: [2][warp][lane] float4 partials
-    off += 2 * warps * 32 * 16;
+    L.csum = off;  // per block and token pair: {c1[2i], c1[2i+1], c2[2i], c2[2i+1]},
+    off += steps * 4 * pairs * 32;  // then the block's 2^-shift of tokens 2i, 2i + 1
+    L.red = off;  // in-CTA K split: [tile][2][warp][lane] float4 partials
+    off += nt * 2 * warps * 32 * 16;
     L.bars = off;  // their mbarriers: [tile group][buffer] {full, empty}
     off += warps * 2 * 2 * 8;
-    L.cpart = off;  // K split over the cluster: [tile][rank][lane] float4 pushed to the owner
-    off += (S > 1) ? max_tiles * S * 32 * 16 : 0;
+    L.cpart = off;  // K split over the cluster: [tile][tile][rank][lane] float4 pushed to the owner
+    off += (S > 1) ? nt * max_tiles * S * 32 * 16 : 0;
     L.total = off + 128;
     return L;
 }
@@ -216,7 +219,8 @@ HmmaChoice plan_hmma_split(const DeviceInfo& dev, int W, int M, int N, int K, in
             // launch's CTA being resident early: two stages per warp there;
             // long runs want three to keep the stream deep
             const int want = units <= 8 ? 2 : 3;
-            const int per_sm = hmma_layout(W, M, sps, S, max_tiles, want).total <= half ? 2 : 1;
+            // 16 tokens: the kernel takes more than half the register file
+            const int per_sm = M <= 8 && hmma_layout(W, M, sps, S, max_tiles, want).total <= half ? 2 : 1;
             if (pair_only && per_sm != 2) continue;
             // clusters of four or more CTAs that could pair up on an SM were
             // placed unevenly (measured 30-60 % slower than S <= 2)
@@ -270,8 +274,8 @@ GemvPlan plan_gemv_simt(const DeviceInfo& dev, int M, int N, int K, int g, int k
 GemvPlan plan_gemv_mma(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
 GemvPlan plan_gemv_tc(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
 GemvPlan plan_gemv_hmma(const DeviceInfo& dev, int M, int N, int K, int g, int k_split_req);
-// True when kernel 4 serves this shape (1..8 tokens, g == 128, K % 512 == 0).
-inline bool hmma_supports(int M, int K, int g) { return M >= 1 && M <= 8 && g == 128 && K % 512 == 0; }
+// True when kernel 4 serves this shape (1..16 tokens, g == 128, K % 512 == 0).
+inline bool hmma_supports(int M, int K, int g) { return M >= 1 && M <= 16 && g == 128 && K % 512 == 0; }
 
 cudaError_t launch_gemv_simt(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);
 cudaError_t launch_gemv_mma(const GemvArgs& a, const GemvPlan& p, cudaStream_t s);

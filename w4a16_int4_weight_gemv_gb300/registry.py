@@ -44,7 +44,7 @@ OPS = {
         "cuda_core": _dense(1),  # subnormal-float CUDA-core kernel, M <= 2
         "warp_mma": _dense(2),   # bf16 mma.sync kernel, M <= 16
         "tcgen05": _dense(3),    # tensor-core (TMEM) kernel, g % 128 == 0
-        "fp16_mma": _dense(4),   # fp16 mma.sync kernel, per-warp cp.async rings, M <= 8, g == 128
+        "fp16_mma": _dense(4),   # fp16 mma.sync kernel, per-warp cp.async rings, M <= 16, g == 128
     },
     # per-slot products of the routed experts, or their routed sum
     "w4a16_grouped": {
