@@ -361,7 +361,8 @@ def moe_chain_time(torch, w, M, steps, warmup, l2, fused=True, bits=4):
 def mlp_decode_chain_time(torch, w, M, steps, warmup, l2, fused=True):
     """One dense SwiGLU MLP of a decode step (hidden 4096, intermediate
     14336), every GEMV with programmatic dependent launch and the
-    resident-weights flag.  fused: gate and up as one GEMV over the two weight
+    resident-weights flag; in the fused chain the down GEMV (which follows
+    the 16-warp gate/up GEMV) is planned without a thread-block cluster.  fused: gate and up as one GEMV over the two weight
     matrices interleaved in 8-row blocks (28672x4096) whose epilogue stores
     the SwiGLU, then the down GEMV (4096x14336): two launches; otherwise gate
     GEMV, up GEMV, w4a16_swiglu, down GEMV (four launches).  Weight sets
@@ -390,7 +391,7 @@ def mlp_decode_chain_time(torch, w, M, steps, warmup, l2, fused=True):
     def step_fused(i):
         gate_up, down = sets[i % R]
         w.w4a16_gemv(x, *gate_up, g, out=h, weights_static=True, swiglu_output=True)
-        w.w4a16_gemv(h, *down, g, out=y, weights_static=True)
+        w.w4a16_gemv(h, *down, g, out=y, weights_static=True, no_cluster=True)
 
     def step_unfused(i):
         gate, up, down = sets[i % R]

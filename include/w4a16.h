@@ -75,6 +75,8 @@ typedef enum w4a16_out_dtype {
                                           still running on the stream (see w4a16_gemv_ex) */
 #define W4A16_FLAG_SWIGLU_OUTPUT 0x2u  /* rows are gate/up pairs of 8-row blocks; y is
                                           bf16(silu(gate) * up) (see w4a16_gemv_ex) */
+#define W4A16_FLAG_NO_CLUSTER 0x4u     /* keep the K split inside a CTA: no thread-block
+                                          cluster launch (see w4a16_gemv_ex) */
 
 /* Bits of the per-device error word (see w4a16_device_error). */
 #define W4A16_DEVERR_EXPERT_ID 0x1u /* an expert id was outside [0, E) */
@@ -214,6 +216,17 @@ W4A16_API w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const u
  *   Requires N % 16 == 0, out_dtype W4A16_OUT_BF16 and a shape the fp16 or
  *   bf16 warp-MMA kernel serves (w4a16_gemv_plan kernel id 4 or 2: g a
  *   multiple of 128); otherwise W4A16_ERR_UNSUPPORTED.
+ *   W4A16_FLAG_NO_CLUSTER plans the launch without a thread-block cluster
+ *   (the K split stays among the warps of a CTA) where the shape allows one;
+ *   otherwise the call plans as without the flag.  w4a16_gemv_plan reports
+ *   the plan without flags.  Which plan is faster depends on the kernel
+ *   before it: a cluster split wins in a run of identical launches, but
+ *   after the 16-warp launch of a gate/up GEMV with the SwiGLU epilogue the
+ *   down GEMV of a decode MLP starts sooner without one -- measured on
+ *   GB300, that two-launch MLP takes 24.5 us per token with the flag on the
+ *   down GEMV and 29.5 us without, although alone the down GEMV is 11 %
+ *   slower with it (and after the small w4a16_swiglu kernel it is slower
+ *   too).
  * Otherwise identical to w4a16_gemv (workspace is not needed).
  */
 W4A16_API w4a16_status w4a16_gemv_ex(const uint16_t* x, const uint32_t* wq, const uint16_t* scale,

@@ -86,8 +86,8 @@ def test_gemv_validation_before_any_launch(lib):
     assert var(A16, A16, A16, A16, A16, 0, 1, 64, 128, 64, 3, 0, None) == Status.ERR_UNSUPPORTED
     assert var(A16, A16, A16, A16, A16, 0, 1, 64, 4096, 128, 3, 16, None) == Status.ERR_UNSUPPORTED
     assert var(A16, A16, A16, A16, A16, 0, 3, 64, 128, 128, 1, 0, None) == Status.ERR_UNSUPPORTED
-    # flags the interface does not define (0x1 and 0x2 are defined)
-    for bad in (0x4, 0x80000000):
+    # flags the interface does not define (0x1, 0x2 and 0x4 are defined)
+    for bad in (0x8, 0x80000000):
         assert lib.w4a16_gemv_ex(A16, A16, A16, A16, A16, 0, 1, 64, 128, 128, bad, None) == \
             Status.ERR_UNSUPPORTED
 

@@ -113,3 +113,26 @@ def test_swiglu_output_refusals(w):
     with pytest.raises(w.W4A16Error) as ei:
         w.w4a16_gemv(xd, wq, s, z, 128, swiglu_output=True)
     assert ei.value.status == w.Status.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_fused_mlp_chain_with_no_cluster_down(w, oracle, M):
+    # the decode MLP as the benchmark chains it: gate/up GEMV with the SwiGLU
+    # epilogue, then the down GEMV planned without a cluster
+    I, H = 1024, 4096
+    x, gate, up = gate_up_problem(M, I, H, 128, 8500 + M)
+    down = synth.dense_problem(M, H, I, 128, "uniform6to10", seed=8510 + M)
+    wq, s, z = interleaved_dev(w, gate, up)
+    h = w.w4a16_gemv(dev(x), wq, s, z, 128, swiglu_output=True, weights_static=True)
+    y = w.w4a16_gemv(h, dev(down["wq"]), dev(down["scale"]), dev(down["zero"]), 128,
+                     out_dtype=torch.float32, weights_static=True, no_cluster=True)
+    torch.cuda.synchronize()
+    h_ref = oracle_swiglu_of_gemvs(oracle, x, gate, up, 128)
+    check_swiglu(h.view(torch.int16).cpu().numpy().view(np.uint16), h_ref, "chain h M=%d" % M)
+    # the down product of the GPU's own h (its bf16 values are the input)
+    h_bits = h.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = oracle.gemv_parallel(h_bits, down["wq"], down["scale"], down["zero"], 128)
+    got = y.cpu().numpy().astype(np.float64)
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert rel <= REL_L2 and np.abs(got - ref).max() <= MAX_REL * np.abs(ref).max(), rel
+    assert w.w4a16_device_error(clear=True) == 0

@@ -212,3 +212,24 @@ def test_hmma_is_deterministic(w):
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     assert torch.equal(s2[0], s2[1])
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 14336), (4, 4096, 14336), (2, 8192, 8192), (1, 1024, 8192),
+                                   (1, 4096, 4096)])
+def test_no_cluster_flag_matches_oracle(w, oracle, M, N, K):
+    # the default plans of the first four use a cluster K split; with the
+    # flag the K split stays inside the CTA (and the 4096 x 4096 plan, which
+    # has no cluster, is unchanged); results within the bar either way
+    p = synth.dense_problem(M, N, K, 128, "uniform6to10", seed=7600 + M)
+    args = dense_dev(p)
+    y = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, no_cluster=True)
+    y0 = w.w4a16_gemv(*args, 128, out_dtype=torch.float32)
+    ys = w.w4a16_gemv(*args, 128, out_dtype=torch.float32, no_cluster=True, weights_static=True)
+    torch.cuda.synchronize()
+    ref = oracle.gemv_parallel(p["x"], p["wq"], p["scale"], p["zero"], 128)
+    check_close(host_f64(y), ref, "no-cluster M=%d N=%d K=%d" % (M, N, K))
+    check_close(host_f64(ys), ref, "no-cluster static M=%d N=%d K=%d" % (M, N, K))
+    assert torch.equal(y, ys)
+    if w.gemv_plan(M, N, K, 128)["k_split"] == 1:
+        assert torch.equal(y, y0)  # no cluster to remove: the same launch
+    assert w.w4a16_device_error(clear=True) == 0

@@ -231,6 +231,7 @@ def gemv_plan(M: int, N: int, K: int, g: int) -> dict:
 
 FLAG_WEIGHTS_STATIC = 0x1
 FLAG_SWIGLU_OUTPUT = 0x2
+FLAG_NO_CLUSTER = 0x4
 
 
 def _host_side(x, out) -> bool:
@@ -257,7 +258,7 @@ def _need_pinned(t, name, dtypes, shape=None):
 
 def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
                kernel_id: int = 0, k_split: int = 0, weights_static: bool = False,
-               swiglu_output: bool = False, stream=None) -> torch.Tensor:
+               swiglu_output: bool = False, no_cluster: bool = False, stream=None) -> torch.Tensor:
     """y[M, N] = x[M, K] . dequant(wq, scale, zero)^T.
 
     kernel_id 0 (default) lets the library choose; 1, 2, 3 or 4 force the
@@ -270,7 +271,9 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
     forced kernel_id or k_split).  swiglu_output: the rows of wq are gate and
     up rows interleaved in blocks of 8 (interleave_gate_up) and y is the
     bf16 [M, N/2] SwiGLU of the two products, formed in the kernel's
-    epilogue (same restriction on forcing).
+    epilogue (same restriction on forcing).  no_cluster: plan without a
+    thread-block cluster where the shape allows (a launch that follows a
+    different kernel starts sooner; same restriction on forcing).
 
     With M == 1, x and out may both be page-locked host tensors: the kernel
     reads x and writes y there directly (over NVLink-C2C on a Grace-Blackwell
@@ -305,10 +308,11 @@ def w4a16_gemv(x, wq, scale, zero, g: int, out=None, out_dtype=torch.bfloat16,
     _need(scale, "scale", _BF16, (N, K // g))
     _need(zero, "zero", _U8, (N, K // g))
     kind = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
-    flags = (FLAG_WEIGHTS_STATIC if weights_static else 0) | (FLAG_SWIGLU_OUTPUT if swiglu_output else 0)
+    flags = ((FLAG_WEIGHTS_STATIC if weights_static else 0) | (FLAG_SWIGLU_OUTPUT if swiglu_output else 0) |
+             (FLAG_NO_CLUSTER if no_cluster else 0))
     if flags and (kernel_id or k_split):
-        raise ValueError("weights_static and swiglu_output apply to the library's own launch "
-                         "choice; they cannot be combined with kernel_id or k_split")
+        raise ValueError("weights_static, swiglu_output and no_cluster apply to the library's own "
+                         "launch choice; they cannot be combined with kernel_id or k_split")
     lib = load_library()
     sh = _stream(stream, device)
     if flags:

@@ -149,7 +149,8 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
                        const uint8_t* zero, void* y, w4a16_out_dtype out_dtype, int M, int64_t N,
                        int64_t K, int64_t g, int kernel_id, int k_split, unsigned flags,
                        void* stream) {
-    if (flags & ~static_cast<unsigned>(W4A16_FLAG_WEIGHTS_STATIC | W4A16_FLAG_SWIGLU_OUTPUT))
+    if (flags & ~static_cast<unsigned>(W4A16_FLAG_WEIGHTS_STATIC | W4A16_FLAG_SWIGLU_OUTPUT |
+                                       W4A16_FLAG_NO_CLUSTER))
         return W4A16_ERR_UNSUPPORTED;
     if (!x || !wq || !scale || !zero || !y) return W4A16_ERR_NULL;
     w4a16_status st = check_gemv_shape(M, N, K, g);
@@ -161,6 +162,16 @@ w4a16_status gemv_impl(const uint16_t* x, const uint32_t* wq, const uint16_t* sc
     DeviceCache* dev = nullptr;
     st = make_plan(M, N, K, g, kernel_id, k_split, &plan, &dev);
     if (st != W4A16_OK) return st;
+    if ((flags & W4A16_FLAG_NO_CLUSTER) && plan.k_split > 1 && k_split == 0 && plan.kernel_id != 3) {
+        // the same kernel with its K split kept inside the CTA (kernel 4:
+        // no cluster, warps per tile chosen anew; kernels 1 and 2: the
+        // plan's warps per tile), where such a plan exists
+        GemvPlan inner{};
+        if (make_plan(M, N, K, g, plan.kernel_id, plan.kernel_id == 4 ? 1 : plan.wpt, &inner, &dev) ==
+                W4A16_OK &&
+            inner.k_split == 1)
+            plan = inner;
+    }
     const int swiglu = (flags & W4A16_FLAG_SWIGLU_OUTPUT) ? 1 : 0;
     // the fused SwiGLU lives in the epilogues of the two warp-MMA kernels,
     // whose lanes hold rows r and r + 8 of a tile (a gate and its up row)
