@@ -826,14 +826,20 @@ def run_reference(args):
     nsteps = max(1, args.steps + args.warmup)
     # one full GEMV per step on all host threads when that fits the budget,
     # else a bounded sample of output rows per step
+    oracle.gemv_parallel(p["x"], p["wq"], p["scale"], p["zero"], g, threads=cores)  # thread start-up
     t0 = time.perf_counter()
     oracle.gemv_parallel(p["x"], p["wq"], p["scale"], p["zero"], g, threads=cores)
     t_full = time.perf_counter() - t0
     full = t_full * nsteps <= budget
     rows_per_step = N
-    if not full:
-        rows_per_step = int(max(1, min(N, N * budget / nsteps / t_full)))
     rng = np.random.default_rng(0)
+    if not full:
+        # the sample runs on one thread: size it by the one-thread rate
+        probe = rng.integers(0, N, 64).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.gemv_rows(p["x"], p["wq"], p["scale"], p["zero"], g, probe)
+        t_row = (time.perf_counter() - t0) / probe.size
+        rows_per_step = int(max(1, min(N, budget / nsteps / t_row)))
 
     def one():
         if full:
