@@ -9,7 +9,8 @@
 // one code), which alone needs ~85 % of that pipe at HBM speed.  An fp16 pair
 // holds two codes, so feeding the codes to the tensor pipe as the A operand of
 // mma.sync.m16n8k16 halves that work, and the multiply-adds leave the CUDA
-// cores altogether; the tokens are the B operand (8 columns, 1..8 used).
+// cores altogether; the tokens are the B operand (8 columns, 1..8 used;
+// 9..16 tokens are two such tiles sharing every A operand).
 //
 // Dequantisation.  (w & 0x000F000F) | 0x64006400 is the fp16 pair
 // {1024 + q0, 1024 + q4} and (w & 0x00F000F0) | 0x64006400 the pair
@@ -41,19 +42,18 @@
 // ring is filled before the loop and a stage is refilled as soon as it is
 // consumed, so a warp with at most `depth` units has them all in flight at
 // once and a longer one keeps depth - 1 in flight while it computes.  (The
-// copy engine is not used: a bulk or
-// tensor copy costs its issuing warp tens of nanoseconds on sm_103a, and
-// with the weights split over many such copies the issue time outweighs the
-// arithmetic.)  Nothing waits on another thread except at named and
-// cluster barriers that every thread reaches.
+// copy engine is not used: a bulk or tensor copy costs its issuing warp tens
+// of nanoseconds on sm_103a, and with the weights split over many such
+// copies the issue time outweighs the arithmetic.)
 //
 // Work split.  The CTAs of a cluster share a range of 16-row tiles, rank r
 // taking the r-th K slice; inside the CTA, WPT warps share a tile, warp part
 // p taking K steps p, p + WPT, ...; tile groups take the CTA's tiles in turn.
-// Parts meet at a named barrier per tile and part 0 adds their partials in
-// part order; ranks push their tile sums into the owner's shared memory and
-// the owner adds them in rank order after a cluster barrier -- fixed orders,
-// so results are deterministic.
+// The other parts hand their partials to part 0 through double-buffered
+// shared memory guarded by mbarriers (every wait bounded), and part 0 adds
+// them in part order; ranks push their tile sums into the owner's shared
+// memory and the owner adds them in rank order after a cluster barrier --
+// fixed orders, so results are deterministic.
 //
 // Launch.  The rings are sized so that two CTAs fit on an SM where possible:
 // with programmatic dependent launch the next GEMV's CTA becomes resident

@@ -119,7 +119,7 @@ SplitChoice choose_split(const DeviceInfo& dev, int ntiles, int units_all, int w
 }
 
 // ---------------------------------------------------------------------------
-// fp16 warp-MMA GEMV (kernel 4): 1..8 tokens, g == 128, K % 512 == 0.
+// fp16 warp-MMA GEMV (kernel 4): 1..16 tokens, g == 128, K % 512 == 0.
 // A unit is one 16-row tile x 512 k: 16 rows of 256 packed bytes (16-byte
 // chunks XOR-swizzled by row), plus the tile's 16 x 4 zero points and 16 x 4
 // scales.  Every warp streams its own units through its own ring of
