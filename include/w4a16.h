@@ -410,6 +410,18 @@ W4A16_API w4a16_status w4a16_swiglu(const uint16_t* gate, const uint16_t* up, in
 W4A16_API int w4a16_host_memory_mapped(const void* p);
 
 /*
+ * w4a16_wait_selftest -- one warp waits on a shared-memory mbarrier with the
+ * bounded wait every kernel of this library uses (tries of up to 100 us
+ * each, at most max_iters, 1..8192).  With arrive != 0 one arrival completes
+ * the phase and the wait returns at once; with arrive == 0 nothing arrives,
+ * the wait gives up after max_iters tries and W4A16_DEVERR_TIMEOUT is set in
+ * the device error word -- the path an expired wait in a GEMV or expert
+ * kernel takes (the kernel returns, the context stays usable).  For tests of
+ * that failure path; asynchronous on `stream`.
+ */
+W4A16_API w4a16_status w4a16_wait_selftest(unsigned max_iters, int arrive, void* stream);
+
+/*
  * w4a16_device_error -- synchronise `stream`, then copy the current device's
  * error word (W4A16_DEVERR_* bits set by kernels since the last clear) to
  * *bits_out (host pointer); reset it to 0 if clear != 0.

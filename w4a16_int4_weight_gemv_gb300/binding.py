@@ -95,6 +95,8 @@ def load_library():
     lib.w4a16_host_memory_mapped.argtypes = [P]
     lib.w4a16_device_error.restype = I32
     lib.w4a16_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), I32, P]
+    lib.w4a16_wait_selftest.restype = I32
+    lib.w4a16_wait_selftest.argtypes = [ctypes.c_uint, I32, P]
     lib.int3_pack.restype = I32
     lib.int3_pack.argtypes = [P, P, I64, I64, P]
     lib.int3_dequant.restype = I32
@@ -403,6 +405,13 @@ def w4a16_device_error(clear: bool = True, stream=None) -> int:
     _check(load_library().w4a16_device_error(ctypes.byref(bits), int(bool(clear)),
                                              _stream(stream)), "w4a16_device_error")
     return int(bits.value)
+
+
+def w4a16_wait_selftest(max_iters: int, arrive: bool, stream=None) -> None:
+    """One bounded mbarrier wait that completes (arrive) or expires
+    (W4A16_DEVERR_TIMEOUT in the device error word)."""
+    _check(load_library().w4a16_wait_selftest(int(max_iters), int(bool(arrive)), _stream(stream)),
+           "w4a16_wait_selftest")
 
 
 def moe_ffn(x, expert_ids, route_w, gate, up, down, g: int, stream=None,

@@ -595,6 +595,24 @@ int w4a16_host_memory_mapped(const void* p) {
     return (at.type == cudaMemoryTypeHost && at.devicePointer == p) ? 1 : 0;
 }
 
+}  // extern "C"
+
+namespace w4a16 {
+// elementwise.cu: one bounded mbarrier wait that completes (arrive != 0) or expires
+cudaError_t launch_wait_selftest(uint32_t max_iters, int arrive, uint32_t* err, cudaStream_t s);
+}  // namespace w4a16
+
+extern "C" {
+
+w4a16_status w4a16_wait_selftest(unsigned max_iters, int arrive, void* stream) {
+    if (max_iters < 1 || max_iters > 8192) return W4A16_ERR_SHAPE;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    return from_cuda(launch_wait_selftest(max_iters, arrive ? 1 : 0, dev->err,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 w4a16_status w4a16_device_error(uint32_t* bits_out, int clear, void* stream) {
     if (!bits_out) return W4A16_ERR_NULL;
     DeviceCache* dev = nullptr;

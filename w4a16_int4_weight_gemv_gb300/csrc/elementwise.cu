@@ -159,6 +159,19 @@ __global__ void k_swiglu(const uint16_t* __restrict__ gate, const uint16_t* __re
     }
 }
 
+// One warp waits, bounded, on an mbarrier that one arrival completes; with
+// arrive == 0 nothing arrives and the wait expires after max_iters tries,
+// which raises W4A16_DEVERR_TIMEOUT exactly as an expired wait in the GEMV
+// and expert kernels does.
+__global__ void k_wait_selftest(uint32_t max_iters, int arrive, uint32_t* err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) mbar_init(&bar, 1);
+    __syncwarp();
+    if (arrive && threadIdx.x == 0) mbar_arrive(&bar);
+    const bool ok = mbar_wait_bounded(&bar, 0, max_iters);
+    if (!ok && threadIdx.x == 0) raise_device_error(err, W4A16_DEVERR_TIMEOUT);
+}
+
 int grid_for(int64_t items, int threads, int sms) {
     int64_t b = (items + threads - 1) / threads;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
@@ -202,6 +215,11 @@ cudaError_t launch_dequant3(const uint32_t* wq3, const uint16_t* scale, const ui
     const int64_t chunks = N * (K / 32);
     if (chunks == 0) return cudaSuccess;
     k_dequant3<<<grid_for(chunks, 256, sms), 256, 0, s>>>(wq3, scale, zero, w, out_f32, N, K, g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint32_t max_iters, int arrive, uint32_t* err, cudaStream_t s) {
+    k_wait_selftest<<<1, 32, 0, s>>>(max_iters, arrive, err);
     return cudaGetLastError();
 }
 
