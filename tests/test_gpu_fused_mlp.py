@@ -60,7 +60,7 @@ def check_swiglu(got_bits, ref_bits, what):
 @pytest.mark.parametrize("M,I,K,g", [(1, 64, 1024, 128), (1, 4096, 4096, 128), (1, 14336, 4096, 128),
                                      (2, 136, 2048, 128), (3, 200, 1536, 128), (4, 1024, 4096, 128),
                                      (8, 512, 4096, 128), (16, 256, 2048, 128), (2, 64, 2048, 256),
-                                     (5, 40, 4096, 256)])
+                                     (5, 40, 4096, 256), (16, 4096, 4096, 128), (11, 4096, 8192, 128)])
 def test_swiglu_output_matches_oracle(w, oracle, M, I, K, g):
     x, gate, up = gate_up_problem(M, I, K, g, 8100 + M * 7 + I)
     wq, s, z = interleaved_dev(w, gate, up)

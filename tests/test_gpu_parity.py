@@ -309,11 +309,12 @@ def test_cuda_core_kernel_small_activations(w, oracle):
 def test_gemv_default_dispatch_is_pinned(w):
     # the dispatch the benchmark times is the library default; pin it: the
     # fp16 warp-MMA kernel for one and two tokens on the square, wide-MLP and
-    # vocabulary shapes and for 3..8 tokens on matrices of 2^25 weights or
-    # more, the bf16 warp-MMA kernel for 3..8 tokens on smaller matrices, for
-    # 9..16 tokens and for one token where kernel 4 does not apply (groups of
-    # 256, K % 512 != 0), the CUDA-core kernel for one or two tokens with
-    # groups of 64
+    # vocabulary shapes and for 3..16 tokens on matrices of 2^25 weights or
+    # more that it has a plan for, the bf16 warp-MMA kernel for 3..16 tokens
+    # on smaller matrices, for 9..16 tokens where kernel 4 has no plan, and
+    # for one token where kernel 4 does not apply (groups of 256,
+    # K % 512 != 0), the CUDA-core kernel for one or two tokens with groups
+    # of 64
     for M in (1, 2):
         for N, K in ((4096, 4096), (14336, 4096), (4096, 14336), (163840, 4096)):
             assert w.gemv_plan(M, N, K, 128)["kernel_id"] == 4
@@ -323,8 +324,10 @@ def test_gemv_default_dispatch_is_pinned(w):
         assert w.gemv_plan(M, 4096, 4096, 128)["kernel_id"] == 2
         assert w.gemv_plan(M, 8191, 4096, 128)["kernel_id"] == 2
     for M in (9, 16):
-        assert w.gemv_plan(M, 14336, 4096, 128)["kernel_id"] == 2
-        assert w.gemv_plan(M, 8192, 8192, 128)["kernel_id"] == 2
+        assert w.gemv_plan(M, 14336, 4096, 128)["kernel_id"] == 4
+        assert w.gemv_plan(M, 8192, 8192, 128)["kernel_id"] == 4
+        assert w.gemv_plan(M, 4096, 14336, 128)["kernel_id"] == 2  # 16 tokens' fragments do not fit
+        assert w.gemv_plan(M, 4096, 4096, 128)["kernel_id"] == 2
     assert w.gemv_plan(1, 4096, 4096, 256)["kernel_id"] == 2
     assert w.gemv_plan(1, 4096, 2304, 128)["kernel_id"] == 2
     assert w.gemv_plan(1, 4096, 4096, 64)["kernel_id"] == 1

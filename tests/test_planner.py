@@ -160,7 +160,8 @@ def hmma_planner(tmp_path_factory):
 
 HMMA_SHAPES = [(1, 4096, 4096), (1, 14336, 4096), (1, 4096, 14336), (1, 163840, 4096),
                (1, 28672, 4096), (1, 1, 512), (1, 17, 512), (2, 257, 2048), (8, 150, 4096),
-               (8, 14336, 4096), (4, 4096, 14336), (1, 64, 14336), (8, 33, 8192)]
+               (8, 14336, 4096), (4, 4096, 14336), (1, 64, 14336), (8, 33, 8192),
+               (16, 14336, 4096), (12, 28672, 4096), (16, 8192, 8192), (9, 200, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", HMMA_SHAPES)
@@ -221,3 +222,15 @@ def test_hmma_forced_cluster_split(hmma_planner, forced):
     assert p["S"] == forced
     # a split that does not divide K / 512 gives no plan
     assert hmma_planner(1, 4096, 1536, 4)["nclusters"] == 0
+
+
+def test_hmma_sixteen_token_plans_take_short_slices(hmma_planner):
+    # 9..16 tokens (two MMA tiles): K slices of at most 2048 k where they fit,
+    # one CTA per SM; the MLP down projection (28 steps of 512 k) has no
+    # plan at 4096 rows (the library then takes the bf16 kernel)
+    for shape, S in (((16, 14336, 4096), 2), ((12, 28672, 4096), 2), ((16, 8192, 8192), 4)):
+        p = hmma_planner(*shape)
+        assert p["S"] == S and p["sps"] <= 4 and p["per_sm"] == 1, (shape, p)
+    assert hmma_planner(16, 4096, 14336)["nclusters"] == 0
+    # where no short slice fits, any slice that does (a small matrix)
+    assert hmma_planner(16, 33, 14336)["nclusters"] > 0

@@ -88,13 +88,14 @@ w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, in
     // at one and two tokens by 0-37 % on the MLP, square and 8192 x 8192
     // shapes; at 3..8 tokens ahead by 5-32 % from 14336 x 4096 up, and behind
     // by up to 20 % on 4096 x 4096 and smaller matrices; at 9..16 tokens
-    // (two MMA tiles, fragments for 16 tokens in shared memory) within
-    // -10..+5 % of kernel 2, which keeps them.)
+    // (two MMA tiles, K slices of at most 2048 k) ahead by 5-40 % from
+    // 14336 x 4096 up where a plan exists, falling back to kernel 2 where
+    // none does, e.g. 4096 x 14336.)
     const int requested = kernel_id;
     const bool automatic = kernel_id == 0;
     if (automatic) {
         const bool k4 = hmma_supports(M, static_cast<int>(K), static_cast<int>(g)) &&
-                        (M <= 2 || (M <= 8 && N * K >= (int64_t(1) << 25)));
+                        (M <= 2 || N * K >= (int64_t(1) << 25));
         kernel_id = k4 ? 4 : (g % 128 == 0) ? 2 : 1;
     }
     if (kernel_id == 1 && M > 2) return W4A16_ERR_UNSUPPORTED;

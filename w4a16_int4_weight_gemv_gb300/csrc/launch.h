@@ -185,7 +185,7 @@ struct HmmaChoice {
 // pair_only: consider only shapes with two CTAs per SM.
 template <class ClusterFn>
 HmmaChoice plan_hmma_split(const DeviceInfo& dev, int W, int M, int N, int K, int forced_S,
-                           bool pair_only, ClusterFn max_clusters) {
+                           bool pair_only, ClusterFn max_clusters, int max_sps = 0) {
     HmmaChoice best{};
     long best_t = -1;
     const int ntiles = (N + 15) / 16;
@@ -195,6 +195,7 @@ HmmaChoice plan_hmma_split(const DeviceInfo& dev, int W, int M, int N, int K, in
         if (forced_S > 0 && S != forced_S) continue;
         if (nsteps % S != 0) continue;
         const int sps = nsteps / S;
+        if (max_sps > 0 && sps > max_sps) continue;
         int cap = dev.sms / S;
         const int need_min = hmma_layout(W, M, sps, S, (ntiles + cap - 1) / cap, 2).total;
         if (need_min > dev.max_smem_optin) continue;
@@ -248,15 +249,29 @@ HmmaChoice plan_hmma_split(const DeviceInfo& dev, int W, int M, int N, int K, in
 // 4096 x 14336, 16 warps by 4-14 % from 28672 x 4096 up to the vocabulary
 // projection.
 template <class ClusterFn8, class ClusterFn16>
-HmmaChoice choose_hmma_plan(const DeviceInfo& dev, int M, int N, int K, int forced_S,
-                            ClusterFn8 max_clusters8, ClusterFn16 max_clusters16) {
+HmmaChoice choose_hmma_plan_sps(const DeviceInfo& dev, int M, int N, int K, int forced_S,
+                                ClusterFn8 max_clusters8, ClusterFn16 max_clusters16, int max_sps) {
     const HmmaChoice paired =
-        plan_hmma_split(dev, kHmmaWarpsPaired, M, N, K, forced_S, true, max_clusters8);
+        plan_hmma_split(dev, kHmmaWarpsPaired, M, N, K, forced_S, true, max_clusters8, max_sps);
     if (paired.nclusters > 0) return paired;
     const HmmaChoice wide =
-        plan_hmma_split(dev, kHmmaWarpsWide, M, N, K, forced_S, false, max_clusters16);
+        plan_hmma_split(dev, kHmmaWarpsWide, M, N, K, forced_S, false, max_clusters16, max_sps);
     if (wide.nclusters > 0) return wide;
-    return plan_hmma_split(dev, kHmmaWarpsPaired, M, N, K, forced_S, false, max_clusters8);
+    return plan_hmma_split(dev, kHmmaWarpsPaired, M, N, K, forced_S, false, max_clusters8, max_sps);
+}
+// 9..16 tokens prefer K slices of at most 2048 k (measured on GB300, 12 and
+// 16 tokens: 14336 x 4096 and 28672 x 4096 5-12 % faster than the bf16
+// warp-MMA kernel with clusters of two, 8192 x 8192 14-40 % with clusters of
+// four; with an unsplit 4096-k slice 10 % slower than it); any slice that
+// fits otherwise
+template <class ClusterFn8, class ClusterFn16>
+HmmaChoice choose_hmma_plan(const DeviceInfo& dev, int M, int N, int K, int forced_S,
+                            ClusterFn8 max_clusters8, ClusterFn16 max_clusters16) {
+    if (M > 8 && forced_S == 0) {
+        const HmmaChoice c = choose_hmma_plan_sps(dev, M, N, K, 0, max_clusters8, max_clusters16, 4);
+        if (c.nclusters > 0) return c;
+    }
+    return choose_hmma_plan_sps(dev, M, N, K, forced_S, max_clusters8, max_clusters16, 0);
 }
 
 // Lets `kernel` run with `bytes` of dynamic shared memory on the current
