@@ -333,12 +333,17 @@ W4A16_API size_t w4a16_moe_ffn_workspace_bytes(int M, int topk, int64_t H, int64
  * names the SwiGLU op), in two launches:
  *   1. gate and up products of every routed slot, both banks in one launch:
  *        G[t][j] = bf16(W^gate_e x[t]),  U[t][j] = bf16(W^up_e x[t]),
- *   2. down products of h[t][j] = bf16(silu(G[t][j]) * U[t][j]) (computed in
- *      fp32 exactly as w4a16_swiglu does, while staging the activations),
- *   3. y[t] = bf16(sum_j route_w[t][j] * (W^down_e h[t][j])) (fp32 sum, j
- *      ascending), formed inside the down launch by the last CTA to finish
- *      each row chunk.
- * Each distinct expert's three matrices are streamed once per call.
+ *      and h[t][j] = bf16(silu(G[t][j]) * U[t][j]) (in fp32 exactly as
+ *      w4a16_swiglu computes it);
+ *   2. down products and the routed sums
+ *        y[t] = bf16(sum_j route_w[t][j] * (W^down_e h[t][j])) (fp32, j ascending).
+ * With 1..8 tokens, M*topk <= 32 and g == 128 (H, F multiples of 128) this is
+ * the fp16 warp-MMA path: launch 1 forms h in its epilogue, launch 2 owns
+ * 16-row output tiles and forms their routed sums in shared memory.
+ * Otherwise the bf16 warp-MMA expert kernel: h is formed while launch 2
+ * stages its activations, and the last CTA to finish each row chunk forms
+ * its routed sums.  Each distinct expert's three matrices are streamed once
+ * per call.
  *   x: bf16 [M][H]; expert_ids: int32 [M][topk]; route_w: fp32 [M][topk];
  *   gate, up: wq [E][F][H/8], scale and zero [E][F][H/g];
  *   down: wq [E][H][F/8], scale and zero [E][H][F/g]; y: bf16 [M][H];
