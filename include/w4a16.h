@@ -203,7 +203,7 @@ W4A16_API w4a16_status w4a16_gemv(const uint16_t* x, const uint32_t* wq, const u
  *   may still be running on the stream writes those three buffers -- the
  *   case of resident model weights in a decode loop.  It is a permission:
  *   what it buys depends on the launch (measured on GB300, back-to-back
- *   4096 x 4096 GEMVs: 4.51 us per call with it, 4.58 us without).
+ *   4096 x 4096 GEMVs: 4.21 us per call with it, 4.39 us without).
  *   W4A16_FLAG_SWIGLU_OUTPUT fuses the SwiGLU of a decode MLP into the
  *   gate/up projection (README technical-detail section: the kernel
  *   registry's SwiGLU op; the expert FFN does the same inside
