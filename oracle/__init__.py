@@ -29,6 +29,8 @@ reading, stated in that file's header), pinned in tests/test_oracle_int3.py:
                      codes 0..7 are INT4 codes), closed form, one-hot
                      activations, fp64 library matmul
   moe_ffn3           pinned: equal to the INT4 chain on the same codes
+  moe_gemv3          pinned: equal to the INT4 expert GEMV on the same codes
+                     (per-slot and routed, shared and per-slot inputs)
 """
 from __future__ import annotations
 
@@ -122,6 +124,8 @@ def _bind(lib):
     lib.oracle3_gemv.argtypes = [P, P, P, P, P, I, I, I, I]
     lib.oracle3_moe_ffn.restype = ctypes.c_int
     lib.oracle3_moe_ffn.argtypes = [P] * 17 + [I] * 6
+    lib.oracle3_moe_gemv.restype = ctypes.c_int
+    lib.oracle3_moe_gemv.argtypes = [P, ctypes.c_int, P, P, P, P, P, P, I, I, I, I, I, I]
     return lib
 
 
@@ -359,6 +363,35 @@ def gemv3(x, wq3, scale, zero, g: int) -> np.ndarray:
     assert wq3.shape[1] == int3_row_words(K)
     y = np.empty((M, N), np.float64)
     lib.oracle3_gemv(px, pw, ps, pz, y.ctypes.data_as(ctypes.c_void_p), M, N, K, g)
+    return y
+
+
+def moe_gemv3(x, ids, route_w, wq3, scale, zero, g: int, x_per_slot: bool = False,
+              allow_bad_ids: bool = False):
+    """Expert-indexed GEMV over INT3 experts: wq3 [E, N, 3K/32], scale/zero
+    [E, N, K/g], ids int32 [M, topk]; x [M, K] or (x_per_slot) [M, topk, K].
+    Returns fp64 [M, topk, N] (route_w None; zero rows for invalid ids) or
+    [M, N] (routed sum, invalid ids skipped).  Invalid ids raise ValueError
+    unless allow_bad_ids."""
+    lib = _load()
+    x, px = _c(x, np.uint16)
+    ids, pi = _c(ids, np.int32)
+    wq3, pw = _c(wq3, np.uint32)
+    scale, ps = _c(scale, np.uint16)
+    zero, pz = _c(zero, np.uint8)
+    E, N, W3 = wq3.shape
+    K = W3 // 12 * 128
+    M, topk = ids.shape
+    if route_w is None:
+        pr = None
+        y = np.empty((M, topk, N), np.float64)
+    else:
+        route_w, pr = _c(route_w, np.float32)
+        y = np.empty((M, N), np.float64)
+    rc = lib.oracle3_moe_gemv(px, int(bool(x_per_slot)), pi, pr, pw, ps, pz,
+                              y.ctypes.data_as(ctypes.c_void_p), M, topk, E, N, K, g)
+    if rc != 0 and not allow_bad_ids:
+        raise ValueError("expert id out of range")
     return y
 
 

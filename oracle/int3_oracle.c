@@ -127,6 +127,49 @@ void oracle3_gemv(const uint16_t* x, const uint32_t* wq3, const uint16_t* scale,
         }
 }
 
+/* ---- expert-indexed GEMV over INT3 experts ------------------------------ */
+
+/* The expert-indexed GEMV of oracle_moe_gemv with INT3 experts: for token t
+ * and slot j with e = ids[t][j], d[t][j][n] = sum_k xin[k] * W_e[n][k], xin
+ * = x[t] (x_per_slot == 0, x [M][K]) or x[t][j] (x [M][topk][K]); expert
+ * e's rows start at wq3 + e*N*3K/32, scale and zero + e*N*(K/g).  Without
+ * route_w, d goes to y[M][topk][N] (zero rows for an invalid id); with it,
+ * y[t][n] = sum_j route_w[t][j] * d[t][j][n] (fp64, j ascending, invalid ids
+ * skipped).  Returns -1 if an id is outside [0, E). */
+int oracle3_moe_gemv(const uint16_t* x, int x_per_slot, const int32_t* ids,
+                     const float* route_w, const uint32_t* wq3, const uint16_t* scale,
+                     const uint8_t* zero, double* y, int64_t M, int64_t topk, int64_t E,
+                     int64_t N, int64_t K, int64_t g)
+{
+    int bad = 0;
+    int64_t G = K / g, wpr = oracle3_row_words(K);
+    if (route_w)
+        for (int64_t i = 0; i < M * N; ++i) y[i] = 0.0;
+    for (int64_t t = 0; t < M; ++t)
+        for (int64_t j = 0; j < topk; ++j) {
+            int64_t e = ids[t * topk + j];
+            if (e < 0 || e >= E) {
+                bad = 1;
+                if (!route_w)
+                    for (int64_t n = 0; n < N; ++n) y[(t * topk + j) * N + n] = 0.0;
+                continue;
+            }
+            const uint16_t* xin = x_per_slot ? x + (t * topk + j) * K : x + t * K;
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += oracle_bf16_to_double(xin[k]) *
+                           oracle3_weight(wq3 + e * N * wpr, scale + e * N * G, zero + e * N * G,
+                                          K, g, n, k);
+                if (route_w)
+                    y[t * N + n] += (double)route_w[t * topk + j] * acc;
+                else
+                    y[(t * topk + j) * N + n] = acc;
+            }
+        }
+    return bad ? -1 : 0;
+}
+
 /* ---- routed SwiGLU FFN over INT3 experts -------------------------------- */
 
 /* The chain of oracle_moe_ffn with INT3 experts: gate/up banks [E][F] rows

@@ -169,3 +169,35 @@ def test_moe_ffn3_rejects_bad_expert_id(oracle):
     ids[0, 1] = 4
     with pytest.raises(ValueError):
         oracle.moe_ffn3(p["x"], ids, p["route_w"], p["gate"], p["up"], p["down"], 128)
+
+
+@pytest.mark.parametrize("x_per_slot", [False, True])
+def test_moe_gemv3_equals_int4_expert_gemv_on_the_same_codes(oracle, x_per_slot):
+    M, E, N, K, topk, g = 3, 5, 24, 384, 2, 128
+    ids, route_w = synth.routing(11, M, topk, E)
+    codes = synth.codes3(11, E * N, K)
+    s = synth.scales(11, E * N, K // g).reshape(E, N, K // g)
+    z = synth.zeros(11, E * N, K // g, "uniform2to6").reshape(E, N, K // g)
+    wq3 = oracle.pack3(codes).reshape(E, N, -1)
+    wq4 = _int4_of(codes).reshape(E, N, -1)
+    x = synth.activations(11, (M, topk, K) if x_per_slot else (M, K))
+    for rw in (None, route_w):
+        y3 = oracle.moe_gemv3(x, ids, rw, wq3, s, z, g, x_per_slot=x_per_slot)
+        y4 = oracle.moe_gemv(x, ids, rw, wq4, s, z, g, x_per_slot=x_per_slot)
+        assert np.array_equal(y3, y4)
+
+
+def test_moe_gemv3_bad_ids(oracle):
+    M, E, N, K, topk, g = 2, 4, 16, 256, 2, 128
+    ids = np.array([[0, 4], [-1, 2]], np.int32)
+    rw = np.full((M, topk), 0.5, np.float32)
+    wq3 = synth.packed_weights3(12, E * N, K).reshape(E, N, -1)
+    s = synth.scales(12, E * N, K // g).reshape(E, N, K // g)
+    z = synth.zeros(12, E * N, K // g, "uniform2to6").reshape(E, N, K // g)
+    x = synth.activations(12, (M, K))
+    with pytest.raises(ValueError):
+        oracle.moe_gemv3(x, ids, rw, wq3, s, z, g)
+    y = oracle.moe_gemv3(x, ids, None, wq3, s, z, g, allow_bad_ids=True)
+    assert np.all(y[0, 1] == 0) and np.all(y[1, 0] == 0)   # invalid slots: zero rows
+    ok = oracle.moe_gemv3(x, np.array([[0, 0], [2, 2]], np.int32), None, wq3, s, z, g)
+    assert np.array_equal(y[0, 0], ok[0, 0]) and np.array_equal(y[1, 1], ok[1, 1])

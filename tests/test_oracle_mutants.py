@@ -58,7 +58,14 @@ MUTANTS3 = [
     ("int3_zero_dropped", [("((double)oracle3_code(wq3, K, n, k) - z) * s", "((double)oracle3_code(wq3, K, n, k)) * s")]),
     ("int3_group_index", [("scale[n * G + k / g]", "scale[n * G + (k / 128) % G]")]),
     ("int3_expert_stride", [("wq_down + e * H * wf", "wq_down + e * H * wh")]),
-    ("int3_chain_route_weight", [("(double)route_w[t * topk + j] * acc", "(double)route_w[j] * acc")]),
+    ("int3_chain_route_weight", [("out[t * H + n] += (double)route_w[t * topk + j] * acc;",
+                                  "out[t * H + n] += (double)route_w[j] * acc;")]),
+    ("int3_gemv_route_weight", [("y[t * N + n] += (double)route_w[t * topk + j] * acc;",
+                                 "y[t * N + n] += (double)route_w[j] * acc;")]),
+    ("int3_gemv_expert_stride", [("wq3 + e * N * wpr, scale + e * N * G", "wq3 + e * wpr, scale + e * N * G")]),
+    ("int3_gemv_scale_stride", [("scale + e * N * G, zero + e * N * G", "scale + e * G, zero + e * N * G")]),
+    ("int3_gemv_slot_input", [("const uint16_t* xin = x_per_slot ? x + (t * topk + j) * K : x + t * K;",
+                               "const uint16_t* xin = x_per_slot ? x + t * K : x + t * K;")]),
 ]
 
 
