@@ -358,6 +358,45 @@ def moe_chain_time(torch, w, M, steps, warmup, l2, fused=True, bits=4):
     return t, float(np.mean(byts))
 
 
+def moe_gemv_time(torch, w, M, steps, warmup, l2, shape="down", bits=4, kernel_id=0):
+    """One expert-indexed GEMV of the MoE workload (64 experts, top-8) over
+    rotated expert banks: shape "gate" (experts [1024, 2304], one activation
+    row per token, per-slot outputs) or "down" (experts [2304, 1024], one
+    row per slot, routed sums).  bits=3: an INT3 bank through w3a16_moe_gemv;
+    otherwise w4a16_moe_gemv with `kernel_id`.  Seconds per call and the
+    distinct-expert bytes it streams."""
+    from w4a16_int4_weight_gemv_gb300 import synth
+    E, topk, g = 64, 8, 128
+    N, K = (1024, 2304) if shape == "gate" else (2304, 1024)
+    x_per_slot, routed = shape == "down", shape == "down"
+    per_bank = E * N * K * (bits / 8.0 + 2.0 / 128)
+    R = max(2, int(math.ceil(2.0 * l2 / per_bank)))
+    ab = algo_bytes if bits == 4 else algo_bytes3
+    sets, byts = [], []
+    for r in range(R):
+        ids, rw = synth.routing(r, M, topk, E)
+        bank = (synth.expert_bank(r, E, N, K, g, "uniform6to10") if bits == 4
+                else synth.expert_bank3(r, E, N, K, g))
+        x = synth.activations(r, (M, topk, K) if x_per_slot else (M, K))
+        out = torch.empty((M, N) if routed else (M, topk, N), dtype=torch.bfloat16, device="cuda")
+        sets.append((_dev(x, torch), _dev(ids, torch), _dev(rw, torch),
+                     tuple(_dev(a, torch) for a in bank), out))
+        rows = M * topk if x_per_slot else M
+        byts.append(len(np.unique(ids)) * ab(0, N, K, g) + rows * K * 2)
+
+    def step(i):
+        x, ids, rw, bank, out = sets[i % R]
+        if bits == 3:
+            w.w3a16_moe_gemv(x, ids, *bank, g, route_w=rw if routed else None,
+                             x_per_slot=x_per_slot, out=out)
+        else:
+            w.w4a16_moe_gemv(x, ids, *bank, g, route_w=rw if routed else None,
+                             x_per_slot=x_per_slot, out=out, kernel_id=kernel_id)
+
+    t = time_steps(torch, step, R, steps, warmup)
+    return t, float(np.mean(byts))
+
+
 def mlp_decode_chain_time(torch, w, M, steps, warmup, l2, fused=True):
     """One dense SwiGLU MLP of a decode step (hidden 4096, intermediate
     14336), every GEMV with programmatic dependent launch and the
@@ -756,6 +795,14 @@ def run_gpu(args):
                                            "frac_measured_peak": round(byts / t / 1e9 / peak, 4),
                                            "tokens_per_s": round(m / t, 1),
                                            "note": "INT3 (~3-bit) expert banks, w3a16_moe_ffn; bytes at 3 bits per weight"}
+        for shape in ("gate", "down"):
+            for m in (1, 4):
+                for bits, kid, tag in ((4, 0, "moe_gemv"), (4, 2, "moe_gemv_bf16_kernel"),
+                                       (3, 0, "moe3_gemv")):
+                    t, byts = moe_gemv_time(torch, w, m, 200, 20, l2, shape, bits, kid)
+                    sweep["%s_%s_M%d" % (tag, shape, m)] = {
+                        "us": round(t * 1e6, 3), "GB/s": round(byts / t / 1e9, 1),
+                        "frac_measured_peak": round(byts / t / 1e9 / peak, 4)}
         extra["sweep"] = sweep
         e2e_steps = max(200, min(args.steps, 3000))
         cabi = e2e_cabi_gbs(torch, w, M, N, K, g, e2e_steps)

@@ -281,6 +281,13 @@ W4A16_API size_t w4a16_moe_workspace_bytes(int M, int topk, int64_t N, int route
  *   route_w != NULL: fp32 [M][topk]; y is bf16 [M][N],
  *                    y[t][n] = sum_j route_w[t][j] * d[t][j][n] (fp32, j ascending);
  *                    needs a workspace of w4a16_moe_workspace_bytes(M, topk, N, 1).
+ * Kernel: the fp16 warp-MMA expert kernel (w4a16_moe_gemv_variant's
+ * kernel 4) where it applies -- M*topk <= 32, g == 128, K % 128 == 0,
+ * N % 16 == 0, the staged activations in shared memory -- else the bf16
+ * warp-MMA expert kernel (kernel 2).  Measured on one GB300, 64 experts,
+ * top-8, M = 1 / 2 / 4: experts [1024, 2304] per slot 7.6 / 9.5 / 13.3 us
+ * against 9.8 / 12.9 / 20.3 for kernel 2; experts [2304, 1024] routed 6.5 /
+ * 9.0 / 17.4 against 9.8 / 13.4 / 21.3.
  * Limits: M*topk <= 256, E >= 1.  Expert ids outside [0, E) are skipped
  * (their contribution is zero) and flagged with W4A16_DEVERR_EXPERT_ID.
  */
@@ -289,6 +296,27 @@ W4A16_API w4a16_status w4a16_moe_gemv(const uint16_t* x, int x_per_slot, const i
                             const uint8_t* zero, uint16_t* y, int M, int topk, int E, int64_t N,
                             int64_t K, int64_t g, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/*
+ * w4a16_moe_gemv_variant -- w4a16_moe_gemv with the kernel named:
+ *   0  the library's choice (what w4a16_moe_gemv runs);
+ *   2  the bf16 warp-MMA expert kernel with TMA rings (any shape within
+ *      w4a16_moe_gemv's limits);
+ *   4  the fp16 warp-MMA expert kernel of w3a16_moe_gemv over INT4 codes
+ *      (the down launch of w4a16_moe_ffn's fp16 path on its own), with its
+ *      limits: M * topk <= 32, g == 128, K a multiple of 128, N a multiple
+ *      of 16, the staged activations in shared memory; routed sums are
+ *      formed in shared memory, so the workspace is not used.
+ * Other ids, or a shape outside the named kernel's limits, give
+ * W4A16_ERR_UNSUPPORTED.  Arguments and results are those of w4a16_moe_gemv.
+ */
+W4A16_API w4a16_status w4a16_moe_gemv_variant(const uint16_t* x, int x_per_slot,
+                                              const int32_t* expert_ids, const float* route_w,
+                                              const uint32_t* wq, const uint16_t* scale,
+                                              const uint8_t* zero, uint16_t* y, int M, int topk,
+                                              int E, int64_t N, int64_t K, int64_t g,
+                                              int kernel_id, void* workspace,
+                                              size_t workspace_bytes, void* stream);
 
 /* Size of the library's fixed scratch buffer (per device), in bytes. */
 #define W4A16_FIXED_SCRATCH_BYTES (1u << 20)
@@ -394,6 +422,39 @@ W4A16_API w4a16_status w3a16_moe_ffn(const uint16_t* x, const int32_t* expert_id
                                      uint16_t* y, int M, int topk, int E, int64_t H, int64_t F,
                                      int64_t g, void* workspace, size_t workspace_bytes,
                                      void* stream);
+
+/*
+ * w3a16_moe_gemv -- the expert-indexed GEMV of w4a16_moe_gemv over an INT3
+ * expert bank (the ~3-bit expert weights above).  For token t and routed
+ * slot j with e = expert_ids[t][j]:
+ *     d[t][j][n] = sum_k xin[k] * W_e[n][k],
+ *     xin = x[t] (x_per_slot == 0, x is [M][K]) or x[t][j] (x is [M][topk][K]).
+ *   wq3 [E][N][3K/32], scale and zero [E][N][K/g].
+ *   route_w == NULL: y is bf16 [M][topk][N], y[t][j] = bf16(d[t][j]), zero
+ *                    rows for an invalid id;
+ *   route_w != NULL: fp32 [M][topk]; y is bf16 [M][N],
+ *                    y[t][n] = bf16(sum_j route_w[t][j] * d[t][j][n]) (fp32,
+ *                    j ascending, invalid ids skipped).
+ * One launch of the fp16 warp-MMA expert kernel (the down launch of
+ * w3a16_moe_ffn on its own).  A tile is 16 output rows of one routed expert
+ * against all of that expert's slots (up to 8 per tile), so each distinct
+ * expert's rows are streamed once whatever the number of slots that select
+ * it.  With route weights a CTA owns whole 16-row output tiles and forms
+ * their routed sums in shared memory; per-slot outputs are stored as each
+ * tile completes, the tiles spread over all CTAs when N / 16 is below the
+ * SM count.  No workspace.
+ * Limits: M * topk <= 32, g == 128, K a multiple of 128 (<= 65536), N a
+ * multiple of 16 (W4A16_ERR_UNSUPPORTED otherwise, or if the staged
+ * activations do not fit in shared memory: 2 * K bytes per token row, or
+ * per slot with x_per_slot, next to the weight rings).
+ * Expert ids outside [0, E) are skipped and flagged with
+ * W4A16_DEVERR_EXPERT_ID.
+ */
+W4A16_API w4a16_status w3a16_moe_gemv(const uint16_t* x, int x_per_slot,
+                                      const int32_t* expert_ids, const float* route_w,
+                                      const uint32_t* wq3, const uint16_t* scale,
+                                      const uint8_t* zero, uint16_t* y, int M, int topk, int E,
+                                      int64_t N, int64_t K, int64_t g, void* stream);
 
 /*
  * w4a16_swiglu -- h[r][n] = bf16(silu(gate[r][n]) * up[r][n]), computed in

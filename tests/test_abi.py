@@ -98,6 +98,11 @@ def test_gemv_without_device_reports_cuda_error(lib):
         pytest.skip("a GPU is present")
     from w4a16_int4_weight_gemv_gb300.binding import Status
     assert _gemv(lib) == Status.ERR_CUDA
+    assert lib.w3a16_moe_gemv(A16, 0, A16, None, A16, A16, A16, A16, 1, 8, 64, 1024, 2304, 128,
+                              None) == Status.ERR_CUDA
+    # kernel 4 takes a routed sum without a workspace: the device is the next check
+    assert lib.w4a16_moe_gemv_variant(A16, 0, A16, A16, A16, A16, A16, A16, 1, 8, 64, 1024, 2304,
+                                      128, 4, None, 0, None) == Status.ERR_CUDA
     assert lib.w4a16_gemv_plan(1, 4096, 4096, 128, None, None, None, None, None) == Status.ERR_CUDA
 
 
@@ -129,6 +134,16 @@ def test_other_entry_points_validate(lib):
     assert moe(A16, 0, A16, A16, A16, A16, A16, A16, 1, 8, 64, 1024, 2304, 128, A16, need - 4,
                None) == Status.ERR_WORKSPACE
     assert lib.w4a16_moe_workspace_bytes(1, 8, 1024, 0) == 0
+    var = lib.w4a16_moe_gemv_variant
+    def mv(kid, M=1, topk=8, N=1024, K=2304, g=128, rw=None, ws=None, nbytes=0):
+        return var(A16, 0, A16, rw, A16, A16, A16, A16, M, topk, 64, N, K, g, kid, ws, nbytes, None)
+    assert mv(3) == Status.ERR_UNSUPPORTED                  # no such expert kernel
+    assert mv(1) == Status.ERR_UNSUPPORTED
+    assert mv(4, M=5) == Status.ERR_UNSUPPORTED             # kernel 4: at most 32 slots
+    assert mv(4, N=1000) == Status.ERR_UNSUPPORTED          # 16-row output tiles
+    assert mv(4, K=2240, g=64) == Status.ERR_UNSUPPORTED    # groups of 128 k
+    assert mv(2, rw=A16) == Status.ERR_WORKSPACE            # kernel 2 needs the routed-sum workspace
+    assert mv(0, rw=A16) == Status.ERR_WORKSPACE            # so does the library's choice
     # fused FFN: 13 pointers, then M, topk, E, H, F, g, workspace, bytes, stream
     ffn = lib.w4a16_moe_ffn
     ptrs = [A16] * 13
@@ -146,6 +161,40 @@ def test_other_entry_points_validate(lib):
     buf = ctypes.create_string_buffer(64)   # ordinary host memory is never reported mapped
     assert lib.w4a16_host_memory_mapped(ctypes.cast(buf, P)) == 0
     assert lib.w4a16_device_error(None, 0, None) == Status.ERR_NULL
+
+
+def test_int3_entry_points_validate(lib):
+    from w4a16_int4_weight_gemv_gb300.binding import Status
+    assert lib.int3_pack(None, A16, 4, 128, None) == Status.ERR_NULL
+    assert lib.int3_pack(A16, A16, 4, 96, None) == Status.ERR_SHAPE      # whole 128-code blocks
+    assert lib.int3_pack(A16, MIS, 4, 128, None) == Status.ERR_ALIGN
+    assert lib.int3_pack(A16, A16, 0, 128, None) == Status.OK
+    assert lib.int3_dequant(A16, A16, A16, None, 0, 4, 128, 128, None) == Status.ERR_NULL
+    assert lib.int3_dequant(A16, A16, A16, A16, 0, 4, 256, 96, None) == Status.ERR_SHAPE
+    assert lib.int3_dequant(A16, A16, A16, A16, 3, 4, 128, 128, None) == Status.ERR_UNSUPPORTED
+    assert lib.int3_dequant(A16, A16, A16, A16, 0, 0, 128, 128, None) == Status.OK
+    ffn = lib.w3a16_moe_ffn
+    ptrs = [A16] * 13
+    need = lib.w3a16_moe_ffn_workspace_bytes(1, 8, 2304, 1024)
+    assert need == 8 * 1024 * 2
+    assert ffn(*([None] + ptrs[1:]), 1, 8, 64, 2304, 1024, 128, A16, need, None) == Status.ERR_NULL
+    assert ffn(*ptrs, 1, 8, 64, 2304, 1000, 128, A16, need, None) == Status.ERR_SHAPE
+    assert ffn(*ptrs, 9, 2, 64, 2304, 1024, 128, A16, need, None) == Status.ERR_UNSUPPORTED
+    assert ffn(*ptrs, 1, 8, 64, 2304, 1024, 128, A16, need - 16, None) == Status.ERR_WORKSPACE
+    assert ffn(*ptrs[:-1], MIS, 1, 8, 64, 2304, 1024, 128, A16, need, None) == Status.ERR_ALIGN
+    # expert GEMV: x, x_per_slot, ids, route_w, wq3, scale, zero, y, M, topk, E, N, K, g, stream
+    def gemv3(x=A16, ids=A16, rw=None, wq3=A16, y=A16, M=1, topk=8, N=1024, K=2304, g=128):
+        return lib.w3a16_moe_gemv(x, 0, ids, rw, wq3, A16, A16, y, M, topk, 64, N, K, g, None)
+    assert gemv3(ids=None) == Status.ERR_NULL
+    assert gemv3(y=None) == Status.ERR_NULL
+    assert gemv3(topk=0) == Status.ERR_SHAPE
+    assert gemv3(K=2300) == Status.ERR_SHAPE                   # whole 128-code blocks
+    assert gemv3(K=64, g=64) == Status.ERR_SHAPE
+    assert gemv3(g=256) == Status.ERR_UNSUPPORTED               # groups of 128 only
+    assert gemv3(M=5) == Status.ERR_UNSUPPORTED                 # 40 slots > 32
+    assert gemv3(N=1000) == Status.ERR_UNSUPPORTED              # 16-row output tiles
+    assert gemv3(wq3=MIS) == Status.ERR_ALIGN
+    assert gemv3(rw=MIS) == Status.ERR_ALIGN
 
 
 def test_binding_rejects_cpu_tensors(lib):

@@ -78,6 +78,7 @@ def run(w, p, ids=None, route_w=None):
     (5, 8, 640, 256, 3),       # H = 5 blocks: one whole and one partial step
     (3, 12, 384, 384, 2),      # 3 blocks: a single partial step in both launches
     (2, 4, 128, 128, 2),       # one block each way, four experts
+    (8, 8, 8192, 128, 2),      # a wide hidden size: launch 1 in 8-warp CTAs (16 do not fit)
 ])
 def test_w3a16_moe_ffn_matches_oracle(w, oracle, M, E, H, F, topk):
     p = synth.moe_problem3(M=M, E=E, H=H, F=F, topk=topk, g=128, seed=9500 + M * 7 + E)
@@ -159,3 +160,119 @@ def test_w3a16_moe_ffn_refusals(w):
     with pytest.raises(w.W4A16Error) as ei:
         w.int3_pack(torch.zeros((2, 96), dtype=torch.uint8, device="cuda"))
     assert ei.value.status == w.Status.ERR_SHAPE
+
+
+# ---- the expert-indexed GEMV over an INT3 bank (w3a16_moe_gemv) ----------
+
+def run_gemv3(w, x, ids, bank3, route_w=None, x_per_slot=False):
+    wq, s, z = bank3
+    y = w.w3a16_moe_gemv(dev(x), dev(ids), dev(wq), dev(s), dev(z), 128,
+                         route_w=None if route_w is None else dev(route_w), x_per_slot=x_per_slot)
+    torch.cuda.synchronize()
+    return y
+
+
+@pytest.mark.parametrize("M,topk,E,N,K,x_per_slot,routed", [
+    (1, 8, 64, 1024, 2304, False, False),   # the MoE workload's gate shape, per slot
+    (1, 8, 64, 2304, 1024, True, True),     # its down shape with the routed sum
+    (4, 8, 64, 2304, 1024, True, True),     # 32 slots: the path's limit
+    (4, 8, 64, 1024, 2304, False, True),    # shared token rows, routed
+    (8, 4, 16, 512, 640, True, False),      # K = 5 blocks: one whole and one partial step
+    (3, 2, 12, 48, 384, False, True),       # 3 row tiles, a single partial step
+    (5, 6, 7, 80, 896, True, False),        # 30 slots of 7 experts: entries of up to 8 slots
+    (2, 3, 5, 16, 128, False, False),       # one row tile, one block
+    (2, 8, 64, 2560, 1024, False, False),   # 160 row tiles: CTAs own whole row tiles
+])
+def test_w3a16_moe_gemv_matches_oracle(w, oracle, M, topk, E, N, K, x_per_slot, routed):
+    seed = 9300 + M * 31 + topk * 7 + E
+    ids, route_w = synth.routing(seed, M, topk, E)
+    bank3 = synth.expert_bank3(seed, E, N, K)
+    x = synth.activations(seed, (M, topk, K) if x_per_slot else (M, K))
+    rw = route_w if routed else None
+    y = run_gemv3(w, x, ids, bank3, rw, x_per_slot)
+    ref = oracle.moe_gemv3(x, ids, rw, *bank3, 128, x_per_slot=x_per_slot)
+    check_close(host_f64(y), ref, "int3 moe_gemv M=%d topk=%d E=%d N=%d K=%d" % (M, topk, E, N, K))
+    assert w.w4a16_device_error(clear=True) == 0
+
+
+def test_w3a16_moe_gemv_one_hot_is_bit_exact(w, oracle):
+    # one nonzero activation per slot: every output is one exact product,
+    # so the bf16 result is the rounding of W_e[n][k0] * x bit for bit
+    M, topk, E, N, K = 2, 4, 6, 64, 640
+    ids, _ = synth.routing(9350, M, topk, E)
+    bank3 = synth.expert_bank3(9350, E, N, K, zero_mode="uniform2to6")
+    x = np.zeros((M, topk, K), np.uint16)
+    ks = [0, 29, 30, 31, 130, 383, 511, 639]
+    for t in range(M):
+        for j in range(topk):
+            x[t, j, ks[t * topk + j]] = 0x3F80 if (t + j) % 2 == 0 else 0xC0A0   # 1.0 or -5.0
+    y = run_gemv3(w, x, ids, bank3, x_per_slot=True)
+    ref = oracle.moe_gemv3(x, ids, None, *bank3, 128, x_per_slot=True)
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.bf16_round(ref))
+
+
+def test_w3a16_moe_gemv_one_expert_in_every_slot(w, oracle):
+    # 32 slots of one expert: four entries of eight slots share its rows
+    M, topk, E, N, K = 4, 8, 9, 256, 1024
+    ids = np.full((M, topk), 7, np.int32)
+    _, route_w = synth.routing(9360, M, topk, E)
+    bank3 = synth.expert_bank3(9360, E, N, K)
+    x = synth.activations(9360, (M, topk, K))
+    for rw in (None, route_w):
+        y = run_gemv3(w, x, ids, bank3, rw, x_per_slot=True)
+        ref = oracle.moe_gemv3(x, ids, rw, *bank3, 128, x_per_slot=True)
+        check_close(host_f64(y), ref, "one expert routed=%s" % (rw is not None))
+    assert w.w4a16_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("routed", [False, True])
+def test_w3a16_moe_gemv_invalid_ids_are_zero_and_flagged(w, oracle, routed):
+    M, topk, E, N, K = 3, 4, 10, 128, 512
+    ids, route_w = synth.routing(9370, M, topk, E)
+    ids = ids.copy()
+    ids[0, 1] = -1
+    ids[2, 3] = E
+    bank3 = synth.expert_bank3(9370, E, N, K)
+    x = synth.activations(9370, (M, K))
+    rw = route_w if routed else None
+    w.w4a16_device_error(clear=True)
+    y = run_gemv3(w, x, ids, bank3, rw)
+    assert w.w4a16_device_error(clear=True) & w.DEVERR_EXPERT_ID
+    ref = oracle.moe_gemv3(x, ids, rw, *bank3, 128, allow_bad_ids=True)
+    if not routed:
+        got = host_f64(y)
+        assert np.all(got[0, 1] == 0) and np.all(got[2, 3] == 0)
+    check_close(host_f64(y), ref, "int3 moe_gemv invalid ids routed=%s" % routed)
+
+
+def test_w3a16_moe_gemv_repeated_calls_and_stream_order(w):
+    M, topk, E, N, K = 2, 8, 64, 2304, 1024
+    ids, route_w = synth.routing(9380, M, topk, E)
+    bank3 = tuple(dev(a) for a in synth.expert_bank3(9380, E, N, K))
+    x = dev(synth.activations(9380, (M, topk, K)))
+    d_ids, d_rw = dev(ids), dev(route_w)
+    outs = [w.w3a16_moe_gemv(x, d_ids, *bank3, 128, route_w=d_rw, x_per_slot=True) for _ in range(3)]
+    # a producer of the activations just before the call: the launch reads
+    # nothing before the preceding kernel has finished
+    x2 = torch.empty_like(x)
+    x2.copy_(x)
+    outs.append(w.w3a16_moe_gemv(x2, d_ids, *bank3, 128, route_w=d_rw, x_per_slot=True))
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+    assert w.w4a16_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("routed", [False, True])
+def test_w3a16_moe_gemv_no_valid_id(w, routed):
+    M, topk, E, N, K = 2, 4, 6, 96, 256
+    ids = np.array([[-1, 6, 7, -2], [100, -1, 6, 9]], np.int32)
+    _, route_w = synth.routing(9390, M, topk, E)
+    bank3 = synth.expert_bank3(9390, E, N, K)
+    x = synth.activations(9390, (M, K))
+    w.w4a16_device_error(clear=True)
+    y = run_gemv3(w, x, ids, bank3, route_w if routed else None)
+    assert w.w4a16_device_error(clear=True) & w.DEVERR_EXPERT_ID
+    assert y.shape == ((M, N) if routed else (M, topk, N))
+    assert torch.count_nonzero(y.float()).item() == 0

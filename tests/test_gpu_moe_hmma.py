@@ -48,6 +48,7 @@ def run(w, p, ids=None, route_w=None):
     (5, 8, 640, 256, 3),       # H = 5 blocks: one whole and one partial step
     (3, 12, 384, 384, 2),      # 3 blocks: a single partial step in both launches
     (2, 4, 128, 128, 2),       # one block each way, four experts
+    (8, 8, 8192, 256, 4),      # a wide hidden size: launch 1 in 8-warp CTAs (16 do not fit)
 ])
 def test_moe_hmma_matches_oracle(w, oracle, M, E, H, F, topk):
     p = synth.moe_problem(M=M, E=E, H=H, F=F, topk=topk, g=128, seed=9000 + M * 7 + E)
@@ -101,3 +102,94 @@ def test_moe_hmma_repeated_calls_are_identical(w):
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     assert w.w4a16_device_error(clear=True) == 0
+
+
+# ---- the down launch on its own: the INT4 expert GEMV (kernel 4) ---------
+
+def bank_dev(b):
+    return tuple(dev(a) for a in b)
+
+
+@pytest.mark.parametrize("M,topk,E,N,K,x_per_slot,routed", [
+    (1, 8, 64, 1024, 2304, False, False),   # the MoE workload's gate shape, per slot
+    (1, 8, 64, 2304, 1024, True, True),     # its down shape with the routed sum
+    (4, 8, 64, 2304, 1024, True, True),     # 32 slots
+    (2, 8, 64, 1024, 2304, False, True),
+    (8, 4, 16, 512, 640, True, False),      # K = 5 blocks: one whole and one partial step
+    (3, 2, 12, 48, 384, False, True),       # 3 row tiles, a single partial step
+    (5, 6, 7, 80, 896, True, False),        # 30 slots of 7 experts
+    (2, 3, 5, 16, 128, False, False),       # one row tile, one block
+    (4, 8, 64, 1024, 2304, False, False),   # 32 slots on 4 staged token rows
+    (2, 8, 64, 2560, 1024, False, False),   # 160 row tiles: CTAs own whole row tiles
+])
+def test_fp16_expert_gemv_matches_oracle(w, oracle, M, topk, E, N, K, x_per_slot, routed):
+    seed = 9400 + M * 31 + topk * 7 + E
+    ids, route_w = synth.routing(seed, M, topk, E)
+    bank = synth.expert_bank(seed, E, N, K, 128, "uniform6to10")
+    x = synth.activations(seed, (M, topk, K) if x_per_slot else (M, K))
+    rw = route_w if routed else None
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *bank_dev(bank), 128,
+                         route_w=None if rw is None else dev(rw), x_per_slot=x_per_slot,
+                         kernel_id=4)
+    torch.cuda.synchronize()
+    ref = oracle.moe_gemv(x, ids, rw, *bank, 128, x_per_slot=x_per_slot)
+    check_close(host_f64(y), ref, "fp16 expert gemv M=%d topk=%d E=%d N=%d K=%d" % (M, topk, E, N, K))
+    assert w.w4a16_device_error(clear=True) == 0
+
+
+def test_fp16_expert_gemv_one_hot_is_bit_exact(w, oracle):
+    M, topk, E, N, K = 2, 4, 6, 64, 640
+    ids, _ = synth.routing(9450, M, topk, E)
+    bank = synth.expert_bank(9450, E, N, K, 128, "uniform6to10")
+    x = np.zeros((M, topk, K), np.uint16)
+    ks = [0, 7, 8, 127, 130, 383, 511, 639]
+    for t in range(M):
+        for j in range(topk):
+            x[t, j, ks[t * topk + j]] = 0x3F80 if (t + j) % 2 == 0 else 0xC0A0   # 1.0 or -5.0
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *bank_dev(bank), 128, x_per_slot=True, kernel_id=4)
+    torch.cuda.synchronize()
+    ref = oracle.moe_gemv(x, ids, None, *bank, 128, x_per_slot=True)
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.bf16_round(ref))
+
+
+@pytest.mark.parametrize("routed", [False, True])
+def test_fp16_expert_gemv_invalid_ids(w, oracle, routed):
+    M, topk, E, N, K = 3, 4, 10, 128, 512
+    ids, route_w = synth.routing(9460, M, topk, E)
+    ids = ids.copy()
+    ids[1, 0] = -7
+    ids[2, 2] = E + 3
+    bank = synth.expert_bank(9460, E, N, K, 128, "uniform6to10")
+    x = synth.activations(9460, (M, K))
+    rw = route_w if routed else None
+    w.w4a16_device_error(clear=True)
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *bank_dev(bank), 128,
+                         route_w=None if rw is None else dev(rw), kernel_id=4)
+    torch.cuda.synchronize()
+    assert w.w4a16_device_error(clear=True) & w.DEVERR_EXPERT_ID
+    # reference: the bad slots given a valid id and, routed, a zero weight
+    ref_ids = ids.copy()
+    ref_ids[1, 0] = ref_ids[2, 2] = 0
+    got = host_f64(y)
+    if routed:
+        ref_rw = route_w.copy()
+        ref_rw[1, 0] = ref_rw[2, 2] = 0.0
+        ref = oracle.moe_gemv(x, ref_ids, ref_rw, *bank, 128)
+    else:
+        ref = oracle.moe_gemv(x, ref_ids, None, *bank, 128)
+        assert np.all(got[1, 0] == 0) and np.all(got[2, 2] == 0)
+        ref[1, 0] = ref[2, 2] = 0.0
+    check_close(got, ref, "fp16 expert gemv invalid ids routed=%s" % routed)
+
+
+def test_fp16_expert_gemv_refusals(w):
+    ids = dev(np.zeros((5, 8), np.int32))   # 40 slots: beyond the kernel
+    bank = bank_dev(synth.expert_bank(9470, 4, 64, 256, 128))
+    x = dev(synth.activations(9470, (5, 256)))
+    with pytest.raises(w.W4A16Error) as ei:
+        w.w4a16_moe_gemv(x, ids, *bank, 128, kernel_id=4)
+    assert ei.value.status == w.Status.ERR_UNSUPPORTED
+    # the library's choice still serves it
+    w.w4a16_moe_gemv(x, ids, *bank, 128)
+    torch.cuda.synchronize()

@@ -435,25 +435,32 @@ def _bank_dev(bank):
     return tuple(dev(a) for a in bank)
 
 
+# the library's choice (the fp16 warp-MMA expert kernel where it applies) and
+# the bf16 warp-MMA expert kernel
+MOE_KERNELS = [0, 2]
+
+
 @pytest.mark.parametrize("M", [1, 2, 4])
-def test_moe_gemv_per_slot(w, oracle, M):
+@pytest.mark.parametrize("kid", MOE_KERNELS)
+def test_moe_gemv_per_slot(kid, w, oracle, M):
     E, N, K, g, topk = 16, 256, 2304, 128, 8
     wq, s, z = synth.expert_bank(61, E, N, K, g)
     ids, _ = synth.routing(61, M, topk, E)
     x = synth.activations(61, (M, K))
-    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g)
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, kernel_id=kid)
     torch.cuda.synchronize()
     ref = oracle.moe_gemv(x, ids, None, wq, s, z, g)
     check_close(host_f64(y), ref, "moe per slot")
     xs = synth.activations(62, (M, topk, K))
-    ys = w.w4a16_moe_gemv(dev(xs), dev(ids), *_bank_dev((wq, s, z)), g, x_per_slot=True)
+    ys = w.w4a16_moe_gemv(dev(xs), dev(ids), *_bank_dev((wq, s, z)), g, kernel_id=kid, x_per_slot=True)
     refs = oracle.moe_gemv(xs, ids, None, wq, s, z, g, x_per_slot=True)
     check_close(host_f64(ys), refs, "moe per slot, x per slot")
 
 
 @pytest.mark.parametrize("M,N,K,g", [(1, 100, 128, 128), (3, 70, 256, 256), (2, 130, 7168, 128),
                                      (5, 40, 9216, 128), (1, 300, 4608, 256)])
-def test_moe_gemv_scale_table_edges(w, oracle, M, N, K, g):
+@pytest.mark.parametrize("kid", MOE_KERNELS)
+def test_moe_gemv_scale_table_edges(kid, w, oracle, M, N, K, g):
     # one group per row (G = 1), tables filled in several load batches
     # (G = 56 over 64 rows), no table at all (G = 72: scales read in the
     # loop), ragged row chunks
@@ -461,26 +468,28 @@ def test_moe_gemv_scale_table_edges(w, oracle, M, N, K, g):
     wq, s, z = synth.expert_bank(66 + K, E, N, K, g)
     ids, r = synth.routing(66 + K, M, topk, E)
     x = synth.activations(66 + K, (M, K))
-    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g)
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, kernel_id=kid)
     torch.cuda.synchronize()
     check_close(host_f64(y), oracle.moe_gemv(x, ids, None, wq, s, z, g), "moe table edges")
     assert w.w4a16_device_error(clear=True) == 0
 
 
-def test_moe_gemv_shared_experts_and_many_slots(w, oracle):
+@pytest.mark.parametrize("kid", MOE_KERNELS)
+def test_moe_gemv_shared_experts_and_many_slots(kid, w, oracle):
     # 12 tokens over 4 experts: every expert serves > 8 slots (two passes at
     # one n-tile for M <= 8 would not be enough)
     M, E, N, K, g, topk = 12, 4, 96, 1024, 128, 3
     wq, s, z = synth.expert_bank(63, E, N, K, g)
     ids, r = synth.routing(63, M, topk, E)
     x = synth.activations(63, (M, K))
-    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, route_w=dev(r))
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, kernel_id=kid, route_w=dev(r))
     torch.cuda.synchronize()
     ref = oracle.moe_gemv(x, ids, r, wq, s, z, g)
     check_close(host_f64(y), ref, "routed sum")
 
 
-def test_moe_gemv_passes_with_several_tiles_per_warp(w, oracle):
+@pytest.mark.parametrize("kid", MOE_KERNELS)
+def test_moe_gemv_passes_with_several_tiles_per_warp(kid, w, oracle):
     # 64 distinct experts over 8 tokens make 128-row CTAs whose warps take two
     # tiles in turn; expert 0 named twice by every token has 16 slots, so its
     # CTAs stream their weights in two passes
@@ -490,33 +499,35 @@ def test_moe_gemv_passes_with_several_tiles_per_warp(w, oracle):
     ids[:, 0] = 0
     ids[:, 1] = 0
     x = synth.activations(67, (M, K))
-    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g)
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, kernel_id=kid)
     torch.cuda.synchronize()
     check_close(host_f64(y), oracle.moe_gemv(x, ids, None, wq, s, z, g), "passes x tiles per warp")
-    yr = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, route_w=dev(r))
+    yr = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, kernel_id=kid, route_w=dev(r))
     torch.cuda.synchronize()
     check_close(host_f64(yr), oracle.moe_gemv(x, ids, r, wq, s, z, g), "routed, passes x tiles per warp")
     assert w.w4a16_device_error(clear=True) == 0
 
 
-def test_moe_gemv_duplicate_ids_in_a_token(w, oracle):
+@pytest.mark.parametrize("kid", MOE_KERNELS)
+def test_moe_gemv_duplicate_ids_in_a_token(kid, w, oracle):
     M, E, N, K, g, topk = 9, 3, 64, 1024, 128, 2
     wq, s, z = synth.expert_bank(64, E, N, K, g)
     ids = np.zeros((M, topk), np.int32)   # every slot on expert 0: 18 slots, > 16
     ids[:, 1] = 0
     x = synth.activations(64, (M, K))
-    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g)
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, kernel_id=kid)
     torch.cuda.synchronize()
     check_close(host_f64(y), oracle.moe_gemv(x, ids, None, wq, s, z, g), "duplicates")
 
 
-def test_moe_bad_expert_id_is_flagged_not_trapped(w, oracle):
+@pytest.mark.parametrize("kid", MOE_KERNELS)
+def test_moe_bad_expert_id_is_flagged_not_trapped(kid, w, oracle):
     M, E, N, K, g, topk = 2, 4, 64, 1024, 128, 2
     wq, s, z = synth.expert_bank(65, E, N, K, g)
     ids = np.array([[1, 7], [-1, 2]], np.int32)
     x = synth.activations(65, (M, K))
     w.w4a16_device_error(clear=True)
-    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g)
+    y = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, kernel_id=kid)
     bits = w.w4a16_device_error(clear=True)
     assert bits & w.DEVERR_EXPERT_ID
     got = host_f64(y)
@@ -526,7 +537,7 @@ def test_moe_bad_expert_id_is_flagged_not_trapped(w, oracle):
     check_close(got[1, 1], good[1, 1], "valid slot 1")
     # routed sum skips the bad slots
     r = np.array([[0.25, 0.75], [0.5, 0.5]], np.float32)
-    yr = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, route_w=dev(r))
+    yr = w.w4a16_moe_gemv(dev(x), dev(ids), *_bank_dev((wq, s, z)), g, kernel_id=kid, route_w=dev(r))
     assert w.w4a16_device_error(clear=True) & w.DEVERR_EXPERT_ID
     want = np.stack([0.25 * good[0, 0], 0.5 * good[1, 1]])
     check_close(host_f64(yr), want, "routed with bad ids")

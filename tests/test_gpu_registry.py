@@ -58,6 +58,21 @@ def test_grouped_variants_match_the_reference(reg, oracle, M):
     assert binding.w4a16_device_error(clear=True) == 0
 
 
+def test_int3_grouped_variants_match_the_reference(reg, oracle):
+    from w4a16_int4_weight_gemv_gb300 import binding
+    E, N, K, g, topk, M = 12, 192, 2304, 128, 4, 3
+    bank3 = synth.expert_bank3(84, E, N, K, g)
+    ids, r = synth.routing(84, M, topk, E)
+    x = synth.activations(84, (M, K))
+    for variant, f in reg.OPS["w3a16_grouped"].items():
+        for rw in (None, r):
+            y = f(dev(x), dev(ids), *(dev(a) for a in bank3), g,
+                  route_w=None if rw is None else dev(rw))
+            torch.cuda.synchronize()
+            check_close(host_f64(y), oracle.moe_gemv3(x, ids, rw, *bank3, g), variant)
+    assert binding.w4a16_device_error(clear=True) == 0
+
+
 @pytest.mark.parametrize("M", [1, 2])
 def test_ffn_variants_match_the_reference(reg, oracle, M):
     from w4a16_int4_weight_gemv_gb300 import binding

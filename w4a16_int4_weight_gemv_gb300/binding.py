@@ -105,6 +105,11 @@ def load_library():
     lib.w3a16_moe_ffn_workspace_bytes.argtypes = [I32, I32, I64, I64]
     lib.w3a16_moe_ffn.restype = I32
     lib.w3a16_moe_ffn.argtypes = [P] * 13 + [I32, I32, I32, I64, I64, I64, P, SZ, P]
+    lib.w4a16_moe_gemv_variant.restype = I32
+    lib.w4a16_moe_gemv_variant.argtypes = [P, I32, P, P, P, P, P, P, I32, I32, I32, I64, I64, I64,
+                                           I32, P, SZ, P]
+    lib.w3a16_moe_gemv.restype = I32
+    lib.w3a16_moe_gemv.argtypes = [P, I32, P, P, P, P, P, P, I32, I32, I32, I64, I64, I64, P]
     _lib = lib
     return lib
 
@@ -336,10 +341,12 @@ def w4a16_moe_workspace_bytes(M: int, topk: int, N: int, route: bool) -> int:
 
 
 def w4a16_moe_gemv(x, expert_ids, wq, scale, zero, g: int, route_w=None, x_per_slot=False,
-                   out=None, workspace=None, stream=None) -> torch.Tensor:
+                   out=None, workspace=None, stream=None, kernel_id: int = 0) -> torch.Tensor:
     """Expert-indexed GEMV.  wq int32 [E, N, K/8]; scale/zero [E, N, K/g];
     expert_ids int32 [M, topk]; x [M, K] or (x_per_slot) [M, topk, K].
-    Returns bf16 [M, topk, N] (no route_w) or [M, N] (routed sum)."""
+    Returns bf16 [M, topk, N] (no route_w) or [M, N] (routed sum).
+    kernel_id: 0 the library's choice, 2 the bf16 warp-MMA expert kernel,
+    4 the fp16 warp-MMA expert kernel (no workspace)."""
     _need(expert_ids, "expert_ids", (torch.int32,))
     M, topk = expert_ids.shape
     _need(wq, "wq", _U32)
@@ -352,10 +359,13 @@ def w4a16_moe_gemv(x, expert_ids, wq, scale, zero, g: int, route_w=None, x_per_s
     if route_w is not None:
         _need(route_w, "route_w", (torch.float32,), (M, topk))
         shape = (M, N)
-        need = w4a16_moe_workspace_bytes(M, topk, N, True)
-        if workspace is None:
+        need = w4a16_moe_workspace_bytes(M, topk, N, True) if kernel_id != 4 else 0
+        if workspace is None and need > 0:
             workspace = torch.empty(need // 4, dtype=torch.float32, device=x.device)
-        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+        if workspace is None:
+            ws_ptr, ws_bytes = None, 0
+        else:
+            ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
         rw = _ptr(route_w)
     else:
         shape = (M, topk, N)
@@ -363,9 +373,17 @@ def w4a16_moe_gemv(x, expert_ids, wq, scale, zero, g: int, route_w=None, x_per_s
     if out is None:
         out = torch.empty(shape, dtype=torch.bfloat16, device=x.device)
     _need(out, "out", _BF16, shape)
-    _check(lib.w4a16_moe_gemv(_ptr(x), int(bool(x_per_slot)), _ptr(expert_ids), rw, _ptr(wq),
-                              _ptr(scale), _ptr(zero), _ptr(out), M, topk, E, N, K, g,
-                              ws_ptr, ws_bytes, _stream(stream, x.get_device())), "w4a16_moe_gemv")
+    if kernel_id == 0:
+        _check(lib.w4a16_moe_gemv(_ptr(x), int(bool(x_per_slot)), _ptr(expert_ids), rw, _ptr(wq),
+                                  _ptr(scale), _ptr(zero), _ptr(out), M, topk, E, N, K, g,
+                                  ws_ptr, ws_bytes, _stream(stream, x.get_device())),
+               "w4a16_moe_gemv")
+    else:
+        _check(lib.w4a16_moe_gemv_variant(_ptr(x), int(bool(x_per_slot)), _ptr(expert_ids), rw,
+                                          _ptr(wq), _ptr(scale), _ptr(zero), _ptr(out), M, topk,
+                                          E, N, K, g, int(kernel_id), ws_ptr, ws_bytes,
+                                          _stream(stream, x.get_device())),
+               "w4a16_moe_gemv_variant")
     return out
 
 
@@ -470,6 +488,37 @@ def w3a16_moe_ffn(x, expert_ids, route_w, gate, up, down, g: int, stream=None) -
                              _ptr(dz), _ptr(y), M, topk, E, H, F, g, _ptr(ws), nbytes,
                              _stream(stream, x.get_device())), "w3a16_moe_ffn")
     return y
+
+
+def w3a16_moe_gemv(x, expert_ids, wq3, scale, zero, g: int, route_w=None, x_per_slot=False,
+                   out=None, stream=None) -> torch.Tensor:
+    """Expert-indexed GEMV over an INT3 (~3-bit) expert bank.  wq3 int32
+    [E, N, 3K/32]; scale/zero [E, N, K/g]; expert_ids int32 [M, topk]; x
+    [M, K] or (x_per_slot) [M, topk, K].  Returns bf16 [M, topk, N] (no
+    route_w) or [M, N] (routed sum).  No workspace."""
+    _need(expert_ids, "expert_ids", (torch.int32,))
+    M, topk = expert_ids.shape
+    _need(wq3, "wq3", _U32)
+    E, N, K3 = wq3.shape
+    if K3 % 12 != 0:
+        raise ValueError("wq3 rows must hold whole 128-code blocks (12 words each)")
+    K = K3 // 12 * 128
+    _need(x, "x", _BF16, (M, topk, K) if x_per_slot else (M, K))
+    _need(scale, "scale", _BF16, (E, N, K // g))
+    _need(zero, "zero", _U8, (E, N, K // g))
+    if route_w is not None:
+        _need(route_w, "route_w", (torch.float32,), (M, topk))
+        shape = (M, N)
+    else:
+        shape = (M, topk, N)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", _BF16, shape)
+    _check(load_library().w3a16_moe_gemv(_ptr(x), int(bool(x_per_slot)), _ptr(expert_ids),
+                                         None if route_w is None else _ptr(route_w), _ptr(wq3),
+                                         _ptr(scale), _ptr(zero), _ptr(out), M, topk, E, N, K, g,
+                                         _stream(stream, x.get_device())), "w3a16_moe_gemv")
+    return out
 
 
 load_library()

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "moe_hmma_gemv.h"
 #include "w4a16.h"
 
 namespace w4a16 {
@@ -391,16 +392,29 @@ w4a16_status w4a16_moe_gemv(const uint16_t* x, int x_per_slot, const int32_t* ex
                             const uint8_t* zero, uint16_t* y, int M, int topk, int E, int64_t N,
                             int64_t K, int64_t g, void* workspace, size_t workspace_bytes,
                             void* stream) {
+    return w4a16_moe_gemv_variant(x, x_per_slot, expert_ids, route_w, wq, scale, zero, y, M, topk,
+                                  E, N, K, g, 0, workspace, workspace_bytes, stream);
+}
+
+w4a16_status w4a16_moe_gemv_variant(const uint16_t* x, int x_per_slot, const int32_t* expert_ids,
+                                    const float* route_w, const uint32_t* wq, const uint16_t* scale,
+                                    const uint8_t* zero, uint16_t* y, int M, int topk, int E,
+                                    int64_t N, int64_t K, int64_t g, int kernel_id,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
     if (!x || !expert_ids || !wq || !scale || !zero || !y) return W4A16_ERR_NULL;
     if (M < 1 || topk < 1 || E < 1 || N < 1 || K < 32 || g < 32) return W4A16_ERR_SHAPE;
     if (K % 32 != 0 || g % 32 != 0 || K % g != 0) return W4A16_ERR_SHAPE;
+    if (kernel_id != 0 && kernel_id != 2 && kernel_id != 4) return W4A16_ERR_UNSUPPORTED;
     if (g % 128 != 0 || M * topk > 256 || K > 65536) return W4A16_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(E) * N > (int64_t(1) << 31) / (K / 8) - 1)
         return W4A16_ERR_UNSUPPORTED;
+    if (kernel_id == 4 && !moe_hmma_gemv_supports(M, topk, N, K, g)) return W4A16_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(expert_ids) || !aligned16(wq) || !aligned16(scale) ||
         !aligned16(zero) || !aligned16(y) || (route_w && !aligned16(route_w)))
         return W4A16_ERR_ALIGN;
-    if (route_w) {
+    // the routed sum's workspace is part of the call's contract whichever
+    // kernel the library picks (kernel 4 alone does without it)
+    if (route_w && kernel_id != 4) {
         const size_t need = w4a16_moe_workspace_bytes(M, topk, N, 1);
         if (!workspace || workspace_bytes < need) return W4A16_ERR_WORKSPACE;
         if (!aligned16(workspace)) return W4A16_ERR_ALIGN;
@@ -408,6 +422,17 @@ w4a16_status w4a16_moe_gemv(const uint16_t* x, int x_per_slot, const int32_t* ex
     DeviceCache* dev = nullptr;
     w4a16_status st = current_device(&dev);
     if (st != W4A16_OK) return st;
+    // the library's choice: the fp16 warp-MMA expert kernel wherever it
+    // applies (faster on every expert shape measured), else kernel 2
+    const bool k4 = (kernel_id == 4 || kernel_id == 0) && moe_hmma_gemv_supports(M, topk, N, K, g) &&
+                    moe_hmma_gemv_fits(dev->info, M, topk, E, N, K, 4, x_per_slot, route_w != nullptr);
+    if (kernel_id == 4 && !k4) return W4A16_ERR_UNSUPPORTED;
+    if (k4) {
+        // routed sums in shared memory: the workspace is not used
+        MoeHmmaGemvArgs a{x, x_per_slot ? 1 : 0, expert_ids, route_w, wq, scale, zero, y,
+                          M, topk, E, N, K, dev->err, 4};
+        return from_cuda(launch_moe_hmma_gemv(a, dev->info, static_cast<cudaStream_t>(stream)));
+    }
     // the whole activation set of one expert pass must fit in shared memory
     if (moe_smem_need(M, static_cast<int>(K), static_cast<int>(g)) > dev->info.max_smem_optin)
         return W4A16_ERR_UNSUPPORTED;
@@ -567,6 +592,27 @@ w4a16_status w3a16_moe_ffn(const uint16_t* x, const int32_t* expert_ids, const f
                   static_cast<uint16_t*>(workspace), y, M, topk, E, H,
                   F,      dev->err,   3};
     return from_cuda(launch_moe_hmma(m, dev->info, static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w3a16_moe_gemv(const uint16_t* x, int x_per_slot, const int32_t* expert_ids,
+                            const float* route_w, const uint32_t* wq3, const uint16_t* scale,
+                            const uint8_t* zero, uint16_t* y, int M, int topk, int E, int64_t N,
+                            int64_t K, int64_t g, void* stream) {
+    if (!x || !expert_ids || !wq3 || !scale || !zero || !y) return W4A16_ERR_NULL;
+    if (M < 1 || topk < 1 || E < 1 || N < 1 || K < 128 || g < 32) return W4A16_ERR_SHAPE;
+    if (K % 128 != 0 || g % 32 != 0 || K % g != 0) return W4A16_ERR_SHAPE;
+    if (!moe_hmma_gemv_supports(M, topk, N, K, g)) return W4A16_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(expert_ids) || !aligned16(wq3) || !aligned16(scale) ||
+        !aligned16(zero) || !aligned16(y) || (route_w && !aligned16(route_w)))
+        return W4A16_ERR_ALIGN;
+    DeviceCache* dev = nullptr;
+    w4a16_status st = current_device(&dev);
+    if (st != W4A16_OK) return st;
+    if (!moe_hmma_gemv_fits(dev->info, M, topk, E, N, K, 3, x_per_slot, route_w != nullptr))
+        return W4A16_ERR_UNSUPPORTED;
+    MoeHmmaGemvArgs a{x, x_per_slot ? 1 : 0, expert_ids, route_w, wq3, scale, zero, y,
+                      M, topk, E, N, K, dev->err, 3};
+    return from_cuda(launch_moe_hmma_gemv(a, dev->info, static_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_swiglu(const uint16_t* gate, const uint16_t* up, int64_t ld_in, uint16_t* h,

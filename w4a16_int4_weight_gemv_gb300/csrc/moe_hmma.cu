@@ -59,6 +59,7 @@
 #include "common.cuh"
 #include "hmma_core.cuh"
 #include "launch.h"
+#include "moe_hmma_gemv.h"
 
 namespace w4a16 {
 namespace {
@@ -91,17 +92,28 @@ struct MoeHK {
     uint16_t* h;               // launch 1 output [M*topk][N]
     uint16_t* y;               // launch 2 output [M][N]
     int M, topk, E, N, K;      // N, K: rows and columns of one expert matrix
-    int ents;                  // staged B columns: M (launch 1) or M * topk
-    int max_rt;                // launch 2: most 16-row output tiles a CTA owns
+    int ents;                  // staged B columns: M (launch 1, and launch 2 with a row per
+                               // token) or M * topk
+    int max_rt;                // launch 2: 16-row output tiles whose products a CTA keeps in
+                               // shared memory for the routed sums (0 with slot_out)
     int wpt, depth;
     uint32_t* err;
+    // launch 2 as an expert GEMV of its own (the kernel's ALONE instantiation):
+    // it reads nothing before its grid-dependency wait and flags invalid ids
+    // itself; slot s
+    // multiplies staged column s / xdiv (1: x a row per slot, topk: a row per
+    // token); slot_out: y is bf16 [M*topk][N] per slot, stored as each tile
+    // completes (zero rows for an invalid id), instead of the routed sums
+    // [M][N]; split (with slot_out): the (row tile, entry) tiles are spread
+    // evenly over all CTAs instead of each CTA owning whole row tiles
+    int xdiv, slot_out, split;
 };
 
 struct MoeHLayout {
     int ring, bfrag, csum, red, bars, ids, ent_e, ent_n, ent_col, ybuf, nent, total;
 };
 __host__ __device__ inline MoeHLayout moeh_layout(int W, int ents, int kblocks, int depth, int max_rt,
-                                                  int bits) {
+                                                  int bits, int slots) {
     MoeHLayout L;
     int off = 0;
     L.ring = off;  // [warp][depth] stages
@@ -123,7 +135,7 @@ __host__ __device__ inline MoeHLayout moeh_layout(int W, int ents, int kblocks, 
     L.ent_col = off;  // [entry][8] slots (launch 2)
     off += kMoeHmmaMaxSlots * 8 * 4;
     L.ybuf = off;  // launch 2: [row tile][slot][16 rows] fp32 products
-    off += max_rt * ents * 16 * 4;
+    off += max_rt * slots * 16 * 4;
     L.nent = off;
     off += 16;
     L.total = off + 128;
@@ -177,7 +189,9 @@ __host__ __device__ constexpr int int3_pair_shift(int P) {  // log2 of the code 
 }
 __host__ __device__ constexpr int int3_pair_lo(int P) { return P == 15 ? 30 : 10 * (P / 5) + P % 5; }
 
-template <int W, int BITS>
+// ALONE: launch 2 as an expert GEMV of its own (the xdiv, slot_out and
+// split fields apply); the FFN's two launches are instantiated without them
+template <int W, int BITS, bool ALONE>
 __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(const MoeHK a) {
     constexpr int T = 32 * W;
     constexpr int kPitch = m_pitch(BITS), kStage = m_stage(BITS);
@@ -195,11 +209,12 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
     const int part = warp - grp * WPT;
     const int D = a.depth;
     const int ENTS = a.ents;
-    const bool p1 = a.phase == 1;
+    const bool p1 = !ALONE && a.phase == 1;
+    const bool slot_out = ALONE && a.slot_out;
 
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw + 127u) & ~127u) - raw);
-    const MoeHLayout L = moeh_layout(W, ENTS, kblocks, D, a.max_rt, BITS);
+    const MoeHLayout L = moeh_layout(W, ENTS, kblocks, D, a.max_rt, BITS, S);
     unsigned char* ring = base + L.ring + warp * D * kStage;
     uint4* bfrag = reinterpret_cast<uint4*>(base + L.bfrag);
     float4* csum = reinterpret_cast<float4*>(base + L.csum);
@@ -225,7 +240,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         if (warp != 0) return;
         const int e = lane < S ? a.ids[lane] : -1;
         const bool valid = lane < S && e >= 0 && e < a.E;
-        if (p1 && lane < S && !valid) raise_device_error(a.err, W4A16_DEVERR_EXPERT_ID);
+        if ((p1 || ALONE) && lane < S && !valid) raise_device_error(a.err, W4A16_DEVERR_EXPERT_ID);
         // the lanes routed to this lane's expert (an invalid slot matches none)
         const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);
         const int first = __ffs(peers) - 1;
@@ -254,6 +269,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         if (lane < kMoeHmmaMaxSlots) s_ids[lane] = valid ? e : -1;
         if (lane == 31) *s_nent = incl;
     };
+    if (ALONE) grid_dependency_wait();  // no input of this launch is known complete
     if (!p1) route();
     __syncthreads();  // barriers initialised, routing of launch 2 published
 
@@ -270,6 +286,16 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
             t0 = static_cast<int>(tt * blockIdx.x / gridDim.x);
             nt = static_cast<int>(tt * (blockIdx.x + 1) / gridDim.x) - t0;
             isz = tpe;
+        } else if (ALONE && a.split && ne > 0) {
+            // an even share of the (row tile, entry) tiles, row-tile-major;
+            // t0 counts from the first entry of the CTA's first row tile
+            const long long tt = static_cast<long long>(ne) * tpe;
+            const long long ta = tt * blockIdx.x / gridDim.x;
+            nt = static_cast<int>(tt * (blockIdx.x + 1) / gridDim.x - ta);
+            rt0 = static_cast<int>(ta / ne);
+            t0 = static_cast<int>(ta - static_cast<long long>(rt0) * ne);
+            nrt = nt > 0 ? (t0 + nt - 1) / ne + 1 : 0;
+            isz = ne;
         } else {
             rt0 = static_cast<int>(static_cast<long long>(tpe) * blockIdx.x / gridDim.x);
             nrt = static_cast<int>(static_cast<long long>(tpe) * (blockIdx.x + 1) / gridDim.x) - rt0;
@@ -426,7 +452,8 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         }
         cp_async_commit();
     };
-    // launch 2: routing and weights are inputs of the whole chain
+    // launch 2: routing and weights are inputs of the whole chain (or, on
+    // its own, read after the wait above)
     if (!p1) {
         if (nu > 0) {
             start_cursor(i_o, i_i);
@@ -460,7 +487,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         // refilled four items ahead as soon as it is converted.
         const int tid = threadIdx.x;
         const int ipc = kblocks * 8;    // items per column
-        const int cols = p1 ? a.M : S;  // staged B columns: tokens or slots
+        const int cols = ENTS;          // staged B columns: tokens or slots
         const int nflat = cols * ipc;
         const int items = (nflat + T - 1) / T;
         auto load_item = [&](int it, uint4 (&v)[2]) {
@@ -517,7 +544,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         // pair's code factor.
         const int tid = threadIdx.x;
         const int cpc = kblocks * 4;    // chunks per column
-        const int cols = p1 ? a.M : S;  // staged B columns: tokens or slots
+        const int cols = ENTS;          // staged B columns: tokens or slots
         const int nflat = cols * cpc;
         const int items = (nflat + T - 1) / T;
         auto load_item = [&](int it, uint4 (&v)[4]) {
@@ -585,7 +612,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
     __syncthreads();
 
     const int g = lane >> 2, c = lane & 3;
-    const int CS = p1 ? a.M : S;  // B column stride of the staged fragments
+    const int CS = ENTS;  // B column stride of the staged fragments
     const int lrow = (lane & 7) + (((lane >> 3) & 1) << 3);
     const int lch = lane >> 4;
     const int sw_s = lane & 7;
@@ -604,7 +631,8 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         tile_of(c_o, c_i, c_ent, c_r);
     }
     // per tile: B column entity of lane g, C column entities 2c, 2c + 1
-    int col_g = 0, col0 = 0, col1 = 0;
+    // (launch 2: staged columns; scol0, scol1 the slots of C columns 2c, 2c + 1)
+    int col_g = 0, col0 = 0, col1 = 0, scol0 = 0, scol1 = 0;
     bool use0 = false, use1 = false, two = false;
     int subz_a = 0, subz_b = 0, subs_a = 0, subs_b = 0;
     auto set_tile = [&]() {
@@ -621,8 +649,15 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
             col_g = cl[g < n ? g : 0];
             use0 = 2 * c < n;
             use1 = 2 * c + 1 < n;
-            col0 = cl[use0 ? 2 * c : 0];
-            col1 = cl[use1 ? 2 * c + 1 : 0];
+            scol0 = cl[use0 ? 2 * c : 0];
+            scol1 = cl[use1 ? 2 * c + 1 : 0];
+            col0 = scol0;
+            col1 = scol1;
+            if (ALONE && a.xdiv != 1) {  // staged columns are tokens
+                col_g /= a.xdiv;
+                col0 /= a.xdiv;
+                col1 /= a.xdiv;
+            }
             two = n > 1;
         }
         const unsigned char *w0, *w8;
@@ -758,16 +793,27 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
                         if (s_ids[t * a.topk + j] == e)
                             a.h[static_cast<size_t>(t * a.topk + j) * a.N + hr] = hv;
                 }
+            } else if (slot_out) {
+                // the entry's slots of output tile c_r, straight to y
+                uint16_t* yr = a.y + static_cast<size_t>(c_r) * 16 + g;
+                if (use0) {
+                    yr[static_cast<size_t>(scol0) * a.N] = f32_to_bf16_rn(tacc.x);
+                    yr[static_cast<size_t>(scol0) * a.N + 8] = f32_to_bf16_rn(tacc.z);
+                }
+                if (use1) {
+                    yr[static_cast<size_t>(scol1) * a.N] = f32_to_bf16_rn(tacc.y);
+                    yr[static_cast<size_t>(scol1) * a.N + 8] = f32_to_bf16_rn(tacc.w);
+                }
             } else {
                 // the entry's slot columns of output tile c_r, to shared memory
                 float* yb = ybuf + static_cast<size_t>(c_r - rt0) * S * 16;
                 if (use0) {
-                    yb[col0 * 16 + g] = tacc.x;
-                    yb[col0 * 16 + g + 8] = tacc.z;
+                    yb[scol0 * 16 + g] = tacc.x;
+                    yb[scol0 * 16 + g + 8] = tacc.z;
                 }
                 if (use1) {
-                    yb[col1 * 16 + g] = tacc.y;
-                    yb[col1 * 16 + g + 8] = tacc.w;
+                    yb[scol1 * 16 + g] = tacc.y;
+                    yb[scol1 * 16 + g + 8] = tacc.w;
                 }
             }
         }
@@ -785,7 +831,17 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
                                           make_float4(0.f, 0.f, 0.f, 0.f));
     cp_async_wait_pending(0);
     if (timed_out && lane == 0) raise_device_error(a.err, W4A16_DEVERR_TIMEOUT);
-    if (!p1) {
+    if (slot_out) {
+        // the valid slots were stored as their tiles completed; the rows of
+        // an invalid slot are zero (a row tile shared by two CTAs gets its
+        // zeros twice)
+        for (int idx = threadIdx.x; idx < nrt * S * 16; idx += T) {
+            const int rl = idx / (S * 16);
+            const int rem = idx - rl * S * 16;
+            const int sl = rem >> 4, row = rem & 15;
+            if (s_ids[sl] < 0) a.y[static_cast<size_t>(sl) * a.N + (rt0 + rl) * 16 + row] = 0;
+        }
+    } else if (!p1) {
         // routed sums of the CTA's output tiles: every slot's product is in
         // shared memory; slots in order, invalid ids skipped
         __syncthreads();
@@ -805,27 +861,31 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
 }
 
 struct MoeHPlan {
-    int warps, ctas, wpt, depth, smem, max_rt;
+    int warps, ctas, wpt, depth, smem, max_rt, split;
 };
 // Warps per CTA.  Launch 1 runs 16-warp CTAs (twice the warps on an SM for
-// its long unit runs).  Launch 2 does too for up to 16 slots; with more, the
-// 16 x 512 k activations of every slot fill shared memory and 8-warp CTAs
-// are faster.  Measured, MoE chain of 64 experts (2304 x 1024), top-8:
-// 8/8 warps 20.1 / 34.4 / 56.6 us at M = 1 / 2 / 4; 16/8 18.4 / 27.0 / 49.3;
-// 16/16 16.4 / 23.3 / 54.0.
-int moe_warps(int phase, int slots) {
-    return (phase == 1 || slots <= 16) ? kMWWide : kMWPaired;
+// its long unit runs).  Launch 2 does too for up to 16 staged columns; with
+// more, the 16 x 512 k activations of every slot fill shared memory and
+// 8-warp CTAs are faster.  Measured, MoE chain of 64 experts (2304 x 1024),
+// top-8: 8/8 warps 20.1 / 34.4 / 56.6 us at M = 1 / 2 / 4; 16/8 18.4 / 27.0
+// / 49.3; 16/16 16.4 / 23.3 / 54.0.
+int moe_warps(int phase, int ents) {
+    return (phase == 1 || ents <= 16) ? kMWWide : kMWPaired;
 }
 // CTAs, warps per tile and ring depth for one launch, at most one CTA per SM
 // (two fit where shared memory allows, for the next launch's).  Launch 1:
 // tiles_max (entry, pair) tiles, the split of K steps over warps that
 // minimises the busiest warp's units.  Launch 2: row_tiles output tiles over
-// the CTAs, tiles_max entries at most.
-MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int kblocks, long long tiles_max,
-                       int row_tiles, int bits) {
+// the CTAs, tiles_max entries at most; `slots` products per row tile kept
+// in shared memory for the routed sums, or none with slot_out -- whose
+// (row tile, entry) tiles are spread over all CTAs when there are fewer row
+// tiles than SMs.
+MoeHPlan plan_moe_hmma_w(const DeviceInfo& dev, int phase, int ents, int slots, int kblocks,
+                         long long tiles_max, int row_tiles, int bits, int slot_out, int warps) {
     MoeHPlan p{};
-    p.warps = moe_warps(phase, ents);
+    p.warps = warps;
     const int nsteps = (kblocks + 3) / 4;
+    int ybuf_rt = 0;
     if (phase == 1) {
         if (tiles_max < 1) return p;
         p.ctas = static_cast<int>(tiles_max < dev.sms ? tiles_max : dev.sms);
@@ -842,28 +902,50 @@ MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int kblocks, 
         }
         p.max_rt = 0;
     } else {
-        if (row_tiles < 1) return p;
-        p.ctas = row_tiles < dev.sms ? row_tiles : dev.sms;
-        p.max_rt = (row_tiles + p.ctas - 1) / p.ctas;
+        if (row_tiles < 1 || tiles_max < 1) return p;
         // tiles_max: at most this many entries.  Each entry's K steps go to
         // one warp, or to a power of two of warps while the CTA's tiles
         // leave warps idle (one token: 8 entries on 16 warps, two each)
-        const long long tiles = static_cast<long long>(p.max_rt) * tiles_max;
+        long long tiles;
+        p.split = slot_out && row_tiles < dev.sms ? 1 : 0;
+        if (p.split) {
+            const long long tt = static_cast<long long>(row_tiles) * tiles_max;
+            p.ctas = static_cast<int>(tt < dev.sms ? tt : dev.sms);
+            tiles = (tt + p.ctas - 1) / p.ctas;
+            p.max_rt = 0;
+        } else {
+            p.ctas = row_tiles < dev.sms ? row_tiles : dev.sms;
+            p.max_rt = (row_tiles + p.ctas - 1) / p.ctas;
+            tiles = static_cast<long long>(p.max_rt) * tiles_max;
+        }
         p.wpt = 1;
         while (p.wpt * 2 <= nsteps && tiles * p.wpt * 2 <= p.warps) p.wpt *= 2;
+        if (slot_out) p.max_rt = 0;  // nothing kept in shared memory
+        ybuf_rt = p.max_rt;
     }
     const int half = dev.smem_per_sm / 2 - 1024;
-    const int budget =
-        p.warps == kMWPaired && moeh_layout(p.warps, ents, kblocks, 2, p.max_rt, bits).total <= half
-            ? half
-            : dev.max_smem_optin;
+    const int budget = p.warps == kMWPaired &&
+                               moeh_layout(p.warps, ents, kblocks, 2, ybuf_rt, bits, slots).total <= half
+                           ? half
+                           : dev.max_smem_optin;
     p.depth = 2;
     while (p.depth < kMMaxDepth &&
-           moeh_layout(p.warps, ents, kblocks, p.depth + 1, p.max_rt, bits).total <= budget)
+           moeh_layout(p.warps, ents, kblocks, p.depth + 1, ybuf_rt, bits, slots).total <= budget)
         ++p.depth;
-    p.smem = moeh_layout(p.warps, ents, kblocks, p.depth, p.max_rt, bits).total;
+    p.smem = moeh_layout(p.warps, ents, kblocks, p.depth, ybuf_rt, bits, slots).total;
     if (p.smem > dev.max_smem_optin) p.ctas = 0;
     return p;
+}
+// moe_warps' choice, or 8-warp CTAs where a 16-warp CTA's rings and staged
+// activations do not fit in shared memory
+MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int slots, int kblocks,
+                       long long tiles_max, int row_tiles, int bits, int slot_out) {
+    const int warps = moe_warps(phase, ents);
+    const MoeHPlan p =
+        plan_moe_hmma_w(dev, phase, ents, slots, kblocks, tiles_max, row_tiles, bits, slot_out, warps);
+    if (p.ctas > 0 || warps == kMWPaired) return p;
+    return plan_moe_hmma_w(dev, phase, ents, slots, kblocks, tiles_max, row_tiles, bits, slot_out,
+                           kMWPaired);
 }
 
 }  // namespace
@@ -883,10 +965,50 @@ static long long moe_entries_bound(int S, int E) {
 bool moe_hmma_fits(const DeviceInfo& dev, int M, int topk, int E, int64_t H, int64_t F, int bits) {
     const int S = M * topk;
     const long long d = E < S ? E : S;
-    return plan_moe_hmma(dev, 1, M, static_cast<int>(H / 128), d * (F / 8), 0, bits).ctas > 0 &&
-           plan_moe_hmma(dev, 2, S, static_cast<int>(F / 128), moe_entries_bound(S, E),
-                         static_cast<int>(H / 16), bits).ctas > 0;
+    return plan_moe_hmma(dev, 1, M, 0, static_cast<int>(H / 128), d * (F / 8), 0, bits, 0).ctas > 0 &&
+           plan_moe_hmma(dev, 2, S, S, static_cast<int>(F / 128), moe_entries_bound(S, E),
+                         static_cast<int>(H / 16), bits, 0).ctas > 0;
 }
+
+namespace {
+// one launch of k_moe_hmma with plan p (BITS 3 or 4; 8- or 16-warp CTAs;
+// ALONE: an expert GEMV of its own)
+template <bool ALONE>
+cudaError_t launch_moe_hmma_one(const MoeHK& k, const MoeHPlan& p, int bits, cudaStream_t s) {
+    const bool wide = p.warps == kMWWide, b3 = bits == 3;
+    const void* kern = b3 ? (wide ? reinterpret_cast<const void*>(k_moe_hmma<kMWWide, 3, ALONE>)
+                                  : reinterpret_cast<const void*>(k_moe_hmma<kMWPaired, 3, ALONE>))
+                          : (wide ? reinterpret_cast<const void*>(k_moe_hmma<kMWWide, 4, ALONE>)
+                                  : reinterpret_cast<const void*>(k_moe_hmma<kMWPaired, 4, ALONE>));
+    cudaError_t e = ensure_dynamic_smem(kern, p.smem);
+    if (e != cudaSuccess) return e;
+    // the two launches ask for different shared memory: with the largest
+    // carve-out for both, a launch-2 CTA can be resident beside a
+    // launch-1 CTA (an SM whose carve-out must change waits to drain)
+    static bool carveout_set[4] = {false, false, false, false};
+    const int ck = (b3 ? 2 : 0) + (wide ? 1 : 0);
+    if (!carveout_set[ck]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        carveout_set[ck] = true;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(p.ctas);
+    cfg.blockDim = dim3(32 * p.warps);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return b3 ? (wide ? cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWWide, 3, ALONE>, k)
+                      : cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWPaired, 3, ALONE>, k))
+              : (wide ? cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWWide, 4, ALONE>, k)
+                      : cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWPaired, 4, ALONE>, k));
+}
+}  // namespace
 
 cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStream_t s) {
     const int S = a.M * a.topk;
@@ -901,6 +1023,7 @@ cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStr
         k.err = a.err;
         k.h = a.h;
         k.y = a.y;
+        k.xdiv = 1;
         long long tiles_max = 0;
         int row_tiles = 0;
         if (phase == 1) {
@@ -926,46 +1049,63 @@ cudaError_t launch_moe_hmma(const MoeHmmaArgs& a, const DeviceInfo& dev, cudaStr
             row_tiles = static_cast<int>(a.H / 16);
             tiles_max = moe_entries_bound(S, a.E);
         }
-        const MoeHPlan p = plan_moe_hmma(dev, phase, k.ents, k.K / 128, tiles_max, row_tiles, a.bits);
+        const MoeHPlan p =
+            plan_moe_hmma(dev, phase, k.ents, S, k.K / 128, tiles_max, row_tiles, a.bits, 0);
         if (p.ctas < 1) return cudaErrorInvalidConfiguration;
         k.max_rt = p.max_rt;
         k.wpt = p.wpt;
         k.depth = p.depth;
-        const bool wide = p.warps == kMWWide, b3 = a.bits == 3;
-        const void* kern = b3 ? (wide ? reinterpret_cast<const void*>(k_moe_hmma<kMWWide, 3>)
-                                      : reinterpret_cast<const void*>(k_moe_hmma<kMWPaired, 3>))
-                              : (wide ? reinterpret_cast<const void*>(k_moe_hmma<kMWWide, 4>)
-                                      : reinterpret_cast<const void*>(k_moe_hmma<kMWPaired, 4>));
-        cudaError_t e = ensure_dynamic_smem(kern, p.smem);
-        if (e != cudaSuccess) return e;
-        // the two launches ask for different shared memory: with the largest
-        // carve-out for both, a launch-2 CTA can be resident beside a
-        // launch-1 CTA (an SM whose carve-out must change waits to drain)
-        static bool carveout_set[4] = {false, false, false, false};
-        const int ck = (b3 ? 2 : 0) + (wide ? 1 : 0);
-        if (!carveout_set[ck]) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
-            if (e != cudaSuccess) return e;
-            carveout_set[ck] = true;
-        }
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(p.ctas);
-        cfg.blockDim = dim3(32 * p.warps);
-        cfg.dynamicSmemBytes = p.smem;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = b3 ? (wide ? cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWWide, 3>, k)
-                       : cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWPaired, 3>, k))
-               : (wide ? cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWWide, 4>, k)
-                       : cudaLaunchKernelEx(&cfg, k_moe_hmma<kMWPaired, 4>, k));
+        const cudaError_t e = launch_moe_hmma_one<false>(k, p, a.bits, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+bool moe_hmma_gemv_supports(int M, int topk, int64_t N, int64_t K, int64_t g) {
+    return g == 128 && M >= 1 && topk >= 1 && M * topk <= kMoeHmmaMaxSlots && N >= 16 &&
+           N % 16 == 0 && K >= 128 && K % 128 == 0 && N <= (int64_t(1) << 24) && K <= 65536;
+}
+
+// staged activation columns: one per slot, or one per token when the slots
+// of a token share its row
+static int moe_gemv_cols(int M, int topk, int x_per_slot) { return x_per_slot ? M * topk : M; }
+
+bool moe_hmma_gemv_fits(const DeviceInfo& dev, int M, int topk, int E, int64_t N, int64_t K, int bits,
+                        int x_per_slot, int routed) {
+    const int S = M * topk;
+    return plan_moe_hmma(dev, 2, moe_gemv_cols(M, topk, x_per_slot), S, static_cast<int>(K / 128),
+                         moe_entries_bound(S, E), static_cast<int>(N / 16), bits, routed ? 0 : 1)
+               .ctas > 0;
+}
+
+cudaError_t launch_moe_hmma_gemv(const MoeHmmaGemvArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+    const int S = a.M * a.topk;
+    MoeHK k{};
+    k.phase = 2;
+    k.x = a.x;
+    k.xdiv = a.x_per_slot ? 1 : a.topk;
+    k.slot_out = a.route_w ? 0 : 1;
+    k.ids = a.ids;
+    k.route_w = a.route_w;
+    k.wq_a = reinterpret_cast<const unsigned char*>(a.wq);
+    k.scale_a = a.scale;
+    k.zero_a = a.zero;
+    k.y = a.y;
+    k.M = a.M;
+    k.topk = a.topk;
+    k.E = a.E;
+    k.N = static_cast<int>(a.N);
+    k.K = static_cast<int>(a.K);
+    k.ents = moe_gemv_cols(a.M, a.topk, a.x_per_slot);
+    k.err = a.err;
+    const MoeHPlan p = plan_moe_hmma(dev, 2, k.ents, S, k.K / 128, moe_entries_bound(S, a.E),
+                                     static_cast<int>(a.N / 16), a.bits, k.slot_out);
+    if (p.ctas < 1) return cudaErrorInvalidConfiguration;
+    k.max_rt = p.max_rt;
+    k.split = p.split;
+    k.wpt = p.wpt;
+    k.depth = p.depth;
+    return launch_moe_hmma_one<true>(k, p, a.bits, s);
 }
 
 }  // namespace w4a16

@@ -30,6 +30,12 @@ def _dense(kernel_id: int):
     return run
 
 
+def _grouped(kernel_id: int):
+    def run(x, expert_ids, wq, scale, zero, g, **kw):
+        return binding.w4a16_moe_gemv(x, expert_ids, wq, scale, zero, g, kernel_id=kernel_id, **kw)
+    return run
+
+
 def _ffn(fused: bool):
     def run(x, expert_ids, route_w, gate, up, down, g, **kw):
         return binding.moe_ffn(x, expert_ids, route_w, gate, up, down, g, fused=fused, **kw)
@@ -48,7 +54,13 @@ OPS = {
     },
     # per-slot products of the routed experts, or their routed sum
     "w4a16_grouped": {
-        "tma": binding.w4a16_moe_gemv,
+        "planned": _grouped(0),   # the library's choice (fp16_mma where it applies, else tma)
+        "tma": _grouped(2),       # bf16 mma.sync expert kernel, TMA rings, M*topk <= 256
+        "fp16_mma": _grouped(4),  # fp16 mma.sync expert kernel, routed sums in shared memory, M*topk <= 32
+    },
+    # the same over an ~3-bit (INT3) expert bank
+    "w3a16_grouped": {
+        "fp16_mma": binding.w3a16_moe_gemv,
     },
     # routed SwiGLU expert FFN
     "w4a16_ffn": {
@@ -64,7 +76,8 @@ OPS = {
 # what an ordinary run gets
 DEFAULTS = {
     "w4a16_dense": "planned",
-    "w4a16_grouped": "tma",
+    "w4a16_grouped": "planned",
+    "w3a16_grouped": "fp16_mma",
     "w4a16_ffn": "fused",
     "w3a16_ffn": "fp16_mma",
 }
