@@ -1,6 +1,7 @@
 // Routed SwiGLU expert FFN of 1..8 tokens on the fp16 warp-MMA path (g ==
 // 128): the grouped expert kernel of the local-kimi README (technical-detail
-// section), as two launches.
+// section), as two launches; the second also serves alone as the expert-
+// indexed GEMV (below).
 //
 //   1. gate/up: for every distinct routed expert e, the gate and up products
 //      of all tokens, h[t][j] = bf16(silu(bf16(W^gate_e x[t])) *
@@ -39,6 +40,16 @@
 // Launch.  Launch 2 reads the routing and its weights before its
 // grid-dependency wait; launch 1 signals its dependents only after its own
 // wait, so everything launch 2 reads early was complete before launch 1 ran.
+//
+// Expert GEMV.  Launch 2 alone (template flag ALONE) is an expert-indexed
+// GEMV: d[t][j] = W_e x_in for every routed slot, x_in a row per slot or per
+// token.  It reads nothing before its wait and flags invalid ids itself.
+// Slots that share a token row share one staged B column (tile columns are
+// slots, their B and sums are looked up through slot / topk).  With route
+// weights the routed sums are formed as in the FFN; per-slot outputs are
+// stored from registers as each tile completes, and when N / 16 row tiles
+// are fewer than the SMs the (row tile, entry) tiles are dealt evenly over
+// all CTAs instead (a 1024-row expert has 64 row tiles).
 //
 // ~3-bit experts (BITS == 3; the README's hardware-requirements paragraph
 // asks for expert weights near three bits, the INT3 format is this
