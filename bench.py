@@ -619,6 +619,9 @@ WORKLOADS = {
 }
 
 
+GEMV_MOE_WORKLOADS = ("moe_gemv_gate", "moe_gemv_down", "moe3_gemv_gate", "moe3_gemv_down")
+
+
 def run_profile(args):
     """Plain stream launches of one workload (no graph, no timing): the
     command ncu captures.  --M overrides the token count."""
@@ -643,6 +646,31 @@ def run_profile(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile_workload": args.workload, "M": M, "launches_per_chain": 2,
                           "chains": args.warmup + args.steps}))
+        return
+    if args.workload in GEMV_MOE_WORKLOADS:
+        # one expert GEMV of the MoE workload (64 experts, top-8): gate shape
+        # [1024, 2304] per slot, or down shape [2304, 1024] with a row per
+        # slot and the routed sum; moe3_*: an INT3 bank
+        from w4a16_int4_weight_gemv_gb300 import synth
+        M = args.M or 1
+        bits = 3 if args.workload.startswith("moe3") else 4
+        down = args.workload.endswith("down")
+        N, K = (2304, 1024) if down else (1024, 2304)
+        ids, rw = synth.routing(0, M, 8, 64)
+        bank = synth.expert_bank3(0, 64, N, K) if bits == 3 else \
+            synth.expert_bank(0, 64, N, K, 128, "uniform6to10")
+        x = _dev(synth.activations(0, (M, 8, K) if down else (M, K)), torch)
+        ids, rw = _dev(ids, torch), _dev(rw, torch)
+        bank = tuple(_dev(a, torch) for a in bank)
+        for i in range(args.warmup + args.steps):
+            if bits == 3:
+                w.w3a16_moe_gemv(x, ids, *bank, 128, route_w=rw if down else None, x_per_slot=down)
+            else:
+                w.w4a16_moe_gemv(x, ids, *bank, 128, route_w=rw if down else None, x_per_slot=down,
+                                 kernel_id=args.kernel_id)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_workload": args.workload, "M": M, "N": N, "K": K,
+                          "launches": args.warmup + args.steps}))
         return
     M, N, K, zmode, od = WORKLOADS[args.workload]
     M = args.M or M
@@ -934,7 +962,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
                     help="plain launches of --workload for a profiler; prints no bench line")
-    ap.add_argument("--workload", default="square", choices=sorted(list(WORKLOADS) + ["moe", "moe3"]))
+    ap.add_argument("--workload", default="square", choices=sorted(list(WORKLOADS) + ["moe", "moe3"] + list(GEMV_MOE_WORKLOADS)))
     ap.add_argument("--M", type=int, default=0)
     ap.add_argument("--kernel-id", type=int, default=0)
     args = ap.parse_args()
