@@ -281,7 +281,12 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         if (lane == 31) *s_nent = incl;
     };
     if (ALONE) grid_dependency_wait();  // no input of this launch is known complete
-    if (!p1) route();
+    // launch 2 in the chain routes now; launch 1 and the INT4 expert GEMV
+    // route while their first activation loads are in flight (measured on
+    // the expert GEMV, 64 experts, top-8: INT4 1-6 % faster at 1..4 tokens,
+    // INT3 -- one staging item in flight, not four -- 1-2 % slower)
+    const bool early_route = !p1 && (!ALONE || BITS == 3);
+    if (early_route) route();
     __syncthreads();  // barriers initialised, routing of launch 2 published
 
     // Tiles.  Launch 1: the CTA's range of the (entry, 8-row pair) tiles,
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
             isz = ne > 0 ? ne : 1;
         }
     };
-    if (!p1) set_range(*s_nent);
+    if (early_route) set_range(*s_nent);
 
     const size_t row_bytes = BITS == 4 ? static_cast<size_t>(a.K) >> 1 : static_cast<size_t>(a.K) / 128 * 48;
     const int sw_h = lane >> 4, sw_c = ((lane & 15) ^ sw_h) << 4;
@@ -338,7 +343,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         my_steps = (nsteps > part) ? (nsteps - part + WPT - 1) / WPT : 0;
         nu = my_tiles * my_steps;
     };
-    if (!p1) set_units();
+    if (early_route) set_units();
     int i_u = 0, i_slot = 0, i_step = part, i_o = 0, i_i = 0;
     auto start_cursor = [&](int& o, int& in) {
         const int t = t0 + grp;
@@ -463,9 +468,8 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
         }
         cp_async_commit();
     };
-    // launch 2: routing and weights are inputs of the whole chain (or, on
-    // its own, read after the wait above)
-    if (!p1) {
+    // launch 2: routing and weights are inputs of the whole chain
+    if (early_route) {
         if (nu > 0) {
             start_cursor(i_o, i_i);
             producer_tile();
@@ -475,10 +479,10 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
     grid_dependency_wait();
     if (p1) grid_dependents_launch();
 
-    // launch 1 routes while its first activation loads are in flight, then
-    // requests its first units
+    // launch 1 (and the INT4 expert GEMV) routes while its first activation
+    // loads are in flight, then requests its first units
     auto start_launch1 = [&]() {
-        if (!p1) return;
+        if (early_route) return;
         route();
         __syncthreads();
         set_range(*s_nent);
