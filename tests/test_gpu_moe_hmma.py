@@ -193,3 +193,34 @@ def test_fp16_expert_gemv_refusals(w):
     # the library's choice still serves it
     w.w4a16_moe_gemv(x, ids, *bank, 128)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("bits", [4, 3])
+def test_expert_gemv_after_a_producing_gemv(w, bits):
+    # the expert GEMV's activations come from the GEMV launched just before
+    # it (a kernel that releases its dependents early): the expert GEMV must
+    # read them only after that GEMV has finished -- its result equals the
+    # one computed after a full synchronisation, call after call
+    M, topk, E, N, K, K0 = 2, 8, 64, 1024, 2304, 4096
+    p = synth.dense_problem(M, K, K0, 128, "uniform6to10", seed=9480)
+    ids, rw = synth.routing(9480, M, topk, E)
+    bank = bank_dev(synth.expert_bank3(9480, E, N, K) if bits == 3 else
+                    synth.expert_bank(9480, E, N, K, 128, "uniform6to10"))
+    x0, wq0, s0, z0 = (dev(p[k]) for k in ("x", "wq", "scale", "zero"))
+    d_ids, d_rw = dev(ids), dev(rw)
+
+    def expert(x, routed):
+        f = w.w3a16_moe_gemv if bits == 3 else w.w4a16_moe_gemv
+        return f(x, d_ids, *bank, 128, route_w=d_rw if routed else None)
+
+    for routed in (False, True):
+        xs = w.w4a16_gemv(x0, wq0, s0, z0, 128)
+        torch.cuda.synchronize()
+        want = expert(xs, routed)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            xc = w.w4a16_gemv(x0, wq0, s0, z0, 128, weights_static=True)
+            got = expert(xc, routed)
+            torch.cuda.synchronize()
+            assert torch.equal(got, want), routed
+    assert w.w4a16_device_error(clear=True) == 0
