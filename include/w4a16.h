@@ -326,13 +326,15 @@ W4A16_API w4a16_status w4a16_moe_gemv_variant(const uint16_t* x, int x_per_slot,
  * allocate device memory or lend a workspace: engines whose device memory is
  * split into fixed pools, plug-ins whose host runtime owns the allocator.
  * (The README has no counterpart; this is an integration convenience of
- * this library.)  Same arguments and results as w4a16_moe_gemv, minus the
- * workspace: the fp32 partials of the routed sum go to a buffer of
- * W4A16_FIXED_SCRATCH_BYTES compiled into the library, one per device, held
- * until the process exits.  Nothing is allocated by the call.
+ * this library.)  Same arguments, kernels and results as w4a16_moe_gemv,
+ * minus the workspace: where the routed sum needs fp32 partials (the bf16
+ * expert kernel; the fp16 one keeps them in shared memory) they go to a
+ * buffer of W4A16_FIXED_SCRATCH_BYTES compiled into the library, one per
+ * device, held until the process exits.  Nothing is allocated by the call.
  *   - Only calls with route_w use the buffer; calls without it need none.
  *   - Requests needing more than W4A16_FIXED_SCRATCH_BYTES
- *     (M * topk * N * 4 bytes with route_w) return W4A16_ERR_WORKSPACE.
+ *     (M * topk * N * 4 bytes with route_w) return W4A16_ERR_WORKSPACE,
+ *     whichever kernel would run.
  *   - The first routed call on a device looks the buffer up
  *     (cudaGetSymbolAddress) and caches its address for the life of the
  *     process: do not use the call after cudaDeviceReset.
