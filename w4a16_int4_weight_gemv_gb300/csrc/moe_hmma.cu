@@ -75,7 +75,7 @@
 namespace w4a16 {
 namespace {
 
-// warps per CTA: 8 (two CTAs fit an SM) or 16 (launch 1 with long runs)
+// warps per CTA: 16, or 8 (two CTAs to an SM) where 16 do not fit
 constexpr int kMWPaired = 8;
 constexpr int kMWWide = 16;
 constexpr int kMMaxDepth = 4;
@@ -878,15 +878,13 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
 struct MoeHPlan {
     int warps, ctas, wpt, depth, smem, max_rt, split;
 };
-// Warps per CTA.  Launch 1 runs 16-warp CTAs (twice the warps on an SM for
-// its long unit runs).  Launch 2 does too for up to 16 staged columns; with
-// more, the 16 x 512 k activations of every slot fill shared memory and
-// 8-warp CTAs are faster.  Measured, MoE chain of 64 experts (2304 x 1024),
-// top-8: 8/8 warps 20.1 / 34.4 / 56.6 us at M = 1 / 2 / 4; 16/8 18.4 / 27.0
-// / 49.3; 16/16 16.4 / 23.3 / 54.0.
-int moe_warps(int phase, int ents) {
-    return (phase == 1 || ents <= 16) ? kMWWide : kMWPaired;
-}
+// Warps per CTA: 16 (two per SMSP for the units' latency), or 8 where a
+// 16-warp CTA's rings and staged activations do not fit in shared memory.
+// Measured, MoE chain of 64 experts (2304 x 1024), top-8, 16- against 8-warp
+// down launches: 35.9 / 43.0 us against 38.5 / 43.5 at M = 3 / 4 (INT3:
+// 37.6 / 39.5 against 38.8 / 42.6); the down-shaped expert GEMV at M = 3:
+// 13.0 against 14.4 us.  (With an earlier, slower unit the 8-warp CTAs had
+// been ahead beyond 16 slots.)
 // CTAs, warps per tile and ring depth for one launch, at most one CTA per SM
 // (two fit where shared memory allows, for the next launch's).  Launch 1:
 // tiles_max (entry, pair) tiles, the split of K steps over warps that
@@ -951,14 +949,12 @@ MoeHPlan plan_moe_hmma_w(const DeviceInfo& dev, int phase, int ents, int slots, 
     if (p.smem > dev.max_smem_optin) p.ctas = 0;
     return p;
 }
-// moe_warps' choice, or 8-warp CTAs where a 16-warp CTA's rings and staged
-// activations do not fit in shared memory
+// 16-warp CTAs, or 8-warp CTAs where those do not fit
 MoeHPlan plan_moe_hmma(const DeviceInfo& dev, int phase, int ents, int slots, int kblocks,
                        long long tiles_max, int row_tiles, int bits, int slot_out) {
-    const int warps = moe_warps(phase, ents);
     const MoeHPlan p =
-        plan_moe_hmma_w(dev, phase, ents, slots, kblocks, tiles_max, row_tiles, bits, slot_out, warps);
-    if (p.ctas > 0 || warps == kMWPaired) return p;
+        plan_moe_hmma_w(dev, phase, ents, slots, kblocks, tiles_max, row_tiles, bits, slot_out, kMWWide);
+    if (p.ctas > 0) return p;
     return plan_moe_hmma_w(dev, phase, ents, slots, kblocks, tiles_max, row_tiles, bits, slot_out,
                            kMWPaired);
 }
