@@ -124,7 +124,7 @@ struct MoeHLayout {
     int ring, bfrag, csum, red, bars, ids, ent_e, ent_n, ent_col, ybuf, nent, total;
 };
 __host__ __device__ inline MoeHLayout moeh_layout(int W, int ents, int kblocks, int depth, int max_rt,
-                                                  int bits, int slots) {
+                                                  int bits, int slots, int wpt) {
     MoeHLayout L;
     int off = 0;
     L.ring = off;  // [warp][depth] stages
@@ -133,8 +133,8 @@ __host__ __device__ inline MoeHLayout moeh_layout(int W, int ents, int kblocks, 
     off += kblocks * 4 * ents * 4 * 16;
     L.csum = off;  // [block][column entity] {1024 sum B, sum x', 2^-sh, 0}
     off += kblocks * ents * 16;
-    L.red = off;  // [2][warp][lane] float4 partials of split tiles
-    off += 2 * W * 32 * 16;
+    L.red = off;  // [2][warp][lane] float4 partials of split tiles (none unsplit)
+    off += wpt > 1 ? 2 * W * 32 * 16 : 0;
     L.bars = off;  // [tile group][buffer] {full, empty}
     off += W * 2 * 2 * 8;
     L.ids = off;  // routed expert of each slot (-1: invalid)
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(32 * W, W == kMWPaired ? 2 : 1) k_moe_hmma(con
 
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw + 127u) & ~127u) - raw);
-    const MoeHLayout L = moeh_layout(W, ENTS, kblocks, D, a.max_rt, BITS, S);
+    const MoeHLayout L = moeh_layout(W, ENTS, kblocks, D, a.max_rt, BITS, S, WPT);
     unsigned char* ring = base + L.ring + warp * D * kStage;
     uint4* bfrag = reinterpret_cast<uint4*>(base + L.bfrag);
     float4* csum = reinterpret_cast<float4*>(base + L.csum);
@@ -938,14 +938,15 @@ MoeHPlan plan_moe_hmma_w(const DeviceInfo& dev, int phase, int ents, int slots, 
     }
     const int half = dev.smem_per_sm / 2 - 1024;
     const int budget = p.warps == kMWPaired &&
-                               moeh_layout(p.warps, ents, kblocks, 2, ybuf_rt, bits, slots).total <= half
+                               moeh_layout(p.warps, ents, kblocks, 2, ybuf_rt, bits, slots, p.wpt).total <=
+                                   half
                            ? half
                            : dev.max_smem_optin;
     p.depth = 2;
     while (p.depth < kMMaxDepth &&
-           moeh_layout(p.warps, ents, kblocks, p.depth + 1, ybuf_rt, bits, slots).total <= budget)
+           moeh_layout(p.warps, ents, kblocks, p.depth + 1, ybuf_rt, bits, slots, p.wpt).total <= budget)
         ++p.depth;
-    p.smem = moeh_layout(p.warps, ents, kblocks, p.depth, ybuf_rt, bits, slots).total;
+    p.smem = moeh_layout(p.warps, ents, kblocks, p.depth, ybuf_rt, bits, slots, p.wpt).total;
     if (p.smem > dev.max_smem_optin) p.ctas = 0;
     return p;
 }
