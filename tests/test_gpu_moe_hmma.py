@@ -224,3 +224,58 @@ def test_expert_gemv_after_a_producing_gemv(w, bits):
             torch.cuda.synchronize()
             assert torch.equal(got, want), routed
     assert w.w4a16_device_error(clear=True) == 0
+
+
+def test_expert_gemv_random_shapes_against_the_oracle(w, oracle):
+    # seeded random shapes within the fp16 kernel's limits: token and slot
+    # counts, experts (often fewer than the slots), row tiles from 1 to more
+    # than the SM count, K from one block up, a row per token or per slot,
+    # per-slot outputs or routed sums, some invalid ids; every case through
+    # the library's choice, the bf16 kernel and (over the same codes) the
+    # INT3 path
+    rng = np.random.default_rng(9490)
+    for case in range(12):
+        topk = int(rng.integers(1, 9))
+        M = int(rng.integers(1, 32 // topk + 1))
+        E = int(rng.integers(1, 40))
+        N = 16 * int(rng.choice([1, 3, 8, 40, 170]))
+        K = 128 * int(rng.integers(1, 12))
+        x_per_slot = bool(rng.integers(0, 2))
+        routed = bool(rng.integers(0, 2))
+        seed = 9491 + case
+        ids, rw = synth.routing(seed, M, topk, E) if topk <= E else (
+            rng.integers(0, E, size=(M, topk)).astype(np.int32), np.full((M, topk), 1.0 / topk, np.float32))
+        if case % 4 == 3:
+            ids = ids.copy()
+            ids[0, 0] = -1
+        codes = synth.codes3(seed, E * N, K)
+        s = synth.scales(seed, E * N, K // 128).reshape(E, N, K // 128)
+        z = synth.zeros(seed, E * N, K // 128, "uniform2to6").reshape(E, N, K // 128)
+        wq4 = oracle.pack(codes).reshape(E, N, -1)
+        wq3 = oracle.pack3(codes).reshape(E, N, -1)
+        x = synth.activations(seed, (M, topk, K) if x_per_slot else (M, K))
+        r = rw if routed else None
+        ref_ids, ref_rw = ids, r
+        if case % 4 == 3:  # the oracle leaves the invalid slot out
+            ref_ids = ids.copy()
+            ref_ids[0, 0] = 0
+            if routed:
+                ref_rw = rw.copy()
+                ref_rw[0, 0] = 0.0
+        ref = oracle.moe_gemv(x, ref_ids, ref_rw, wq4, s, z, 128, x_per_slot=x_per_slot)
+        if case % 4 == 3 and not routed:
+            ref[0, 0] = 0.0
+        what = "case %d: M=%d topk=%d E=%d N=%d K=%d per_slot=%d routed=%d" % (
+            case, M, topk, E, N, K, x_per_slot, routed)
+        args = (dev(x), dev(ids))
+        for kid in (0, 2):
+            y = w.w4a16_moe_gemv(*args, dev(wq4), dev(s), dev(z), 128,
+                                 route_w=None if r is None else dev(r), x_per_slot=x_per_slot,
+                                 kernel_id=kid)
+            torch.cuda.synchronize()
+            check_close(host_f64(y), ref, what + " kernel %d" % kid)
+        y3 = w.w3a16_moe_gemv(*args, dev(wq3), dev(s), dev(z), 128,
+                              route_w=None if r is None else dev(r), x_per_slot=x_per_slot)
+        torch.cuda.synchronize()
+        check_close(host_f64(y3), ref, what + " INT3")
+        w.w4a16_device_error(clear=True)
