@@ -517,6 +517,54 @@ def e2e_cabi_gbs(torch, w, M, N, K, g, steps):
                     "cudaStreamSynchronize"}
 
 
+def host_loop_path():
+    """Build (once, when missing or older than its source or the library)
+    the plain C caller of the library (w4a16_int4_weight_gemv_gb300/
+    host_loop.c) and return its path, or None if it cannot be built."""
+    import subprocess
+    from w4a16_int4_weight_gemv_gb300 import binding
+    pkg = os.path.join(ROOT, "w4a16_int4_weight_gemv_gb300")
+    src = os.path.join(pkg, "host_loop.c")
+    lib = binding.lib_path()
+    out = os.path.join(os.path.dirname(lib), "host_loop")
+    nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    try:
+        if (os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src)
+                and os.path.getmtime(out) >= os.path.getmtime(lib)):
+            return out
+        libdir = os.path.dirname(lib)
+        subprocess.run([nvcc, "-O2", "-I", os.path.join(ROOT, "include"), src, "-o", out,
+                        "-L", libdir, "-lw4a16", "-Xlinker", "-rpath=" + libdir],
+                       check=True, capture_output=True, text=True)
+        return out
+    except (OSError, subprocess.CalledProcessError):
+        return None
+
+
+def e2e_c_host_loop(M, N, K, g, steps):
+    """The C interface end to end from a plain C program (host_loop.c): per
+    step cudaMemcpyAsync of x from page-locked memory, w4a16_gemv on resident
+    weights, cudaMemcpyAsync of y back, cudaStreamSynchronize; its last
+    result is checked bit for bit against the same GEMV on device buffers.
+    None if the program cannot be built or run."""
+    import subprocess
+    exe = host_loop_path()
+    if exe is None:
+        return None
+    r = subprocess.run([exe, str(M), str(N), str(K), str(g), str(steps), "200"],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        return None
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    us = d["us_per_step"]
+    return {"value": algo_bytes(M, N, K, g) / (us * 1e-6) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": d["h2d_bytes_per_step"],
+            "d2h_bytes_per_step": d["d2h_bytes_per_step"], "us_per_step": us,
+            "check": d["check"],
+            "path": "C program (host_loop.c): cudaMemcpyAsync H2D, w4a16_gemv, "
+                    "cudaMemcpyAsync D2H, cudaStreamSynchronize"}
+
+
 def e2e_gbs(torch, w, M, N, K, g, steps):
     """Public API with host buffers: per step copy x from pinned host memory,
     run w4a16_gemv on resident weights, read y back to host."""
@@ -833,9 +881,11 @@ def run_gpu(args):
                         "frac_measured_peak": round(byts / t / 1e9 / peak, 4)}
         extra["sweep"] = sweep
         e2e_steps = max(200, min(args.steps, 3000))
+        c_loop = e2e_c_host_loop(M, N, K, g, 5000)
         cabi = e2e_cabi_gbs(torch, w, M, N, K, g, e2e_steps)
         binding_e2e = e2e_gbs(torch, w, M, N, K, g, e2e_steps)
-        extra["e2e"] = cabi if cabi is not None else binding_e2e
+        extra["e2e"] = c_loop if c_loop is not None else (cabi if cabi is not None else binding_e2e)
+        extra["e2e_ctypes"] = cabi
         extra["e2e_python_binding"] = binding_e2e
         if M == 1:
             extra["e2e_zero_copy"] = e2e_zero_copy_gbs(torch, w, M, N, K, g, e2e_steps)

@@ -214,3 +214,22 @@ def test_product_path_does_not_import_oracle():
         if name.endswith(".py"):
             text = open(os.path.join(pkg, name)).read()
             assert "import oracle" not in text and "from oracle" not in text, name
+
+
+def test_plain_c_caller_builds_against_the_header(lib):
+    # the C caller the benchmark times (host_loop.c) compiles against
+    # include/w4a16.h and links against the library; without a GPU it stops
+    # at its first CUDA call with an error message, not a crash
+    import subprocess
+    import torch
+    import bench
+    exe = bench.host_loop_path()
+    if exe is None:
+        pytest.skip("nvcc not available")
+    r = subprocess.run([exe, "1", "256", "512", "128", "2", "1"], capture_output=True, text=True)
+    if torch.cuda.is_available():
+        assert r.returncode == 0, r.stderr
+        assert '"check": "bit-equal"' in r.stdout
+    else:
+        assert r.returncode == 1 and r.stderr.strip()
+    assert subprocess.run([exe], capture_output=True).returncode == 2   # usage
