@@ -164,7 +164,8 @@ W4A16_API size_t w4a16_gemv_workspace_bytes(int M, int64_t N, int64_t K, int64_t
  * as bf16 (round to nearest-even) or fp32 per out_dtype.
  *   workspace/workspace_bytes: may be NULL/0 (none is needed; see above).
  * Kernel choice (fixed by M, N, K, g; see w4a16_gemv_plan):
- *   - g == 128, K % 512 == 0 and either M <= 2, or M <= 16 with
+ *   - g == 128, K % 512 == 0 and either M <= 2, or M <= 4 with
+ *     N * K >= 2^24, or M <= 16 with
  *     N * K >= 2^25 where it has a launch plan (9..16 tokens take K slices of
  *     at most 2048 k): the fp16 warp-MMA kernel (id 4), which takes any
  *     finite bf16 x (each 128-k block of x is scaled by a power of two into

@@ -309,7 +309,8 @@ def test_cuda_core_kernel_small_activations(w, oracle):
 def test_gemv_default_dispatch_is_pinned(w):
     # the dispatch the benchmark times is the library default; pin it: the
     # fp16 warp-MMA kernel for one and two tokens on the square, wide-MLP and
-    # vocabulary shapes and for 3..16 tokens on matrices of 2^25 weights or
+    # vocabulary shapes, for three and four tokens on matrices of 2^24
+    # weights or more, and for 3..16 tokens on matrices of 2^25 weights or
     # more that it has a plan for, the bf16 warp-MMA kernel for 3..16 tokens
     # on smaller matrices, for 9..16 tokens where kernel 4 has no plan, and
     # for one token where kernel 4 does not apply (groups of 256,
@@ -321,8 +322,10 @@ def test_gemv_default_dispatch_is_pinned(w):
     for M in (3, 4, 8):
         for N, K in ((14336, 4096), (4096, 14336), (8192, 4096)):
             assert w.gemv_plan(M, N, K, 128)["kernel_id"] == 4
-        assert w.gemv_plan(M, 4096, 4096, 128)["kernel_id"] == 2
-        assert w.gemv_plan(M, 8191, 4096, 128)["kernel_id"] == 2
+        assert w.gemv_plan(M, 4096, 4096, 128)["kernel_id"] == (4 if M <= 4 else 2)
+        assert w.gemv_plan(M, 6144, 4096, 128)["kernel_id"] == (4 if M <= 4 else 2)
+        assert w.gemv_plan(M, 2048, 4096, 128)["kernel_id"] == 2
+        assert w.gemv_plan(M, 8191, 4096, 128)["kernel_id"] == (4 if M <= 4 else 2)
     for M in (9, 16):
         assert w.gemv_plan(M, 14336, 4096, 128)["kernel_id"] == 4
         assert w.gemv_plan(M, 8192, 8192, 128)["kernel_id"] == 4

@@ -82,7 +82,8 @@ w4a16_status check_gemv_shape(int M, int64_t N, int64_t K, int64_t g) {
 w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, int k_split,
                        GemvPlan* plan, DeviceCache** dev) {
     // default: the fp16 warp-MMA kernel where it applies (g == 128,
-    // K % 512 == 0) -- for one or two tokens always, for 3..8 tokens on
+    // K % 512 == 0) -- for one or two tokens always, for three or four
+    // tokens on matrices of at least 2^24 weights, for 3..16 tokens on
     // matrices of at least 2^25 weights; otherwise the bf16 warp-MMA kernel
     // where the groups are multiples of 128 k; the CUDA-core kernel for one
     // or two tokens with finer groups.  (Measured on GB300: kernel 4 ahead
@@ -91,12 +92,16 @@ w4a16_status make_plan(int M, int64_t N, int64_t K, int64_t g, int kernel_id, in
     // by up to 20 % on 4096 x 4096 and smaller matrices; at 9..16 tokens
     // (two MMA tiles, K slices of at most 2048 k) ahead by 5-40 % from
     // 14336 x 4096 up where a plan exists, falling back to kernel 2 where
-    // none does, e.g. 4096 x 14336.)
+    // none does, e.g. 4096 x 14336.  Between 2^24 and 2^25 weights, over
+    // nine shapes from 4096 x 4096 to 8192 x 2048: at three and four tokens
+    // 12 % ahead on average, at most 2 % behind; at 8 and 16 tokens from
+    // 46 % ahead to 23 % behind, so kernel 2 stays there.)
     const int requested = kernel_id;
     const bool automatic = kernel_id == 0;
     if (automatic) {
         const bool k4 = hmma_supports(M, static_cast<int>(K), static_cast<int>(g)) &&
-                        (M <= 2 || N * K >= (int64_t(1) << 25));
+                        (M <= 2 || N * K >= (int64_t(1) << 25) ||
+                         (M <= 4 && N * K >= (int64_t(1) << 24)));
         kernel_id = k4 ? 4 : (g % 128 == 0) ? 2 : 1;
     }
     if (kernel_id == 1 && M > 2) return W4A16_ERR_UNSUPPORTED;
