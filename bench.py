@@ -822,6 +822,15 @@ def run_gpu(args):
                 "note": "one GEMV over 8-row-interleaved gate|up weights with the SwiGLU in its "
                         "epilogue, then the down GEMV (two launches, PDL, resident-weights flag); "
                         "unfused: gate, up, w4a16_swiglu, down"}
+        # a fused QKV projection (6144 x 4096) at three and four tokens: the
+        # library's choice (the fp16 warp-MMA kernel) and the bf16 one
+        for m in (3, 4):
+            for kid, tag in ((0, "qkv"), (2, "qkv_bf16_kernel")):
+                t = gpu_gemv_gbs(torch, w, m, 6144, 4096, 128, "uniform6to10", l2, sw_steps, sw_warm,
+                                 kernel_id=kid)
+                sweep["%s_M%d" % (tag, m)] = {
+                    "us": round(t * 1e6, 3), "GB/s": round(algo_bytes(m, 6144, 4096, 128) / t / 1e9, 1),
+                    "frac_measured_peak": round(algo_bytes(m, 6144, 4096, 128) / t / 1e9 / peak, 4)}
         t = gpu_gemv_gbs(torch, w, 1, 163840, 4096, 128, "uniform6to10", l2, 200, 20,
                          out_dtype=torch.float32)
         sweep["vocab_M1"] = {"us": round(t * 1e6, 3),
