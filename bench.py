@@ -358,6 +358,16 @@ def moe_chain_time(torch, w, M, steps, warmup, l2, fused=True, bits=4):
     return t, float(np.mean(byts))
 
 
+def moe_gemv_bytes(ids, N, K, g, bits, x_per_slot):
+    """Algorithmic bytes of one expert-indexed GEMV: every distinct routed
+    expert's packed weights and scales once, plus the activation rows (one
+    per token, or one per slot with x_per_slot)."""
+    ab = algo_bytes if bits == 4 else algo_bytes3
+    M, topk = ids.shape
+    rows = M * topk if x_per_slot else M
+    return len(np.unique(ids)) * ab(0, N, K, g) + rows * K * 2
+
+
 def moe_gemv_time(torch, w, M, steps, warmup, l2, shape="down", bits=4, kernel_id=0):
     """One expert-indexed GEMV of the MoE workload (64 experts, top-8) over
     rotated expert banks: shape "gate" (experts [1024, 2304], one activation
@@ -371,7 +381,6 @@ def moe_gemv_time(torch, w, M, steps, warmup, l2, shape="down", bits=4, kernel_i
     x_per_slot, routed = shape == "down", shape == "down"
     per_bank = E * N * K * (bits / 8.0 + 2.0 / 128)
     R = max(2, int(math.ceil(2.0 * l2 / per_bank)))
-    ab = algo_bytes if bits == 4 else algo_bytes3
     sets, byts = [], []
     for r in range(R):
         ids, rw = synth.routing(r, M, topk, E)
@@ -381,8 +390,7 @@ def moe_gemv_time(torch, w, M, steps, warmup, l2, shape="down", bits=4, kernel_i
         out = torch.empty((M, N) if routed else (M, topk, N), dtype=torch.bfloat16, device="cuda")
         sets.append((_dev(x, torch), _dev(ids, torch), _dev(rw, torch),
                      tuple(_dev(a, torch) for a in bank), out))
-        rows = M * topk if x_per_slot else M
-        byts.append(len(np.unique(ids)) * ab(0, N, K, g) + rows * K * 2)
+        byts.append(moe_gemv_bytes(ids, N, K, g, bits, x_per_slot))
 
     def step(i):
         x, ids, rw, bank, out = sets[i % R]

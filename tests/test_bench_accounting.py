@@ -45,3 +45,13 @@ def test_profiled_traffic_follows_the_kernel_source(monkeypatch):
     # a different kernel source: the stored counter no longer applies
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
     assert bench.profiled_traffic() is None
+
+
+def test_expert_gemv_bytes_count_each_distinct_expert_once():
+    import numpy as np
+    ids = np.array([[3, 7, 3, 9], [7, 7, 1, 3]], np.int32)   # experts 1, 3, 7, 9
+    per4 = 1024 * 2304 // 2 + 1024 * (2304 // 128) * 2
+    per3 = 1024 * 2304 * 3 // 8 + 1024 * (2304 // 128) * 2
+    assert bench.moe_gemv_bytes(ids, 1024, 2304, 128, 4, False) == 4 * per4 + 2 * 2304 * 2
+    assert bench.moe_gemv_bytes(ids, 1024, 2304, 128, 4, True) == 4 * per4 + 8 * 2304 * 2
+    assert bench.moe_gemv_bytes(ids, 1024, 2304, 128, 3, False) == 4 * per3 + 2 * 2304 * 2
