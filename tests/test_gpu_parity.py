@@ -587,3 +587,20 @@ def test_moe_ffn_bad_ids_and_shared_experts(w, oracle):
     ref_rw[2, 3] = 0.0
     ref = oracle.moe_ffn(p["x"], ref_ids, ref_rw, p["gate"], p["up"], p["down"], 128)
     check_close(host_f64(out), ref["out"], "moe ffn shared/bad ids")
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 6144, 4096), (4, 4096, 4096), (4, 8192, 2048), (3, 4096, 6144)])
+def test_gemv_three_and_four_tokens_on_mid_size_matrices(w, oracle, M, N, K):
+    # the default from 2^24 weights at three and four tokens is the fp16
+    # warp-MMA kernel: every output against the oracle, and equal to the
+    # forced kernel 4
+    assert w.gemv_plan(M, N, K, 128)["kernel_id"] == 4
+    p = synth.dense_problem(M, N, K, 128, "uniform6to10", seed=9500 + M)
+    args = dense_dev(p)
+    y = w.w4a16_gemv(*args, 128)
+    y4 = w.w4a16_gemv(*args, 128, kernel_id=4)
+    torch.cuda.synchronize()
+    check_close(host_f64(y), oracle.gemv(p["x"], p["wq"], p["scale"], p["zero"], 128),
+                "M=%d %dx%d" % (M, N, K))
+    assert torch.equal(y, y4)
+    assert w.w4a16_device_error(clear=True) == 0
