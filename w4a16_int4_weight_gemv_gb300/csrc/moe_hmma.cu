@@ -931,8 +931,12 @@ MoeHPlan plan_moe_hmma_w(const DeviceInfo& dev, int phase, int ents, int slots, 
             p.max_rt = (row_tiles + p.ctas - 1) / p.ctas;
             tiles = static_cast<long long>(p.max_rt) * tiles_max;
         }
+        // (spread tiles take at most two warps each: with four, the INT3
+        // expert GEMV of one token, 64 experts of 1024 x 2304, measured 3 %
+        // slower; INT4 the same either way)
+        const int wpt_cap = p.split ? 2 : nsteps;
         p.wpt = 1;
-        while (p.wpt * 2 <= nsteps && tiles * p.wpt * 2 <= p.warps) p.wpt *= 2;
+        while (p.wpt * 2 <= nsteps && p.wpt * 2 <= wpt_cap && tiles * p.wpt * 2 <= p.warps) p.wpt *= 2;
         if (slot_out) p.max_rt = 0;  // nothing kept in shared memory
         ybuf_rt = p.max_rt;
     }
